@@ -1,0 +1,117 @@
+/*
+ * apa.h -- C ABI of libapa.so: adaptive-precision causal attention prefill
+ * with GQA packing on GB300 (sm_103a).
+ *
+ * The method is the one of "APA: sloppy attention, exact where it counts"
+ * (rfriedmann.de blog):
+ *   - pass 1 ("Pass 1: FP4 everywhere, with a hot test") computes every 64-key
+ *     tile in block-scaled NVFP4 (E2M1 elements, one UE4M3 scale per 16 values,
+ *     one FP32 scale per head; keys mean-centred per channel) and flags "hot"
+ *     tiles, those where a row of a 16-row group has FP4 tile mass above
+ *     eps times its running sum lambda;
+ *   - pass 2 ("Pass 2: exact FP16 on the hot tiles") recomputes only the hot
+ *     tiles exactly (here in BF16 with FP32 accumulation);
+ *   - the two online-softmax states, which share one logit frame, are merged
+ *     exactly by log-sum-exp ("The merge that makes it exact").
+ * Shapes and masking follow SDPA (ffpa-attn.readthedocs.io, the "Note" on
+ * cross-, GQA and causal attention): BHSD layout, Hq % Hkv == 0, and with
+ * causal != 0 the queries are aligned to the key tail: query row i sees key j
+ * iff j <= i + (Nkv - Nq), which needs Nkv >= Nq.  The softmax scale is 1/sqrt(d).
+ *
+ * Common conventions:
+ *   - All pointer arguments of the device entry points are device memory owned
+ *     by the caller; the library never frees them.  q, k, v must be 16-byte
+ *     aligned.
+ *   - Calls are asynchronous: they enqueue work on `stream` and return.
+ *     Asynchronous kernel errors surface at the caller's next synchronisation;
+ *     a device-side wait that timed out is recorded in a library-wide device
+ *     error word that apa_check_error() reports.
+ *   - Results are deterministic: reruns with the same inputs are bitwise equal.
+ *   - On a negative status nothing has been enqueued.  No C++ exception crosses
+ *     the ABI.
+ */
+#ifndef APA_H
+#define APA_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* status codes */
+#define APA_OK 0
+#define APA_ERR_NULL (-1)      /* a required pointer is null */
+#define APA_ERR_SHAPE (-2)     /* B, Hq, Hkv, Nq, Nkv out of range, Hq % Hkv != 0, or causal with Nkv < Nq */
+#define APA_ERR_EPS (-3)       /* eps < 0 or NaN */
+#define APA_ERR_HEAD_DIM (-4)  /* d not in {64, 128, 256} */
+#define APA_ERR_CUDA (-5)      /* a CUDA call or launch failed; cudaGetLastError() holds the cause */
+#define APA_ERR_NOMEM (-6)     /* the workspace could not be allocated, or the given one is too small */
+#define APA_ERR_DEVICE (-7)    /* a kernel recorded a device-side timeout (apa_check_error) */
+#define APA_ERR_ALIGN (-8)     /* q, k or v not 16-byte aligned */
+
+/* Adaptive-precision attention, eps >= 0:
+ *   q        bf16 [B, Hq, Nq, d], contiguous
+ *   k, v     bf16 [B, Hkv, Nkv, d], contiguous
+ *   causal   0: every key visible; else tail-aligned causal mask
+ *   eps      hot-test threshold.  0 runs every visible tile exactly (the all-BF16
+ *            path, pass 2 only); +inf makes every tile cold (all-FP4 pass 1).
+ *   out      fp32 [B, Hq, Nq, d] (required)
+ *   lse      fp32 [B, Hq, Nq], natural-log log-sum-exp of the scaled scores (nullable)
+ *   hot_mask uint32 [B, Hkv, ceil(G*Nq/16), ceil(T/32)] with G = Hq/Hkv and
+ *            T = ceil(Nkv/64): bit t%32 of word t/32 is set iff key tile t was
+ *            hot for that 16-row group of GQA-packed rows (packed row p = pos*G + g
+ *            holds query head h*G + g at position pos).  At eps = 0 every tile the
+ *            group can see is marked.  Nullable.
+ * The workspace is allocated stream-ordered on `stream` (cudaMallocAsync) and
+ * released the same way.  Returns APA_OK or a negative status. */
+int apa_attention(const void* q, const void* k, const void* v, int B, int Hq, int Hkv, int Nq, int Nkv, int d,
+                  int causal, float eps, float* out, float* lse, uint32_t* hot_mask, cudaStream_t stream);
+
+/* Bytes of device workspace apa_attention_ws() needs for this problem (0 at eps = 0). */
+size_t apa_workspace_bytes(int B, int Hq, int Hkv, int Nq, int Nkv, int d, float eps);
+
+/* apa_attention() with a caller-provided device workspace of at least
+ * apa_workspace_bytes() bytes, 256-byte aligned; it allocates nothing.
+ * Two calls that overlap on the GPU must not share a workspace. */
+int apa_attention_ws(const void* q, const void* k, const void* v, int B, int Hq, int Hkv, int Nq, int Nkv, int d,
+                     int causal, float eps, float* out, float* lse, uint32_t* hot_mask, void* workspace,
+                     size_t workspace_bytes, cudaStream_t stream);
+
+/* apa_attention() on HOST buffers (page-locked memory recommended): copies q, k,
+ * v to the device, runs, copies out (and lse / hot_mask when non-null) back, all
+ * on `stream`, and synchronizes `stream` before returning.  Device memory is
+ * allocated stream-ordered for the duration of the call. */
+int apa_attention_host(const void* q, const void* k, const void* v, int B, int Hq, int Hkv, int Nq, int Nkv, int d,
+                       int causal, float eps, float* out, float* lse, uint32_t* hot_mask, cudaStream_t stream);
+
+/* The pass-1 NVFP4 operands on their own (blog, "Pass 1" and "Mean-centred K"):
+ *   kv_blob  uint8 [B*Hkv][T][apa_kv_blob_bytes / (B*Hkv*T)]: per 64-key tile the
+ *            E2M1 codes of the centred keys and of V^T with their UE4M3 scales, in
+ *            the tcgen05 shared-memory image (layout in the library's
+ *            apa_internal.h; 9216 bytes per tile at d = 128)
+ *   q_blob   uint8 [B*Hkv][ceil(G*Nq/128)][72*d]: E2M1 codes and UE4M3 scales of
+ *            128 GQA-packed query rows per block
+ *   mu       fp32 [B, Hkv, d]  per-channel key mean
+ *   s_q      fp32 [B, Hq]; s_k, s_v fp32 [B, Hkv]: FP32 per-head scales
+ * Temporary statistics are allocated stream-ordered on `stream`. */
+int apa_quantize(const void* q, const void* k, const void* v, int B, int Hq, int Hkv, int Nq, int Nkv, int d,
+                 uint8_t* kv_blob, uint8_t* q_blob, float* mu, float* s_q, float* s_k, float* s_v,
+                 cudaStream_t stream);
+size_t apa_kv_blob_bytes(int B, int Hkv, int Nkv, int d);
+size_t apa_q_blob_bytes(int B, int Hq, int Hkv, int Nq, int d);
+
+/* Synchronizes `stream`, then returns APA_ERR_DEVICE (and clears the word) if a
+ * kernel of this library recorded a device-side timeout on the current device,
+ * APA_ERR_CUDA if the stream reported an error, APA_OK otherwise. */
+int apa_check_error(cudaStream_t stream);
+
+/* Human-readable text for a status code (static storage). */
+const char* apa_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* APA_H */

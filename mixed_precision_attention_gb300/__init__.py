@@ -1,0 +1,135 @@
+"""Adaptive-precision causal attention prefill with GQA packing for GB300 (sm_103a).
+
+Thin Python binding over the C ABI of ``libapa.so`` (``include/apa.h``): it
+checks and marshals arguments; every step of the computation runs in the
+library's CUDA kernels.  PyTorch is used for device memory and the current
+stream only.  There is no CPU fallback: without the built library (see
+``mixed_precision_attention_gb300.build``) every compute call raises.
+
+Method: "APA: sloppy attention, exact where it counts" (rfriedmann.de blog).
+Pass 1 computes every 64-key tile in block-scaled NVFP4 and flags the tiles
+whose FP4 softmax mass exceeds eps times a row's running sum; pass 2 recomputes
+those exactly in BF16; the two states are merged exactly by log-sum-exp.
+"""
+from __future__ import annotations
+
+import ctypes
+
+from . import _lib
+from ._lib import ApaError, status_string
+
+__all__ = ["attention", "attention_host", "quantize", "workspace_bytes", "check_error", "ApaError",
+           "status_string", "hot_mask_shape", "TILE", "GROUP_ROWS", "BLOCK_ROWS"]
+
+TILE = 64          # keys per tile
+GROUP_ROWS = 16    # rows per hot-test group
+BLOCK_ROWS = 128   # GQA-packed rows per CTA
+
+
+def _ptr(t):
+    return ctypes.c_void_p(0 if t is None else t.data_ptr())
+
+
+def _stream(device):
+    import torch
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def hot_mask_shape(B, Hq, Hkv, Nq, Nkv):
+    G = Hq // Hkv
+    ng = (G * Nq + GROUP_ROWS - 1) // GROUP_ROWS
+    T = (Nkv + TILE - 1) // TILE
+    return (B, Hkv, ng, (T + 31) // 32)
+
+
+def _check_qkv(q, k, v):
+    import torch
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not isinstance(t, torch.Tensor) or t.dtype != torch.bfloat16 or t.dim() != 4:
+            raise TypeError(f"{name} must be a 4-D torch.bfloat16 tensor (BHSD)")
+        if not t.is_cuda:
+            raise ValueError(f"{name} must be on a CUDA device")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    B, Hq, Nq, d = q.shape
+    if k.shape != v.shape or k.shape[0] != B or k.shape[3] != d:
+        raise ValueError("k and v must be [B, Hkv, Nkv, d] with q's B and d")
+    return B, Hq, k.shape[1], Nq, k.shape[2], d
+
+
+def workspace_bytes(B, Hq, Hkv, Nq, Nkv, d, eps):
+    return int(_lib.load().apa_workspace_bytes(B, Hq, Hkv, Nq, Nkv, d, float(eps)))
+
+
+def attention(q, k, v, causal: bool = True, eps: float = 0.005, return_hot_mask: bool = False,
+              return_lse: bool = True, workspace=None):
+    """Adaptive-precision attention.
+
+    q: [B, Hq, Nq, d] bf16; k, v: [B, Hkv, Nkv, d] bf16 (CUDA, contiguous).
+    causal: tail-aligned causal mask (query row i sees keys j <= i + Nkv - Nq).
+    eps: hot-test threshold; 0 = every visible tile exact (BF16), inf = all FP4.
+    Returns (out fp32 [B,Hq,Nq,d], lse fp32 [B,Hq,Nq] or None, hot_mask or None);
+    hot_mask is int32 [B, Hkv, ceil(G*Nq/16), ceil(T/32)] holding uint32 bit
+    words (bit t%32 of word t/32: tile t hot for that 16-row group).
+    workspace: optional uint8 CUDA tensor of at least workspace_bytes(...) bytes.
+    """
+    import torch
+    lib = _lib.load()
+    B, Hq, Hkv, Nq, Nkv, d = _check_qkv(q, k, v)
+    dev = q.device
+    out = torch.empty((B, Hq, Nq, d), dtype=torch.float32, device=dev)
+    lse = torch.empty((B, Hq, Nq), dtype=torch.float32, device=dev) if return_lse else None
+    mask = torch.empty(hot_mask_shape(B, Hq, Hkv, Nq, Nkv), dtype=torch.int32, device=dev) if return_hot_mask else None
+    need = workspace_bytes(B, Hq, Hkv, Nq, Nkv, d, eps)
+    if workspace is None and need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    nbytes = 0 if workspace is None else workspace.numel()
+    st = lib.apa_attention_ws(_ptr(q), _ptr(k), _ptr(v), B, Hq, Hkv, Nq, Nkv, d, int(bool(causal)), float(eps),
+                              _ptr(out), _ptr(lse), _ptr(mask), _ptr(workspace), nbytes, _stream(dev))
+    _lib.check(st, "apa_attention_ws")
+    return out, lse, mask
+
+
+def attention_host(q, k, v, causal: bool = True, eps: float = 0.005, return_hot_mask: bool = False, stream=None):
+    """apa_attention_host: the same computation on HOST tensors (torch CPU, bf16,
+    contiguous; pinned memory recommended).  Copies in, runs, copies out and
+    synchronizes the stream.  Returns CPU tensors (out, lse, hot_mask or None)."""
+    import torch
+    lib = _lib.load()
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if t.dtype != torch.bfloat16 or t.is_cuda or not t.is_contiguous() or t.dim() != 4:
+            raise ValueError(f"{name} must be a contiguous 4-D bf16 CPU tensor")
+    B, Hq, Nq, d = q.shape
+    Hkv, Nkv = k.shape[1], k.shape[2]
+    out = torch.empty((B, Hq, Nq, d), dtype=torch.float32, pin_memory=True)
+    lse = torch.empty((B, Hq, Nq), dtype=torch.float32, pin_memory=True)
+    mask = torch.empty(hot_mask_shape(B, Hq, Hkv, Nq, Nkv), dtype=torch.int32) if return_hot_mask else None
+    s = ctypes.c_void_p(stream.cuda_stream) if stream is not None else _stream(None)
+    st = lib.apa_attention_host(_ptr(q), _ptr(k), _ptr(v), B, Hq, Hkv, Nq, Nkv, d, int(bool(causal)), float(eps),
+                                _ptr(out), _ptr(lse), _ptr(mask), s)
+    _lib.check(st, "apa_attention_host")
+    return out, lse, mask
+
+
+def quantize(q, k, v):
+    """The pass-1 NVFP4 operands (apa_quantize): dict of CUDA tensors
+    kv_blob, q_blob (uint8), mu [B,Hkv,d], s_q [B,Hq], s_k, s_v [B,Hkv] (fp32)."""
+    import torch
+    lib = _lib.load()
+    B, Hq, Hkv, Nq, Nkv, d = _check_qkv(q, k, v)
+    dev = q.device
+    r = dict(kv_blob=torch.empty(lib.apa_kv_blob_bytes(B, Hkv, Nkv, d), dtype=torch.uint8, device=dev),
+             q_blob=torch.empty(lib.apa_q_blob_bytes(B, Hq, Hkv, Nq, d), dtype=torch.uint8, device=dev),
+             mu=torch.empty((B, Hkv, d), dtype=torch.float32, device=dev),
+             s_q=torch.empty((B, Hq), dtype=torch.float32, device=dev),
+             s_k=torch.empty((B, Hkv), dtype=torch.float32, device=dev),
+             s_v=torch.empty((B, Hkv), dtype=torch.float32, device=dev))
+    st = lib.apa_quantize(_ptr(q), _ptr(k), _ptr(v), B, Hq, Hkv, Nq, Nkv, d, _ptr(r["kv_blob"]), _ptr(r["q_blob"]),
+                          _ptr(r["mu"]), _ptr(r["s_q"]), _ptr(r["s_k"]), _ptr(r["s_v"]), _stream(dev))
+    _lib.check(st, "apa_quantize")
+    return r
+
+
+def check_error(device=None):
+    """Synchronizes the current stream and raises if a kernel recorded a device-side timeout."""
+    _lib.check(_lib.load().apa_check_error(_stream(device)), "apa_check_error")

@@ -1,0 +1,266 @@
+// apa.cu -- the C ABI: argument checks, workspace layout and the launch
+// sequence stats -> finalize -> quantize -> pass 1 -> pass 2 (+ merge).
+#include <cmath>
+#include <cstring>
+
+#include "../../include/apa.h"
+#include "apa_internal.h"
+
+namespace apa {
+
+namespace {
+
+__device__ int g_device_error;  // set by bounded waits that gave up
+
+constexpr size_t kAlign = 256;
+size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+__global__ void visible_mask_kernel(Shape s, uint32_t* mask) {
+  const int ngroups = s.ngroups(), T = s.T(), nwords = (T + 31) / 32;
+  const size_t total = (size_t)s.BH() * ngroups * nwords;
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < total; i += (size_t)gridDim.x * blockDim.x) {
+    const int w = (int)(i % nwords);
+    const int grp = (int)((i / nwords) % ngroups);
+    const int last_row = min(s.R(), (grp + 1) * kGroupRows) - 1;
+    const int t_last = s.causal ? min(T - 1, (last_row / s.G() + s.off()) / kTile) : T - 1;
+    const int lo = w * 32, hi = min(t_last, lo + 31);
+    uint32_t bits = 0;
+    if (hi >= lo) bits = (hi - lo == 31) ? 0xFFFFFFFFu : ((1u << (hi - lo + 1)) - 1u);
+    mask[i] = bits;
+  }
+}
+
+int validate(const void* q, const void* k, const void* v, const float* out, int B, int Hq, int Hkv, int Nq, int Nkv,
+             int d, int causal, float eps, bool need_out) {
+  if (!q || !k || !v || (need_out && !out)) return APA_ERR_NULL;
+  if (B < 1 || Hq < 1 || Hkv < 1 || Nq < 1 || Nkv < 1 || Hq % Hkv) return APA_ERR_SHAPE;
+  if (causal && Nkv < Nq) return APA_ERR_SHAPE;
+  if ((Nkv + kTile - 1) / kTile > 65535) return APA_ERR_SHAPE;  // tile index is stored in 16 bits
+  if ((long long)(Hq / Hkv) * Nq > (1ll << 30)) return APA_ERR_SHAPE;
+  if (d != 64 && d != 128 && d != 256) return APA_ERR_HEAD_DIM;
+  if (std::isnan(eps) || eps < 0.f) return APA_ERR_EPS;
+  if (((uintptr_t)q | (uintptr_t)k | (uintptr_t)v) & 15) return APA_ERR_ALIGN;
+  return APA_OK;
+}
+
+}  // namespace
+
+int* device_error_word() {
+  static int* addr[64] = {nullptr};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  if (!addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return nullptr;
+    addr[dev] = static_cast<int*>(p);
+  }
+  return addr[dev];
+}
+
+size_t workspace_layout(const Shape& s, bool apa_mode, Workspace* ws, void* base) {
+  Workspace w{};
+  if (!apa_mode) {
+    if (ws) *ws = w;
+    return 0;
+  }
+  const size_t BH = s.BH(), T = s.T(), d = s.d, nblk = s.nblk(), BHq = (size_t)s.B * s.Hq;
+  size_t off = 0;
+  uint8_t* b = static_cast<uint8_t*>(base);
+  auto take = [&](size_t bytes) -> void* {
+    void* p = b ? b + off : nullptr;
+    off += align_up(bytes);
+    return p;
+  };
+  w.ksum = (float*)take(BH * T * d * 4);
+  w.kmin = (uint32_t*)take(BH * d * 4);
+  w.kmax = (uint32_t*)take(BH * d * 4);
+  w.vamax = (uint32_t*)take(BH * 4);
+  w.qamax = (uint32_t*)take(BHq * 4);
+  w.mu = (float*)take(BH * d * 4);
+  w.s_k = (float*)take(BH * 4);
+  w.s_v = (float*)take(BH * 4);
+  w.s_q = (float*)take(BHq * 4);
+  w.kv_blob = (uint8_t*)take(BH * T * blob_bytes((int)d));
+  w.q_blob = (uint8_t*)take(BH * nblk * qblob_bytes((int)d));
+  w.state_o = (float*)take(BH * nblk * kBlockRows * d * 4);
+  w.state_ml = (float2*)take(BH * nblk * kBlockRows * 8);
+  w.hot_list = (uint32_t*)take(BH * nblk * T * 4);
+  w.hot_count = (uint32_t*)take(BH * nblk * 4);
+  if (ws) *ws = w;
+  return off;
+}
+
+cudaError_t launch_visible_mask(const Shape& s, uint32_t* hot_mask, cudaStream_t st) {
+  visible_mask_kernel<<<256, 256, 0, st>>>(s, hot_mask);
+  return cudaGetLastError();
+}
+
+static int run_attention(const Shape& s, const void* q, const void* k, const void* v, float eps, float* out, float* lse,
+                         uint32_t* hot_mask, void* workspace, cudaStream_t stream) {
+  if (eps == 0.f) {
+    if (hot_mask && launch_visible_mask(s, hot_mask, stream) != cudaSuccess) return APA_ERR_CUDA;
+    return launch_pass2(s, q, k, v, nullptr, out, lse, stream) == cudaSuccess ? APA_OK : APA_ERR_CUDA;
+  }
+  Workspace ws;
+  workspace_layout(s, true, &ws, workspace);
+  if (hot_mask) {
+    const size_t words = (size_t)s.BH() * s.ngroups() * ((s.T() + 31) / 32);
+    if (cudaMemsetAsync(hot_mask, 0, words * 4, stream) != cudaSuccess) return APA_ERR_CUDA;
+  }
+  if (launch_quantize(s, q, k, v, ws, true, true, stream) != cudaSuccess) return APA_ERR_CUDA;
+  if (launch_pass1(s, ws, eps, hot_mask, stream) != cudaSuccess) return APA_ERR_CUDA;
+  if (launch_pass2(s, q, k, v, &ws, out, lse, stream) != cudaSuccess) return APA_ERR_CUDA;
+  return APA_OK;
+}
+
+}  // namespace apa
+
+using apa::Shape;
+
+extern "C" {
+
+size_t apa_workspace_bytes(int B, int Hq, int Hkv, int Nq, int Nkv, int d, float eps) {
+  if (B < 1 || Hq < 1 || Hkv < 1 || Nq < 1 || Nkv < 1 || Hq % Hkv) return 0;
+  Shape s{B, Hq, Hkv, Nq, Nkv, d, 1};
+  return apa::workspace_layout(s, eps != 0.f, nullptr, nullptr);
+}
+
+int apa_attention_ws(const void* q, const void* k, const void* v, int B, int Hq, int Hkv, int Nq, int Nkv, int d,
+                     int causal, float eps, float* out, float* lse, uint32_t* hot_mask, void* workspace,
+                     size_t workspace_bytes, cudaStream_t stream) {
+  int st = apa::validate(q, k, v, out, B, Hq, Hkv, Nq, Nkv, d, causal, eps, true);
+  if (st) return st;
+  Shape s{B, Hq, Hkv, Nq, Nkv, d, causal ? 1 : 0};
+  const size_t need = apa::workspace_layout(s, eps != 0.f, nullptr, nullptr);
+  if (need > 0 && (!workspace || workspace_bytes < need || ((uintptr_t)workspace & 255))) return APA_ERR_NOMEM;
+  return apa::run_attention(s, q, k, v, eps, out, lse, hot_mask, workspace, stream);
+}
+
+int apa_attention(const void* q, const void* k, const void* v, int B, int Hq, int Hkv, int Nq, int Nkv, int d,
+                  int causal, float eps, float* out, float* lse, uint32_t* hot_mask, cudaStream_t stream) {
+  int st = apa::validate(q, k, v, out, B, Hq, Hkv, Nq, Nkv, d, causal, eps, true);
+  if (st) return st;
+  Shape s{B, Hq, Hkv, Nq, Nkv, d, causal ? 1 : 0};
+  const size_t need = apa::workspace_layout(s, eps != 0.f, nullptr, nullptr);
+  void* ws = nullptr;
+  if (need && cudaMallocAsync(&ws, need, stream) != cudaSuccess) return APA_ERR_NOMEM;
+  st = apa::run_attention(s, q, k, v, eps, out, lse, hot_mask, ws, stream);
+  if (ws && cudaFreeAsync(ws, stream) != cudaSuccess && st == APA_OK) st = APA_ERR_CUDA;
+  return st;
+}
+
+int apa_attention_host(const void* q, const void* k, const void* v, int B, int Hq, int Hkv, int Nq, int Nkv, int d,
+                       int causal, float eps, float* out, float* lse, uint32_t* hot_mask, cudaStream_t stream) {
+  int st = apa::validate(q, k, v, out, B, Hq, Hkv, Nq, Nkv, d, causal, eps, true);
+  if (st) return st;
+  Shape s{B, Hq, Hkv, Nq, Nkv, d, causal ? 1 : 0};
+  const size_t nq = (size_t)B * Hq * Nq * d, nkv = (size_t)B * Hkv * Nkv * d;
+  const size_t nmask = (size_t)s.BH() * s.ngroups() * ((s.T() + 31) / 32);
+  const size_t need = apa::workspace_layout(s, eps != 0.f, nullptr, nullptr);
+  size_t off = 0;
+  auto slot = [&](size_t bytes) {
+    const size_t o = off;
+    off += apa::align_up(bytes);
+    return o;
+  };
+  const size_t oq = slot(nq * 2), ok = slot(nkv * 2), ov = slot(nkv * 2), oo = slot(nq * 4);
+  const size_t ol = slot(lse ? (size_t)B * Hq * Nq * 4 : 0), om = slot(hot_mask ? nmask * 4 : 0), ow = slot(need);
+  uint8_t* dev = nullptr;
+  if (cudaMallocAsync((void**)&dev, off, stream) != cudaSuccess) return APA_ERR_NOMEM;
+  st = APA_OK;
+  if (cudaMemcpyAsync(dev + oq, q, nq * 2, cudaMemcpyHostToDevice, stream) != cudaSuccess ||
+      cudaMemcpyAsync(dev + ok, k, nkv * 2, cudaMemcpyHostToDevice, stream) != cudaSuccess ||
+      cudaMemcpyAsync(dev + ov, v, nkv * 2, cudaMemcpyHostToDevice, stream) != cudaSuccess)
+    st = APA_ERR_CUDA;
+  if (st == APA_OK)
+    st = apa::run_attention(s, dev + oq, dev + ok, dev + ov, eps, (float*)(dev + oo), lse ? (float*)(dev + ol) : nullptr,
+                            hot_mask ? (uint32_t*)(dev + om) : nullptr, need ? dev + ow : nullptr, stream);
+  if (st == APA_OK) {
+    if (cudaMemcpyAsync(out, dev + oo, nq * 4, cudaMemcpyDeviceToHost, stream) != cudaSuccess) st = APA_ERR_CUDA;
+    if (lse && cudaMemcpyAsync(lse, dev + ol, (size_t)B * Hq * Nq * 4, cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+      st = APA_ERR_CUDA;
+    if (hot_mask && cudaMemcpyAsync(hot_mask, dev + om, nmask * 4, cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+      st = APA_ERR_CUDA;
+  }
+  if (cudaFreeAsync(dev, stream) != cudaSuccess && st == APA_OK) st = APA_ERR_CUDA;
+  if (cudaStreamSynchronize(stream) != cudaSuccess && st == APA_OK) st = APA_ERR_CUDA;
+  return st;
+}
+
+size_t apa_kv_blob_bytes(int B, int Hkv, int Nkv, int d) {
+  if (B < 1 || Hkv < 1 || Nkv < 1) return 0;
+  return (size_t)B * Hkv * ((Nkv + apa::kTile - 1) / apa::kTile) * apa::blob_bytes(d);
+}
+
+size_t apa_q_blob_bytes(int B, int Hq, int Hkv, int Nq, int d) {
+  if (B < 1 || Hq < 1 || Hkv < 1 || Nq < 1 || Hq % Hkv) return 0;
+  Shape s{B, Hq, Hkv, Nq, 1, d, 0};
+  return (size_t)s.BH() * s.nblk() * apa::qblob_bytes(d);
+}
+
+int apa_quantize(const void* q, const void* k, const void* v, int B, int Hq, int Hkv, int Nq, int Nkv, int d,
+                 uint8_t* kv_blob, uint8_t* q_blob, float* mu, float* s_q, float* s_k, float* s_v,
+                 cudaStream_t stream) {
+  int st = apa::validate(q, k, v, nullptr, B, Hq, Hkv, Nq, Nkv, d, 0, 1.f, false);
+  if (st) return st;
+  if (!kv_blob || !q_blob || !mu || !s_q || !s_k || !s_v) return APA_ERR_NULL;
+  Shape s{B, Hq, Hkv, Nq, Nkv, d, 0};
+  const size_t BH = s.BH(), T = s.T(), BHq = (size_t)B * Hq;
+  // scratch: per-tile key sums and the min / max / amax words
+  size_t off = 0;
+  auto slot = [&](size_t bytes) {
+    const size_t o = off;
+    off += apa::align_up(bytes);
+    return o;
+  };
+  const size_t o_sum = slot(BH * T * d * 4), o_min = slot(BH * d * 4), o_max = slot(BH * d * 4), o_va = slot(BH * 4),
+               o_qa = slot(BHq * 4);
+  uint8_t* scratch = nullptr;
+  if (cudaMallocAsync((void**)&scratch, off, stream) != cudaSuccess) return APA_ERR_NOMEM;
+  apa::Workspace ws{};
+  ws.ksum = (float*)(scratch + o_sum);
+  ws.kmin = (uint32_t*)(scratch + o_min);
+  ws.kmax = (uint32_t*)(scratch + o_max);
+  ws.vamax = (uint32_t*)(scratch + o_va);
+  ws.qamax = (uint32_t*)(scratch + o_qa);
+  ws.mu = mu;
+  ws.s_k = s_k;
+  ws.s_v = s_v;
+  ws.s_q = s_q;
+  ws.kv_blob = kv_blob;
+  ws.q_blob = q_blob;
+  st = apa::launch_quantize(s, q, k, v, ws, true, true, stream) == cudaSuccess ? APA_OK : APA_ERR_CUDA;
+  if (cudaFreeAsync(scratch, stream) != cudaSuccess && st == APA_OK) st = APA_ERR_CUDA;
+  return st;
+}
+
+int apa_check_error(cudaStream_t stream) {
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return APA_ERR_CUDA;
+  int* w = apa::device_error_word();
+  if (!w) return APA_ERR_CUDA;
+  int h = 0;
+  if (cudaMemcpy(&h, w, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return APA_ERR_CUDA;
+  if (h) {
+    const int zero = 0;
+    cudaMemcpy(w, &zero, sizeof(int), cudaMemcpyHostToDevice);
+    return APA_ERR_DEVICE;
+  }
+  return APA_OK;
+}
+
+const char* apa_status_string(int status) {
+  switch (status) {
+    case APA_OK: return "ok";
+    case APA_ERR_NULL: return "a required pointer is null";
+    case APA_ERR_SHAPE: return "invalid shape (B, Hq, Hkv, Nq, Nkv; Hq % Hkv; causal needs Nkv >= Nq)";
+    case APA_ERR_EPS: return "eps must be >= 0 and not NaN";
+    case APA_ERR_HEAD_DIM: return "head dimension must be 64, 128 or 256";
+    case APA_ERR_CUDA: return "CUDA error (see cudaGetLastError)";
+    case APA_ERR_NOMEM: return "workspace allocation failed or workspace too small";
+    case APA_ERR_DEVICE: return "a kernel timed out waiting on the device";
+    case APA_ERR_ALIGN: return "q, k and v must be 16-byte aligned";
+  }
+  return "unknown status";
+}
+
+}  // extern "C"

@@ -1,0 +1,99 @@
+// apa_internal.h -- layouts and launchers shared by the library's .cu files.
+//
+// Notation: G = Hq/Hkv query heads share one KV head; packed row p = pos*G + g
+// of KV head h holds query head h*G + g at position pos (GQA packing, so one
+// K/V tile serves all G heads); R = G*Nq packed rows; rows come in 128-row
+// blocks (one tcgen05 M tile) made of eight 16-row groups (the hot-test
+// granularity); keys come in 64-key tiles, T = ceil(Nkv/64).
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace apa {
+
+constexpr int kTile = 64;        // keys per tile
+constexpr int kBlockRows = 128;  // packed rows per block (tcgen05 M)
+constexpr int kGroupRows = 16;   // rows per hot-test group
+constexpr float kTau = 4.0f;     // lazy-max threshold (log2 units)
+constexpr float kColdOffset = 32.0f;  // a hot tile lifts the frame to at most c - 32
+constexpr float kLog2e = 1.4426950408889634f;
+
+struct Shape {
+  int B, Hq, Hkv, Nq, Nkv, d, causal;
+  __host__ __device__ int G() const { return Hq / Hkv; }
+  __host__ __device__ int R() const { return G() * Nq; }
+  __host__ __device__ int T() const { return (Nkv + kTile - 1) / kTile; }
+  __host__ __device__ int nblk() const { return (R() + kBlockRows - 1) / kBlockRows; }
+  __host__ __device__ int ngroups() const { return (R() + kGroupRows - 1) / kGroupRows; }
+  __host__ __device__ int off() const { return Nkv - Nq; }
+  __host__ __device__ int BH() const { return B * Hkv; }
+};
+
+// ------------------------------------------------------------------ NVFP4 tile blob
+// One blob per (b, KV head, 64-key tile), in the exact shared-memory image the
+// pass-1 MMAs read, so one bulk copy brings a tile in:
+//   [0, 32d)        K codes:   B operand of S = Q K^T (N = 64 keys, K = d),
+//                              canonical no-swizzle core matrices (8 rows x 16 B),
+//                              LBO 128 B (along K), SBO 4d B (8-key groups);
+//   [32d, 64d)      V^T codes: B operand of O += P V (N = d channels, K = 64 keys),
+//                              LBO 128 B, SBO 256 B;
+//   [64d, +ksf)     K scales: per pair of 64-channel k-blocks one 512-B chunk of
+//                   32 rows x 16 B; row l = [key l kb0][key l+32 kb0][key l kb1][key l+32 kb1]
+//                   (4 UE4M3 bytes each, one per 16 channels), copied to TMEM with
+//                   tcgen05.cp 32x128b.warpx4 (k-block kb at column 4*(kb/2) + 2*(kb%2));
+//   [.., +vsf)      V scales: per 128 channels one 512-B atom, byte (c%32)*16 + (c/32)*4 + kb16.
+// E2M1 codes are packed two per byte, the lower index in the low nibble.
+__host__ __device__ constexpr int sf_chunks(int d) { return (d + 127) / 128; }
+__host__ __device__ constexpr int blob_kcodes(int) { return 0; }
+__host__ __device__ constexpr int blob_vcodes(int d) { return 32 * d; }
+__host__ __device__ constexpr int blob_ksf(int d) { return 64 * d; }
+__host__ __device__ constexpr int blob_vsf(int d) { return 64 * d + 512 * sf_chunks(d); }
+__host__ __device__ constexpr int blob_bytes(int d) { return 64 * d + 1024 * sf_chunks(d); }
+// Q blob per 128-row block: codes (A operand, M = 128, K = d; LBO 128, SBO 4d) then
+// one 512-B scale atom per 64-channel k-block (row p: byte (p%32)*16 + (p/32)*4 + kb16).
+__host__ __device__ constexpr int qblob_sf(int d) { return 64 * d; }
+__host__ __device__ constexpr int qblob_bytes(int d) { return 64 * d + 512 * (d / 64); }
+
+// byte offset of the 8 code bytes of (row n, 16-element block cb) in a K-major
+// no-swizzle operand whose rows hold `kbytes` bytes (K/2)
+__host__ __device__ inline int fp4_kmajor_off(int n, int cb, int kbytes) {
+  return (n >> 3) * (kbytes * 8) + (cb >> 1) * 128 + (n & 7) * 16 + 8 * (cb & 1);
+}
+// byte offset of the scale of (row r < 128, k16 block) in a 512-B scale atom
+__host__ __device__ inline int sf_atom_off(int r, int k16) { return (r & 31) * 16 + (r >> 5) * 4 + k16; }
+
+// ------------------------------------------------------------------ workspace
+struct Workspace {
+  // quantizer
+  float* ksum;        // [BH][T][d] FP32 per-tile key sums
+  uint32_t* kmin;     // [BH][d] orderable-encoded per-channel min of K
+  uint32_t* kmax;     // [BH][d]
+  uint32_t* vamax;    // [BH] max |v| (float bits)
+  uint32_t* qamax;    // [B*Hq] max |q| (float bits)
+  float* mu;          // [BH][d]
+  float* s_k;         // [BH]
+  float* s_v;         // [BH]
+  float* s_q;         // [B*Hq]
+  uint8_t* kv_blob;   // [BH][T][blob_bytes(d)]
+  uint8_t* q_blob;    // [BH][nblk][qblob_bytes(d)]
+  // pass 1 -> pass 2
+  float* state_o;     // [BH][nblk*128][d]: pass-1 o (scaled by s_v)
+  float2* state_ml;   // [BH][nblk*128]: pass-1 frame m and cold sum l
+  uint32_t* hot_list; // [BH*nblk][T]: tile | group mask << 16
+  uint32_t* hot_count;// [BH*nblk]
+};
+size_t workspace_layout(const Shape& s, bool apa_mode, Workspace* ws, void* base);
+
+int* device_error_word();  // library-wide device error word (set by bounded waits)
+
+// ------------------------------------------------------------------ launchers
+cudaError_t launch_quantize(const Shape& s, const void* q, const void* k, const void* v, const Workspace& ws,
+                            bool do_q, bool do_kv, cudaStream_t st);
+cudaError_t launch_pass1(const Shape& s, const Workspace& ws, float eps, uint32_t* hot_mask, cudaStream_t st);
+cudaError_t launch_pass2(const Shape& s, const void* q, const void* k, const void* v, const Workspace* ws,
+                         float* out, float* lse, cudaStream_t st);
+cudaError_t launch_visible_mask(const Shape& s, uint32_t* hot_mask, cudaStream_t st);
+
+}  // namespace apa

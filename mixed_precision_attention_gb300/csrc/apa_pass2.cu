@@ -1,0 +1,437 @@
+// apa_pass2.cu -- exact BF16 attention over a list of key tiles, merged with
+// the pass-1 state.
+//
+// "APA: sloppy attention, exact where it counts" (rfriedmann.de blog),
+// "Pass 2: exact FP16 on the hot tiles": a pass-2 CTA takes the same rows as a
+// pass-1 CTA, collects the union of their hot tiles, computes each row only on
+// its own group's hot tiles with an FP32 online softmax, and merges with the
+// pass-1 state ("The merge that makes it exact").  Logits are centred by the
+// same per-channel key mean as pass 1 (q.k - q.mu), so both states share one
+// frame; the natural-log LSE adds q.mu/sqrt(d) back.
+//
+// With eps = 0 the same kernel is the all-exact path: every visible tile of the
+// block, no pass-1 state, uncentred logits.
+//
+// GB300 design: one CTA = one 128-row block of GQA-packed rows of one KV head
+// (tcgen05 M = 128), 6 warps:
+//   warps 0-3  softmax, one thread per row (TMEM lane = row);
+//   warp 4     TMA producer: K and V tiles (64 keys x d, bf16, 128-byte swizzle)
+//              into an NS-stage ring;
+//   warp 5     TMEM owner and MMA issuer: S = Q K^T (kind::f16, K-major x K-major)
+//              into a double-buffered S in TMEM, O += P V (V MN-major) into O in TMEM.
+// The running max moves lazily (only when a score exceeds it by more than 8 in
+// log2 units), so O in TMEM is rarely rescaled.  P goes to the tensor cores as
+// two BF16 terms, P = P_hi + P_lo (P_lo the BF16 rounding of the residual), so
+// the PV product and the row sum carry ~16 mantissa bits of P instead of 8.
+#include <cuda_bf16.h>
+
+#include "apa_internal.h"
+#include "tc.cuh"
+
+namespace apa {
+
+namespace {
+
+struct P2Params {
+  Shape s;
+  const uint16_t* q;
+  const float* mu;            // null in the all-exact mode
+  const float* state_o;       // pass-1 o [BH][nblk*128][d] or null
+  const float2* state_ml;     // pass-1 (m, l) [BH][nblk*128] or null
+  const uint32_t* hot_list;   // [BH*nblk][T] or null (all visible tiles)
+  const uint32_t* hot_count;  // [BH*nblk] or null
+  float* out;                 // [B,Hq,Nq,d]
+  float* lse;                 // [B,Hq,Nq] or null
+  int* err;
+};
+
+constexpr int kThreads = 192;
+constexpr float kTau2 = 8.0f;  // pass-2 lazy rescale threshold (log2 units)
+
+template <int D>
+struct P2Cfg {
+  static constexpr int NS = D >= 256 ? 2 : 3;
+  static constexpr int kAtoms = D / 64;
+  static constexpr int kQBytes = 128 * D * 2;
+  static constexpr int kKVBytes = 64 * D * 2;  // one of K or V per stage
+  static constexpr int kPBytes = 128 * 64 * 2;  // one BF16 term of P
+  static constexpr int NP = D >= 256 ? 1 : 2;    // P buffers (each holds P_hi and P_lo)
+  static constexpr int kQOff = 0;
+  static constexpr int kStageOff = kQBytes;
+  static constexpr int kPOff = kStageOff + NS * 2 * kKVBytes;
+  static constexpr int kSmem = kPOff + NP * 2 * kPBytes + 1024;  // + alignment slack
+  static constexpr uint32_t kTmemCols = D + 128 <= 256 ? 256 : 512;
+  static constexpr uint32_t kOCol = 0, kSCol = D;
+};
+
+__device__ __forceinline__ void wait_bounded(uint32_t bar, uint32_t parity, int* err) {
+  // used only while unwinding: waits for copies already in flight, ignoring the abort flag
+  const unsigned long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity)) {
+    if (clock64() - t0 > APA_WAIT_LIMIT_CYCLES) {
+      if (err) atomicCAS(err, 0, APA_DEVERR_TIMEOUT);
+      return;
+    }
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    pass2_kernel(const P2Params p, const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap) {
+  using C = P2Cfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  __shared__ __align__(8) uint64_t bars[2 * C::NS + 9];
+  __shared__ uint32_t tmem_slot;
+  __shared__ int abort_flag;
+
+  const Shape& s = p.s;
+  const int nblk = s.nblk(), BH = s.BH(), G = s.G(), R = s.R(), T = s.T(), off = s.off();
+  // heavy (late, causal) blocks first
+  const int bh = blockIdx.x % BH, blk = nblk - 1 - (int)(blockIdx.x / BH);
+  const int b = bh / s.Hkv, h = bh % s.Hkv;
+  const int p0 = blk * kBlockRows;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t bar0 = smem_u32(bars);
+  auto kv_full = [&](int st) { return bar0 + 8u * st; };
+  auto kv_empty = [&](int st) { return bar0 + 8u * (C::NS + st); };
+  auto s_full = [&](int b2) { return bar0 + 8u * (2 * C::NS + b2); };
+  auto s_free = [&](int b2) { return bar0 + 8u * (2 * C::NS + 2 + b2); };
+  auto p_full = [&](int b2) { return bar0 + 8u * (2 * C::NS + 4 + b2); };
+  auto pv_done = [&](int b2) { return bar0 + 8u * (2 * C::NS + 6 + b2); };
+  const uint32_t drain = bar0 + 8u * (2 * C::NS + 8);
+  // every lane of a softmax warp waits; the warp proceeds only if all lanes succeeded
+  auto warp_wait = [&](uint32_t bar, uint32_t parity) -> bool {
+    const bool okl = mbar_wait(bar, parity, &abort_flag, p.err);
+    return __all_sync(0xffffffffu, okl);
+  };
+
+  // the block's tile list
+  const bool apa_mode = p.hot_list != nullptr;
+  const int last_row = min(R, p0 + kBlockRows) - 1;
+  const int t_hi = s.causal ? min(T - 1, (last_row / G + off) / kTile) : T - 1;
+  const int n = apa_mode ? (int)p.hot_count[(size_t)bh * nblk + blk] : t_hi + 1;
+  const uint32_t* list = apa_mode ? p.hot_list + ((size_t)bh * nblk + blk) * T : nullptr;
+  auto tile_of = [&](int i, uint32_t& gmask) -> int {
+    if (apa_mode) {
+      const uint32_t e = list[i];
+      gmask = e >> 16;
+      return (int)(e & 0xFFFFu);
+    }
+    gmask = 0xFFu;
+    return i == 0 ? 0 : t_hi + 1 - i;
+  };
+
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    for (int i = 0; i < 2 * C::NS + 9; ++i) {
+      const bool per_warp = (i >= 2 * C::NS + 2 && i < 2 * C::NS + 6);  // s_free, p_full: one arrive per softmax warp
+      mbar_init(bar0 + 8u * i, per_warp ? 4u : 1u);
+    }
+    fence_mbar_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(smem_u32(&tmem_slot), C::kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == 4 && lane == 0) {
+    prefetch_tmap(&kmap);
+    prefetch_tmap(&vmap);
+  }
+
+  // ---- softmax-thread setup: Q row into smem (128-byte swizzle, K-major), q.mu
+  const int r = threadIdx.x;  // row within the block for warps 0-3
+  const int P = p0 + r;
+  const bool row_valid = warp < 4 && P < R;
+  const int pos = row_valid ? P / G : 0;
+  const int hq = h * G + (row_valid ? P % G : 0);
+  float qmu = 0.f;
+  if (warp < 4) {
+    const uint4* src = reinterpret_cast<const uint4*>(p.q + (((size_t)b * s.Hq + hq) * s.Nq + pos) * D);
+    const float* mu = p.mu ? p.mu + (size_t)bh * D : nullptr;
+#pragma unroll 4
+    for (int j = 0; j < D / 8; ++j) {
+      uint4 val = row_valid ? src[j] : make_uint4(0u, 0u, 0u, 0u);
+      const int atom = j >> 3, chunk = j & 7;
+      *reinterpret_cast<uint4*>(smem + C::kQOff + atom * 16384 + r * 128 + ((chunk ^ (r & 7)) << 4)) = val;
+      if (mu) {
+        const uint32_t w[4] = {val.x, val.y, val.z, val.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          qmu = fmaf(__uint_as_float(w[e] << 16), mu[j * 8 + 2 * e], qmu);
+          qmu = fmaf(__uint_as_float(w[e] & 0xFFFF0000u), mu[j * 8 + 2 * e + 1], qmu);
+        }
+      }
+    }
+    fence_proxy_async_smem();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+
+  if (warp == 4) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int issued = 0;
+      for (int i = 0; i < n; ++i) {
+        const int st = i % C::NS;
+        if (i >= C::NS && !mbar_wait(kv_empty(st), ((i / C::NS) - 1) & 1, &abort_flag, p.err)) break;
+        uint32_t gm;
+        const int t = tile_of(i, gm);
+        mbar_arrive_expect_tx(kv_full(st), 2 * C::kKVBytes);
+        const uint32_t kdst = sbase + C::kStageOff + st * 2 * C::kKVBytes;
+#pragma unroll
+        for (int a = 0; a < C::kAtoms; ++a) {
+          tma_load_3d(kdst + a * 8192, &kmap, a * 64, t * kTile, bh, kv_full(st));
+          tma_load_3d(kdst + C::kKVBytes + a * 8192, &vmap, a * 64, t * kTile, bh, kv_full(st));
+        }
+        issued = i + 1;
+      }
+      if (abort_flag) {  // let copies in flight land before the CTA exits
+        for (int i = max(0, issued - C::NS); i < issued; ++i) wait_bounded(kv_full(i % C::NS), (i / C::NS) & 1, p.err);
+      }
+    }
+  } else if (warp == 5) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0 && n > 0) {
+      const uint32_t idS = idesc_bf16(128, 64, 0), idO = idesc_bf16(128, D, 1);
+      auto issue_s = [&](int i) -> bool {
+        const int st = i % C::NS;
+        if (!mbar_wait(kv_full(st), (i / C::NS) & 1, &abort_flag, p.err)) return false;
+        if (i >= 2 && !mbar_wait(s_free(i & 1), ((i >> 1) - 1) & 1, &abort_flag, p.err)) return false;
+        tc_fence_after();
+        const uint32_t kaddr = sbase + C::kStageOff + st * 2 * C::kKVBytes;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint64_t ad = smem_desc(sbase + C::kQOff + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024, kSwizzle128B);
+          const uint64_t bd = smem_desc(kaddr + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024, kSwizzle128B);
+          mma_bf16(tmem + C::kSCol + 64 * (i & 1), ad, bd, idS, kk > 0);
+        }
+        mma_commit(s_full(i & 1));
+        return true;
+      };
+      bool ok = issue_s(0);
+      for (int i = 0; ok && i < n; ++i) {
+        if (i + 1 < n && !(ok = issue_s(i + 1))) break;
+        if (!(ok = mbar_wait(p_full(i & 1), (i >> 1) & 1, &abort_flag, p.err))) break;
+        tc_fence_after();
+        const uint32_t vaddr = sbase + C::kStageOff + (i % C::NS) * 2 * C::kKVBytes + C::kKVBytes;
+        const uint32_t paddr = sbase + C::kPOff + (i % C::NP) * 2 * C::kPBytes;
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          const uint64_t bd = smem_desc(vaddr + kk * 2048, 8192, 1024, kSwizzle128B);
+          mma_bf16(tmem + C::kOCol, smem_desc(paddr + kk * 32, 16, 1024, kSwizzle128B), bd, idO,
+                   (i > 0 || kk > 0) ? 1u : 0u);
+          mma_bf16(tmem + C::kOCol, smem_desc(paddr + C::kPBytes + kk * 32, 16, 1024, kSwizzle128B), bd, idO, 1u);
+        }
+        mma_commit(pv_done(i & 1));
+        mma_commit(kv_empty(i % C::NS));
+      }
+      // drain: every tcgen05 op issued by this thread has completed before TMEM is freed
+      mma_commit(drain);
+      wait_bounded(drain, 0, p.err);
+    }
+  } else {
+    // ------------------------------------------------------------ softmax (one thread per row)
+    const float c2 = kLog2e * rsqrtf((float)D);
+    const float shift = p.mu ? qmu * c2 : 0.f;
+    const int vis_last = s.causal ? pos + off : s.Nkv - 1;  // last visible key of this row
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    float m2 = -INFINITY, l2 = 0.f;
+    bool ok = true;
+    for (int i = 0; i < n; ++i) {
+      uint32_t gm;
+      const int t = tile_of(i, gm);
+      if (!(ok = warp_wait(s_full(i & 1), (i >> 1) & 1))) break;
+      tc_fence_after();
+      uint32_t raw[64];
+      tmem_ld_x32(tmem + lane_base + C::kSCol + 64 * (i & 1), raw);
+      tmem_ld_x32(tmem + lane_base + C::kSCol + 64 * (i & 1) + 32, raw + 32);
+      tmem_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(s_free(i & 1));
+      const bool row_hot = row_valid && ((gm >> (r >> 4)) & 1u);
+      const int j0 = t * kTile;
+      const int nvis = row_hot ? min(kTile, vis_last + 1 - j0) : 0;  // keys j0 .. j0+nvis-1 visible
+      float sv[64];
+      float c = -INFINITY;
+#pragma unroll
+      for (int j = 0; j < 64; ++j) {
+        sv[j] = j < nvis ? fmaf(__uint_as_float(raw[j]), c2, -shift) : -INFINITY;
+        c = fmaxf(c, sv[j]);
+      }
+      float f = 1.f;
+      bool rescale = false;
+      if (c > m2 + kTau2 || (m2 == -INFINITY && c > -INFINITY)) {
+        if (l2 > 0.f) {
+          f = ex2_approx(m2 - c);
+          rescale = true;
+        }
+        m2 = c;
+      }
+      // this P buffer is free once PV(i - NP) has completed
+      if (i >= C::NP && !(ok = warp_wait(pv_done((i - C::NP) & 1), ((i - C::NP) >> 1) & 1))) break;
+      uint8_t* prow = smem + C::kPOff + (i % C::NP) * 2 * C::kPBytes + r * 128;
+      float psum = 0.f;
+#pragma unroll
+      for (int ch = 0; ch < 8; ++ch) {
+        uint32_t hi[4], lo[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int j = 8 * ch + 2 * e;
+          const float a0 = ex2_approx(sv[j] - m2), a1 = ex2_approx(sv[j + 1] - m2);
+          const __nv_bfloat162 h2 = __floats2bfloat162_rn(a0, a1);
+          const float2 hf = __bfloat1622float2(h2);
+          const __nv_bfloat162 l2v = __floats2bfloat162_rn(a0 - hf.x, a1 - hf.y);
+          const float2 lf = __bfloat1622float2(l2v);
+          psum += (hf.x + lf.x) + (hf.y + lf.y);
+          hi[e] = *reinterpret_cast<const uint32_t*>(&h2);
+          lo[e] = *reinterpret_cast<const uint32_t*>(&l2v);
+        }
+        const int sw = (ch ^ (r & 7)) << 4;
+        *reinterpret_cast<uint4*>(prow + sw) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        *reinterpret_cast<uint4*>(prow + C::kPBytes + sw) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+      }
+      l2 = l2 * f + psum;
+      if (__any_sync(0xffffffffu, rescale)) {
+        // O must not be read before PV(i-1) has landed
+        if (!(ok = warp_wait(pv_done((i - 1) & 1), ((i - 1) >> 1) & 1))) break;
+        tc_fence_after();
+#pragma unroll 1
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          uint32_t o[32];
+          tmem_ld_x32(tmem + lane_base + C::kOCol + c0, o);
+          tmem_wait_ld();
+#pragma unroll
+          for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * f);
+          tmem_st_x16(tmem + lane_base + C::kOCol + c0, o);
+          tmem_st_x16(tmem + lane_base + C::kOCol + c0 + 16, o + 16);
+        }
+        tmem_wait_st();
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(p_full(i & 1));
+    }
+    // ---- epilogue: merge with the pass-1 state, write out and lse
+    if (ok && n > 0) ok = warp_wait(pv_done((n - 1) & 1), ((n - 1) >> 1) & 1);
+    tc_fence_after();
+    if (ok) {
+      float m1 = -INFINITY, l1 = 0.f;
+      const float* st = nullptr;
+      if (p.state_o) {
+        st = p.state_o + ((size_t)bh * nblk * kBlockRows + P) * D;
+        if (row_valid) {
+          const float2 ml = p.state_ml[(size_t)bh * nblk * kBlockRows + P];
+          m1 = ml.x;
+          l1 = ml.y;
+        }
+      }
+      const float e1 = l1 > 0.f ? m1 : -INFINITY, e2 = l2 > 0.f ? m2 : -INFINITY;
+      const float M = fmaxf(e1, e2);
+      const float w1 = e1 == -INFINITY ? 0.f : exp2f(e1 - M), w2 = e2 == -INFINITY ? 0.f : exp2f(e2 - M);
+      const float L = w1 * l1 + w2 * l2;
+      const float invL = 1.f / L;
+      float* orow = p.out + (((size_t)b * s.Hq + hq) * s.Nq + pos) * D;
+#pragma unroll 1
+      for (int c0 = 0; c0 < D; c0 += 32) {
+        uint32_t o[32];
+        if (n > 0) {
+          tmem_ld_x32(tmem + lane_base + C::kOCol + c0, o);
+          tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) o[j] = 0u;
+        }
+        if (row_valid) {
+#pragma unroll
+          for (int j = 0; j < 32; j += 4) {
+            float4 res;
+            float* rr = &res.x;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float a1 = st ? st[c0 + j + e] : 0.f;
+              rr[e] = (w1 * a1 + w2 * __uint_as_float(o[j + e])) * invL;
+            }
+            *reinterpret_cast<float4*>(orow + c0 + j) = res;
+          }
+        }
+      }
+      if (row_valid && p.lse) {
+        const float lg = M + log2f(L);
+        p.lse[((size_t)b * s.Hq + hq) * s.Nq + pos] = 0.6931471805599453f * lg + (p.mu ? qmu * rsqrtf((float)D) : 0.f);
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+bool make_kv_map(CUtensorMap* map, const void* base, const Shape& s) {
+  using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+  static EncodeFn encode = nullptr;
+  if (!encode) {
+    cudaDriverEntryPointQueryResult q;
+    void* fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !fn)
+      return false;
+    encode = reinterpret_cast<EncodeFn>(fn);
+  }
+  const cuuint64_t dims[3] = {(cuuint64_t)s.d, (cuuint64_t)s.Nkv, (cuuint64_t)s.BH()};
+  const cuuint64_t strides[2] = {(cuuint64_t)s.d * 2, (cuuint64_t)s.Nkv * s.d * 2};
+  const cuuint32_t box[3] = {64, 64, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int D>
+cudaError_t launch_d(const P2Params& prm, const CUtensorMap& km, const CUtensorMap& vm, cudaStream_t st) {
+  const int smem = P2Cfg<D>::kSmem;
+  cudaError_t e = cudaFuncSetAttribute(pass2_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e) return e;
+  const int grid = prm.s.BH() * prm.s.nblk();
+  pass2_kernel<D><<<grid, kThreads, smem, st>>>(prm, km, vm);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_pass2(const Shape& s, const void* q, const void* k, const void* v, const Workspace* ws, float* out,
+                         float* lse, cudaStream_t st) {
+  CUtensorMap km, vm;
+  if (!make_kv_map(&km, k, s) || !make_kv_map(&vm, v, s)) return cudaErrorInvalidValue;
+  P2Params prm{};
+  prm.s = s;
+  prm.q = (const uint16_t*)q;
+  prm.mu = ws ? ws->mu : nullptr;
+  prm.state_o = ws ? ws->state_o : nullptr;
+  prm.state_ml = ws ? ws->state_ml : nullptr;
+  prm.hot_list = ws ? ws->hot_list : nullptr;
+  prm.hot_count = ws ? ws->hot_count : nullptr;
+  prm.out = out;
+  prm.lse = lse;
+  prm.err = device_error_word();
+  switch (s.d) {
+    case 64: return launch_d<64>(prm, km, vm, st);
+    case 128: return launch_d<128>(prm, km, vm, st);
+    case 256: return launch_d<256>(prm, km, vm, st);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace apa

@@ -1,0 +1,286 @@
+// apa_quant.cu -- per-head statistics and the NVFP4 quantizer.
+//
+// "APA: sloppy attention, exact where it counts" (rfriedmann.de blog),
+// section "Pass 1: FP4 everywhere, with a hot test": operands are E2M1 with one
+// UE4M3 scale per 16 values and one FP32 scale per head, so the head's largest
+// magnitude maps to 6 * 448 = 2688; keys are mean-centred per channel first
+// ("Mean-centred K"), and a prep stage writes K and V^T as one blob per 64-key
+// tile ("A 9216-byte blob per tile").
+//
+// The quantizer is bit-exact by construction: every FP32 operation is an
+// explicitly rounded intrinsic (no contraction), in this order per 16-block:
+//   a = max|x|;  sb = UE4M3_rn_sat(a / (6 s));  if sb == 0 all codes are 0,
+//   else code = E2M1_rn_sat(x * rcp_rn(UE4M3(sb) * s)).
+// The key mean is an FP32 sum per 64-key tile in ascending key order, the tile
+// sums added in ascending tile order in FP64, divided by Nkv in FP64 and
+// rounded to FP32.
+//
+// Kernels:
+//   stats_kernel     K/V tiles: per-tile FP32 key sums, per-channel min/max of K
+//                    (atomics on an order-preserving encoding: exact, so order-free),
+//                    max |V|; Q rows: max |Q| per query head.
+//   finalize_kernel  per (b, KV head): mu, FP32 head scales s_k, s_v, s_q.
+//   quant_kernel     K/V tiles -> blobs; 128-row Q blocks (GQA-packed) -> Q blobs.
+#include "apa_internal.h"
+#include "tc.cuh"
+
+namespace apa {
+
+namespace {
+
+constexpr int kThreads = 256;
+
+__device__ __forceinline__ uint32_t ord_enc(float f) {
+  uint32_t b = __float_as_uint(f);
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+__device__ __forceinline__ float ord_dec(uint32_t e) {
+  return __uint_as_float((e & 0x80000000u) ? (e & 0x7FFFFFFFu) : ~e);
+}
+__device__ __forceinline__ float bf16f(uint16_t h) { return __uint_as_float((uint32_t)h << 16); }
+__device__ __forceinline__ float ue4m3_value(uint32_t code) {
+  uint32_t E = code >> 3, m = code & 7;
+  if (E == 0) return (float)m * 0.001953125f;  // m * 2^-9
+  return __uint_as_float(((E + 120u) << 23) | (m << 20));
+}
+__device__ __forceinline__ float head_scale(float amax) { return amax == 0.f ? 1.f : __fdiv_rn(amax, 2688.f); }
+
+// Quantizes 16 values with head scale s; returns the scale code, writes 8 code bytes.
+__device__ __forceinline__ uint32_t quant16(const float* x, float s, uint2* codes) {
+  float a = 0.f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) a = fmaxf(a, fabsf(x[i]));
+  const float r = __fdiv_rn(a, __fmul_rn(6.f, s));
+  const uint32_t sb = cvt_ue4m3(r);
+  if (sb == 0) {
+    *codes = make_uint2(0u, 0u);
+    return 0;
+  }
+  const float inv = __frcp_rn(__fmul_rn(ue4m3_value(sb), s));
+  uint32_t w[2] = {0u, 0u};
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const uint32_t byte = cvt_e2m1x2(__fmul_rn(x[2 * i], inv), __fmul_rn(x[2 * i + 1], inv));
+    w[i >> 2] |= byte << (8 * (i & 3));
+  }
+  *codes = make_uint2(w[0], w[1]);
+  return sb;
+}
+
+// Loads rows [j0, j0 + nk) of a [rows, d] bf16 slice into smem (zero-filled to 64 rows).
+__device__ __forceinline__ void load_tile(uint16_t* sm, const uint16_t* g, int nk, int d) {
+  const int chunks = kTile * d / 8;  // 16-byte chunks
+  for (int i = threadIdx.x; i < chunks; i += blockDim.x) {
+    const int row = i / (d / 8);
+    uint4 val = make_uint4(0u, 0u, 0u, 0u);
+    if (row < nk) val = reinterpret_cast<const uint4*>(g)[i];
+    reinterpret_cast<uint4*>(sm)[i] = val;
+  }
+}
+
+__device__ __forceinline__ float block_max(float v, float* red) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    v = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : 0.f;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  }
+  __syncthreads();
+  return v;  // valid in warp 0
+}
+
+__global__ void __launch_bounds__(kThreads) stats_kernel(Shape s, const uint16_t* __restrict__ q,
+                                                          const uint16_t* __restrict__ k,
+                                                          const uint16_t* __restrict__ v, Workspace ws,
+                                                          int n_kv_blocks, int q_rows_per_block, int do_kv) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  __shared__ float red[32];
+  const int d = s.d, T = s.T();
+  if (do_kv && (int)blockIdx.x < n_kv_blocks) {
+    const int bh = blockIdx.x / T, t = blockIdx.x % T;
+    const int j0 = t * kTile, nk = min(kTile, s.Nkv - j0);
+    uint16_t* ks = reinterpret_cast<uint16_t*>(smem);
+    const size_t base = ((size_t)bh * s.Nkv + j0) * d;
+    load_tile(ks, k + base, nk, d);
+    // max |V| over the tile, straight from global
+    float vm = 0.f;
+    for (int i = threadIdx.x; i < nk * d / 8; i += blockDim.x) {
+      const uint4 val = reinterpret_cast<const uint4*>(v + base)[i];
+      const uint32_t w[4] = {val.x, val.y, val.z, val.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) vm = fmaxf(vm, fmaxf(fabsf(bf16f(w[e] & 0xFFFF)), fabsf(bf16f(w[e] >> 16))));
+    }
+    __syncthreads();
+    for (int c = threadIdx.x; c < d; c += blockDim.x) {
+      float acc = 0.f, mn = INFINITY, mx = -INFINITY;
+      for (int j = 0; j < nk; ++j) {
+        const float x = bf16f(ks[j * d + c]);
+        acc = __fadd_rn(acc, x);
+        mn = fminf(mn, x);
+        mx = fmaxf(mx, x);
+      }
+      ws.ksum[((size_t)bh * T + t) * d + c] = acc;
+      atomicMin(&ws.kmin[(size_t)bh * d + c], ord_enc(mn));
+      atomicMax(&ws.kmax[(size_t)bh * d + c], ord_enc(mx));
+    }
+    vm = block_max(vm, red);
+    if (threadIdx.x == 0) atomicMax(&ws.vamax[bh], __float_as_uint(vm));
+    return;
+  }
+  // max |Q| over a chunk of rows of one query head
+  const int qb = blockIdx.x - (do_kv ? n_kv_blocks : 0);
+  const int chunks_per_head = (s.Nq + q_rows_per_block - 1) / q_rows_per_block;
+  const int bhq = qb / chunks_per_head, ch = qb % chunks_per_head;
+  const int r0 = ch * q_rows_per_block, nr = min(q_rows_per_block, s.Nq - r0);
+  const uint4* src = reinterpret_cast<const uint4*>(q + ((size_t)bhq * s.Nq + r0) * d);
+  float qm = 0.f;
+  for (int i = threadIdx.x; i < nr * d / 8; i += blockDim.x) {
+    const uint4 val = src[i];
+    const uint32_t w[4] = {val.x, val.y, val.z, val.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) qm = fmaxf(qm, fmaxf(fabsf(bf16f(w[e] & 0xFFFF)), fabsf(bf16f(w[e] >> 16))));
+  }
+  qm = block_max(qm, red);
+  if (threadIdx.x == 0) atomicMax(&ws.qamax[bhq], __float_as_uint(qm));
+}
+
+__global__ void __launch_bounds__(kThreads) finalize_kernel(Shape s, Workspace ws, int do_q, int do_kv) {
+  __shared__ float red[32];
+  const int bh = blockIdx.x, d = s.d, T = s.T();
+  if (do_kv) {
+    float am = 0.f;
+    for (int c = threadIdx.x; c < d; c += blockDim.x) {
+      double S = 0.0;
+      for (int t = 0; t < T; ++t) S += (double)ws.ksum[((size_t)bh * T + t) * d + c];
+      const float mu = __double2float_rn(S / (double)s.Nkv);
+      ws.mu[(size_t)bh * d + c] = mu;
+      const float mn = ord_dec(ws.kmin[(size_t)bh * d + c]), mx = ord_dec(ws.kmax[(size_t)bh * d + c]);
+      am = fmaxf(am, fmaxf(fabsf(__fsub_rn(mx, mu)), fabsf(__fsub_rn(mn, mu))));
+    }
+    am = block_max(am, red);
+    if (threadIdx.x == 0) {
+      ws.s_k[bh] = head_scale(am);
+      ws.s_v[bh] = head_scale(__uint_as_float(ws.vamax[bh]));
+    }
+  }
+  if (do_q) {
+    const int b = bh / s.Hkv, h = bh % s.Hkv, G = s.G();
+    for (int g = threadIdx.x; g < G; g += blockDim.x) {
+      const int hq = b * s.Hq + h * G + g;
+      ws.s_q[hq] = head_scale(__uint_as_float(ws.qamax[hq]));
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kThreads) quant_kernel(Shape s, const uint16_t* __restrict__ q,
+                                                          const uint16_t* __restrict__ k,
+                                                          const uint16_t* __restrict__ v, Workspace ws,
+                                                          int n_kv_blocks, int do_kv) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  const int d = s.d, T = s.T();
+  if (do_kv && (int)blockIdx.x < n_kv_blocks) {
+    const int bh = blockIdx.x / T, t = blockIdx.x % T;
+    const int j0 = t * kTile, nk = min(kTile, s.Nkv - j0);
+    uint16_t* ks = reinterpret_cast<uint16_t*>(smem);
+    uint16_t* vs = ks + kTile * d;
+    float* mus = reinterpret_cast<float*>(vs + kTile * d);
+    const size_t base = ((size_t)bh * s.Nkv + j0) * d;
+    load_tile(ks, k + base, nk, d);
+    load_tile(vs, v + base, nk, d);
+    for (int c = threadIdx.x; c < d; c += blockDim.x) mus[c] = ws.mu[(size_t)bh * d + c];
+    __syncthreads();
+    const float sk = ws.s_k[bh], sv = ws.s_v[bh];
+    uint8_t* blob = ws.kv_blob + ((size_t)bh * T + t) * blob_bytes(d);
+    const int ncb = d / 16;
+    // K: per (key n, 16-channel block cb), centred
+    for (int it = threadIdx.x; it < kTile * ncb; it += blockDim.x) {
+      const int n = it / ncb, cb = it % ncb;
+      uint2 codes = make_uint2(0u, 0u);
+      uint32_t sb = 0;
+      if (n < nk) {
+        float x[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) x[i] = __fsub_rn(bf16f(ks[n * d + cb * 16 + i]), mus[cb * 16 + i]);
+        sb = quant16(x, sk, &codes);
+      }
+      *reinterpret_cast<uint2*>(blob + blob_kcodes(d) + fp4_kmajor_off(n, cb, d / 2)) = codes;
+      const int kb = cb >> 2, k16 = cb & 3;
+      blob[blob_ksf(d) + (kb >> 1) * 512 + (n & 31) * 16 + ((n >> 5) + 2 * (kb & 1)) * 4 + k16] = (uint8_t)sb;
+    }
+    // V^T: per (channel c, 16-key block kb16); keys past Nkv are zero
+    for (int it = threadIdx.x; it < d * 4; it += blockDim.x) {
+      const int c = it % d, kb16 = it / d;
+      float x[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) x[i] = bf16f(vs[(kb16 * 16 + i) * d + c]);
+      uint2 codes;
+      const uint32_t sb = quant16(x, sv, &codes);
+      *reinterpret_cast<uint2*>(blob + blob_vcodes(d) + fp4_kmajor_off(c, kb16, 32)) = codes;
+      blob[blob_vsf(d) + (c >> 7) * 512 + sf_atom_off(c & 127, kb16)] = (uint8_t)sb;
+    }
+    return;
+  }
+  // Q: one 128-row block of packed rows p = pos*G + g
+  const int qb = blockIdx.x - (do_kv ? n_kv_blocks : 0);
+  const int nblk = s.nblk(), G = s.G(), R = s.R();
+  const int bh = qb / nblk, blk = qb % nblk;
+  const int b = bh / s.Hkv, h = bh % s.Hkv;
+  uint8_t* qblob = ws.q_blob + ((size_t)bh * nblk + blk) * qblob_bytes(d);
+  const int ncb = d / 16;
+  for (int it = threadIdx.x; it < kBlockRows * ncb; it += blockDim.x) {
+    const int p = it / ncb, cb = it % ncb, P = blk * kBlockRows + p;
+    uint2 codes = make_uint2(0u, 0u);
+    uint32_t sb = 0;
+    if (P < R) {
+      const int g = P % G, pos = P / G, hq = b * s.Hq + h * G + g;
+      const uint4* src = reinterpret_cast<const uint4*>(q + ((size_t)hq * s.Nq + pos) * d + cb * 16);
+      const uint4 a0 = src[0], a1 = src[1];
+      const uint32_t w[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+      float x[16];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        x[2 * i] = bf16f(w[i] & 0xFFFF);
+        x[2 * i + 1] = bf16f(w[i] >> 16);
+      }
+      sb = quant16(x, ws.s_q[hq], &codes);
+    }
+    *reinterpret_cast<uint2*>(qblob + fp4_kmajor_off(p, cb, d / 2)) = codes;
+    qblob[qblob_sf(d) + (cb >> 2) * 512 + sf_atom_off(p, cb & 3)] = (uint8_t)sb;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_quantize(const Shape& s, const void* q, const void* k, const void* v, const Workspace& ws,
+                            bool do_q, bool do_kv, cudaStream_t st) {
+  const int BH = s.BH(), d = s.d, T = s.T();
+  cudaError_t e;
+  if (do_kv) {
+    if ((e = cudaMemsetAsync(ws.kmin, 0xFF, sizeof(uint32_t) * BH * d, st))) return e;
+    if ((e = cudaMemsetAsync(ws.kmax, 0x00, sizeof(uint32_t) * BH * d, st))) return e;
+    if ((e = cudaMemsetAsync(ws.vamax, 0x00, sizeof(uint32_t) * BH, st))) return e;
+  }
+  if (do_q && (e = cudaMemsetAsync(ws.qamax, 0x00, sizeof(uint32_t) * s.B * s.Hq, st))) return e;
+  const int n_kv = do_kv ? BH * T : 0;
+  const int q_rows = 64;
+  const int n_q = do_q ? s.B * s.Hq * ((s.Nq + q_rows - 1) / q_rows) : 0;
+  const size_t sm1 = (size_t)kTile * d * 2;
+  if (n_kv + n_q > 0)
+    stats_kernel<<<n_kv + n_q, kThreads, sm1, st>>>(s, (const uint16_t*)q, (const uint16_t*)k, (const uint16_t*)v, ws,
+                                                    n_kv, q_rows, do_kv);
+  if ((e = cudaGetLastError())) return e;
+  finalize_kernel<<<BH, kThreads, 0, st>>>(s, ws, do_q, do_kv);
+  if ((e = cudaGetLastError())) return e;
+  const int n_qb = do_q ? BH * s.nblk() : 0;
+  const size_t sm2 = (size_t)kTile * d * 2 * 2 + d * 4;
+  if (sm2 > 48 * 1024) cudaFuncSetAttribute(quant_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm2);
+  if (n_kv + n_qb > 0)
+    quant_kernel<<<n_kv + n_qb, kThreads, sm2, st>>>(s, (const uint16_t*)q, (const uint16_t*)k, (const uint16_t*)v,
+                                                     ws, n_kv, do_kv);
+  return cudaGetLastError();
+}
+
+}  // namespace apa

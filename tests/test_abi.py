@@ -1,0 +1,82 @@
+"""The C-ABI library builds, loads and exports what include/apa.h declares; its
+host-side argument checks return the documented statuses (CPU only: no call
+here reaches the GPU)."""
+import ctypes
+import math
+
+import pytest
+
+from mixed_precision_attention_gb300 import _lib, build
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return _lib.load()
+
+
+def test_exports_every_declared_symbol(lib):
+    names = _lib.declared_functions()
+    assert len(names) >= 9
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings(lib):
+    seen = set()
+    for s in range(0, -9, -1):
+        text = _lib.status_string(s)
+        assert text and text != "unknown status"
+        seen.add(text)
+    assert len(seen) == 9
+    assert _lib.status_string(-99) == "unknown status"
+
+
+P = ctypes.c_void_p
+OK_PTR = (P(0x10000), P(0x20000), P(0x30000))
+
+
+def _call(lib, q=OK_PTR[0], k=OK_PTR[1], v=OK_PTR[2], B=1, Hq=2, Hkv=1, Nq=128, Nkv=512, d=64, causal=1,
+          eps=0.005, out=P(0x40000)):
+    # every case below is rejected before anything is enqueued, so the fake
+    # pointers are never dereferenced
+    return lib.apa_attention(q, k, v, B, Hq, Hkv, Nq, Nkv, d, causal, eps, out, None, None, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(q=None), -1), (dict(k=None), -1), (dict(v=None), -1), (dict(out=None), -1),
+    (dict(B=0), -2), (dict(Hq=3, Hkv=2), -2), (dict(Nq=0), -2), (dict(Nkv=100, Nq=128), -2),
+    (dict(Nkv=64 * 65536), -2),
+    (dict(eps=-0.1), -3), (dict(eps=math.nan), -3),
+    (dict(d=96), -4), (dict(d=32), -4), (dict(d=512), -4),
+    (dict(v=P(0x30008)), -8),
+])
+def test_argument_errors(lib, kw, status):
+    assert _call(lib, **kw) == status
+
+
+def test_sizes(lib):
+    # one 9216-byte blob per 64-key tile at d = 128 (135.0 MiB at 8 heads x 122880 keys)
+    assert lib.apa_kv_blob_bytes(1, 8, 122880, 128) == 1920 * 8 * 9216
+    assert lib.apa_kv_blob_bytes(1, 1, 65, 128) == 2 * 9216
+    # 128 packed rows x 72 d bytes per Q block; GQA packs G * Nq rows
+    assert lib.apa_q_blob_bytes(1, 24, 8, 2048, 128) == 8 * 48 * 72 * 128
+    assert lib.apa_workspace_bytes(1, 24, 8, 2048, 122880, 128, 0.0) == 0
+    assert lib.apa_workspace_bytes(1, 24, 8, 2048, 122880, 128, 0.005) > 141557760
+    assert lib.apa_workspace_bytes(1, 3, 2, 16, 64, 64, 0.005) == 0  # Hq % Hkv != 0
+
+
+def test_workspace_too_small_is_rejected(lib):
+    need = lib.apa_workspace_bytes(1, 2, 1, 128, 512, 64, 0.005)
+    st = lib.apa_attention_ws(*OK_PTR, 1, 2, 1, 128, 512, 64, 1, 0.005, P(0x40000), None, None,
+                              P(0x50000), need - 1, None)
+    assert st == -6
+    st = lib.apa_attention_ws(*OK_PTR, 1, 2, 1, 128, 512, 64, 1, 0.005, P(0x40000), None, None,
+                              P(0x50010), need, None)  # not 256-byte aligned
+    assert st == -6
+
+
+def test_quantize_argument_errors(lib):
+    z = P(0x60000)
+    assert lib.apa_quantize(*OK_PTR, 1, 2, 1, 128, 512, 64, None, z, z, z, z, z, None) == -1
+    assert lib.apa_quantize(*OK_PTR, 1, 2, 1, 128, 512, 80, z, z, z, z, z, z, None) == -4

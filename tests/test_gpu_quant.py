@@ -1,0 +1,85 @@
+"""The CUDA NVFP4 quantizer against the oracle: codes, scales, key mean and
+head scales bit-exact (blog, "Pass 1: FP4 everywhere, with a hot test" and
+"Mean-centred K")."""
+import numpy as np
+import pytest
+
+import oracle
+from mixed_precision_attention_gb300 import synth
+from tests import _gpu
+
+pytestmark = pytest.mark.gpu
+
+CASES = [
+    dict(B=1, Hq=2, Hkv=1, Nq=128, Nkv=512, d=64, n_outliers=0),      # the tiny workload
+    dict(B=2, Hq=6, Hkv=2, Nq=37, Nkv=1000, d=128, n_outliers=4),    # G=3, ragged keys and rows
+    dict(B=1, Hq=4, Hkv=2, Nq=20, Nkv=333, d=256, n_outliers=4),     # d=256, ragged
+    dict(B=1, Hq=32, Hkv=8, Nq=256, Nkv=4096, d=128, n_outliers=4),  # prefill-shaped
+]
+
+
+def _quant_gpu(q, k, v):
+    import mixed_precision_attention_gb300 as apa
+    r = apa.quantize(_gpu.to_dev(q), _gpu.to_dev(k), _gpu.to_dev(v))
+    apa.check_error()
+    return {n: t.cpu().numpy() for n, t in r.items()}
+
+
+@pytest.mark.parametrize("case", CASES)
+def test_quantizer_bit_exact(case):
+    w = synth.small(sink_gain=4.0, **case)
+    q, k, v = synth.generate(w)
+    B, Hq, Hkv, Nq, Nkv, d = w.B, w.Hq, w.Hkv, w.Nq, w.Nkv, w.d
+    g = _quant_gpu(q, k, v)
+    ok = oracle.quantize_kv(k, v)
+    oq = oracle.quantize_q(q)
+    # key mean and FP32 head scales: bitwise
+    assert np.array_equal(g["mu"].view(np.uint32), ok["mu"].view(np.uint32))
+    assert np.array_equal(g["s_k"], ok["s_k"].astype(np.float32))
+    assert np.array_equal(g["s_v"], ok["s_v"].astype(np.float32))
+    assert np.array_equal(g["s_q"], oq["s_q"].astype(np.float32))
+    kc, ksf, vc, vsf = _gpu.decode_kv_blob(g["kv_blob"], B, Hkv, Nkv, d)
+    assert np.array_equal(kc[:, :, :Nkv], ok["kcodes"])
+    assert np.array_equal(ksf[:, :, :Nkv], ok["ksf"])
+    assert not kc[:, :, Nkv:].any() and not ksf[:, :, Nkv:].any()
+    Npad = ok["vcodes"].shape[-1]
+    assert np.array_equal(vc[..., :Npad], ok["vcodes"])
+    assert np.array_equal(vsf[..., :Npad // 16], ok["vsf"])
+    assert not vc[..., Npad:].any() and not vsf[..., Npad // 16:].any()
+    qc, qsf, pad_c, pad_s = _gpu.decode_q_blob(g["q_blob"], B, Hq, Hkv, Nq, d)
+    assert np.array_equal(qc, oq["codes"]) and np.array_equal(qsf, oq["sf"])
+    assert not pad_c.any() and not pad_s.any()
+
+
+def test_quantizer_adversarial_blocks():
+    """Ties, zeros, an all-zero head and tiny blocks with subnormal scales."""
+    B, Hq, Hkv, Nq, Nkv, d = 1, 2, 2, 64, 256, 64
+    rng = np.random.default_rng(7)
+    qf = rng.standard_normal((B, Hq, Nq, d)).astype(np.float32)
+    kf = rng.standard_normal((B, Hkv, Nkv, d)).astype(np.float32)
+    vf = rng.standard_normal((B, Hkv, Nkv, d)).astype(np.float32)
+    qf[0, 1] = 0.0                                   # an all-zero head: scale 1, every code 0
+    vf[0, 0, :16, :] = 0.0                           # zero V blocks
+    kf[0, 1, 5, :] = np.tile([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, 6.0], 8)  # E2M1 midpoints
+    qf[0, 0, 3, :16] = 1e-6                          # a tiny block next to large ones
+    qf[0, 0, 3, 16:] = 100.0
+    vf[0, 1, 32:48, 7] = 3e-7 * np.arange(16)        # subnormal UE4M3 block scale
+    q, k, v = (synth.f32_to_bf16_bits(a) for a in (qf, kf, vf))
+    g = _quant_gpu(q, k, v)
+    ok = oracle.quantize_kv(k, v)
+    oq = oracle.quantize_q(q)
+    kc, ksf, vc, vsf = _gpu.decode_kv_blob(g["kv_blob"], B, Hkv, Nkv, d)
+    assert np.array_equal(kc, ok["kcodes"]) and np.array_equal(ksf, ok["ksf"])
+    assert np.array_equal(vc, ok["vcodes"]) and np.array_equal(vsf, ok["vsf"])
+    qc, qsf, _, _ = _gpu.decode_q_blob(g["q_blob"], B, Hq, Hkv, Nq, d)
+    assert np.array_equal(qc, oq["codes"]) and np.array_equal(qsf, oq["sf"])
+    assert g["s_q"][0, 1] == 1.0 and not qc[0, 1].any()
+    assert (vsf[0, 1, 7, 2] < 8)  # the subnormal scale really occurs
+
+
+def test_quantizer_deterministic():
+    w = synth.small(B=1, Hq=4, Hkv=2, Nq=100, Nkv=2000, d=128, n_outliers=4)
+    q, k, v = synth.generate(w)
+    a, b = _quant_gpu(q, k, v), _quant_gpu(q, k, v)
+    for n in a:
+        assert np.array_equal(a[n], b[n])
