@@ -1,0 +1,380 @@
+#!/usr/bin/env python
+"""Benchmark of adaptive-precision attention prefill on GB300.
+
+One step = one call of the whole path (key/value statistics, NVFP4 quantizer,
+pass 1 with the hot test, pass 2 on the hot tiles, log-sum-exp merge) on the
+2048-query x 122880-key Llama-3.2-3B-shaped GQA layer (B=1, Hq=24, Hkv=8,
+d=128, tail-aligned causal, eps=0.005), synthetic seeded bf16 inputs resident
+in HBM (516 MB, larger than L2).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gpu|reference]
+
+Prints one JSON line.  Under torchrun every rank processes its own layer
+(weak scaling, no data-path collective); the time is the max over ranks.
+The reference arm times the CPU oracle (FP64 emulation of the same method)
+on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import os
+import re
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from mixed_precision_attention_gb300 import synth  # noqa: E402
+
+WORKLOAD = "llama3b_2048x122880"
+METRIC = "ms and effective TFLOP/s, 2048q x 122880k GQA layer; % of tensor-core roofline"
+UNIT = "TFLOP/s"
+PAGE_APA_MS = 5.200  # the blog's APA time for this layer on an RTX 5090 (context)
+FP4_PER_BF16 = 13.5 / 2.25  # nominal dense FP4 : BF16 tensor ratio
+FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+KERNELS_PER_STEP = 5  # stats, finalize, quantize, pass 1, pass 2 (+merge)
+
+
+# ----------------------------------------------------------------------------- helpers
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return {k: float(p[k]) for k in FALLBACK}, "measured"
+    return dict(FALLBACK), "fallback"
+
+
+def visible_counts(w: synth.Workload):
+    """[ng, T] visible (row, key) pairs per (16-row group, 64-key tile) of one KV head."""
+    G, R, T, off = w.G, w.G * w.Nq, (w.Nkv + 63) // 64, w.Nkv - w.Nq
+    ng = (R + 15) // 16
+    p = np.arange(ng * 16)
+    valid = p < R
+    last = (p // G + off) if w.causal else np.full(p.shape, w.Nkv - 1)
+    t0 = np.arange(T) * 64
+    cnt = np.clip(np.minimum(last[:, None] + 1, w.Nkv) - t0[None, :], 0, 64) * valid[:, None]
+    return cnt.reshape(ng, 16, T).sum(1)
+
+
+def algorithmic(w: synth.Workload, hot_mask):
+    """Algorithmic work: FP4 flops of pass 1, BF16 flops of pass 2, pair counts."""
+    vis = visible_counts(w)  # [ng, T]
+    T = vis.shape[1]
+    m = np.ascontiguousarray(hot_mask).view(np.uint32)
+    bits = np.unpackbits(m.view(np.uint8), bitorder="little").reshape(m.shape[:-1] + (-1,))[..., :T].astype(bool)
+    pairs = int(vis.sum()) * w.B * w.Hkv
+    hot_pairs = int((bits * vis[None, None]).sum())
+    cold_pairs = pairs - hot_pairs
+    d = w.d
+    F1 = pairs * (2 * d + 32) + cold_pairs * 2 * d  # QK^T + ones-MMA on every pair, PV on cold pairs
+    F2 = hot_pairs * 4 * d                         # exact QK^T and PV on hot pairs
+    tiles_vis = int((vis > 0).sum()) * w.B * w.Hkv
+    hot_tiles = int((bits & (vis > 0)[None, None]).sum())
+    return dict(pairs=pairs, hot_pairs=hot_pairs, cold_pairs=cold_pairs, F1=F1, F2=F2,
+                hot_frac=hot_tiles / max(1, tiles_vis), hot_pair_frac=hot_pairs / max(1, pairs))
+
+
+def kernel_source_hash(files):
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, "mixed_precision_attention_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel: str, src_hash: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on this source."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{WORKLOAD}.md")
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    hm = re.search(r"source hash:\s*`?([0-9a-f]{16})", text)
+    tm = re.search(r"dram bytes per launch:\s*`?([0-9.eE+]+)", text)
+    if not hm or not tm or hm.group(1) != src_hash:
+        return None
+    return float(tm.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+    FIELDS = ("index,pci.bus_id,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, pci_bus_id=None):
+        self.pci = (pci_bus_id or "").lower()
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-lms", "200", "-f", self.path], stdout=subprocess.DEVNULL,
+                                         stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 10:
+                    continue
+                if self.pci and self.pci[-12:] not in parts[1].lower():
+                    continue
+                rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[2]) for r in rows if num(r[2])]
+        smax = [num(r[3]) for r in rows if num(r[3])]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[6:10]) if v.lower() == "active"})
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def dist_setup():
+    return int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")), \
+        int(os.environ.get("LOCAL_RANK", "0"))
+
+
+def cpu_sample(w: synth.Workload, q, k, v, heads=(0,), groups_per_head=16, seed=0):
+    """The oracle's APA emulation on a bounded sample: `groups_per_head` 16-row
+    groups spread over the rows of each listed KV head.  Returns (seconds, flops
+    of exact attention on the sampled rows, rows, threads)."""
+    import oracle
+    ng = oracle.n_groups(w.Hq, w.Hkv, w.Nq)
+    rng = np.random.default_rng(seed)
+    units = []
+    for h in heads:
+        for g in np.sort(rng.choice(ng, size=min(groups_per_head, ng), replace=False)):
+            units.append((0, h, int(g)))
+    units = np.array(units, np.int32)
+    rows = [rr for (b, h, g) in units for rr in oracle.group_rows(w.Hq, w.Hkv, w.Nq, b, h, g)]
+    off = w.Nkv - w.Nq
+    flops = sum(4.0 * w.d * (min(w.Nkv, pos + off + 1) if w.causal else w.Nkv) for (_, _, pos) in rows)
+    t0 = time.perf_counter()
+    oracle.apa(q, k, v, causal=w.causal, eps=w.eps, units=units)
+    return time.perf_counter() - t0, flops, len(rows), oracle.num_threads()
+
+
+def config_dict(w):
+    return {"workload": WORKLOAD, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "Nq": w.Nq, "Nkv": w.Nkv, "d": w.d,
+            "causal": w.causal, "eps": w.eps, "key_tile": 64, "gqa_packing": True,
+            "l2": "inputs larger than L2 (bf16 Q/K/V 516 MB vs 126 MB L2); no flush"}
+
+
+# ----------------------------------------------------------------------------- reference arm
+def run_reference(args):
+    _, rank, _ = dist_setup()
+    if rank != 0:
+        return 0
+    import oracle
+    oracle.build()
+    w = synth.WORKLOADS[WORKLOAD]
+    q, k, v = synth.generate(w)
+    times, flops_all, nrows, threads = [], [], 0, 1
+    for step in range(args.warmup + args.steps):
+        dt, fl, nrows, threads = cpu_sample(w, q, k, v, heads=(step % w.Hkv,), groups_per_head=8, seed=step)
+        if step >= args.warmup:
+            times.append(dt)
+            flops_all.append(fl)
+    t = float(np.sum(times))
+    value = float(np.sum(flops_all)) / t / 1e12
+    cores = len(os.sched_getaffinity(0))
+    sample = (f"oracle APA emulation (FP64, OpenMP) of 8 sixteen-row groups of one KV head per step "
+              f"({nrows} query rows x up to {w.Nkv} keys, incl. that head's NVFP4 quantization), "
+              f"KV head = step mod 8")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t / len(times),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": config_dict(w),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": min(cores, threads), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ----------------------------------------------------------------------------- GPU arm
+def run_gpu(args):
+    import torch
+
+    import mixed_precision_attention_gb300 as apa
+    from mixed_precision_attention_gb300 import _lib
+
+    world, rank, local = dist_setup()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    lib = _lib.load()
+
+    w = synth.WORKLOADS[WORKLOAD]
+    q, k, v = synth.generate(w, seed=w.seed + rank)  # each rank: its own layer
+    tq, tk, tv = (synth.to_torch_bf16(a, dev) for a in (q, k, v))
+    B, Hq, Hkv, Nq, Nkv, d = w.B, w.Hq, w.Hkv, w.Nq, w.Nkv, w.d
+    workspace = torch.empty(apa.workspace_bytes(B, Hq, Hkv, Nq, Nkv, d, w.eps), dtype=torch.uint8, device=dev)
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    def max_over_ranks(x):
+        if world == 1:
+            return x
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        return float(t.item())
+
+    # one untimed call with the hot mask: the algorithmic work of this layer
+    _, _, mask = apa.attention(tq, tk, tv, causal=w.causal, eps=w.eps, return_hot_mask=True, workspace=workspace)
+    apa.check_error(dev)
+    work = algorithmic(w, mask.cpu().numpy())
+    flops_exact = w.flops_exact
+
+    def timed(eps, steps, warmup, ws_tensor, sample_clocks=False):
+        for _ in range(warmup):
+            apa.attention(tq, tk, tv, causal=w.causal, eps=eps, workspace=ws_tensor)
+        torch.cuda.synchronize(dev)
+        barrier()
+        torch.cuda.synchronize(dev)
+        clk = None
+        if sample_clocks:
+            pci = getattr(torch.cuda.get_device_properties(dev), "pci_bus_id", None)
+            clk = ClockSampler(pci if isinstance(pci, str) else None)
+            clk.start()
+        lib.apa_stage_timing(1)
+        stream = torch.cuda.current_stream(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            apa.attention(tq, tk, tv, causal=w.causal, eps=eps, workspace=ws_tensor)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier()
+        torch.cuda.synchronize(dev)
+        ms3 = (ctypes.c_float * 3)()
+        calls = ctypes.c_int()
+        lib.apa_stage_timing_read(ms3, ctypes.byref(calls))
+        lib.apa_stage_timing(0)
+        clocks = clk.stop() if clk else None
+        apa.check_error(dev)
+        return e0.elapsed_time(e1) / steps, [x / max(1, calls.value) for x in ms3], clocks
+
+    ms, stages, clocks = timed(w.eps, args.steps, args.warmup, workspace, sample_clocks=True)
+    ms = max_over_ranks(ms)
+    value = world * flops_exact / (ms * 1e-3) / 1e12
+
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": PAGE_APA_MS / ms, "dtype": "nvfp4 (e2m1 x ue4m3) + bf16, fp32 accumulate",
+            "data": "synthetic", "config": config_dict(w), "gpu_launches": KERNELS_PER_STEP * args.steps}
+
+    pk, pk_kind = peaks()
+    fp4_peak = pk["bf16_tflops_sustained"] * FP4_PER_BF16
+    bf16_peak = pk["bf16_tflops_sustained"]
+    t_q, t_p1, t_p2 = stages
+    src = kernel_source_hash(["apa_pass1.cu", "tc.cuh", "apa_internal.h"])
+    p1_ach = work["F1"] / (t_p1 * 1e-3) / 1e12
+    traffic = profiled_traffic("pass1", src)
+    line["roofline"] = {"kernel": "pass1 (tcgen05 kind::mxf4nvf4)", "bound": "tensor", "achieved": p1_ach,
+                        "peak": fp4_peak, "unit": "TFLOP/s", "frac": p1_ach / fp4_peak, "traffic": traffic,
+                        "peak_note": f"dense NVFP4 = {pk_kind} sustained bf16 x {FP4_PER_BF16:g} (nominal ratio)",
+                        "flops_per_launch": work["F1"], "ms_per_launch": t_p1}
+    p2_ach = work["F2"] / (t_p2 * 1e-3) / 1e12 if t_p2 > 0 else 0.0
+    q_bytes = (B * Hq * Nq * d + 2 * B * Hkv * Nkv * d) * (2 + 0.5625)
+    line["stages"] = {
+        "quantize": {"ms": t_q, "hbm_gbs": q_bytes / (t_q * 1e-3) / 1e9,
+                     "hbm_frac": q_bytes / (t_q * 1e-3) / 1e9 / pk["hbm_gbs"]},
+        "pass1": {"ms": t_p1, "tflops_fp4": p1_ach, "frac_fp4_peak": p1_ach / fp4_peak},
+        "pass2_merge": {"ms": t_p2, "tflops_bf16": p2_ach, "frac_bf16_peak": p2_ach / bf16_peak},
+    }
+    line["tensor_roofline_frac"] = (work["F1"] / fp4_peak + work["F2"] / bf16_peak) / 1e12 / (ms * 1e-3)
+    line["hot_tile_frac"] = work["hot_frac"]
+    line["hot_pair_frac"] = work["hot_pair_frac"]
+    line["peaks"] = {"source": pk_kind, **pk}
+    line["clocks"] = clocks
+
+    if not args.skip_extras:
+        # the same library at eps = 0: every visible tile exact in BF16 (no workspace needed)
+        ms0, _, _ = timed(0.0, max(3, args.steps // 4), 3, None)
+        ms0 = max_over_ranks(ms0)
+        line["eps0_all_bf16"] = {"ms_per_step": ms0, "tflops": world * flops_exact / (ms0 * 1e-3) / 1e12,
+                                 "speedup_of_apa": ms0 / ms}
+        # end to end through the host-buffer entry point: H2D of q, k, v from pinned
+        # memory, the whole path, D2H of out and lse, every step
+        hq, hk, hv = (synth.to_torch_bf16(a).pin_memory() for a in (q, k, v))
+        apa.attention_host(hq, hk, hv, causal=w.causal, eps=w.eps)
+        n_e2e = max(3, min(args.steps, 10))
+        barrier()
+        t0 = time.perf_counter()
+        for _ in range(n_e2e):
+            apa.attention_host(hq, hk, hv, causal=w.causal, eps=w.eps)
+        e2e_ms = max_over_ranks((time.perf_counter() - t0) * 1e3 / n_e2e)
+        line["e2e"] = {"value": world * flops_exact / (e2e_ms * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": e2e_ms,
+                       "h2d_bytes_per_step": q.nbytes + k.nbytes + v.nbytes,
+                       "d2h_bytes_per_step": B * Hq * Nq * d * 4 + B * Hq * Nq * 4}
+        if rank == 0 and world == 1:
+            dt, fl, nrows, threads = cpu_sample(w, q, k, v, heads=(0, 5), groups_per_head=8)
+            line["cpu_baseline"] = {
+                "value": fl / dt / 1e12, "unit": UNIT, "cores": min(threads, len(os.sched_getaffinity(0))),
+                "kind": "oracle", "seconds": dt,
+                "sample": f"oracle APA emulation (FP64, OpenMP) of 16 sixteen-row groups ({nrows} query rows) "
+                          f"of KV heads 0 and 5, all {w.Nkv} keys each, incl. the per-head NVFP4 quantization"}
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["gpu", "reference"], default="gpu")
+    ap.add_argument("--skip-extras", action="store_true",
+                    help="time the main loop only (no eps=0 / host / CPU legs); used for profiler runs")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        print("warning: fewer than 3 warm-up steps", file=sys.stderr)
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

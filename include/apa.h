@@ -103,6 +103,15 @@ int apa_quantize(const void* q, const void* k, const void* v, int B, int Hq, int
 size_t apa_kv_blob_bytes(int B, int Hkv, int Nkv, int d);
 size_t apa_q_blob_bytes(int B, int Hq, int Hkv, int Nq, int d);
 
+/* Measurement aid, off by default.  While enabled, every apa_attention* call
+ * records CUDA events on its stream around its three stages (quantizer, pass 1,
+ * pass 2 with the merge); enabling or disabling resets the record. */
+int apa_stage_timing(int enable);
+/* Waits for the recorded events and returns the summed milliseconds per stage in
+ * ms[0..2] (quantizer, pass 1, pass 2) and the number of calls in *calls, then
+ * clears the record.  At eps = 0 only the pass-2 stage has work. */
+int apa_stage_timing_read(float* ms, int* calls);
+
 /* Synchronizes `stream`, then returns APA_ERR_DEVICE (and clears the word) if a
  * kernel of this library recorded a device-side timeout on the current device,
  * APA_ERR_CUDA if the stream reported an error, APA_OK otherwise. */

@@ -27,6 +27,8 @@ _SIGS = {
     "apa_kv_blob_bytes": (SZ, [I, I, I, I]),
     "apa_q_blob_bytes": (SZ, [I, I, I, I, I]),
     "apa_check_error": (I, [P]),
+    "apa_stage_timing": (I, [I]),
+    "apa_stage_timing_read": (I, [P, P]),
     "apa_status_string": (ctypes.c_char_p, [I]),
 }
 

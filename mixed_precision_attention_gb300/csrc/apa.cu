@@ -2,6 +2,8 @@
 // sequence stats -> finalize -> quantize -> pass 1 -> pass 2 (+ merge).
 #include <cmath>
 #include <cstring>
+#include <mutex>
+#include <vector>
 
 #include "../../include/apa.h"
 #include "apa_internal.h"
@@ -95,21 +97,59 @@ cudaError_t launch_visible_mask(const Shape& s, uint32_t* hot_mask, cudaStream_t
   return cudaGetLastError();
 }
 
+// ------------------------------------------------------------------ stage timing
+// Opt-in measurement aid: events recorded on the call's stream before the
+// quantizer, before pass 1, before pass 2 and after pass 2.
+namespace {
+struct StageTiming {
+  std::mutex mu;
+  bool on = false;
+  std::vector<cudaEvent_t> ev;  // 4 per recorded call
+  size_t used = 0;
+} g_timing;
+
+size_t begin_call() {
+  std::lock_guard<std::mutex> lk(g_timing.mu);
+  if (!g_timing.on) return SIZE_MAX;
+  if (g_timing.used * 4 + 4 > g_timing.ev.size()) {
+    for (int i = 0; i < 4; ++i) {
+      cudaEvent_t e;
+      if (cudaEventCreate(&e) != cudaSuccess) return SIZE_MAX;
+      g_timing.ev.push_back(e);
+    }
+  }
+  return g_timing.used++;
+}
+}  // namespace
+
 static int run_attention(const Shape& s, const void* q, const void* k, const void* v, float eps, float* out, float* lse,
                          uint32_t* hot_mask, void* workspace, cudaStream_t stream) {
+  const size_t call = begin_call();
+  auto stage = [&](int slot) {
+    if (call != SIZE_MAX) cudaEventRecord(g_timing.ev[call * 4 + slot], stream);
+  };
   if (eps == 0.f) {
+    stage(0);
+    stage(1);
     if (hot_mask && launch_visible_mask(s, hot_mask, stream) != cudaSuccess) return APA_ERR_CUDA;
-    return launch_pass2(s, q, k, v, nullptr, out, lse, stream) == cudaSuccess ? APA_OK : APA_ERR_CUDA;
+    stage(2);
+    const int st = launch_pass2(s, q, k, v, nullptr, out, lse, stream) == cudaSuccess ? APA_OK : APA_ERR_CUDA;
+    stage(3);
+    return st;
   }
   Workspace ws;
   workspace_layout(s, true, &ws, workspace);
+  stage(0);
   if (hot_mask) {
     const size_t words = (size_t)s.BH() * s.ngroups() * ((s.T() + 31) / 32);
     if (cudaMemsetAsync(hot_mask, 0, words * 4, stream) != cudaSuccess) return APA_ERR_CUDA;
   }
   if (launch_quantize(s, q, k, v, ws, true, true, stream) != cudaSuccess) return APA_ERR_CUDA;
+  stage(1);
   if (launch_pass1(s, ws, eps, hot_mask, stream) != cudaSuccess) return APA_ERR_CUDA;
+  stage(2);
   if (launch_pass2(s, q, k, v, &ws, out, lse, stream) != cudaSuccess) return APA_ERR_CUDA;
+  stage(3);
   return APA_OK;
 }
 
@@ -232,6 +272,31 @@ int apa_quantize(const void* q, const void* k, const void* v, int B, int Hq, int
   st = apa::launch_quantize(s, q, k, v, ws, true, true, stream) == cudaSuccess ? APA_OK : APA_ERR_CUDA;
   if (cudaFreeAsync(scratch, stream) != cudaSuccess && st == APA_OK) st = APA_ERR_CUDA;
   return st;
+}
+
+int apa_stage_timing(int enable) {
+  std::lock_guard<std::mutex> lk(apa::g_timing.mu);
+  apa::g_timing.on = enable != 0;
+  apa::g_timing.used = 0;
+  return APA_OK;
+}
+
+int apa_stage_timing_read(float* ms, int* calls) {
+  if (!ms || !calls) return APA_ERR_NULL;
+  std::lock_guard<std::mutex> lk(apa::g_timing.mu);
+  for (int i = 0; i < 3; ++i) ms[i] = 0.f;
+  for (size_t c = 0; c < apa::g_timing.used; ++c) {
+    if (cudaEventSynchronize(apa::g_timing.ev[c * 4 + 3]) != cudaSuccess) return APA_ERR_CUDA;
+    for (int i = 0; i < 3; ++i) {
+      float t = 0.f;
+      if (cudaEventElapsedTime(&t, apa::g_timing.ev[c * 4 + i], apa::g_timing.ev[c * 4 + i + 1]) != cudaSuccess)
+        return APA_ERR_CUDA;
+      ms[i] += t;
+    }
+  }
+  *calls = (int)apa::g_timing.used;
+  apa::g_timing.used = 0;
+  return APA_OK;
 }
 
 int apa_check_error(cudaStream_t stream) {
