@@ -51,6 +51,10 @@ extern "C" {
 #define APA_ERR_NOMEM (-6)     /* the workspace could not be allocated, or the given one is too small */
 #define APA_ERR_DEVICE (-7)    /* a kernel recorded a device-side timeout (apa_check_error) */
 #define APA_ERR_ALIGN (-8)     /* q, k or v not 16-byte aligned */
+#define APA_ERR_SCRATCH (-9)   /* too large for the fixed scratch of apa_quantize_noalloc */
+
+/* Size of the fixed device scratch array behind apa_quantize_noalloc (16 MiB). */
+#define APA_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
 
 /* Adaptive-precision attention, eps >= 0:
  *   q        bf16 [B, Hq, Nq, d], contiguous
@@ -101,6 +105,32 @@ int apa_quantize(const void* q, const void* k, const void* v, int B, int Hq, int
                  uint8_t* kv_blob, uint8_t* q_blob, float* mu, float* s_q, float* s_k, float* s_v,
                  cudaStream_t stream);
 size_t apa_kv_blob_bytes(int B, int Hkv, int Nkv, int d);
+
+/* apa_quantize() for callers that must not allocate device memory during the
+ * call: engines that reserve the whole GPU for their own memory arena up front,
+ * plugin interfaces that receive buffers but have no allocator to call, and
+ * latency-critical paths where a device allocation (which can synchronize) is
+ * not acceptable.  The blog has no counterpart to this entry point.
+ *   Same arguments, outputs and results as apa_quantize(); no cudaMalloc,
+ *   cudaFree or other allocating call is made.  The temporary statistics live in
+ *   one fixed array of APA_NOALLOC_SCRATCH_BYTES in the library's device image,
+ *   which every GPU that loads the library holds until the process exits.
+ *   Problems whose statistics need more than that
+ *   (apa_quantize_noalloc_scratch_bytes() > APA_NOALLOC_SCRATCH_BYTES, roughly
+ *   B*Hkv*ceil(Nkv/64)*d*4 bytes) are rejected with APA_ERR_SCRATCH before any
+ *   work is enqueued.
+ *   The first call on a device looks up the array's device address
+ *   (cudaGetSymbolAddress) with that device current; make that first call before
+ *   any stream capture.
+ *   Every call shares the one array per device, and each call overwrites what
+ *   the last one left there: calls that can overlap on the GPU (different
+ *   streams without ordering between them) race on it and must be serialized by
+ *   the caller. */
+int apa_quantize_noalloc(const void* q, const void* k, const void* v, int B, int Hq, int Hkv, int Nq, int Nkv,
+                         int d, uint8_t* kv_blob, uint8_t* q_blob, float* mu, float* s_q, float* s_k, float* s_v,
+                         cudaStream_t stream);
+/* Scratch bytes apa_quantize_noalloc needs for this problem (0 for invalid sizes). */
+size_t apa_quantize_noalloc_scratch_bytes(int B, int Hq, int Hkv, int Nkv, int d);
 size_t apa_q_blob_bytes(int B, int Hq, int Hkv, int Nq, int d);
 
 /* Measurement aid, off by default.  While enabled, every apa_attention* call

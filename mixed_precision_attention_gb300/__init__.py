@@ -18,7 +18,7 @@ import ctypes
 from . import _lib
 from ._lib import ApaError, status_string
 
-__all__ = ["attention", "attention_host", "quantize", "workspace_bytes", "check_error", "ApaError",
+__all__ = ["attention", "attention_host", "quantize", "quantize_noalloc", "workspace_bytes", "check_error", "ApaError",
            "status_string", "hot_mask_shape", "TILE", "GROUP_ROWS", "BLOCK_ROWS"]
 
 TILE = 64          # keys per tile
@@ -127,6 +127,32 @@ def quantize(q, k, v):
     st = lib.apa_quantize(_ptr(q), _ptr(k), _ptr(v), B, Hq, Hkv, Nq, Nkv, d, _ptr(r["kv_blob"]), _ptr(r["q_blob"]),
                           _ptr(r["mu"]), _ptr(r["s_q"]), _ptr(r["s_k"]), _ptr(r["s_v"]), _stream(dev))
     _lib.check(st, "apa_quantize")
+    return r
+
+
+def quantize_noalloc(q, k, v, out=None):
+    """quantize() through apa_quantize_noalloc, for callers that cannot allocate
+    device memory during the call: the library keeps the temporary statistics in
+    a fixed 16 MiB device array.  Pass `out` (a dict shaped like quantize()'s
+    result) to write into existing buffers; without it the outputs are allocated
+    here, before the call.  Raises ApaError(APA_ERR_SCRATCH) when the problem's
+    statistics do not fit the fixed array."""
+    lib = _lib.load()
+    B, Hq, Hkv, Nq, Nkv, d = _check_qkv(q, k, v)
+    r = out
+    if r is None:
+        import torch
+        dev = q.device
+        r = dict(kv_blob=torch.empty(lib.apa_kv_blob_bytes(B, Hkv, Nkv, d), dtype=torch.uint8, device=dev),
+                 q_blob=torch.empty(lib.apa_q_blob_bytes(B, Hq, Hkv, Nq, d), dtype=torch.uint8, device=dev),
+                 mu=torch.empty((B, Hkv, d), dtype=torch.float32, device=dev),
+                 s_q=torch.empty((B, Hq), dtype=torch.float32, device=dev),
+                 s_k=torch.empty((B, Hkv), dtype=torch.float32, device=dev),
+                 s_v=torch.empty((B, Hkv), dtype=torch.float32, device=dev))
+    st = lib.apa_quantize_noalloc(_ptr(q), _ptr(k), _ptr(v), B, Hq, Hkv, Nq, Nkv, d, _ptr(r["kv_blob"]),
+                                  _ptr(r["q_blob"]), _ptr(r["mu"]), _ptr(r["s_q"]), _ptr(r["s_k"]),
+                                  _ptr(r["s_v"]), _stream(q.device))
+    _lib.check(st, "apa_quantize_noalloc")
     return r
 
 

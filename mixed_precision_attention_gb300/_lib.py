@@ -24,6 +24,8 @@ _SIGS = {
     "apa_attention_host": (I, [P, P, P, I, I, I, I, I, I, I, F, P, P, P, P]),
     "apa_workspace_bytes": (SZ, [I, I, I, I, I, I, F]),
     "apa_quantize": (I, [P, P, P, I, I, I, I, I, I, P, P, P, P, P, P, P]),
+    "apa_quantize_noalloc": (I, [P, P, P, I, I, I, I, I, I, P, P, P, P, P, P, P]),
+    "apa_quantize_noalloc_scratch_bytes": (SZ, [I, I, I, I, I]),
     "apa_kv_blob_bytes": (SZ, [I, I, I, I]),
     "apa_q_blob_bytes": (SZ, [I, I, I, I, I]),
     "apa_check_error": (I, [P]),

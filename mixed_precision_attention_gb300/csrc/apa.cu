@@ -324,6 +324,7 @@ const char* apa_status_string(int status) {
     case APA_ERR_NOMEM: return "workspace allocation failed or workspace too small";
     case APA_ERR_DEVICE: return "a kernel timed out waiting on the device";
     case APA_ERR_ALIGN: return "q, k and v must be 16-byte aligned";
+    case APA_ERR_SCRATCH: return "problem too large for the fixed scratch of apa_quantize_noalloc";
   }
   return "unknown status";
 }

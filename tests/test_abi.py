@@ -80,3 +80,15 @@ def test_quantize_argument_errors(lib):
     z = P(0x60000)
     assert lib.apa_quantize(*OK_PTR, 1, 2, 1, 128, 512, 64, None, z, z, z, z, z, None) == -1
     assert lib.apa_quantize(*OK_PTR, 1, 2, 1, 128, 512, 80, z, z, z, z, z, z, None) == -4
+
+
+def test_noalloc_quantizer_rejects_oversized_problems(lib):
+    # statistics of the 2 x 8 heads x 131072 keys x d=256 problem need ~34 MB, more
+    # than the fixed 16 MiB array: rejected before anything touches the GPU
+    z = P(0x60000)
+    need = lib.apa_quantize_noalloc_scratch_bytes(2, 32, 8, 131072, 256)
+    assert need > 16 * 2 ** 20
+    assert lib.apa_quantize_noalloc(*OK_PTR, 2, 32, 8, 128, 131072, 256, z, z, z, z, z, z, None) == -9
+    assert _lib.status_string(-9) != "unknown status"
+    assert lib.apa_quantize_noalloc_scratch_bytes(1, 24, 8, 122880, 128) <= 16 * 2 ** 20
+    assert lib.apa_quantize_noalloc(*OK_PTR, 1, 2, 1, 128, 512, 64, None, z, z, z, z, z, None) == -1
