@@ -19,14 +19,16 @@ method depends on:
   at all");
 * V ~ N(0, 1).
 
-Everything is computed in float64 and rounded once to float32 and then to
-bfloat16 with round-to-nearest-even, so the bytes are the same on x86 and Arm.
-Draw order per sequence b (numpy ``Generator(PCG64(seed + b))``): u [Hkv, d];
-outlier channels per KV head; nQ per query head; nK per KV head; V per KV head.
+Normals are drawn as float32 (numpy ``Generator(PCG64(seed + b))`` per
+sequence b, in the order u [Hkv, d]; outlier channels per KV head; nQ per query
+head; nK per KV head; V per KV head).  RoPE angles and their cos / sin are
+computed in float64 and rounded to float32; the rest is float32 arithmetic,
+rounded to bfloat16 with round-to-nearest-even.
 """
 from __future__ import annotations
 
 import hashlib
+import os
 from dataclasses import dataclass, field
 
 import numpy as np
@@ -88,11 +90,18 @@ WORKLOADS = {
 }
 
 
-def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
-    """Round float32 values to bfloat16 (nearest, ties to even); returns uint16 bits."""
-    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
-    r = (u + 0x7FFF + ((u >> 16) & 1)) >> 16
-    return r.astype(np.uint16)
+def f32_to_bf16_bits(x: np.ndarray, out: np.ndarray | None = None) -> np.ndarray:
+    """Round finite float32 values to bfloat16 (nearest, ties to even); returns uint16 bits."""
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
+    r = u >> np.uint32(16)
+    r &= np.uint32(1)
+    r += u
+    r += np.uint32(0x7FFF)
+    r >>= np.uint32(16)
+    if out is None:
+        return r.astype(np.uint16)
+    out[...] = r
+    return out
 
 
 def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:
@@ -103,13 +112,19 @@ def _rope_tables(n_pos: int, d: int):
     half = d // 2
     inv_freq = ROPE_THETA ** (-(2.0 * np.arange(half, dtype=np.float64)) / d)
     ang = np.arange(n_pos, dtype=np.float64)[:, None] * inv_freq[None, :]
-    return np.cos(ang), np.sin(ang)
+    return np.cos(ang).astype(np.float32), np.sin(ang).astype(np.float32)
 
 
 def _rope(x: np.ndarray, cos: np.ndarray, sin: np.ndarray) -> np.ndarray:
+    """Half-split rotary embedding, float32."""
     half = x.shape[-1] // 2
+    out = np.empty_like(x)
     x1, x2 = x[..., :half], x[..., half:]
-    return np.concatenate([x1 * cos - x2 * sin, x2 * cos + x1 * sin], axis=-1)
+    np.multiply(x1, cos, out=out[..., :half])
+    out[..., :half] -= x2 * sin
+    np.multiply(x2, cos, out=out[..., half:])
+    out[..., half:] += x1 * sin
+    return out
 
 
 def generate(w: Workload, seed: int | None = None):
@@ -125,26 +140,46 @@ def generate(w: Workload, seed: int | None = None):
     q = np.empty((B, Hq, Nq, d), dtype=np.uint16)
     k = np.empty((B, Hkv, Nkv, d), dtype=np.uint16)
     v = np.empty((B, Hkv, Nkv, d), dtype=np.uint16)
+    from concurrent.futures import ThreadPoolExecutor
+    pool = ThreadPoolExecutor(max_workers=min(8, os.cpu_count() or 1))
+    jobs = []
+
+    def finish_q(dst, x, c, si):
+        f32_to_bf16_bits(_rope(x, c, si), out=dst)
+
+    def finish_k(dst, x, gain):
+        y = _rope(x, cos, sin)
+        y[0] *= np.float32(gain)
+        f32_to_bf16_bits(y, out=dst)
+
     for b in range(B):
         rng = np.random.Generator(np.random.PCG64(base + b))
         gain = w.sink_gains[b % len(w.sink_gains)]
-        u = rng.standard_normal((Hkv, d))
+        f32 = np.float32
+        u = rng.standard_normal((Hkv, d), dtype=f32)
         outl = [np.sort(rng.choice(d, size=w.n_outliers, replace=False))
                 if w.n_outliers else np.zeros(0, dtype=np.int64) for _ in range(Hkv)]
         for h in range(Hq):
             hk = h // G
-            x = u[hk][None, :] + 0.5 * rng.standard_normal((Nq, d))
-            x[:, outl[hk]] *= w.outlier_gain
-            x = _rope(x, cos[off:off + Nq], sin[off:off + Nq])
-            q[b, h] = f32_to_bf16_bits(x.astype(np.float32))
+            x = rng.standard_normal((Nq, d), dtype=f32)
+            x *= f32(0.5)
+            x += u[hk][None, :]
+            x[:, outl[hk]] *= f32(w.outlier_gain)
+            jobs.append(pool.submit(finish_q, q[b, h], x, cos[off:off + Nq], sin[off:off + Nq]))
         for h in range(Hkv):
-            x = u[h][None, :] + 0.5 * rng.standard_normal((Nkv, d))
-            x[:, outl[h]] *= w.outlier_gain
-            x = _rope(x, cos, sin)
-            x[0] *= gain
-            k[b, h] = f32_to_bf16_bits(x.astype(np.float32))
+            x = rng.standard_normal((Nkv, d), dtype=f32)
+            x *= f32(0.5)
+            x += u[h][None, :]
+            x[:, outl[h]] *= f32(w.outlier_gain)
+            jobs.append(pool.submit(finish_k, k[b, h], x, gain))
         for h in range(Hkv):
-            v[b, h] = f32_to_bf16_bits(rng.standard_normal((Nkv, d)).astype(np.float32))
+            jobs.append(pool.submit(f32_to_bf16_bits, rng.standard_normal((Nkv, d), dtype=f32), v[b, h]))
+        # bound the memory held by pending float32 copies
+        while sum(not j.done() for j in jobs) > 16:
+            jobs[[j.done() for j in jobs].index(False)].result()
+    for j in jobs:
+        j.result()
+    pool.shutdown()
     return q, k, v
 
 

@@ -209,7 +209,7 @@ def test_apa_accuracy_against_exact():
     allfp4 = oracle.apa(q, k, v, eps=np.inf)
     assert not allfp4["hot_mask"].any()
     cos4 = (ex * allfp4["out"]).sum() / np.linalg.norm(ex) / np.linalg.norm(allfp4["out"])
-    assert 0.95 < cos4 < cos
+    assert 0.8 < cos4 < cos
 
 
 def _sink_row_case():
