@@ -459,11 +459,13 @@ static void apa_group(const uint16_t* q, const uint16_t* k, const uint16_t* v, i
       }
       lt[r] = sum;
     }
-    /* the hot test: one verdict for the group */
+    /* the hot test: one verdict for the group.  eps = 0 is the all-exact run:
+     * every tile the group can see is hot, even one whose FP4 mass rounds to 0. */
     int hot = 0;
     if (!isinf(P->eps)) {
       for (int r = 0; r < nr; ++r) {
         if (empty[r]) continue;
+        if (P->eps == 0.0) { hot = 1; continue; }
         if (m[r] == -INFINITY) { if (lt[r] > 0.0) hot = 1; continue; }
         if (lt[r] * exp2(mt[r] - m[r]) > P->eps * lam[r]) hot = 1;
       }

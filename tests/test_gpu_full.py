@@ -1,0 +1,132 @@
+"""Full-size parity: the five workloads at their real sizes, checked on sampled
+rows the oracle can afford, plus properties that hold at any size.
+
+Each (batch, KV head) is an independent problem for the method (per-head
+scales, per-head key mean, its own rows and keys), so the oracle runs on the
+slice q[b, heads of h], k[b, h], v[b, h] and its 16-row groups are compared with
+the same groups of the GPU output.  Acceptance as in test_gpu_attention.py.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from mixed_precision_attention_gb300 import synth
+from tests import _gpu
+
+pytestmark = pytest.mark.gpu
+
+_CACHE = {}
+
+
+def _inputs(name):
+    if name not in _CACHE:
+        _CACHE.clear()  # hold one workload at a time
+        _CACHE[name] = synth.generate(synth.WORKLOADS[name])
+    return _CACHE[name]
+
+
+def _sample(w, n_heads=2, per_head=6, seed=0):
+    """(b, hkv, [groups]) samples: the first and last group of each head plus random ones."""
+    rng = np.random.default_rng(seed)
+    ng = oracle.n_groups(w.Hq, w.Hkv, w.Nq)
+    heads = [(0, 0), (w.B - 1, w.Hkv - 1)][:n_heads]
+    out = []
+    for b, h in heads:
+        g = {0, ng - 1} | set(int(x) for x in rng.choice(ng, size=min(ng, per_head - 2), replace=False))
+        out.append((b, h, sorted(g)))
+    return out
+
+
+def _run_gpu(w, q, k, v, eps):
+    import mixed_precision_attention_gb300 as apa
+    tq, tk, tv = (_gpu.to_dev(a) for a in (q, k, v))
+    out, lse, mask = apa.attention(tq, tk, tv, causal=w.causal, eps=eps, return_hot_mask=True)
+    apa.check_error()
+    import torch
+    assert bool(torch.isfinite(out).all()) and bool(torch.isfinite(lse).all())
+    return out, lse, mask.cpu().numpy().view(np.uint32)
+
+
+def _rows(w, grp):
+    G = w.G
+    return [(p % G, p // G) for p in range(grp * 16, min(w.G * w.Nq, (grp + 1) * 16))]
+
+
+def _check(name, eps):
+    w = synth.WORKLOADS[name]
+    q, k, v = _inputs(name)
+    out, lse, mask = _run_gpu(w, q, k, v, eps)
+    T = (w.Nkv + 63) // 64
+    G = w.G
+    ng = oracle.n_groups(w.Hq, w.Hkv, w.Nq)
+    vis_all = _gpu.group_visible(w.Hq, w.Hkv, w.Nq, w.Nkv, w.causal, ng, T)
+    bits = _gpu.hot_bits(mask, T)
+    assert not (bits & ~vis_all[None, None]).any()
+    if eps == 0:
+        assert np.array_equal(bits, np.broadcast_to(vis_all, bits.shape))
+    if np.isinf(eps):
+        assert not bits.any()
+    got_rows, ref_rows, ex_rows = [], [], []
+    n_agree = n_vis = 0
+    worst = 0.0
+    for b, h, groups in _sample(w):
+        qs = np.ascontiguousarray(q[b:b + 1, h * G:(h + 1) * G])
+        ks, vs = np.ascontiguousarray(k[b:b + 1, h:h + 1]), np.ascontiguousarray(v[b:b + 1, h:h + 1])
+        units = np.array([(0, 0, g) for g in groups], np.int32)
+        ref = oracle.apa(qs, ks, vs, causal=w.causal, eps=eps, units=units, diag=True)
+        rows = [(0, g_off, pos) for g in groups for (g_off, pos) in _rows(w, g)]
+        ex, _ = oracle.exact(qs, ks, vs, causal=w.causal, rows=np.array(rows, np.int32))
+        gpu_out = out[b, h * G:(h + 1) * G].cpu().numpy().astype(np.float64)
+        for (_, g_off, pos) in rows:
+            got_rows.append(gpu_out[g_off, pos])
+            ref_rows.append(ref["out"][0, g_off, pos])
+            ex_rows.append(ex[0, g_off, pos])
+        o_bits = _gpu.hot_bits(ref["hot_mask"][0, 0], T)
+        for i, g in enumerate(groups):
+            vis = vis_all[g]
+            n_vis += vis.sum()
+            n_agree += (bits[b, h, g] == o_bits[g])[vis].sum()
+            if eps > 0 and not np.isinf(eps):
+                ell, lam = ref["ell"][i], ref["lam"][i]
+                cold = vis & ~bits[b, h, g]
+                ok_rows = ~np.isnan(lam)
+                r = np.where(np.isnan(ell), 0.0, ell)[ok_rows] / lam[ok_rows, None]
+                if cold.any():
+                    worst = max(worst, float(r[:, cold].max()))
+    got, refo, exo = np.array(got_rows), np.array(ref_rows), np.array(ex_rows)
+    if eps == 0:
+        assert np.abs(got - exo).max() <= 4e-3
+        assert _gpu.cosine(got, exo) >= 0.99999
+    else:
+        assert np.abs(got - refo).max() <= 1e-2, np.abs(got - refo).max()
+        assert _gpu.cosine(got, refo) >= 0.9999
+        if not np.isinf(eps):
+            assert _gpu.cosine(got, exo) >= 0.999
+    assert n_agree / n_vis >= 0.999, n_agree / n_vis
+    assert worst <= eps * 1.02 or np.isinf(eps)
+    return bits[np.broadcast_to(vis_all, bits.shape)].mean()
+
+
+@pytest.mark.parametrize("name", ["llama3b_2048x122880", "batched_32k", "shortq_131k_d256"])
+@pytest.mark.parametrize("eps", ["workload", 0.0])
+def test_full_size_workloads(name, eps):
+    w = synth.WORKLOADS[name]
+    _check(name, w.eps if eps == "workload" else eps)
+
+
+@pytest.mark.parametrize("eps", [0.0, 0.001, 0.005, 0.02, float("inf")])
+def test_prefill_8k_eps_sweep(eps):
+    hot = _check("prefill_8k", eps)
+    if eps == 0:
+        assert hot == 1.0
+
+
+def test_tiny_workload_full():
+    # the tiny workload is small enough to compare every row
+    w = synth.WORKLOADS["tiny"]
+    q, k, v = synth.generate(w)
+    out, lse, mask = _run_gpu(w, q, k, v, w.eps)
+    ref = oracle.apa(q, k, v, eps=w.eps)
+    got = out.cpu().numpy().astype(np.float64)
+    assert np.abs(got - ref["out"]).max() <= 1e-2
+    assert _gpu.cosine(got, ref["out"]) >= 0.9999

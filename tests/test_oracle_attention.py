@@ -282,3 +282,18 @@ def test_apa_group_subset_matches_full():
         for (bb, hq, pos) in oracle.group_rows(4, 2, 40, b, h, g):
             assert np.array_equal(part["out"][bb, hq, pos], full["out"][bb, hq, pos])
         assert np.array_equal(part["hot_mask"][b, h, g], full["hot_mask"][b, h, g])
+
+
+def test_eps0_marks_every_visible_tile_hot_even_when_fp4_mass_underflows():
+    """eps = 0 is the all-exact run: a tile whose FP4 row sums round to zero (its
+    scores sit far below the frame) is still hot and is computed exactly."""
+    q, k, v = _sink_row_case()
+    kf = synth.bf16_bits_to_f32(k).copy()
+    kf[0, 0, 5 * 64:6 * 64, 0] = -60.0  # tile 5: ~70 log2 units below the sink
+    k2 = synth.f32_to_bf16_bits(kf)
+    probe = oracle.apa(q, k2, v, eps=1e-12, diag=True)
+    assert np.all(probe["ell"][0, :, 5] == 0.0)  # the FP4 mass of tile 5 underflows
+    r = oracle.apa(q, k2, v, eps=0.0)
+    assert _hot_bits(r["hot_mask"][0, 0], 48)[0].all()
+    ex, _ = oracle.exact(q, k2, v)
+    assert np.max(np.abs(r["out"] - ex)) < 1e-12
