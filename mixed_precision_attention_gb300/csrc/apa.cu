@@ -78,6 +78,7 @@ size_t workspace_layout(const Shape& s, bool apa_mode, Workspace* ws, void* base
   w.kmax = (uint32_t*)take(BH * d * 4);
   w.vamax = (uint32_t*)take(BH * 4);
   w.qamax = (uint32_t*)take(BHq * 4);
+  w.kcamax = (uint32_t*)take(BH * 4);
   w.mu = (float*)take(BH * d * 4);
   w.s_k = (float*)take(BH * 4);
   w.s_v = (float*)take(BH * 4);
@@ -254,7 +255,7 @@ int apa_quantize(const void* q, const void* k, const void* v, int B, int Hq, int
     return o;
   };
   const size_t o_sum = slot(BH * T * d * 4), o_min = slot(BH * d * 4), o_max = slot(BH * d * 4), o_va = slot(BH * 4),
-               o_qa = slot(BHq * 4);
+               o_qa = slot(BHq * 4), o_kc = slot(BH * 4);
   uint8_t* scratch = nullptr;
   if (cudaMallocAsync((void**)&scratch, off, stream) != cudaSuccess) return APA_ERR_NOMEM;
   apa::Workspace ws{};
@@ -263,6 +264,7 @@ int apa_quantize(const void* q, const void* k, const void* v, int B, int Hq, int
   ws.kmax = (uint32_t*)(scratch + o_max);
   ws.vamax = (uint32_t*)(scratch + o_va);
   ws.qamax = (uint32_t*)(scratch + o_qa);
+  ws.kcamax = (uint32_t*)(scratch + o_kc);
   ws.mu = mu;
   ws.s_k = s_k;
   ws.s_v = s_v;

@@ -72,6 +72,7 @@ struct Workspace {
   uint32_t* kmax;     // [BH][d]
   uint32_t* vamax;    // [BH] max |v| (float bits)
   uint32_t* qamax;    // [B*Hq] max |q| (float bits)
+  uint32_t* kcamax;   // [BH] max |k - mu| (float bits)
   float* mu;          // [BH][d]
   float* s_k;         // [BH]
   float* s_v;         // [BH]

@@ -7,7 +7,7 @@
 // allocator, and latency-critical loops where a cudaMalloc (which may
 // synchronize the device) is not acceptable.  For them this entry point keeps
 // the quantizer's temporary statistics (per-tile key sums, per-channel key
-// min/max, per-head max |v| and max |q|) in one fixed array that lives in the
+// min/max, per-head max |v|, |q| and |k - mu|) in one fixed array that lives in the
 // library's device image instead of a stream-ordered allocation.  The caller
 // still passes every input and output buffer.
 #include <mutex>
@@ -51,7 +51,7 @@ extern "C" size_t apa_quantize_noalloc_scratch_bytes(int B, int Hq, int Hkv, int
   if (B < 1 || Hq < 1 || Hkv < 1 || Nkv < 1 || d < 1) return 0;
   const size_t BH = (size_t)B * Hkv, T = (Nkv + apa::kTile - 1) / apa::kTile, BHq = (size_t)B * Hq;
   return apa::align256(BH * T * d * 4) + 2 * apa::align256(BH * d * 4) + apa::align256(BH * 4) +
-         apa::align256(BHq * 4);
+         apa::align256(BHq * 4) + apa::align256(BH * 4);
 }
 
 extern "C" int apa_quantize_noalloc(const void* q, const void* k, const void* v, int B, int Hq, int Hkv, int Nq,
@@ -80,6 +80,7 @@ extern "C" int apa_quantize_noalloc(const void* q, const void* k, const void* v,
   ws.kmax = (uint32_t*)take(BH * d * 4);
   ws.vamax = (uint32_t*)take(BH * 4);
   ws.qamax = (uint32_t*)take(BHq * 4);
+  ws.kcamax = (uint32_t*)take(BH * 4);
   ws.mu = mu;
   ws.s_k = s_k;
   ws.s_v = s_v;

@@ -26,8 +26,15 @@
 //   warp 5     TMEM owner and MMA issuer (tcgen05.mma kind::mxf4nvf4,
 //              scale_vec::4X): S (M128 N64), ones (M128 N16), PV (M128 N=d), the
 //              scale copies (tcgen05.cp), and the block's hot-tile list.
-// At d <= 128 a CTA uses 256 TMEM columns and ~55 KB of shared memory, so two
-// CTAs share an SM and hide each other's softmax-to-MMA round trips.
+// Software pipelining: the P encoding of tile t+1 depends on the verdict of
+// tile t only through the frame, and only when tile t lifts it (c > m + tau);
+// otherwise m and the lambda update are the same whether t is hot or cold.  So
+// while the ones-MMA of tile t is in flight the softmax warps already encode
+// tile t+1, and judge tile t afterwards; a warp whose rows lifted the frame at
+// tile t judges it first.  The issuer runs S(t+2), PV(t), ones(t+1) in that order.
+// At d <= 128 a CTA holds 256 TMEM columns and ~55 KB of shared memory, so two
+// CTAs share an SM.  (Two threads per row, swapping group maxima, was measured
+// slower: the per-warp waits and exchanges outweighed the halved encode.)
 #include "apa_internal.h"
 #include "tc.cuh"
 
@@ -51,7 +58,9 @@ struct P1Params {
   int* err;
 };
 
-constexpr int kThreads = 192;
+constexpr int kSoftWarps = 4;
+constexpr int kThreads = (kSoftWarps + 2) * 32;
+constexpr int kProducerWarp = kSoftWarps, kMmaWarp = kSoftWarps + 1;
 
 template <int D>
 struct P1Cfg {
@@ -65,10 +74,11 @@ struct P1Cfg {
   static constexpr int kOnesSfOff = kOnesOff + 512;     // 512-B scale atom of UE4M3 1.0
   static constexpr int kSmem = kOnesSfOff + 512 + 128;
   static constexpr uint32_t kTmemCols = D <= 128 ? 256 : 512;
+  static constexpr uint32_t kSfc = 4 * sf_chunks(D);  // TMEM columns of one K or V scale set
   static constexpr uint32_t kO = 0, kS = D, kL = D + 64, kSFQ = D + 80;
-  static constexpr uint32_t kSFK = kSFQ + 4 * (D / 64);      // 2 buffers of 4 * sf_chunks(D)
-  static constexpr uint32_t kSFV = kSFK + 8 * sf_chunks(D);  // 2 buffers of 4 * sf_chunks(D)
-  static constexpr uint32_t kSFP = kSFV + 8 * sf_chunks(D);  // 2 buffers of 4
+  static constexpr uint32_t kSFK = kSFQ + 4 * (D / 64);  // 3 buffers (tile % 3)
+  static constexpr uint32_t kSFV = kSFK + 3 * kSfc;      // 3 buffers (tile % 3)
+  static constexpr uint32_t kSFP = kSFV + 3 * kSfc;      // 2 buffers (tile % 2)
   static constexpr uint32_t kSFO = kSFP + 8;
   static_assert(kSFO + 4 <= kTmemCols, "TMEM budget");
 };
@@ -93,6 +103,25 @@ __device__ __forceinline__ float lg2_approx(float x) {
   asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
+// Eight FP32 values -> one word of eight E2M1 codes, x[0] in the lowest nibble.
+__device__ __forceinline__ uint32_t pack8_e2m1(const float* x) {
+  uint32_t w;
+  asm("{\n.reg .b8 b0, b1, b2, b3;\n"
+      "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n"
+      "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n"
+      "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n"
+      "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n"
+      "mov.b32 %0, {b0, b1, b2, b3};\n}"
+      : "=r"(w)
+      : "f"(x[0]), "f"(x[1]), "f"(x[2]), "f"(x[3]), "f"(x[4]), "f"(x[5]), "f"(x[6]), "f"(x[7]));
+  return w;
+}
+// What a row keeps between encoding a tile and judging it.
+struct Pending {
+  float c, mt;
+  uint32_t sfw;
+  bool empty, lift;
+};
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, (D <= 128 ? 2 : 1)) pass1_kernel(const P1Params p) {
@@ -100,7 +129,7 @@ __global__ void __launch_bounds__(kThreads, (D <= 128 ? 2 : 1)) pass1_kernel(con
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
   // barriers: q_full, blob_full[4], blob_empty[4], s_full, s_free, p_full[2], l_full, dec[2], pv_done[2], drain
-  __shared__ __align__(8) uint64_t bars[18];
+  __shared__ __align__(8) uint64_t bars[19];
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
   __shared__ uint32_t gbits[2][4];
@@ -121,9 +150,7 @@ __global__ void __launch_bounds__(kThreads, (D <= 128 ? 2 : 1)) pass1_kernel(con
   const uint32_t l_full = bar0 + 8u * 13;
   auto dec = [&](int b2) { return bar0 + 8u * (14 + b2); };
   auto pv_done = [&](int b2) { return bar0 + 8u * (16 + b2); };
-  // drain shares the last slot with nothing else
-  __shared__ __align__(8) uint64_t drain_bar;
-  const uint32_t drain = smem_u32(&drain_bar);
+  const uint32_t drain = bar0 + 8u * 18;
   auto warp_wait = [&](uint32_t bar, uint32_t parity) -> bool {
     const bool okl = mbar_wait(bar, parity, &abort_flag, p.err);
     return __all_sync(0xffffffffu, okl);
@@ -138,18 +165,17 @@ __global__ void __launch_bounds__(kThreads, (D <= 128 ? 2 : 1)) pass1_kernel(con
 
   if (threadIdx.x == 0) {
     abort_flag = 0;
-    for (int i = 0; i < 18; ++i) {
+    for (int i = 0; i < 19; ++i) {
       const bool per_warp = (i == 10) || (i >= 11 && i <= 12) || (i >= 14 && i <= 15);  // s_free, p_full, dec
-      mbar_init(bar0 + 8u * i, per_warp ? 4u : 1u);
+      mbar_init(bar0 + 8u * i, per_warp ? (uint32_t)kSoftWarps : 1u);
     }
-    mbar_init(drain, 1);
     fence_mbar_init();
   }
-  if (warp == 5) {
+  if (warp == kMmaWarp) {
     tmem_alloc(smem_u32(&tmem_slot), C::kTmemCols);
     tmem_relinquish();
   }
-  if (warp < 4) {
+  if (threadIdx.x < 128) {
     // the ones tile (E2M1 1.0 = code 2) and its scale atom (UE4M3 1.0 = 0x38)
     reinterpret_cast<uint2*>(smem + C::kOnesOff)[threadIdx.x] =
         threadIdx.x < 64 ? make_uint2(0x22222222u, 0x22222222u) : make_uint2(0x38383838u, 0x38383838u);
@@ -160,7 +186,7 @@ __global__ void __launch_bounds__(kThreads, (D <= 128 ? 2 : 1)) pass1_kernel(con
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
 
-  if (warp == 4) {
+  if (warp == kProducerWarp) {
     // ------------------------------------------------------------ bulk-copy producer
     if (lane == 0) {
       const uint8_t* qsrc = p.q_blob + ((size_t)bh * nblk + blk) * C::kQBlob;
@@ -180,7 +206,7 @@ __global__ void __launch_bounds__(kThreads, (D <= 128 ? 2 : 1)) pass1_kernel(con
         for (int i = max(0, issued - C::NS); i < issued; ++i) wait_bounded(blob_full(i % C::NS), (i / C::NS) & 1, p.err);
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       const uint32_t idS = idesc_nvf4(128, 64), idL = idesc_nvf4(128, 16), idO = idesc_nvf4(128, D);
@@ -194,14 +220,15 @@ __global__ void __launch_bounds__(kThreads, (D <= 128 ? 2 : 1)) pass1_kernel(con
           tmem_cp_32x128b_x4(tmem + C::kSFQ + 4 * a, smem_desc(sbase + C::kQOff + qblob_sf(D) + 512 * a, 128, 128, 0));
         tmem_cp_32x128b_x4(tmem + C::kSFO, smem_desc(sbase + C::kOnesSfOff, 128, 128, 0));
       }
+      // S(i) into the single S buffer once tile i-1 has been read out of it
       auto issue_s = [&](int i) -> bool {
         const int st = i % C::NS;
         if (!mbar_wait(blob_full(st), (i / C::NS) & 1, &abort_flag, p.err)) return false;
         if (i >= 1 && !mbar_wait(s_free, (i - 1) & 1, &abort_flag, p.err)) return false;
         tc_fence_after();
         const uint32_t blob = sbase + C::kStageOff + st * C::kBlob;
-        const uint32_t sfk = tmem + C::kSFK + 4 * sf_chunks(D) * (i & 1);
-        const uint32_t sfv = tmem + C::kSFV + 4 * sf_chunks(D) * (i & 1);
+        const uint32_t sfk = tmem + C::kSFK + C::kSfc * (i % 3);
+        const uint32_t sfv = tmem + C::kSFV + C::kSfc * (i % 3);
 #pragma unroll
         for (int c = 0; c < sf_chunks(D); ++c) {
           tmem_cp_32x128b_x4(sfk + 4 * c, smem_desc(blob + blob_ksf(D) + 512 * c, 128, 128, 0));
@@ -216,29 +243,35 @@ __global__ void __launch_bounds__(kThreads, (D <= 128 ? 2 : 1)) pass1_kernel(con
         mma_commit(s_full);
         return true;
       };
+      // ones(i): the FP4 row sums of P(i)
+      auto issue_ones = [&](int i) -> bool {
+        if (!mbar_wait(p_full(i & 1), (i >> 1) & 1, &abort_flag, p.err)) return false;
+        tc_fence_after();
+        mma_nvf4(tmem + C::kL, smem_desc(sbase + C::kPOff + 4096 * (i & 1), 128, 256, 0),
+                 smem_desc(sbase + C::kOnesOff, 128, 256, 0), idL, tmem + C::kSFP + 4 * (i & 1), tmem + C::kSFO, 0);
+        mma_commit(l_full);
+        return true;
+      };
       if (ok) ok = issue_s(0);
+      if (ok && n > 1) ok = issue_s(1);
+      if (ok) ok = issue_ones(0);
       uint32_t pv_issued = 0;
       for (int i = 0; ok && i < n; ++i) {
-        if (i + 1 < n && !(ok = issue_s(i + 1))) break;
-        if (!(ok = mbar_wait(p_full(i & 1), (i >> 1) & 1, &abort_flag, p.err))) break;
-        tc_fence_after();
-        const uint32_t pdesc_addr = sbase + C::kPOff + 4096 * (i & 1);
-        const uint32_t sfp = tmem + C::kSFP + 4 * (i & 1);
-        mma_nvf4(tmem + C::kL, smem_desc(pdesc_addr, 128, 256, 0), smem_desc(sbase + C::kOnesOff, 128, 256, 0), idL,
-                 sfp, tmem + C::kSFO, 0);
-        mma_commit(l_full);
+        if (i + 2 < n && !(ok = issue_s(i + 2))) break;
         if (!(ok = mbar_wait(dec(i & 1), (i >> 1) & 1, &abort_flag, p.err))) break;
         tc_fence_after();
         const uint32_t hot = gbits[i & 1][0] | gbits[i & 1][1] | gbits[i & 1][2] | gbits[i & 1][3];
         if (hot) list[count++] = (uint32_t)tile_of(i) | (hot << 16);
         if ((hot | invalid_groups) != 0xFFu) {
           const uint32_t blob = sbase + C::kStageOff + (i % C::NS) * C::kBlob;
-          mma_nvf4(tmem + C::kO, smem_desc(pdesc_addr, 128, 256, 0), smem_desc(blob + blob_vcodes(D), 128, 256, 0),
-                   idO, sfp, tmem + C::kSFV + 4 * sf_chunks(D) * (i & 1), pv_issued > 0);
+          mma_nvf4(tmem + C::kO, smem_desc(sbase + C::kPOff + 4096 * (i & 1), 128, 256, 0),
+                   smem_desc(blob + blob_vcodes(D), 128, 256, 0), idO, tmem + C::kSFP + 4 * (i & 1),
+                   tmem + C::kSFV + C::kSfc * (i % 3), pv_issued > 0);
           ++pv_issued;
         }
         mma_commit(pv_done(i & 1));
         mma_commit(blob_empty(i % C::NS));
+        if (i + 1 < n && !(ok = issue_ones(i + 1))) break;
       }
       p.hot_count[(size_t)bh * nblk + blk] = count;
       mma_commit(drain);
@@ -255,25 +288,28 @@ __global__ void __launch_bounds__(kThreads, (D <= 128 ? 2 : 1)) pass1_kernel(con
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
     const float eps = p.eps;
     const bool eps_inf = isinf(eps);
+    const int ngroups = s.ngroups(), nwords = (T + 31) / 32;
     float m = -INFINITY, lam = 0.f, l = 0.f;
     bool ok = true;
-    const int ngroups = s.ngroups(), nwords = (T + 31) / 32;
-    for (int i = 0; i < n; ++i) {
+
+    // Encodes P of tile i in the frame that follows from the current m and
+    // hands it to the MMA issuer (codes in smem, scales in TMEM).
+    auto encode = [&](int i, Pending& pd) -> bool {
       const int t = tile_of(i), j0 = t * kTile;
       const int nvis = valid ? min(kTile, vis_last + 1 - j0) : 0;
-      if (!(ok = warp_wait(s_full, i & 1))) break;
+      if (!warp_wait(s_full, i & 1)) return false;
       tc_fence_after();
-      uint32_t sraw[64];
-      tmem_ld_x32(tmem + lane_base + C::kS, sraw);
-      tmem_ld_x32(tmem + lane_base + C::kS + 32, sraw + 32);
+      uint32_t sr[64];
+      tmem_ld_x32(tmem + lane_base + C::kS, sr);
+      tmem_ld_x32(tmem + lane_base + C::kS + 32, sr + 32);
       tmem_wait_ld();
-      float raw[64];
-#pragma unroll
-      for (int j = 0; j < 64; ++j) raw[j] = __uint_as_float(sraw[j]);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(s_free);
-      if (nvis < kTile) {
+      float raw[64];
+#pragma unroll
+      for (int j = 0; j < 64; ++j) raw[j] = __uint_as_float(sr[j]);
+      if (__any_sync(0xffffffffu, nvis < kTile)) {
 #pragma unroll
         for (int j = 0; j < 64; ++j)
           if (j >= nvis) raw[j] = -INFINITY;
@@ -281,78 +317,78 @@ __global__ void __launch_bounds__(kThreads, (D <= 128 ? 2 : 1)) pass1_kernel(con
       float g[4];
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
-        float a = raw[16 * k];
+        float a = max3(raw[16 * k], raw[16 * k + 1], raw[16 * k + 2]);
 #pragma unroll
-        for (int j = 1; j < 15; j += 2) a = max3(a, raw[16 * k + j], raw[16 * k + j + 1]);
+        for (int j = 3; j < 15; j += 2) a = max3(a, raw[16 * k + j], raw[16 * k + j + 1]);
         g[k] = fmaxf(a, raw[16 * k + 15]);
       }
-      const float c = fmaxf(fmaxf(g[0], g[1]), fmaxf(g[2], g[3])) * cs;  // tile max, log2 units
-      const bool empty = (c == -INFINITY);
-      const float mt = (c > m + kTau) ? c : m;  // candidate frame (lazy maximum)
+      pd.c = fmaxf(fmaxf(g[0], g[1]), fmaxf(g[2], g[3])) * cs;  // tile max, log2 units
+      pd.empty = (pd.c == -INFINITY);
+      pd.mt = (pd.c > m + kTau) ? pd.c : m;  // candidate frame (lazy maximum)
+      pd.lift = !pd.empty && pd.mt != m;
       uint32_t pw[8];
-      uint32_t sfw = 0x08080808u;  // 2^-6 where nothing is visible
-      if (!empty) {
-        sfw = 0;
+      pd.sfw = 0x08080808u;  // 2^-6 where nothing is visible
+      if (!pd.empty) {
+        pd.sfw = 0;
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-          uint32_t sc = cvt_ue4m3(ex2_approx(fmaf(g[k], cs, -mt)) * (1.f / 6.f));
+          uint32_t sc = cvt_ue4m3(ex2_approx(fmaf(g[k], cs, -pd.mt)) * (1.f / 6.f));
           sc = max(sc, 8u);  // clamp the group scale at 2^-6
-          sfw |= sc << (8 * k);
-          const float bias = mt + lg2_approx(ue4m3_value(sc));
+          pd.sfw |= sc << (8 * k);
+          const float nb = -(pd.mt + lg2_approx(ue4m3_value(sc)));
 #pragma unroll
           for (int w = 0; w < 2; ++w) {
-            uint32_t word = 0;
+            float y[8];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int j = 16 * k + 8 * w + 2 * e;
-              const float a0 = ex2_approx(fmaf(raw[j], cs, -bias));
-              const float a1 = ex2_approx(fmaf(raw[j + 1], cs, -bias));
-              word |= cvt_e2m1x2(a0, a1) << (8 * e);
-            }
-            pw[2 * k + w] = word;
+            for (int e = 0; e < 8; ++e) y[e] = ex2_approx(fmaf(raw[16 * k + 8 * w + e], cs, nb));
+            pw[2 * k + w] = pack8_e2m1(y);
           }
         }
       } else {
 #pragma unroll
         for (int w = 0; w < 8; ++w) pw[w] = 0u;
       }
-      // P buffer (and its scales) of this parity are free once PV(i-2) has completed
-      if (i >= 2 && !(ok = warp_wait(pv_done(i & 1), ((i >> 1) - 1) & 1))) break;
+      // this P buffer (and its scales) is free once PV(i-2) has completed
+      if (i >= 2 && !warp_wait(pv_done(i & 1), ((i >> 1) - 1) & 1)) return false;
       uint8_t* pb = smem + C::kPOff + 4096 * (i & 1) + (r >> 3) * 256 + (r & 7) * 16;
       *reinterpret_cast<uint4*>(pb) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
       *reinterpret_cast<uint4*>(pb + 128) = make_uint4(pw[4], pw[5], pw[6], pw[7]);
-      const uint32_t sfp = tmem + lane_base + C::kSFP + 4 * (i & 1);
-      tmem_st_x4(sfp, sfw, sfw, sfw, sfw);
+      tmem_st_x4(tmem + lane_base + C::kSFP + 4 * (i & 1), pd.sfw, pd.sfw, pd.sfw, pd.sfw);
       tmem_wait_st();
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(p_full(i & 1));
-      // row sum of the quantized P (ones-MMA)
-      if (!(ok = warp_wait(l_full, i & 1))) break;
+      return true;
+    };
+
+    // Judges tile i from its FP4 row sums and commits frame, lambda and l.
+    auto judge = [&](int i, const Pending& pd) -> bool {
+      const int t = tile_of(i);
+      if (!warp_wait(l_full, i & 1)) return false;
       tc_fence_after();
       uint32_t lb;
       tmem_ld_x1(tmem + lane_base + C::kL, lb);
       tmem_wait_ld();
       const float ell = __uint_as_float(lb);
-      // hot test: the group is hot if any of its rows exceeds eps * lambda
       bool vote = false;
-      if (valid && !empty && !eps_inf) vote = (m == -INFINITY) ? (ell > 0.f) : (ell * ex2_approx(mt - m) > eps * lam);
+      if (valid && !pd.empty && !eps_inf)
+        vote = (eps == 0.f) || ((m == -INFINITY) ? (ell > 0.f) : (ell * ex2_approx(pd.mt - m) > eps * lam));
       const uint32_t bal = __ballot_sync(0xffffffffu, vote);
       const bool hot_lo = (bal & 0x0000FFFFu) != 0, hot_hi = (bal & 0xFFFF0000u) != 0;
       const bool hot = lane < 16 ? hot_lo : hot_hi;
       bool rescale = false;
       float f = 1.f;
-      if (!empty) {
+      if (!pd.empty) {
         const float l_before = l;
         float mn;
         if (hot) {
-          mn = fmaxf(m, c - kColdOffset);
+          mn = fmaxf(m, pd.c - kColdOffset);
           f = (m == -INFINITY) ? 0.f : ex2_approx(m - mn);
-          lam = lam * f + ell * ex2_approx(mt - mn);
+          lam = lam * f + ell * ex2_approx(pd.mt - mn);
           l *= f;
         } else {
-          mn = mt;
+          mn = pd.mt;
           f = (m == -INFINITY) ? 0.f : ex2_approx(m - mn);
           lam = lam * f + ell;
           l = l * f + ell;
@@ -360,9 +396,13 @@ __global__ void __launch_bounds__(kThreads, (D <= 128 ? 2 : 1)) pass1_kernel(con
         rescale = (f != 1.f) && (l_before > 0.f);
         m = mn;
       }
-      if (__any_sync(0xffffffffu, hot)) tmem_st_x4(sfp, hot ? 0u : sfw, hot ? 0u : sfw, hot ? 0u : sfw, hot ? 0u : sfw);
+      if (__any_sync(0xffffffffu, hot)) {
+        const uint32_t z = hot ? 0u : pd.sfw;  // a hot group's P drops out of PV
+        tmem_st_x4(tmem + lane_base + C::kSFP + 4 * (i & 1), z, z, z, z);
+      }
       if (__any_sync(0xffffffffu, rescale)) {
-        if (!(ok = warp_wait(pv_done((i - 1) & 1), ((i - 1) >> 1) & 1))) break;
+        // O must not be touched before PV(i-1) has landed
+        if (!warp_wait(pv_done((i - 1) & 1), ((i - 1) >> 1) & 1)) return false;
         tc_fence_after();
         const float fr = rescale ? f : 1.f;
 #pragma unroll 1
@@ -385,8 +425,28 @@ __global__ void __launch_bounds__(kThreads, (D <= 128 ? 2 : 1)) pass1_kernel(con
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(dec(i & 1));
+      return true;
+    };
+
+    Pending cur, nxt;
+    ok = encode(0, cur);
+    for (int i = 0; ok && i < n; ++i) {
+      if (i + 1 < n) {
+        // tile i+1 can be encoded before tile i is judged unless a row of this
+        // warp lifted its frame at tile i (then m after tile i depends on the verdict)
+        if (!__any_sync(0xffffffffu, cur.lift)) {
+          if (!(ok = encode(i + 1, nxt))) break;
+          if (!(ok = judge(i, cur))) break;
+        } else {
+          if (!(ok = judge(i, cur))) break;
+          if (!(ok = encode(i + 1, nxt))) break;
+        }
+        cur = nxt;
+      } else {
+        ok = judge(i, cur);
+      }
     }
-    // ---- epilogue: write the pass-1 state (o scaled by s_v, frame m, cold sum l)
+    // ---- epilogue: the pass-1 state (o scaled by s_v, frame m, cold sum l)
     if (ok && n > 0) ok = warp_wait(pv_done((n - 1) & 1), ((n - 1) >> 1) & 1);
     tc_fence_after();
     if (ok) {
@@ -410,7 +470,7 @@ __global__ void __launch_bounds__(kThreads, (D <= 128 ? 2 : 1)) pass1_kernel(con
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, C::kTmemCols);
   }

@@ -246,6 +246,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t gm;
       const int t = tile_of(i, gm);
       if (!(ok = warp_wait(s_full(i & 1), (i >> 1) & 1))) break;
+      const bool row_hot = row_valid && ((gm >> (r >> 4)) & 1u);
+      const int j0 = t * kTile;
+      const int nvis = row_hot ? min(kTile, vis_last + 1 - j0) : 0;  // keys j0 .. j0+nvis-1 visible
+      if (!__any_sync(0xffffffffu, nvis > 0)) {
+        // neither of this warp's two groups takes part in this tile: its P rows are zero
+        __syncwarp();
+        if (lane == 0) mbar_arrive(s_free(i & 1));
+        if (i >= C::NP && !(ok = warp_wait(pv_done((i - C::NP) & 1), ((i - C::NP) >> 1) & 1))) break;
+        uint8_t* prow = smem + C::kPOff + (i % C::NP) * 2 * C::kPBytes + r * 128;
+#pragma unroll
+        for (int ch = 0; ch < 8; ++ch) {
+          const int sw = (ch ^ (r & 7)) << 4;  // same swizzled order as the computed rows: no bank conflicts
+          *reinterpret_cast<uint4*>(prow + sw) = make_uint4(0u, 0u, 0u, 0u);
+          *reinterpret_cast<uint4*>(prow + C::kPBytes + sw) = make_uint4(0u, 0u, 0u, 0u);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(p_full(i & 1));
+        continue;
+      }
       tc_fence_after();
       uint32_t raw[64];
       tmem_ld_x32(tmem + lane_base + C::kSCol + 64 * (i & 1), raw);
@@ -254,9 +274,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(s_free(i & 1));
-      const bool row_hot = row_valid && ((gm >> (r >> 4)) & 1u);
-      const int j0 = t * kTile;
-      const int nvis = row_hot ? min(kTile, vis_last + 1 - j0) : 0;  // keys j0 .. j0+nvis-1 visible
       float sv[64];
       float c = -INFINITY;
 #pragma unroll

@@ -11,16 +11,17 @@
 // explicitly rounded intrinsic (no contraction), in this order per 16-block:
 //   a = max|x|;  sb = UE4M3_rn_sat(a / (6 s));  if sb == 0 all codes are 0,
 //   else code = E2M1_rn_sat(x * rcp_rn(UE4M3(sb) * s)).
-// The key mean is an FP32 sum per 64-key tile in ascending key order, the tile
-// sums added in ascending tile order in FP64, divided by Nkv in FP64 and
-// rounded to FP32.
+// The key mean is an FP32 sum per 64-key tile in ascending key order; the tile
+// sums are added in FP64 per range of 64 consecutive tiles (ascending), the
+// range sums in ascending order; divided by Nkv in FP64 and rounded to FP32.
 //
 // Kernels:
 //   stats_kernel     K/V tiles: per-tile FP32 key sums, per-channel min/max of K
 //                    (atomics on an order-preserving encoding: exact, so order-free),
 //                    max |V|; Q rows: max |Q| per query head.
-//   finalize_kernel  per (b, KV head): mu, FP32 head scales s_k, s_v, s_q.
-//   quant_kernel     K/V tiles -> blobs; 128-row Q blocks (GQA-packed) -> Q blobs.
+//   finalize_kernel  per (b, KV head, 32 channels): mu and the head's max |k - mu|.
+//   quant_kernel     FP32 head scales from the maxima; K/V tiles -> blobs;
+//                    128-row Q blocks (GQA-packed) -> Q blobs.
 #include "apa_internal.h"
 #include "tc.cuh"
 
@@ -102,10 +103,8 @@ __global__ void __launch_bounds__(kThreads) stats_kernel(Shape s, const uint16_t
   if (do_kv && (int)blockIdx.x < n_kv_blocks) {
     const int bh = blockIdx.x / T, t = blockIdx.x % T;
     const int j0 = t * kTile, nk = min(kTile, s.Nkv - j0);
-    uint16_t* ks = reinterpret_cast<uint16_t*>(smem);
     const size_t base = ((size_t)bh * s.Nkv + j0) * d;
-    load_tile(ks, k + base, nk, d);
-    // max |V| over the tile, straight from global
+    // max |V| over the tile
     float vm = 0.f;
     for (int i = threadIdx.x; i < nk * d / 8; i += blockDim.x) {
       const uint4 val = reinterpret_cast<const uint4*>(v + base)[i];
@@ -113,18 +112,30 @@ __global__ void __launch_bounds__(kThreads) stats_kernel(Shape s, const uint16_t
 #pragma unroll
       for (int e = 0; e < 4; ++e) vm = fmaxf(vm, fmaxf(fabsf(bf16f(w[e] & 0xFFFF)), fabsf(bf16f(w[e] >> 16))));
     }
+    // per channel pair: FP32 sum over the tile's keys in ascending order, min, max
+    // (the tile is staged in shared memory by all threads with 16-byte loads)
+    uint16_t* ks = reinterpret_cast<uint16_t*>(smem);
+    load_tile(ks, k + base, nk, d);
     __syncthreads();
-    for (int c = threadIdx.x; c < d; c += blockDim.x) {
-      float acc = 0.f, mn = INFINITY, mx = -INFINITY;
+    for (int cp = threadIdx.x; cp < d / 2; cp += blockDim.x) {
+      const uint32_t* col = reinterpret_cast<const uint32_t*>(ks) + cp;
+      float acc0 = 0.f, acc1 = 0.f, mn0 = INFINITY, mn1 = INFINITY, mx0 = -INFINITY, mx1 = -INFINITY;
       for (int j = 0; j < nk; ++j) {
-        const float x = bf16f(ks[j * d + c]);
-        acc = __fadd_rn(acc, x);
-        mn = fminf(mn, x);
-        mx = fmaxf(mx, x);
+        const uint32_t w = col[j * (d / 2)];
+        const float x0 = bf16f(w & 0xFFFF), x1 = bf16f(w >> 16);
+        acc0 = __fadd_rn(acc0, x0);
+        acc1 = __fadd_rn(acc1, x1);
+        mn0 = fminf(mn0, x0);
+        mx0 = fmaxf(mx0, x0);
+        mn1 = fminf(mn1, x1);
+        mx1 = fmaxf(mx1, x1);
       }
-      ws.ksum[((size_t)bh * T + t) * d + c] = acc;
-      atomicMin(&ws.kmin[(size_t)bh * d + c], ord_enc(mn));
-      atomicMax(&ws.kmax[(size_t)bh * d + c], ord_enc(mx));
+      const size_t c = 2 * (size_t)cp;
+      *reinterpret_cast<float2*>(&ws.ksum[((size_t)bh * T + t) * d + c]) = make_float2(acc0, acc1);
+      atomicMin(&ws.kmin[(size_t)bh * d + c], ord_enc(mn0));
+      atomicMax(&ws.kmax[(size_t)bh * d + c], ord_enc(mx0));
+      atomicMin(&ws.kmin[(size_t)bh * d + c + 1], ord_enc(mn1));
+      atomicMax(&ws.kmax[(size_t)bh * d + c + 1], ord_enc(mx1));
     }
     vm = block_max(vm, red);
     if (threadIdx.x == 0) atomicMax(&ws.vamax[bh], __float_as_uint(vm));
@@ -147,31 +158,49 @@ __global__ void __launch_bounds__(kThreads) stats_kernel(Shape s, const uint16_t
   if (threadIdx.x == 0) atomicMax(&ws.qamax[bhq], __float_as_uint(qm));
 }
 
-__global__ void __launch_bounds__(kThreads) finalize_kernel(Shape s, Workspace ws, int do_q, int do_kv) {
-  __shared__ float red[32];
-  const int bh = blockIdx.x, d = s.d, T = s.T();
-  if (do_kv) {
-    float am = 0.f;
-    for (int c = threadIdx.x; c < d; c += blockDim.x) {
-      double S = 0.0;
-      for (int t = 0; t < T; ++t) S += (double)ws.ksum[((size_t)bh * T + t) * d + c];
-      const float mu = __double2float_rn(S / (double)s.Nkv);
-      ws.mu[(size_t)bh * d + c] = mu;
-      const float mn = ord_dec(ws.kmin[(size_t)bh * d + c]), mx = ord_dec(ws.kmax[(size_t)bh * d + c]);
-      am = fmaxf(am, fmaxf(fabsf(__fsub_rn(mx, mu)), fabsf(__fsub_rn(mn, mu))));
+// Key mean per channel from the tile sums, in the pinned order: FP64 sums over
+// ranges of kMeanRange consecutive tiles (ascending), then the range sums in
+// ascending order.  One block per (b, KV head, 32 channels): 8 lanes per channel
+// sum different ranges in parallel, one lane per channel adds the range sums.
+// Also the maximum |k - mu| of the head (atomic max on the float bits).
+constexpr int kMeanRange = 64;
+constexpr int kRangesPerPass = 64;
+
+__global__ void __launch_bounds__(kThreads) finalize_kernel(Shape s, Workspace ws) {
+  __shared__ double rs[kRangesPerPass][32];
+  const int cblocks = s.d / 32;
+  const int bh = blockIdx.x / cblocks, cl = threadIdx.x & 31, lane8 = threadIdx.x >> 5;
+  const int c = (blockIdx.x % cblocks) * 32 + cl;
+  const int d = s.d, T = s.T(), nR = (T + kMeanRange - 1) / kMeanRange;
+  const float* col = ws.ksum + (size_t)bh * T * d + c;
+  double S = 0.0;
+  for (int r0 = 0; r0 < nR; r0 += kRangesPerPass) {
+    for (int r = r0 + lane8; r < min(nR, r0 + kRangesPerPass); r += 8) {
+      const int t0 = r * kMeanRange, t1 = min(T, t0 + kMeanRange);
+      double Sr = 0.0;
+      for (int t = t0; t < t1; t += 16) {
+        float x[16];
+#pragma unroll
+        for (int u = 0; u < 16; ++u) x[u] = t + u < t1 ? col[(size_t)(t + u) * d] : 0.f;
+#pragma unroll
+        for (int u = 0; u < 16; ++u)
+          if (t + u < t1) Sr += (double)x[u];
+      }
+      rs[r - r0][cl] = Sr;
     }
-    am = block_max(am, red);
-    if (threadIdx.x == 0) {
-      ws.s_k[bh] = head_scale(am);
-      ws.s_v[bh] = head_scale(__uint_as_float(ws.vamax[bh]));
-    }
+    __syncthreads();
+    if (lane8 == 0)
+      for (int r = 0; r < min(kRangesPerPass, nR - r0); ++r) S += rs[r][cl];
+    __syncthreads();
   }
-  if (do_q) {
-    const int b = bh / s.Hkv, h = bh % s.Hkv, G = s.G();
-    for (int g = threadIdx.x; g < G; g += blockDim.x) {
-      const int hq = b * s.Hq + h * G + g;
-      ws.s_q[hq] = head_scale(__uint_as_float(ws.qamax[hq]));
-    }
+  if (lane8 == 0) {
+    const float mu = __double2float_rn(S / (double)s.Nkv);
+    ws.mu[(size_t)bh * d + c] = mu;
+    const float mn = ord_dec(ws.kmin[(size_t)bh * d + c]), mx = ord_dec(ws.kmax[(size_t)bh * d + c]);
+    float am = fmaxf(fabsf(__fsub_rn(mx, mu)), fabsf(__fsub_rn(mn, mu)));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
+    if (cl == 0) atomicMax(&ws.kcamax[bh], __float_as_uint(am));
   }
 }
 
@@ -192,34 +221,59 @@ __global__ void __launch_bounds__(kThreads) quant_kernel(Shape s, const uint16_t
     load_tile(vs, v + base, nk, d);
     for (int c = threadIdx.x; c < d; c += blockDim.x) mus[c] = ws.mu[(size_t)bh * d + c];
     __syncthreads();
-    const float sk = ws.s_k[bh], sv = ws.s_v[bh];
+    // FP32 head scales from the head maxima (the head's largest magnitude maps to 2688)
+    const float sk = head_scale(__uint_as_float(ws.kcamax[bh])), sv = head_scale(__uint_as_float(ws.vamax[bh]));
+    if (t == 0 && threadIdx.x == 0) {
+      ws.s_k[bh] = sk;
+      ws.s_v[bh] = sv;
+    }
     uint8_t* blob = ws.kv_blob + ((size_t)bh * T + t) * blob_bytes(d);
     const int ncb = d / 16;
-    // K: per (key n, 16-channel block cb), centred
-    for (int it = threadIdx.x; it < kTile * ncb; it += blockDim.x) {
-      const int n = it / ncb, cb = it % ncb;
-      uint2 codes = make_uint2(0u, 0u);
-      uint32_t sb = 0;
-      if (n < nk) {
-        float x[16];
+    // K: per (key n, 16-channel block cb), centred.  blockDim is a multiple of
+    // ncb, so each thread keeps one cb and its 16 means in registers.
+    {
+      const int cb = threadIdx.x % ncb;
+      float mu16[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) x[i] = __fsub_rn(bf16f(ks[n * d + cb * 16 + i]), mus[cb * 16 + i]);
-        sb = quant16(x, sk, &codes);
+      for (int i = 0; i < 16; ++i) mu16[i] = mus[cb * 16 + i];
+      for (int n = threadIdx.x / ncb; n < kTile; n += blockDim.x / ncb) {
+        uint2 codes = make_uint2(0u, 0u);
+        uint32_t sb = 0;
+        if (n < nk) {
+          const uint4* src = reinterpret_cast<const uint4*>(ks + n * d + cb * 16);
+          const uint4 a0 = src[0], a1 = src[1];
+          const uint32_t w[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+          float x[16];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            x[2 * i] = __fsub_rn(bf16f(w[i] & 0xFFFF), mu16[2 * i]);
+            x[2 * i + 1] = __fsub_rn(bf16f(w[i] >> 16), mu16[2 * i + 1]);
+          }
+          sb = quant16(x, sk, &codes);
+        }
+        *reinterpret_cast<uint2*>(blob + blob_kcodes(d) + fp4_kmajor_off(n, cb, d / 2)) = codes;
+        const int kb = cb >> 2, k16 = cb & 3;
+        blob[blob_ksf(d) + (kb >> 1) * 512 + (n & 31) * 16 + ((n >> 5) + 2 * (kb & 1)) * 4 + k16] = (uint8_t)sb;
       }
-      *reinterpret_cast<uint2*>(blob + blob_kcodes(d) + fp4_kmajor_off(n, cb, d / 2)) = codes;
-      const int kb = cb >> 2, k16 = cb & 3;
-      blob[blob_ksf(d) + (kb >> 1) * 512 + (n & 31) * 16 + ((n >> 5) + 2 * (kb & 1)) * 4 + k16] = (uint8_t)sb;
     }
-    // V^T: per (channel c, 16-key block kb16); keys past Nkv are zero
-    for (int it = threadIdx.x; it < d * 4; it += blockDim.x) {
-      const int c = it % d, kb16 = it / d;
-      float x[16];
+    // V^T: per (channel pair, 16-key block kb16); keys past Nkv are zero
+    for (int it = threadIdx.x; it < (d / 2) * 4; it += blockDim.x) {
+      const int cp = it % (d / 2), kb16 = it / (d / 2);
+      float x0[16], x1[16];
 #pragma unroll
-      for (int i = 0; i < 16; ++i) x[i] = bf16f(vs[(kb16 * 16 + i) * d + c]);
-      uint2 codes;
-      const uint32_t sb = quant16(x, sv, &codes);
-      *reinterpret_cast<uint2*>(blob + blob_vcodes(d) + fp4_kmajor_off(c, kb16, 32)) = codes;
-      blob[blob_vsf(d) + (c >> 7) * 512 + sf_atom_off(c & 127, kb16)] = (uint8_t)sb;
+      for (int i = 0; i < 16; ++i) {
+        const uint32_t w = reinterpret_cast<const uint32_t*>(vs + (kb16 * 16 + i) * d)[cp];
+        x0[i] = bf16f(w & 0xFFFF);
+        x1[i] = bf16f(w >> 16);
+      }
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int c = 2 * cp + e;
+        uint2 codes;
+        const uint32_t sb = quant16(e ? x1 : x0, sv, &codes);
+        *reinterpret_cast<uint2*>(blob + blob_vcodes(d) + fp4_kmajor_off(c, kb16, 32)) = codes;
+        blob[blob_vsf(d) + (c >> 7) * 512 + sf_atom_off(c & 127, kb16)] = (uint8_t)sb;
+      }
     }
     return;
   }
@@ -229,6 +283,11 @@ __global__ void __launch_bounds__(kThreads) quant_kernel(Shape s, const uint16_t
   const int bh = qb / nblk, blk = qb % nblk;
   const int b = bh / s.Hkv, h = bh % s.Hkv;
   uint8_t* qblob = ws.q_blob + ((size_t)bh * nblk + blk) * qblob_bytes(d);
+  if (blk == 0)
+    for (int g = threadIdx.x; g < G; g += blockDim.x) {
+      const int hq = b * s.Hq + h * G + g;
+      ws.s_q[hq] = head_scale(__uint_as_float(ws.qamax[hq]));
+    }
   const int ncb = d / 16;
   for (int it = threadIdx.x; it < kBlockRows * ncb; it += blockDim.x) {
     const int p = it / ncb, cb = it % ncb, P = blk * kBlockRows + p;
@@ -245,7 +304,7 @@ __global__ void __launch_bounds__(kThreads) quant_kernel(Shape s, const uint16_t
         x[2 * i] = bf16f(w[i] & 0xFFFF);
         x[2 * i + 1] = bf16f(w[i] >> 16);
       }
-      sb = quant16(x, ws.s_q[hq], &codes);
+      sb = quant16(x, head_scale(__uint_as_float(ws.qamax[hq])), &codes);
     }
     *reinterpret_cast<uint2*>(qblob + fp4_kmajor_off(p, cb, d / 2)) = codes;
     qblob[qblob_sf(d) + (cb >> 2) * 512 + sf_atom_off(p, cb & 3)] = (uint8_t)sb;
@@ -262,6 +321,7 @@ cudaError_t launch_quantize(const Shape& s, const void* q, const void* k, const 
     if ((e = cudaMemsetAsync(ws.kmin, 0xFF, sizeof(uint32_t) * BH * d, st))) return e;
     if ((e = cudaMemsetAsync(ws.kmax, 0x00, sizeof(uint32_t) * BH * d, st))) return e;
     if ((e = cudaMemsetAsync(ws.vamax, 0x00, sizeof(uint32_t) * BH, st))) return e;
+    if ((e = cudaMemsetAsync(ws.kcamax, 0x00, sizeof(uint32_t) * BH, st))) return e;
   }
   if (do_q && (e = cudaMemsetAsync(ws.qamax, 0x00, sizeof(uint32_t) * s.B * s.Hq, st))) return e;
   const int n_kv = do_kv ? BH * T : 0;
@@ -272,8 +332,10 @@ cudaError_t launch_quantize(const Shape& s, const void* q, const void* k, const 
     stats_kernel<<<n_kv + n_q, kThreads, sm1, st>>>(s, (const uint16_t*)q, (const uint16_t*)k, (const uint16_t*)v, ws,
                                                     n_kv, q_rows, do_kv);
   if ((e = cudaGetLastError())) return e;
-  finalize_kernel<<<BH, kThreads, 0, st>>>(s, ws, do_q, do_kv);
-  if ((e = cudaGetLastError())) return e;
+  if (do_kv) {
+    finalize_kernel<<<BH * (d / 32), kThreads, 0, st>>>(s, ws);
+    if ((e = cudaGetLastError())) return e;
+  }
   const int n_qb = do_q ? BH * s.nblk() : 0;
   const size_t sm2 = (size_t)kTile * d * 2 * 2 + d * 4;
   if (sm2 > 48 * 1024) cudaFuncSetAttribute(quant_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm2);

@@ -132,20 +132,29 @@ void oracle_quantize_blocks(const float* x, int64_t nblk, double s, uint8_t* cod
   }
 }
 
+/* Tiles per range of the key-mean sum. */
+#define MEAN_RANGE_TILES 64
+
 /* Per-channel key mean mu_c of one KV head (blog, "Mean-centred K").  The
  * rounding is pinned so that the kernels can reproduce it bit for bit:
- * per 64-key tile an FP32 sum over the tile's keys in ascending order, the
- * tile sums added in ascending tile order in FP64, divided by Nkv in FP64 and
- * rounded to FP32. */
+ *   1. per 64-key tile, an FP32 sum over the tile's keys in ascending order;
+ *   2. per range of 64 consecutive tiles, an FP64 sum of the tile sums in
+ *      ascending order (starting from 0);
+ *   3. the range sums added in ascending order in FP64;
+ *   4. divided by Nkv in FP64 and rounded to FP32. */
 void oracle_key_mean(const uint16_t* k, int Nkv, int d, float* mu) {
   int T = (Nkv + TILE - 1) / TILE;
   for (int c = 0; c < d; ++c) {
     double S = 0.0;
-    for (int t = 0; t < T; ++t) {
-      double acc = 0.0;
-      int j1 = (t + 1) * TILE < Nkv ? (t + 1) * TILE : Nkv;
-      for (int j = t * TILE; j < j1; ++j) acc = f32(acc + oracle_bf16_to_double(k[(int64_t)j * d + c]));
-      S += acc;
+    for (int t0 = 0; t0 < T; t0 += MEAN_RANGE_TILES) {
+      double Sr = 0.0;
+      for (int t = t0; t < t0 + MEAN_RANGE_TILES && t < T; ++t) {
+        double acc = 0.0;
+        int j1 = (t + 1) * TILE < Nkv ? (t + 1) * TILE : Nkv;
+        for (int j = t * TILE; j < j1; ++j) acc = f32(acc + oracle_bf16_to_double(k[(int64_t)j * d + c]));
+        Sr += acc;
+      }
+      S += Sr;
     }
     mu[c] = (float)(S / (double)Nkv);
   }

@@ -109,6 +109,11 @@ def test_key_mean_against_exact_sum():
         # FP32 sums of <= 64 bf16 values: rounding error <= 64 * 2^-24 relative to the tile magnitude
         tol = 64 * 2.0 ** -24 * (np.abs(synth.bf16_bits_to_f32(kb)).max()) + np.spacing(np.abs(exact).astype(np.float32))
         assert np.all(np.abs(mu - exact) <= tol)
+    # more than one 64-tile range: still the mean within the FP32 tile-sum rounding bound
+    kf = (rng.standard_normal((64 * 64 * 3 + 100, 64)) + 3.0).astype(np.float32)
+    kb = synth.f32_to_bf16_bits(kf)
+    exact = np.array([math.fsum(col) for col in synth.bf16_bits_to_f32(kb).astype(np.float64).T]) / kb.shape[0]
+    assert np.all(np.abs(oracle.key_mean(kb) - exact) <= 64 * 2.0 ** -24 * 8.0 + np.spacing(np.float32(4.0)))
     # all keys equal: the mean is that value exactly
     kb = synth.f32_to_bf16_bits(np.full((300, 64), 1.5, np.float32))
     assert np.all(oracle.key_mean(kb) == 1.5)
