@@ -69,17 +69,19 @@ struct P1Cfg {
   static constexpr int kQBlob = qblob_bytes(D);
   static constexpr int kQOff = 0;
   static constexpr int kStageOff = (kQBlob + 1023) / 1024 * 1024;
-  static constexpr int kPOff = kStageOff + NS * kBlob;  // 2 x (128 rows x 32 B)
-  static constexpr int kOnesOff = kPOff + 2 * 4096;     // 16 rows x 32 B of E2M1 1.0
+  static constexpr int NP = 3;                          // P buffers (codes, scales in smem and TMEM)
+  static constexpr int kPOff = kStageOff + NS * kBlob;  // NP x (128 rows x 32 B)
+  static constexpr int kOnesOff = kPOff + NP * 4096;    // 16 rows x 32 B of E2M1 1.0
   static constexpr int kOnesSfOff = kOnesOff + 512;     // 512-B scale atom of UE4M3 1.0
-  static constexpr int kSmem = kOnesSfOff + 512 + 128;
+  static constexpr int kPsfOff = kOnesSfOff + 512;      // NP x 512-B scale atoms of P
+  static constexpr int kSmem = kPsfOff + NP * 512 + 128;
   static constexpr uint32_t kTmemCols = D <= 128 ? 256 : 512;
   static constexpr uint32_t kSfc = 4 * sf_chunks(D);  // TMEM columns of one K or V scale set
   static constexpr uint32_t kO = 0, kS = D, kL = D + 64, kSFQ = D + 80;
   static constexpr uint32_t kSFK = kSFQ + 4 * (D / 64);  // 3 buffers (tile % 3)
   static constexpr uint32_t kSFV = kSFK + 3 * kSfc;      // 3 buffers (tile % 3)
-  static constexpr uint32_t kSFP = kSFV + 3 * kSfc;      // 2 buffers (tile % 2)
-  static constexpr uint32_t kSFO = kSFP + 8;
+  static constexpr uint32_t kSFP = kSFV + 3 * kSfc;      // NP buffers (tile % NP)
+  static constexpr uint32_t kSFO = kSFP + 4 * NP;
   static_assert(kSFO + 4 <= kTmemCols, "TMEM budget");
 };
 
@@ -152,6 +154,7 @@ __global__ void __launch_bounds__(kThreads, (D <= 128 ? 2 : 1)) pass1_kernel(con
   auto pv_done = [&](int b2) { return bar0 + 8u * (16 + b2); };
   const uint32_t drain = bar0 + 8u * 18;
   auto warp_wait = [&](uint32_t bar, uint32_t parity) -> bool {
+    if (__all_sync(0xffffffffu, mbar_test_wait(bar, parity))) return true;  // already complete: no spin
     const bool okl = mbar_wait(bar, parity, &abort_flag, p.err);
     return __all_sync(0xffffffffu, okl);
   };
@@ -247,8 +250,10 @@ __global__ void __launch_bounds__(kThreads, (D <= 128 ? 2 : 1)) pass1_kernel(con
       auto issue_ones = [&](int i) -> bool {
         if (!mbar_wait(p_full(i & 1), (i >> 1) & 1, &abort_flag, p.err)) return false;
         tc_fence_after();
-        mma_nvf4(tmem + C::kL, smem_desc(sbase + C::kPOff + 4096 * (i & 1), 128, 256, 0),
-                 smem_desc(sbase + C::kOnesOff, 128, 256, 0), idL, tmem + C::kSFP + 4 * (i & 1), tmem + C::kSFO, 0);
+        const int pb = i % C::NP;
+        tmem_cp_32x128b_x4(tmem + C::kSFP + 4 * pb, smem_desc(sbase + C::kPsfOff + 512 * pb, 128, 128, 0));
+        mma_nvf4(tmem + C::kL, smem_desc(sbase + C::kPOff + 4096 * pb, 128, 256, 0),
+                 smem_desc(sbase + C::kOnesOff, 128, 256, 0), idL, tmem + C::kSFP + 4 * pb, tmem + C::kSFO, 0);
         mma_commit(l_full);
         return true;
       };
@@ -264,8 +269,11 @@ __global__ void __launch_bounds__(kThreads, (D <= 128 ? 2 : 1)) pass1_kernel(con
         if (hot) list[count++] = (uint32_t)tile_of(i) | (hot << 16);
         if ((hot | invalid_groups) != 0xFFu) {
           const uint32_t blob = sbase + C::kStageOff + (i % C::NS) * C::kBlob;
-          mma_nvf4(tmem + C::kO, smem_desc(sbase + C::kPOff + 4096 * (i & 1), 128, 256, 0),
-                   smem_desc(blob + blob_vcodes(D), 128, 256, 0), idO, tmem + C::kSFP + 4 * (i & 1),
+          const int pb = i % C::NP;
+          if (hot)  // the hot groups' P scales were zeroed in smem: copy them again for PV
+            tmem_cp_32x128b_x4(tmem + C::kSFP + 4 * pb, smem_desc(sbase + C::kPsfOff + 512 * pb, 128, 128, 0));
+          mma_nvf4(tmem + C::kO, smem_desc(sbase + C::kPOff + 4096 * pb, 128, 256, 0),
+                   smem_desc(blob + blob_vcodes(D), 128, 256, 0), idO, tmem + C::kSFP + 4 * pb,
                    tmem + C::kSFV + C::kSfc * (i % 3), pv_issued > 0);
           ++pv_issued;
         }
@@ -348,13 +356,15 @@ __global__ void __launch_bounds__(kThreads, (D <= 128 ? 2 : 1)) pass1_kernel(con
 #pragma unroll
         for (int w = 0; w < 8; ++w) pw[w] = 0u;
       }
-      // this P buffer (and its scales) is free once PV(i-2) has completed
-      if (i >= 2 && !warp_wait(pv_done(i & 1), ((i >> 1) - 1) & 1)) return false;
-      uint8_t* pb = smem + C::kPOff + 4096 * (i & 1) + (r >> 3) * 256 + (r & 7) * 16;
+      // P buffer i % 3 was last read by PV(i-3) and the ones-MMA of tile i-3; both
+      // completed before the ones-MMA of tile i-1, which judge(i-1) waited for
+      // (tcgen05 ops of the issuing thread complete in order and a commit covers
+      // all earlier ones), so the buffer is free without another wait.
+      const int pbuf = i % C::NP;
+      uint8_t* pb = smem + C::kPOff + 4096 * pbuf + (r >> 3) * 256 + (r & 7) * 16;
       *reinterpret_cast<uint4*>(pb) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
       *reinterpret_cast<uint4*>(pb + 128) = make_uint4(pw[4], pw[5], pw[6], pw[7]);
-      tmem_st_x4(tmem + lane_base + C::kSFP + 4 * (i & 1), pd.sfw, pd.sfw, pd.sfw, pd.sfw);
-      tmem_wait_st();
+      *reinterpret_cast<uint32_t*>(smem + C::kPsfOff + 512 * pbuf + sf_atom_off(r, 0)) = pd.sfw;
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
@@ -363,7 +373,9 @@ __global__ void __launch_bounds__(kThreads, (D <= 128 ? 2 : 1)) pass1_kernel(con
     };
 
     // Judges tile i from its FP4 row sums and commits frame, lambda and l.
-    auto judge = [&](int i, const Pending& pd) -> bool {
+    // `lifted`: some row of this warp moved its frame at tile i (else every row
+    // keeps m, so lambda += l_t and, if cold, l += l_t: no exponentials, no rescale).
+    auto judge = [&](int i, const Pending& pd, bool lifted) -> bool {
       const int t = tile_of(i);
       if (!warp_wait(l_full, i & 1)) return false;
       tc_fence_after();
@@ -371,57 +383,66 @@ __global__ void __launch_bounds__(kThreads, (D <= 128 ? 2 : 1)) pass1_kernel(con
       tmem_ld_x1(tmem + lane_base + C::kL, lb);
       tmem_wait_ld();
       const float ell = __uint_as_float(lb);
-      bool vote = false;
-      if (valid && !pd.empty && !eps_inf)
-        vote = (eps == 0.f) || ((m == -INFINITY) ? (ell > 0.f) : (ell * ex2_approx(pd.mt - m) > eps * lam));
+      // hot test: l_t (in the committed frame) > eps * lambda; thr is -1 at eps = 0 (every
+      // visible tile hot) and NaN at eps = inf with lambda = 0 (never hot)
+      const float thr = eps == 0.f ? -1.f : eps * lam;
+      bool vote;
+      if (!lifted) vote = valid && !pd.empty && ell > thr;
+      else vote = valid && !pd.empty && !eps_inf &&
+                  ((m == -INFINITY) ? (eps == 0.f || ell > 0.f) : (ell * ex2_approx(pd.mt - m) > thr));
       const uint32_t bal = __ballot_sync(0xffffffffu, vote);
       const bool hot_lo = (bal & 0x0000FFFFu) != 0, hot_hi = (bal & 0xFFFF0000u) != 0;
       const bool hot = lane < 16 ? hot_lo : hot_hi;
-      bool rescale = false;
-      float f = 1.f;
-      if (!pd.empty) {
-        const float l_before = l;
-        float mn;
-        if (hot) {
-          mn = fmaxf(m, pd.c - kColdOffset);
-          f = (m == -INFINITY) ? 0.f : ex2_approx(m - mn);
-          lam = lam * f + ell * ex2_approx(pd.mt - mn);
-          l *= f;
-        } else {
-          mn = pd.mt;
-          f = (m == -INFINITY) ? 0.f : ex2_approx(m - mn);
-          lam = lam * f + ell;
-          l = l * f + ell;
+      if (!lifted) {
+        if (!pd.empty) {
+          lam += ell;
+          if (!hot) l += ell;
         }
-        rescale = (f != 1.f) && (l_before > 0.f);
-        m = mn;
-      }
-      if (__any_sync(0xffffffffu, hot)) {
-        const uint32_t z = hot ? 0u : pd.sfw;  // a hot group's P drops out of PV
-        tmem_st_x4(tmem + lane_base + C::kSFP + 4 * (i & 1), z, z, z, z);
-      }
-      if (__any_sync(0xffffffffu, rescale)) {
-        // O must not be touched before PV(i-1) has landed
-        if (!warp_wait(pv_done((i - 1) & 1), ((i - 1) >> 1) & 1)) return false;
-        tc_fence_after();
-        const float fr = rescale ? f : 1.f;
+      } else {
+        bool rescale = false;
+        float f = 1.f;
+        if (!pd.empty) {
+          const float l_before = l;
+          float mn;
+          if (hot) {
+            mn = fmaxf(m, pd.c - kColdOffset);
+            f = (m == -INFINITY) ? 0.f : ex2_approx(m - mn);
+            lam = lam * f + ell * ex2_approx(pd.mt - mn);
+            l *= f;
+          } else {
+            mn = pd.mt;
+            f = (m == -INFINITY) ? 0.f : ex2_approx(m - mn);
+            lam = lam * f + ell;
+            l = l * f + ell;
+          }
+          rescale = (f != 1.f) && (l_before > 0.f);
+          m = mn;
+        }
+        if (__any_sync(0xffffffffu, rescale)) {
+          // PV(i-1) has landed: it was issued before the ones-MMA of tile i, waited for above
+          const float fr = rescale ? f : 1.f;
 #pragma unroll 1
-        for (int c0 = 0; c0 < D; c0 += 32) {
-          uint32_t o[32];
-          tmem_ld_x32(tmem + lane_base + C::kO + c0, o);
-          tmem_wait_ld();
+          for (int c0 = 0; c0 < D; c0 += 32) {
+            uint32_t o[32];
+            tmem_ld_x32(tmem + lane_base + C::kO + c0, o);
+            tmem_wait_ld();
 #pragma unroll
-          for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * fr);
-          tmem_st_x16(tmem + lane_base + C::kO + c0, o);
-          tmem_st_x16(tmem + lane_base + C::kO + c0 + 16, o + 16);
+            for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * fr);
+            tmem_st_x16(tmem + lane_base + C::kO + c0, o);
+            tmem_st_x16(tmem + lane_base + C::kO + c0 + 16, o + 16);
+          }
+          tmem_wait_st();
         }
+      }
+      if (hot) {  // a hot group's P drops out of PV: zero its scales in smem
+        *reinterpret_cast<uint32_t*>(smem + C::kPsfOff + 512 * (i % C::NP) + sf_atom_off(r, 0)) = 0u;
+        fence_proxy_async_smem();
       }
       if (lane == 0) gbits[i & 1][warp] = ((uint32_t)hot_lo << (2 * warp)) | ((uint32_t)hot_hi << (2 * warp + 1));
       if (p.hot_mask && (lane == 0 || lane == 16) && hot) {
         const int grp = (p0 + 32 * warp + lane) / kGroupRows;
         if (grp < ngroups) atomicOr(&p.hot_mask[((size_t)bh * ngroups + grp) * nwords + t / 32], 1u << (t % 32));
       }
-      tmem_wait_st();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(dec(i & 1));
@@ -431,19 +452,20 @@ __global__ void __launch_bounds__(kThreads, (D <= 128 ? 2 : 1)) pass1_kernel(con
     Pending cur, nxt;
     ok = encode(0, cur);
     for (int i = 0; ok && i < n; ++i) {
+      const bool lifted = __any_sync(0xffffffffu, cur.lift);
       if (i + 1 < n) {
         // tile i+1 can be encoded before tile i is judged unless a row of this
         // warp lifted its frame at tile i (then m after tile i depends on the verdict)
-        if (!__any_sync(0xffffffffu, cur.lift)) {
+        if (!lifted) {
           if (!(ok = encode(i + 1, nxt))) break;
-          if (!(ok = judge(i, cur))) break;
+          if (!(ok = judge(i, cur, false))) break;
         } else {
-          if (!(ok = judge(i, cur))) break;
+          if (!(ok = judge(i, cur, true))) break;
           if (!(ok = encode(i + 1, nxt))) break;
         }
         cur = nxt;
       } else {
-        ok = judge(i, cur);
+        ok = judge(i, cur, lifted);
       }
     }
     // ---- epilogue: the pass-1 state (o scaled by s_v, frame m, cold sum l)
