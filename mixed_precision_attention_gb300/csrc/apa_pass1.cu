@@ -35,6 +35,9 @@
 // At d <= 128 a CTA holds 256 TMEM columns and ~55 KB of shared memory, so two
 // CTAs share an SM.  (Two threads per row, swapping group maxima, was measured
 // slower: the per-warp waits and exchanges outweighed the halved encode.)
+#include <cstdlib>
+#include <cstring>
+
 #include "apa_internal.h"
 #include "tc.cuh"
 
@@ -118,6 +121,17 @@ __device__ __forceinline__ uint32_t pack8_e2m1(const float* x) {
       : "f"(x[0]), "f"(x[1]), "f"(x[2]), "f"(x[3]), "f"(x[4]), "f"(x[5]), "f"(x[6]), "f"(x[7]));
   return w;
 }
+// Twice the E2M1 values of eight non-negative codes, summed (exact integer):
+// a byte table lookup (prmt: code -> 2 * value) and two 4-byte dot products.
+__device__ __forceinline__ uint32_t code_sum2(uint32_t w) {
+  uint32_t lo, hi, acc;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(lo) : "r"(0x03020100u), "r"(0x0C080604u), "r"(w));
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(hi) : "r"(0x03020100u), "r"(0x0C080604u), "r"(w >> 16));
+  asm("dp4a.u32.u32 %0, %1, %2, %3;" : "=r"(acc) : "r"(lo), "r"(0x01010101u), "r"(0u));
+  asm("dp4a.u32.u32 %0, %1, %2, %3;" : "=r"(acc) : "r"(hi), "r"(0x01010101u), "r"(acc));
+  return acc;
+}
+
 // What a row keeps between encoding a tile and judging it.
 struct Pending {
   float c, mt;
@@ -125,7 +139,13 @@ struct Pending {
   bool empty, lift;
 };
 
-template <int D>
+// kOnesMma: the tile row sums come from an extra MMA of P against an E2M1 ones
+// tile (the blog's form: the softmax warps encode tile t+1 while the row sums
+// of tile t are in flight).  Otherwise each thread sums its own row's quantized
+// P exactly in registers (a byte table lookup of the codes), so the hot test
+// follows the encode directly, a hot group's P scales are written as zero, and
+// a tile costs the softmax warps one wait and two arrives.
+template <int D, bool kOnesMma>
 __global__ void __launch_bounds__(kThreads, (D <= 128 ? 2 : 1)) pass1_kernel(const P1Params p) {
   using C = P1Cfg<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -257,10 +277,33 @@ __global__ void __launch_bounds__(kThreads, (D <= 128 ? 2 : 1)) pass1_kernel(con
         mma_commit(l_full);
         return true;
       };
+      uint32_t pv_issued = 0;
+      if (!kOnesMma) {
+        // S(i+1) as soon as S(i) has been read out; PV(i) once P(i) and its verdicts are in
+        if (ok) ok = issue_s(0);
+        for (int i = 0; ok && i < n; ++i) {
+          if (i + 1 < n && !(ok = issue_s(i + 1))) break;
+          if (!(ok = mbar_wait(p_full(i & 1), (i >> 1) & 1, &abort_flag, p.err))) break;
+          tc_fence_after();
+          const uint32_t hot = gbits[i & 1][0] | gbits[i & 1][1] | gbits[i & 1][2] | gbits[i & 1][3];
+          if (hot) list[count++] = (uint32_t)tile_of(i) | (hot << 16);
+          if ((hot | invalid_groups) != 0xFFu) {
+            const uint32_t blob = sbase + C::kStageOff + (i % C::NS) * C::kBlob;
+            const int pb = i % C::NP;
+            tmem_cp_32x128b_x4(tmem + C::kSFP + 4 * pb, smem_desc(sbase + C::kPsfOff + 512 * pb, 128, 128, 0));
+            mma_nvf4(tmem + C::kO, smem_desc(sbase + C::kPOff + 4096 * pb, 128, 256, 0),
+                     smem_desc(blob + blob_vcodes(D), 128, 256, 0), idO, tmem + C::kSFP + 4 * pb,
+                     tmem + C::kSFV + C::kSfc * (i % 3), pv_issued > 0);
+            ++pv_issued;
+          }
+          mma_commit(pv_done(i & 1));
+          mma_commit(blob_empty(i % C::NS));
+        }
+        ok = false;  // skip the ones-MMA schedule below
+      }
       if (ok) ok = issue_s(0);
       if (ok && n > 1) ok = issue_s(1);
       if (ok) ok = issue_ones(0);
-      uint32_t pv_issued = 0;
       for (int i = 0; ok && i < n; ++i) {
         if (i + 2 < n && !(ok = issue_s(i + 2))) break;
         if (!(ok = mbar_wait(dec(i & 1), (i >> 1) & 1, &abort_flag, p.err))) break;
@@ -449,23 +492,155 @@ __global__ void __launch_bounds__(kThreads, (D <= 128 ? 2 : 1)) pass1_kernel(con
       return true;
     };
 
-    Pending cur, nxt;
-    ok = encode(0, cur);
-    for (int i = 0; ok && i < n; ++i) {
-      const bool lifted = __any_sync(0xffffffffu, cur.lift);
-      if (i + 1 < n) {
-        // tile i+1 can be encoded before tile i is judged unless a row of this
-        // warp lifted its frame at tile i (then m after tile i depends on the verdict)
-        if (!lifted) {
-          if (!(ok = encode(i + 1, nxt))) break;
-          if (!(ok = judge(i, cur, false))) break;
+    if (kOnesMma) {
+      Pending cur, nxt;
+      ok = encode(0, cur);
+      for (int i = 0; ok && i < n; ++i) {
+        const bool lifted = __any_sync(0xffffffffu, cur.lift);
+        if (i + 1 < n) {
+          // tile i+1 can be encoded before tile i is judged unless a row of this
+          // warp lifted its frame at tile i (then m after tile i depends on the verdict)
+          if (!lifted) {
+            if (!(ok = encode(i + 1, nxt))) break;
+            if (!(ok = judge(i, cur, false))) break;
+          } else {
+            if (!(ok = judge(i, cur, true))) break;
+            if (!(ok = encode(i + 1, nxt))) break;
+          }
+          cur = nxt;
         } else {
-          if (!(ok = judge(i, cur, true))) break;
-          if (!(ok = encode(i + 1, nxt))) break;
+          ok = judge(i, cur, lifted);
         }
-        cur = nxt;
-      } else {
-        ok = judge(i, cur, lifted);
+      }
+    } else {
+      // ---- row sums in registers: encode, sum, judge and hand over, one tile at a time
+      for (int i = 0; ok && i < n; ++i) {
+        const int t = tile_of(i), j0 = t * kTile;
+        const int nvis = valid ? min(kTile, vis_last + 1 - j0) : 0;
+        if (!(ok = warp_wait(s_full, i & 1))) break;
+        tc_fence_after();
+        uint32_t sr[64];
+        tmem_ld_x32(tmem + lane_base + C::kS, sr);
+        tmem_ld_x32(tmem + lane_base + C::kS + 32, sr + 32);
+        tmem_wait_ld();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(s_free);
+        float raw[64];
+#pragma unroll
+        for (int j = 0; j < 64; ++j) raw[j] = __uint_as_float(sr[j]);
+        if (__any_sync(0xffffffffu, nvis < kTile)) {
+#pragma unroll
+          for (int j = 0; j < 64; ++j)
+            if (j >= nvis) raw[j] = -INFINITY;
+        }
+        float g[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          float a = max3(raw[16 * k], raw[16 * k + 1], raw[16 * k + 2]);
+#pragma unroll
+          for (int j = 3; j < 15; j += 2) a = max3(a, raw[16 * k + j], raw[16 * k + j + 1]);
+          g[k] = fmaxf(a, raw[16 * k + 15]);
+        }
+        const float c = fmaxf(fmaxf(g[0], g[1]), fmaxf(g[2], g[3])) * cs;  // tile max, log2 units
+        const bool empty = (c == -INFINITY);
+        const float mt = (c > m + kTau) ? c : m;  // candidate frame (lazy maximum)
+        uint32_t pw[8];
+        uint32_t sfw = 0x08080808u;  // 2^-6 where nothing is visible
+        float ell = 0.f;             // l_t: exact sum of the quantized P of this row
+        if (!empty) {
+          sfw = 0;
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            uint32_t sc = cvt_ue4m3(ex2_approx(fmaf(g[k], cs, -mt)) * (1.f / 6.f));
+            sc = max(sc, 8u);  // clamp the group scale at 2^-6
+            sfw |= sc << (8 * k);
+            const float scv = ue4m3_value(sc);
+            const float nb = -(mt + lg2_approx(scv));
+#pragma unroll
+            for (int w = 0; w < 2; ++w) {
+              float y[8];
+#pragma unroll
+              for (int e = 0; e < 8; ++e) y[e] = ex2_approx(fmaf(raw[16 * k + 8 * w + e], cs, nb));
+              pw[2 * k + w] = pack8_e2m1(y);
+            }
+            ell = fmaf((float)(code_sum2(pw[2 * k]) + code_sum2(pw[2 * k + 1])), 0.5f * scv, ell);
+          }
+        } else {
+#pragma unroll
+          for (int w = 0; w < 8; ++w) pw[w] = 0u;
+        }
+        // hot test: l_t (in the committed frame) > eps * lambda
+        const bool lift = !empty && mt != m;
+        const bool lifted = __any_sync(0xffffffffu, lift);
+        const float thr = eps == 0.f ? -1.f : eps * lam;
+        bool vote;
+        if (!lifted) vote = valid && !empty && ell > thr;
+        else vote = valid && !empty && !eps_inf &&
+                    ((m == -INFINITY) ? (eps == 0.f || ell > 0.f) : (ell * ex2_approx(mt - m) > thr));
+        const uint32_t bal = __ballot_sync(0xffffffffu, vote);
+        const bool hot_lo = (bal & 0x0000FFFFu) != 0, hot_hi = (bal & 0xFFFF0000u) != 0;
+        const bool hot = lane < 16 ? hot_lo : hot_hi;
+        if (!lifted) {
+          if (!empty) {
+            lam += ell;
+            if (!hot) l += ell;
+          }
+        } else {
+          bool rescale = false;
+          float f = 1.f;
+          if (!empty) {
+            const float l_before = l;
+            float mn;
+            if (hot) {
+              mn = fmaxf(m, c - kColdOffset);
+              f = (m == -INFINITY) ? 0.f : ex2_approx(m - mn);
+              lam = lam * f + ell * ex2_approx(mt - mn);
+              l *= f;
+            } else {
+              mn = mt;
+              f = (m == -INFINITY) ? 0.f : ex2_approx(m - mn);
+              lam = lam * f + ell;
+              l = l * f + ell;
+            }
+            rescale = (f != 1.f) && (l_before > 0.f);
+            m = mn;
+          }
+          if (__any_sync(0xffffffffu, rescale)) {
+            // O must not be touched before PV(i-1) has landed
+            if (!(ok = warp_wait(pv_done((i - 1) & 1), ((i - 1) >> 1) & 1))) break;
+            tc_fence_after();
+            const float fr = rescale ? f : 1.f;
+#pragma unroll 1
+            for (int c0 = 0; c0 < D; c0 += 32) {
+              uint32_t o[32];
+              tmem_ld_x32(tmem + lane_base + C::kO + c0, o);
+              tmem_wait_ld();
+#pragma unroll
+              for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * fr);
+              tmem_st_x16(tmem + lane_base + C::kO + c0, o);
+              tmem_st_x16(tmem + lane_base + C::kO + c0 + 16, o + 16);
+            }
+            tmem_wait_st();
+          }
+        }
+        // P buffer i % 3 was last read by PV(i-3), issued before S(i), whose completion
+        // was waited for above: free without another wait.  A hot group's scales are
+        // zero, so its rows drop out of PV.
+        const int pbuf = i % C::NP;
+        uint8_t* pbp = smem + C::kPOff + 4096 * pbuf + (r >> 3) * 256 + (r & 7) * 16;
+        *reinterpret_cast<uint4*>(pbp) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
+        *reinterpret_cast<uint4*>(pbp + 128) = make_uint4(pw[4], pw[5], pw[6], pw[7]);
+        *reinterpret_cast<uint32_t*>(smem + C::kPsfOff + 512 * pbuf + sf_atom_off(r, 0)) = hot ? 0u : sfw;
+        if (lane == 0) gbits[i & 1][warp] = ((uint32_t)hot_lo << (2 * warp)) | ((uint32_t)hot_hi << (2 * warp + 1));
+        if (p.hot_mask && (lane == 0 || lane == 16) && hot) {
+          const int grp = (p0 + 32 * warp + lane) / kGroupRows;
+          if (grp < ngroups) atomicOr(&p.hot_mask[((size_t)bh * ngroups + grp) * nwords + t / 32], 1u << (t % 32));
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(p_full(i & 1));
       }
     }
     // ---- epilogue: the pass-1 state (o scaled by s_v, frame m, cold sum l)
@@ -498,13 +673,29 @@ __global__ void __launch_bounds__(kThreads, (D <= 128 ? 2 : 1)) pass1_kernel(con
   }
 }
 
+template <int D, bool kOnesMma>
+cudaError_t launch_dv(const P1Params& prm, cudaStream_t st) {
+  const int smem = P1Cfg<D>::kSmem;
+  cudaError_t e =
+      cudaFuncSetAttribute(pass1_kernel<D, kOnesMma>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e) return e;
+  pass1_kernel<D, kOnesMma><<<prm.s.BH() * prm.s.nblk(), kThreads, smem, st>>>(prm);
+  return cudaGetLastError();
+}
+
+// APA_PASS1_ROWSUM=mma selects the ones-MMA row sums (for comparison); the
+// default sums each row's quantized P in registers.
+bool rowsum_by_mma() {
+  static const bool v = [] {
+    const char* e = getenv("APA_PASS1_ROWSUM");
+    return e && strcmp(e, "mma") == 0;
+  }();
+  return v;
+}
+
 template <int D>
 cudaError_t launch_d(const P1Params& prm, cudaStream_t st) {
-  const int smem = P1Cfg<D>::kSmem;
-  cudaError_t e = cudaFuncSetAttribute(pass1_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (e) return e;
-  pass1_kernel<D><<<prm.s.BH() * prm.s.nblk(), kThreads, smem, st>>>(prm);
-  return cudaGetLastError();
+  return rowsum_by_mma() ? launch_dv<D, true>(prm, st) : launch_dv<D, false>(prm, st);
 }
 
 }  // namespace
