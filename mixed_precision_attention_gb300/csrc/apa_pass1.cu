@@ -121,6 +121,45 @@ __device__ __forceinline__ uint32_t pack8_e2m1(const float* x) {
       : "f"(x[0]), "f"(x[1]), "f"(x[2]), "f"(x[3]), "f"(x[4]), "f"(x[5]), "f"(x[6]), "f"(x[7]));
   return w;
 }
+// Eight P values 2^(raw * cs + nb) -> one word of eight E2M1 codes (x[0] in the
+// lowest nibble); the affine step runs as four packed FP32 FMAs.
+__device__ __forceinline__ uint32_t encode8(const float* x, float cs, float nb) {
+  uint32_t w;
+  asm("{\n.reg .b64 a0, a1, a2, a3, c2, n2;\n"
+      ".reg .f32 y0, y1, y2, y3, y4, y5, y6, y7;\n"
+      ".reg .b8 b0, b1, b2, b3;\n"
+      "mov.b64 c2, {%9, %9};\n"
+      "mov.b64 n2, {%10, %10};\n"
+      "mov.b64 a0, {%1, %2};\n"
+      "mov.b64 a1, {%3, %4};\n"
+      "mov.b64 a2, {%5, %6};\n"
+      "mov.b64 a3, {%7, %8};\n"
+      "fma.rn.f32x2 a0, a0, c2, n2;\n"
+      "fma.rn.f32x2 a1, a1, c2, n2;\n"
+      "fma.rn.f32x2 a2, a2, c2, n2;\n"
+      "fma.rn.f32x2 a3, a3, c2, n2;\n"
+      "mov.b64 {y0, y1}, a0;\n"
+      "mov.b64 {y2, y3}, a1;\n"
+      "mov.b64 {y4, y5}, a2;\n"
+      "mov.b64 {y6, y7}, a3;\n"
+      "ex2.approx.ftz.f32 y0, y0;\n"
+      "ex2.approx.ftz.f32 y1, y1;\n"
+      "ex2.approx.ftz.f32 y2, y2;\n"
+      "ex2.approx.ftz.f32 y3, y3;\n"
+      "ex2.approx.ftz.f32 y4, y4;\n"
+      "ex2.approx.ftz.f32 y5, y5;\n"
+      "ex2.approx.ftz.f32 y6, y6;\n"
+      "ex2.approx.ftz.f32 y7, y7;\n"
+      "cvt.rn.satfinite.e2m1x2.f32 b0, y1, y0;\n"
+      "cvt.rn.satfinite.e2m1x2.f32 b1, y3, y2;\n"
+      "cvt.rn.satfinite.e2m1x2.f32 b2, y5, y4;\n"
+      "cvt.rn.satfinite.e2m1x2.f32 b3, y7, y6;\n"
+      "mov.b32 %0, {b0, b1, b2, b3};\n}"
+      : "=r"(w)
+      : "f"(x[0]), "f"(x[1]), "f"(x[2]), "f"(x[3]), "f"(x[4]), "f"(x[5]), "f"(x[6]), "f"(x[7]), "f"(cs), "f"(nb));
+  return w;
+}
+
 // Twice the E2M1 values of eight non-negative codes, summed (exact integer):
 // a byte table lookup (prmt: code -> 2 * value) and two 4-byte dot products.
 __device__ __forceinline__ uint32_t code_sum2(uint32_t w) {
@@ -558,12 +597,7 @@ __global__ void __launch_bounds__(kThreads, (D <= 128 ? 2 : 1)) pass1_kernel(con
             const float scv = ue4m3_value(sc);
             const float nb = -(mt + lg2_approx(scv));
 #pragma unroll
-            for (int w = 0; w < 2; ++w) {
-              float y[8];
-#pragma unroll
-              for (int e = 0; e < 8; ++e) y[e] = ex2_approx(fmaf(raw[16 * k + 8 * w + e], cs, nb));
-              pw[2 * k + w] = pack8_e2m1(y);
-            }
+            for (int w = 0; w < 2; ++w) pw[2 * k + w] = encode8(raw + 16 * k + 8 * w, cs, nb);
             ell = fmaf((float)(code_sum2(pw[2 * k]) + code_sum2(pw[2 * k + 1])), 0.5f * scv, ell);
           }
         } else {
