@@ -707,6 +707,404 @@ __global__ void __launch_bounds__(kThreads, (D <= 128 ? 2 : 1)) pass1_kernel(con
   }
 }
 
+// ----------------------------------------------------------------------------
+// Pass 1 with U row blocks of one KV head per CTA (d <= 128).
+//
+// TMEM holds U output accumulators (U * d columns) and one S buffer that the
+// units take in turn; at d = 128 and U = 3 that is all 512 columns, so one CTA
+// per SM keeps 3 blocks (384 rows) in flight instead of 2.  The units walk one
+// common tile order 0, T_max, ..., 1 (T_max: the last tile any of them sees; a
+// tile past a unit's own diagonal is fully masked for it, so a no-op) and share
+// each K/V blob and its scales.  Per unit the softmax work is the
+// register-row-sum form of the single-block kernel.
+//
+// Two warps issue the tensor-core work, so that neither issue stream is a
+// serial bottleneck for three units: the S warp issues S(0,i), S(1,i), ... in
+// the order in which the units hand the S buffer on; the PV warp issues
+// PV(u,i) as each unit publishes P(u,i).
+template <int D, int U>
+struct P1MCfg {
+  static constexpr int NS = 4;
+  static constexpr int kBlob = blob_bytes(D);
+  static constexpr int kQBlob = qblob_bytes(D);
+  static constexpr int kQStride = (kQBlob + 1023) / 1024 * 1024;
+  static constexpr int kStageOff = U * kQStride;
+  static constexpr int kPOff = kStageOff + NS * kBlob;  // [U][2] x (128 rows x 32 B)
+  static constexpr int kPsfOff = kPOff + U * 2 * 4096;  // [U][2] x 512-B scale atoms
+  static constexpr int kSmem = kPsfOff + U * 2 * 512 + 128;
+  static constexpr uint32_t kTmemCols = 512;
+  static constexpr uint32_t kSfc = 4 * sf_chunks(D);
+  static constexpr uint32_t kS = U * D;
+  static constexpr uint32_t kSFQ = kS + 64;                   // U x 4 * (D/64)
+  static constexpr uint32_t kSFK = kSFQ + U * 4 * (D / 64);   // 2 buffers (tile % 2)
+  static constexpr uint32_t kSFV = kSFK + 2 * kSfc;           // 2 buffers (tile % 2)
+  static constexpr uint32_t kSFP = kSFV + 2 * kSfc;           // [U][2] buffers (tile % 2)
+  static_assert(kSFP + 8 * U <= kTmemCols, "TMEM budget");
+  static constexpr int kThreads = (4 * U + 3) * 32;
+};
+
+template <int D, int U>
+__global__ void __launch_bounds__(P1MCfg<D, U>::kThreads, 1) pass1_multi_kernel(const P1Params p) {
+  using C = P1MCfg<D, U>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+  // barriers: q_full, blob_full[NS], blob_empty[NS], s_full[U], s_free[U], p_full[U][2], pv_done[U][2],
+  // drain_s, drain_pv
+  constexpr int kBars = 1 + 2 * C::NS + 6 * U + 2;
+  __shared__ __align__(8) uint64_t bars[kBars];
+  __shared__ uint32_t tmem_slot;
+  __shared__ int abort_flag;
+  __shared__ uint32_t gbits[U][2][4];
+
+  const Shape& s = p.s;
+  const int nblk = s.nblk(), BH = s.BH(), G = s.G(), R = s.R(), T = s.T(), off = s.off();
+  const int ngrp = (nblk + U - 1) / U;
+  const int bh = blockIdx.x % BH, grp = ngrp - 1 - (int)(blockIdx.x / BH);  // heavy (late) blocks first
+  const int b = bh / s.Hkv, h = bh % s.Hkv;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int kProd = 4 * U, kMmaS = 4 * U + 1, kMmaPV = 4 * U + 2;
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t bar0 = smem_u32(bars);
+  const uint32_t q_full = bar0;
+  auto blob_full = [&](int st) { return bar0 + 8u * (1 + st); };
+  auto blob_empty = [&](int st) { return bar0 + 8u * (1 + C::NS + st); };
+  auto s_full = [&](int u) { return bar0 + 8u * (1 + 2 * C::NS + u); };
+  auto s_free = [&](int u) { return bar0 + 8u * (1 + 2 * C::NS + U + u); };
+  auto p_full = [&](int u, int par) { return bar0 + 8u * (1 + 2 * C::NS + 2 * U + 2 * u + par); };
+  auto pv_done = [&](int u, int par) { return bar0 + 8u * (1 + 2 * C::NS + 4 * U + 2 * u + par); };
+  const uint32_t drain_s = bar0 + 8u * (kBars - 2), drain_pv = bar0 + 8u * (kBars - 1);
+  auto warp_wait = [&](uint32_t bar, uint32_t parity) -> bool {
+    if (__all_sync(0xffffffffu, mbar_test_wait(bar, parity))) return true;
+    const bool okl = mbar_wait(bar, parity, &abort_flag, p.err);
+    return __all_sync(0xffffffffu, okl);
+  };
+
+  // the units: blocks grp*U + u of this head; the common tile order ends at T_max
+  const int blk_last = min(nblk, (grp + 1) * U) - 1;
+  const int last_row = min(R, (blk_last + 1) * kBlockRows) - 1;
+  const int t_hi = s.causal ? min(T - 1, (last_row / G + off) / kTile) : T - 1;
+  const int n = t_hi + 1;
+  auto tile_of = [&](int i) { return i == 0 ? 0 : t_hi + 1 - i; };
+
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    for (int i = 0; i < kBars; ++i) {
+      const int j = i - (1 + 2 * C::NS);
+      uint32_t count = 1;
+      if (j >= U && j < 4 * U) count = 4;           // s_free, p_full: the unit's four warps
+      if (i >= 1 + C::NS && i < 1 + 2 * C::NS) count = 2;  // blob_empty: both issuers
+      mbar_init(bar0 + 8u * i, count);
+    }
+    fence_mbar_init();
+  }
+  if (warp == kMmaS) {
+    tmem_alloc(smem_u32(&tmem_slot), C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+
+  if (warp == kProd) {
+    // ------------------------------------------------------------ bulk-copy producer
+    if (lane == 0) {
+      uint32_t qbytes = 0;
+      for (int u = 0; u < U; ++u)
+        if (grp * U + u < nblk) qbytes += C::kQBlob;
+      mbar_arrive_expect_tx(q_full, qbytes);
+      for (int u = 0; u < U; ++u)
+        if (grp * U + u < nblk)
+          bulk_g2s(sbase + u * C::kQStride, p.q_blob + ((size_t)bh * nblk + grp * U + u) * C::kQBlob, C::kQBlob,
+                   q_full);
+      int issued = 0;
+      for (int i = 0; i < n; ++i) {
+        const int st = i % C::NS;
+        if (i >= C::NS && !mbar_wait(blob_empty(st), ((i / C::NS) - 1) & 1, &abort_flag, p.err)) break;
+        mbar_arrive_expect_tx(blob_full(st), C::kBlob);
+        bulk_g2s(sbase + C::kStageOff + st * C::kBlob, p.kv_blob + ((size_t)bh * T + tile_of(i)) * C::kBlob,
+                 C::kBlob, blob_full(st));
+        issued = i + 1;
+      }
+      if (abort_flag) {
+        wait_bounded(q_full, 0, p.err);
+        for (int i = max(0, issued - C::NS); i < issued; ++i) wait_bounded(blob_full(i % C::NS), (i / C::NS) & 1, p.err);
+      }
+    }
+  } else if (warp == kMmaS) {
+    // ------------------------------------------------------------ S issuer
+    if (lane == 0) {
+      const uint32_t idS = idesc_nvf4(128, 64);
+      bool ok = mbar_wait(q_full, 0, &abort_flag, p.err);
+      if (ok) {
+        tc_fence_after();
+        for (int u = 0; u < U; ++u)
+#pragma unroll
+          for (int a = 0; a < D / 64; ++a)
+            tmem_cp_32x128b_x4(tmem + C::kSFQ + 4 * ((D / 64) * u + a),
+                               smem_desc(sbase + u * C::kQStride + qblob_sf(D) + 512 * a, 128, 128, 0));
+      }
+      for (int i = 0; ok && i < n; ++i) {
+        const int st = i % C::NS;
+        const uint32_t blob = sbase + C::kStageOff + st * C::kBlob;
+        const uint32_t sfk = tmem + C::kSFK + C::kSfc * (i & 1);
+        for (int u = 0; ok && u < U; ++u) {
+          // S(u, i) once the previous user of the S buffer has read it out
+          if (u > 0) {
+            if (!(ok = mbar_wait(s_free(u - 1), i & 1, &abort_flag, p.err))) break;
+          } else {
+            if (!(ok = mbar_wait(blob_full(st), (i / C::NS) & 1, &abort_flag, p.err))) break;
+            if (i > 0 && !(ok = mbar_wait(s_free(U - 1), (i - 1) & 1, &abort_flag, p.err))) break;
+            tc_fence_after();
+            // K scales of tile i; their buffer was last read by S(*, i-2), which the units have read out
+#pragma unroll
+            for (int c = 0; c < sf_chunks(D); ++c)
+              tmem_cp_32x128b_x4(sfk + 4 * c, smem_desc(blob + blob_ksf(D) + 512 * c, 128, 128, 0));
+          }
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < D / 64; ++kk) {
+            const uint64_t ad = smem_desc(sbase + u * C::kQStride + 256 * kk, 128, 4 * D, 0);
+            const uint64_t bd = smem_desc(blob + blob_kcodes(D) + 256 * kk, 128, 4 * D, 0);
+            mma_nvf4(tmem + C::kS, ad, bd, idS, tmem + C::kSFQ + 4 * ((D / 64) * u + kk),
+                     sfk + 4 * (kk >> 1) + 2 * (kk & 1), kk > 0);
+          }
+          mma_commit(s_full(u));
+        }
+        if (ok) mma_commit(blob_empty(st));
+      }
+      mma_commit(drain_s);
+      wait_bounded(drain_s, 0, p.err);
+    }
+  } else if (warp == kMmaPV) {
+    // ------------------------------------------------------------ PV issuer and hot lists
+    if (lane == 0) {
+      const uint32_t idO = idesc_nvf4(128, D);
+      uint32_t count[U], pv_issued[U];
+      for (int u = 0; u < U; ++u) count[u] = pv_issued[u] = 0;
+      bool ok = true;
+      for (int i = 0; ok && i < n; ++i) {
+        const int st = i % C::NS;
+        const uint32_t blob = sbase + C::kStageOff + st * C::kBlob;
+        const uint32_t sfv = tmem + C::kSFV + C::kSfc * (i & 1);
+        for (int u = 0; ok && u < U; ++u) {
+          if (!(ok = mbar_wait(p_full(u, i & 1), (i >> 1) & 1, &abort_flag, p.err))) break;
+          if (u == 0) {
+            // V scales of tile i; their buffer was last read by PV(*, i-2), covered by the
+            // commit of pv_done(U-1, i-2)
+            if (!(ok = mbar_wait(blob_full(st), (i / C::NS) & 1, &abort_flag, p.err))) break;
+            if (i >= 2 && !(ok = mbar_wait(pv_done(U - 1, i & 1), ((i - 2) >> 1) & 1, &abort_flag, p.err))) break;
+            tc_fence_after();
+#pragma unroll
+            for (int c = 0; c < sf_chunks(D); ++c)
+              tmem_cp_32x128b_x4(sfv + 4 * c, smem_desc(blob + blob_vsf(D) + 512 * c, 128, 128, 0));
+          }
+          tc_fence_after();
+          const int blk = grp * U + u;
+          if (blk < nblk) {
+            const int nvg = (min(R, (blk + 1) * kBlockRows) - blk * kBlockRows + kGroupRows - 1) / kGroupRows;
+            const uint32_t invalid = 0xFFu & ~((1u << nvg) - 1u);
+            const uint32_t hot = gbits[u][i & 1][0] | gbits[u][i & 1][1] | gbits[u][i & 1][2] | gbits[u][i & 1][3];
+            if (hot) p.hot_list[((size_t)bh * nblk + blk) * T + count[u]++] = (uint32_t)tile_of(i) | (hot << 16);
+            if ((hot | invalid) != 0xFFu) {
+              // P buffer (u, i % 2) and its TMEM scales were last read by PV(u, i-2); unit u
+              // waited for it before writing P(u, i)
+              const int pb = 2 * u + (i & 1);
+              tmem_cp_32x128b_x4(tmem + C::kSFP + 4 * pb, smem_desc(sbase + C::kPsfOff + 512 * pb, 128, 128, 0));
+              mma_nvf4(tmem + D * u, smem_desc(sbase + C::kPOff + 4096 * pb, 128, 256, 0),
+                       smem_desc(blob + blob_vcodes(D), 128, 256, 0), idO, tmem + C::kSFP + 4 * pb, sfv,
+                       pv_issued[u] > 0);
+              ++pv_issued[u];
+            }
+          }
+          mma_commit(pv_done(u, i & 1));
+        }
+        if (ok) mma_commit(blob_empty(st));
+      }
+      for (int u = 0; u < U; ++u)
+        if (grp * U + u < nblk) p.hot_count[(size_t)bh * nblk + grp * U + u] = count[u];
+      mma_commit(drain_pv);
+      wait_bounded(drain_pv, 0, p.err);
+    }
+  } else {
+    // ------------------------------------------------------------ one thread per row of unit u
+    const int u = warp >> 2, qw = warp & 3;
+    const int blk = grp * U + u;
+    const int r = qw * 32 + lane, P = blk * kBlockRows + r;
+    const bool valid = blk < nblk && P < R;
+    const int pos = valid ? P / G : 0;
+    const int hq = h * G + (valid ? P % G : 0);
+    const float cs = p.s_q[b * s.Hq + hq] * p.s_k[bh] * (kLog2e * rsqrtf((float)D));
+    const int vis_last = s.causal ? pos + off : s.Nkv - 1;
+    const uint32_t lane_base = (uint32_t)(qw * 32) << 16;
+    const uint32_t tO = tmem + lane_base + D * u;
+    const float eps = p.eps;
+    const bool eps_inf = isinf(eps);
+    const int ngroups = s.ngroups(), nwords = (T + 31) / 32;
+    float m = -INFINITY, lam = 0.f, l = 0.f;
+    bool ok = true;
+    for (int i = 0; ok && i < n; ++i) {
+      const int t = tile_of(i), j0 = t * kTile;
+      const int nvis = valid ? min(kTile, vis_last + 1 - j0) : 0;
+      if (!(ok = warp_wait(s_full(u), i & 1))) break;
+      tc_fence_after();
+      uint32_t sr[64];
+      tmem_ld_x32(tmem + lane_base + C::kS, sr);
+      tmem_ld_x32(tmem + lane_base + C::kS + 32, sr + 32);
+      tmem_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(s_free(u));
+      float raw[64];
+#pragma unroll
+      for (int j = 0; j < 64; ++j) raw[j] = __uint_as_float(sr[j]);
+      if (__any_sync(0xffffffffu, nvis < kTile)) {
+#pragma unroll
+        for (int j = 0; j < 64; ++j)
+          if (j >= nvis) raw[j] = -INFINITY;
+      }
+      float g[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        float a = max3(raw[16 * k], raw[16 * k + 1], raw[16 * k + 2]);
+#pragma unroll
+        for (int j = 3; j < 15; j += 2) a = max3(a, raw[16 * k + j], raw[16 * k + j + 1]);
+        g[k] = fmaxf(a, raw[16 * k + 15]);
+      }
+      const float c = fmaxf(fmaxf(g[0], g[1]), fmaxf(g[2], g[3])) * cs;  // tile max, log2 units
+      const bool empty = (c == -INFINITY);
+      const float mt = (c > m + kTau) ? c : m;  // candidate frame (lazy maximum)
+      uint32_t pw[8];
+      uint32_t sfw = 0x08080808u;  // 2^-6 where nothing is visible
+      float ell = 0.f;             // l_t: exact sum of the quantized P of this row
+      if (!empty) {
+        sfw = 0;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          uint32_t sc = cvt_ue4m3(ex2_approx(fmaf(g[k], cs, -mt)) * (1.f / 6.f));
+          sc = max(sc, 8u);  // clamp the group scale at 2^-6
+          sfw |= sc << (8 * k);
+          const float scv = ue4m3_value(sc);
+          const float nb = -(mt + lg2_approx(scv));
+#pragma unroll
+          for (int w = 0; w < 2; ++w) pw[2 * k + w] = encode8(raw + 16 * k + 8 * w, cs, nb);
+          ell = fmaf((float)(code_sum2(pw[2 * k]) + code_sum2(pw[2 * k + 1])), 0.5f * scv, ell);
+        }
+      } else {
+#pragma unroll
+        for (int w = 0; w < 8; ++w) pw[w] = 0u;
+      }
+      // hot test: l_t (in the committed frame) > eps * lambda
+      const bool lift = !empty && mt != m;
+      const bool lifted = __any_sync(0xffffffffu, lift);
+      const float thr = eps == 0.f ? -1.f : eps * lam;
+      bool vote;
+      if (!lifted) vote = valid && !empty && ell > thr;
+      else vote = valid && !empty && !eps_inf &&
+                  ((m == -INFINITY) ? (eps == 0.f || ell > 0.f) : (ell * ex2_approx(mt - m) > thr));
+      const uint32_t bal = __ballot_sync(0xffffffffu, vote);
+      const bool hot_lo = (bal & 0x0000FFFFu) != 0, hot_hi = (bal & 0xFFFF0000u) != 0;
+      const bool hot = lane < 16 ? hot_lo : hot_hi;
+      if (!lifted) {
+        if (!empty) {
+          lam += ell;
+          if (!hot) l += ell;
+        }
+      } else {
+        bool rescale = false;
+        float f = 1.f;
+        if (!empty) {
+          const float l_before = l;
+          float mn;
+          if (hot) {
+            mn = fmaxf(m, c - kColdOffset);
+            f = (m == -INFINITY) ? 0.f : ex2_approx(m - mn);
+            lam = lam * f + ell * ex2_approx(mt - mn);
+            l *= f;
+          } else {
+            mn = mt;
+            f = (m == -INFINITY) ? 0.f : ex2_approx(m - mn);
+            lam = lam * f + ell;
+            l = l * f + ell;
+          }
+          rescale = (f != 1.f) && (l_before > 0.f);
+          m = mn;
+        }
+        if (__any_sync(0xffffffffu, rescale)) {
+          // O must not be touched before PV(u, i-1) has landed
+          if (!(ok = warp_wait(pv_done(u, (i - 1) & 1), ((i - 1) >> 1) & 1))) break;
+          tc_fence_after();
+          const float fr = rescale ? f : 1.f;
+#pragma unroll 1
+          for (int c0 = 0; c0 < D; c0 += 32) {
+            uint32_t o[32];
+            tmem_ld_x32(tO + c0, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * fr);
+            tmem_st_x16(tO + c0, o);
+            tmem_st_x16(tO + c0 + 16, o + 16);
+          }
+          tmem_wait_st();
+        }
+      }
+      // P buffer (u, i % 2) was last read by PV(u, i-2).  A hot group's scales are zero.
+      if (i >= 2 && !(ok = warp_wait(pv_done(u, i & 1), ((i - 2) >> 1) & 1))) break;
+      const int pbuf = 2 * u + (i & 1);
+      uint8_t* pbp = smem + C::kPOff + 4096 * pbuf + (r >> 3) * 256 + (r & 7) * 16;
+      *reinterpret_cast<uint4*>(pbp) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
+      *reinterpret_cast<uint4*>(pbp + 128) = make_uint4(pw[4], pw[5], pw[6], pw[7]);
+      *reinterpret_cast<uint32_t*>(smem + C::kPsfOff + 512 * pbuf + sf_atom_off(r, 0)) = hot ? 0u : sfw;
+      if (lane == 0) gbits[u][i & 1][qw] = ((uint32_t)hot_lo << (2 * qw)) | ((uint32_t)hot_hi << (2 * qw + 1));
+      if (p.hot_mask && (lane == 0 || lane == 16) && hot) {
+        const int gi = (blk * kBlockRows + 32 * qw + lane) / kGroupRows;
+        if (gi < ngroups) atomicOr(&p.hot_mask[((size_t)bh * ngroups + gi) * nwords + t / 32], 1u << (t % 32));
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(p_full(u, i & 1));
+    }
+    // ---- epilogue: the pass-1 state (o scaled by s_v, frame m, cold sum l)
+    if (ok && n > 0) ok = warp_wait(pv_done(u, (n - 1) & 1), ((n - 1) >> 1) & 1);
+    tc_fence_after();
+    if (ok && blk < nblk) {
+      const float sv = p.s_v[bh];
+      float* orow = p.state_o + ((size_t)bh * nblk * kBlockRows + P) * D;
+#pragma unroll 1
+      for (int c0 = 0; c0 < D; c0 += 32) {
+        uint32_t o[32];
+        tmem_ld_x32(tO + c0, o);
+        tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 32; j += 4)
+          *reinterpret_cast<float4*>(orow + c0 + j) =
+              l > 0.f ? make_float4(__uint_as_float(o[j]) * sv, __uint_as_float(o[j + 1]) * sv,
+                                    __uint_as_float(o[j + 2]) * sv, __uint_as_float(o[j + 3]) * sv)
+                      : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+      p.state_ml[(size_t)bh * nblk * kBlockRows + P] = make_float2(m, l);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaS) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+template <int D, int U>
+cudaError_t launch_multi(const P1Params& prm, cudaStream_t st) {
+  using C = P1MCfg<D, U>;
+  cudaError_t e = cudaFuncSetAttribute(pass1_multi_kernel<D, U>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+  if (e) return e;
+  const int ngrp = (prm.s.nblk() + U - 1) / U;
+  pass1_multi_kernel<D, U><<<prm.s.BH() * ngrp, C::kThreads, C::kSmem, st>>>(prm);
+  return cudaGetLastError();
+}
+
 template <int D, bool kOnesMma>
 cudaError_t launch_dv(const P1Params& prm, cudaStream_t st) {
   const int smem = P1Cfg<D>::kSmem;
@@ -727,9 +1125,22 @@ bool rowsum_by_mma() {
   return v;
 }
 
+// APA_PASS1_UNITS=1 selects the one-block-per-CTA kernel at d <= 128 (for comparison).
+bool single_unit() {
+  static const bool v = [] {
+    const char* e = getenv("APA_PASS1_UNITS");
+    return e && strcmp(e, "1") == 0;
+  }();
+  return v;
+}
+
 template <int D>
 cudaError_t launch_d(const P1Params& prm, cudaStream_t st) {
-  return rowsum_by_mma() ? launch_dv<D, true>(prm, st) : launch_dv<D, false>(prm, st);
+  if (rowsum_by_mma()) return launch_dv<D, true>(prm, st);
+  if constexpr (D <= 128) {
+    if (!single_unit()) return launch_multi<D, 3>(prm, st);
+  }
+  return launch_dv<D, false>(prm, st);
 }
 
 }  // namespace
