@@ -851,10 +851,10 @@ __global__ void __launch_bounds__(P1MCfg<D, U>::kThreads, 1) pass1_multi_kernel(
         for (int u = 0; ok && u < U; ++u) {
           // S(u, i) once the previous user of the S buffer has read it out
           if (u > 0) {
-            if (!(ok = mbar_wait(s_free(u - 1), i & 1, &abort_flag, p.err))) break;
+            if (!(ok = mbar_spin_wait(s_free(u - 1), i & 1, &abort_flag, p.err))) break;
           } else {
             if (!(ok = mbar_wait(blob_full(st), (i / C::NS) & 1, &abort_flag, p.err))) break;
-            if (i > 0 && !(ok = mbar_wait(s_free(U - 1), (i - 1) & 1, &abort_flag, p.err))) break;
+            if (i > 0 && !(ok = mbar_spin_wait(s_free(U - 1), (i - 1) & 1, &abort_flag, p.err))) break;
             tc_fence_after();
             // K scales of tile i; their buffer was last read by S(*, i-2), which the units have read out
 #pragma unroll

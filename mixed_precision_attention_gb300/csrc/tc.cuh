@@ -77,6 +77,24 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   }
 }
 
+// The same wait as a tight test_wait loop with no suspension, for a single
+// issuing thread whose wake-up latency is on the critical path.
+__device__ __forceinline__ bool mbar_spin_wait(uint32_t bar, uint32_t parity, volatile int* abort, int* err) {
+  if (mbar_test_wait(bar, parity)) return true;
+  const unsigned long long t0 = clock64();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_test_wait(bar, parity)) return true;
+    if ((it & 63) == 0) {
+      if (*abort) return false;
+      if (clock64() - t0 > APA_WAIT_LIMIT_CYCLES) {
+        *abort = 1;
+        if (err) atomicCAS(err, 0, APA_DEVERR_TIMEOUT);
+        return false;
+      }
+    }
+  }
+}
+
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
