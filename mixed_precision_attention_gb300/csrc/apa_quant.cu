@@ -16,12 +16,14 @@
 // range sums in ascending order; divided by Nkv in FP64 and rounded to FP32.
 //
 // Kernels:
-//   stats_kernel     K/V tiles: per-tile FP32 key sums, per-channel min/max of K
-//                    (atomics on an order-preserving encoding: exact, so order-free),
-//                    max |V|; Q rows: max |Q| per query head.
-//   finalize_kernel  per (b, KV head, 32 channels): mu and the head's max |k - mu|.
-//   quant_kernel     FP32 head scales from the maxima; K/V tiles -> blobs;
-//                    128-row Q blocks (GQA-packed) -> Q blobs.
+//   stats_kernel     K/V tiles (bulk-copied to shared memory): per-tile FP32 key
+//                    sums, per-channel min/max of K (atomics on an order-preserving
+//                    encoding: exact, so order-free), max |V|; Q rows: max |Q| per
+//                    query head.
+//   finalize_kernel  per (b, KV head, 8 channels): mu and the head's max |k - mu|.
+//   quant_kernel     FP32 head scales from the maxima; K/V tiles (bulk-copied) ->
+//                    blobs and 128-row Q blocks (GQA-packed) -> Q blobs, each
+//                    assembled in shared memory and written with 16-byte stores.
 #include "apa_internal.h"
 #include "tc.cuh"
 
@@ -68,15 +70,32 @@ __device__ __forceinline__ uint32_t quant16(const float* x, float s, uint2* code
   return sb;
 }
 
-// Loads rows [j0, j0 + nk) of a [rows, d] bf16 slice into smem (zero-filled to 64 rows).
-__device__ __forceinline__ void load_tile(uint16_t* sm, const uint16_t* g, int nk, int d) {
-  const int chunks = kTile * d / 8;  // 16-byte chunks
-  for (int i = threadIdx.x; i < chunks; i += blockDim.x) {
-    const int row = i / (d / 8);
-    uint4 val = make_uint4(0u, 0u, 0u, 0u);
-    if (row < nk) val = reinterpret_cast<const uint4*>(g)[i];
-    reinterpret_cast<uint4*>(sm)[i] = val;
+// One elected thread brings rows [j0, j0 + nk) of the K and V slices of a tile
+// into shared memory with two bulk copies (rows are 2d bytes, a multiple of 16;
+// the slices start on 16-byte boundaries).  Every thread then waits, bounded;
+// false if the wait gave up (the error word is set).
+__device__ __forceinline__ bool load_kv_tile(uint16_t* ks, uint16_t* vs, const uint16_t* k, const uint16_t* v,
+                                             int nk, int d, uint64_t* bar, int* err) {
+  const uint32_t b = smem_u32(bar);
+  if (threadIdx.x == 0) {
+    mbar_init(b, 1);
+    fence_mbar_init();
   }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const uint32_t bytes = (uint32_t)nk * d * 2;
+    mbar_arrive_expect_tx(b, 2 * bytes);
+    bulk_g2s(smem_u32(ks), k, bytes, b);
+    bulk_g2s(smem_u32(vs), v, bytes, b);
+  }
+  const unsigned long long t0 = clock64();
+  while (!mbar_try_wait(b, 0)) {
+    if (clock64() - t0 > APA_WAIT_LIMIT_CYCLES) {
+      if (err) atomicCAS(err, 0, APA_DEVERR_TIMEOUT);
+      return false;
+    }
+  }
+  return true;
 }
 
 __device__ __forceinline__ float block_max(float v, float* red) {
@@ -93,49 +112,46 @@ __device__ __forceinline__ float block_max(float v, float* red) {
   return v;  // valid in warp 0
 }
 
+__device__ __forceinline__ float absmax8(uint4 val) {
+  const uint32_t w[4] = {val.x, val.y, val.z, val.w};
+  float m = 0.f;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) m = fmaxf(m, fmaxf(fabsf(bf16f(w[e] & 0xFFFF)), fabsf(bf16f(w[e] >> 16))));
+  return m;
+}
+
 __global__ void __launch_bounds__(kThreads) stats_kernel(Shape s, const uint16_t* __restrict__ q,
                                                           const uint16_t* __restrict__ k,
                                                           const uint16_t* __restrict__ v, Workspace ws,
-                                                          int n_kv_blocks, int q_rows_per_block, int do_kv) {
-  extern __shared__ __align__(16) uint8_t smem[];
+                                                          int n_kv_blocks, int q_rows_per_block, int do_kv,
+                                                          int* err) {
+  extern __shared__ __align__(128) uint8_t smem[];
   __shared__ float red[32];
+  __shared__ __align__(8) uint64_t bar;
   const int d = s.d, T = s.T();
   if (do_kv && (int)blockIdx.x < n_kv_blocks) {
     const int bh = blockIdx.x / T, t = blockIdx.x % T;
     const int j0 = t * kTile, nk = min(kTile, s.Nkv - j0);
     const size_t base = ((size_t)bh * s.Nkv + j0) * d;
+    uint16_t* ks = reinterpret_cast<uint16_t*>(smem);
+    uint16_t* vs = ks + kTile * d;
+    if (!load_kv_tile(ks, vs, k + base, v + base, nk, d, &bar, err)) return;
     // max |V| over the tile
     float vm = 0.f;
-    for (int i = threadIdx.x; i < nk * d / 8; i += blockDim.x) {
-      const uint4 val = reinterpret_cast<const uint4*>(v + base)[i];
-      const uint32_t w[4] = {val.x, val.y, val.z, val.w};
-#pragma unroll
-      for (int e = 0; e < 4; ++e) vm = fmaxf(vm, fmaxf(fabsf(bf16f(w[e] & 0xFFFF)), fabsf(bf16f(w[e] >> 16))));
-    }
-    // per channel pair: FP32 sum over the tile's keys in ascending order, min, max
-    // (the tile is staged in shared memory by all threads with 16-byte loads)
-    uint16_t* ks = reinterpret_cast<uint16_t*>(smem);
-    load_tile(ks, k + base, nk, d);
-    __syncthreads();
-    for (int cp = threadIdx.x; cp < d / 2; cp += blockDim.x) {
-      const uint32_t* col = reinterpret_cast<const uint32_t*>(ks) + cp;
-      float acc0 = 0.f, acc1 = 0.f, mn0 = INFINITY, mn1 = INFINITY, mx0 = -INFINITY, mx1 = -INFINITY;
+    for (int i = threadIdx.x; i < nk * d / 8; i += blockDim.x) vm = fmaxf(vm, absmax8(reinterpret_cast<const uint4*>(vs)[i]));
+    // per channel: FP32 sum over the tile's keys in ascending order, min, max
+    for (int c = threadIdx.x; c < d; c += blockDim.x) {
+      float acc = 0.f, mn = INFINITY, mx = -INFINITY;
+#pragma unroll 8
       for (int j = 0; j < nk; ++j) {
-        const uint32_t w = col[j * (d / 2)];
-        const float x0 = bf16f(w & 0xFFFF), x1 = bf16f(w >> 16);
-        acc0 = __fadd_rn(acc0, x0);
-        acc1 = __fadd_rn(acc1, x1);
-        mn0 = fminf(mn0, x0);
-        mx0 = fmaxf(mx0, x0);
-        mn1 = fminf(mn1, x1);
-        mx1 = fmaxf(mx1, x1);
+        const float x = bf16f(ks[j * d + c]);
+        acc = __fadd_rn(acc, x);
+        mn = fminf(mn, x);
+        mx = fmaxf(mx, x);
       }
-      const size_t c = 2 * (size_t)cp;
-      *reinterpret_cast<float2*>(&ws.ksum[((size_t)bh * T + t) * d + c]) = make_float2(acc0, acc1);
-      atomicMin(&ws.kmin[(size_t)bh * d + c], ord_enc(mn0));
-      atomicMax(&ws.kmax[(size_t)bh * d + c], ord_enc(mx0));
-      atomicMin(&ws.kmin[(size_t)bh * d + c + 1], ord_enc(mn1));
-      atomicMax(&ws.kmax[(size_t)bh * d + c + 1], ord_enc(mx1));
+      ws.ksum[((size_t)bh * T + t) * d + c] = acc;
+      atomicMin(&ws.kmin[(size_t)bh * d + c], ord_enc(mn));
+      atomicMax(&ws.kmax[(size_t)bh * d + c], ord_enc(mx));
     }
     vm = block_max(vm, red);
     if (threadIdx.x == 0) atomicMax(&ws.vamax[bh], __float_as_uint(vm));
@@ -148,34 +164,31 @@ __global__ void __launch_bounds__(kThreads) stats_kernel(Shape s, const uint16_t
   const int r0 = ch * q_rows_per_block, nr = min(q_rows_per_block, s.Nq - r0);
   const uint4* src = reinterpret_cast<const uint4*>(q + ((size_t)bhq * s.Nq + r0) * d);
   float qm = 0.f;
-  for (int i = threadIdx.x; i < nr * d / 8; i += blockDim.x) {
-    const uint4 val = src[i];
-    const uint32_t w[4] = {val.x, val.y, val.z, val.w};
-#pragma unroll
-    for (int e = 0; e < 4; ++e) qm = fmaxf(qm, fmaxf(fabsf(bf16f(w[e] & 0xFFFF)), fabsf(bf16f(w[e] >> 16))));
-  }
+  for (int i = threadIdx.x; i < nr * d / 8; i += blockDim.x) qm = fmaxf(qm, absmax8(src[i]));
   qm = block_max(qm, red);
   if (threadIdx.x == 0) atomicMax(&ws.qamax[bhq], __float_as_uint(qm));
 }
 
 // Key mean per channel from the tile sums, in the pinned order: FP64 sums over
 // ranges of kMeanRange consecutive tiles (ascending), then the range sums in
-// ascending order.  One block per (b, KV head, 32 channels): 8 lanes per channel
+// ascending order.  One block per (b, KV head, 8 channels): 32 lanes per channel
 // sum different ranges in parallel, one lane per channel adds the range sums.
 // Also the maximum |k - mu| of the head (atomic max on the float bits).
 constexpr int kMeanRange = 64;
 constexpr int kRangesPerPass = 64;
+constexpr int kFinChannels = 8;
 
 __global__ void __launch_bounds__(kThreads) finalize_kernel(Shape s, Workspace ws) {
-  __shared__ double rs[kRangesPerPass][32];
-  const int cblocks = s.d / 32;
-  const int bh = blockIdx.x / cblocks, cl = threadIdx.x & 31, lane8 = threadIdx.x >> 5;
-  const int c = (blockIdx.x % cblocks) * 32 + cl;
+  __shared__ double rs[kRangesPerPass][kFinChannels];
+  const int cblocks = s.d / kFinChannels;
+  const int bh = blockIdx.x / cblocks, cl = threadIdx.x % kFinChannels, lane = threadIdx.x / kFinChannels;
+  constexpr int kLanes = kThreads / kFinChannels;
+  const int c = (blockIdx.x % cblocks) * kFinChannels + cl;
   const int d = s.d, T = s.T(), nR = (T + kMeanRange - 1) / kMeanRange;
   const float* col = ws.ksum + (size_t)bh * T * d + c;
   double S = 0.0;
   for (int r0 = 0; r0 < nR; r0 += kRangesPerPass) {
-    for (int r = r0 + lane8; r < min(nR, r0 + kRangesPerPass); r += 8) {
+    for (int r = r0 + lane; r < min(nR, r0 + kRangesPerPass); r += kLanes) {
       const int t0 = r * kMeanRange, t1 = min(T, t0 + kMeanRange);
       double Sr = 0.0;
       for (int t = t0; t < t1; t += 16) {
@@ -189,37 +202,50 @@ __global__ void __launch_bounds__(kThreads) finalize_kernel(Shape s, Workspace w
       rs[r - r0][cl] = Sr;
     }
     __syncthreads();
-    if (lane8 == 0)
+    if (lane == 0)
       for (int r = 0; r < min(kRangesPerPass, nR - r0); ++r) S += rs[r][cl];
     __syncthreads();
   }
-  if (lane8 == 0) {
+  if (lane == 0) {
     const float mu = __double2float_rn(S / (double)s.Nkv);
     ws.mu[(size_t)bh * d + c] = mu;
     const float mn = ord_dec(ws.kmin[(size_t)bh * d + c]), mx = ord_dec(ws.kmax[(size_t)bh * d + c]);
     float am = fmaxf(fabsf(__fsub_rn(mx, mu)), fabsf(__fsub_rn(mn, mu)));
+    // the kFinChannels lane-0 threads are lanes 0..7 of warp 0
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
+    for (int o = kFinChannels / 2; o > 0; o >>= 1) am = fmaxf(am, __shfl_xor_sync(0x000000FFu, am, o));
     if (cl == 0) atomicMax(&ws.kcamax[bh], __float_as_uint(am));
   }
+}
+
+// Copies a blob image from shared memory to global memory with 16-byte stores.
+__device__ __forceinline__ void store_image(uint8_t* dst, const uint8_t* img, int bytes) {
+  for (int i = threadIdx.x; i < bytes / 16; i += blockDim.x)
+    reinterpret_cast<uint4*>(dst)[i] = reinterpret_cast<const uint4*>(img)[i];
 }
 
 __global__ void __launch_bounds__(kThreads) quant_kernel(Shape s, const uint16_t* __restrict__ q,
                                                           const uint16_t* __restrict__ k,
                                                           const uint16_t* __restrict__ v, Workspace ws,
-                                                          int n_kv_blocks, int do_kv) {
-  extern __shared__ __align__(16) uint8_t smem[];
+                                                          int n_kv_blocks, int do_kv, int* err) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ __align__(8) uint64_t bar;
   const int d = s.d, T = s.T();
   if (do_kv && (int)blockIdx.x < n_kv_blocks) {
     const int bh = blockIdx.x / T, t = blockIdx.x % T;
     const int j0 = t * kTile, nk = min(kTile, s.Nkv - j0);
     uint16_t* ks = reinterpret_cast<uint16_t*>(smem);
     uint16_t* vs = ks + kTile * d;
-    float* mus = reinterpret_cast<float*>(vs + kTile * d);
+    uint8_t* img = reinterpret_cast<uint8_t*>(vs + kTile * d);  // the blob, assembled here
+    float* mus = reinterpret_cast<float*>(img + blob_bytes(d));
     const size_t base = ((size_t)bh * s.Nkv + j0) * d;
-    load_tile(ks, k + base, nk, d);
-    load_tile(vs, v + base, nk, d);
+    // keys past Nkv quantize as zero V; the image starts zeroed (padding included)
+    for (int i = threadIdx.x; i < (kTile - nk) * d / 8; i += blockDim.x)
+      reinterpret_cast<uint4*>(vs + nk * d)[i] = make_uint4(0u, 0u, 0u, 0u);
+    for (int i = threadIdx.x; i < blob_bytes(d) / 16; i += blockDim.x)
+      reinterpret_cast<uint4*>(img)[i] = make_uint4(0u, 0u, 0u, 0u);
     for (int c = threadIdx.x; c < d; c += blockDim.x) mus[c] = ws.mu[(size_t)bh * d + c];
+    if (!load_kv_tile(ks, vs, k + base, v + base, nk, d, &bar, err)) return;
     __syncthreads();
     // FP32 head scales from the head maxima (the head's largest magnitude maps to 2688)
     const float sk = head_scale(__uint_as_float(ws.kcamax[bh])), sv = head_scale(__uint_as_float(ws.vamax[bh]));
@@ -227,7 +253,6 @@ __global__ void __launch_bounds__(kThreads) quant_kernel(Shape s, const uint16_t
       ws.s_k[bh] = sk;
       ws.s_v[bh] = sv;
     }
-    uint8_t* blob = ws.kv_blob + ((size_t)bh * T + t) * blob_bytes(d);
     const int ncb = d / 16;
     // K: per (key n, 16-channel block cb), centred.  blockDim is a multiple of
     // ncb, so each thread keeps one cb and its 16 means in registers.
@@ -236,27 +261,24 @@ __global__ void __launch_bounds__(kThreads) quant_kernel(Shape s, const uint16_t
       float mu16[16];
 #pragma unroll
       for (int i = 0; i < 16; ++i) mu16[i] = mus[cb * 16 + i];
-      for (int n = threadIdx.x / ncb; n < kTile; n += blockDim.x / ncb) {
-        uint2 codes = make_uint2(0u, 0u);
-        uint32_t sb = 0;
-        if (n < nk) {
-          const uint4* src = reinterpret_cast<const uint4*>(ks + n * d + cb * 16);
-          const uint4 a0 = src[0], a1 = src[1];
-          const uint32_t w[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-          float x[16];
+      for (int n = threadIdx.x / ncb; n < nk; n += blockDim.x / ncb) {
+        const uint4* src = reinterpret_cast<const uint4*>(ks + n * d + cb * 16);
+        const uint4 a0 = src[0], a1 = src[1];
+        const uint32_t w[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+        float x[16];
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            x[2 * i] = __fsub_rn(bf16f(w[i] & 0xFFFF), mu16[2 * i]);
-            x[2 * i + 1] = __fsub_rn(bf16f(w[i] >> 16), mu16[2 * i + 1]);
-          }
-          sb = quant16(x, sk, &codes);
+        for (int i = 0; i < 8; ++i) {
+          x[2 * i] = __fsub_rn(bf16f(w[i] & 0xFFFF), mu16[2 * i]);
+          x[2 * i + 1] = __fsub_rn(bf16f(w[i] >> 16), mu16[2 * i + 1]);
         }
-        *reinterpret_cast<uint2*>(blob + blob_kcodes(d) + fp4_kmajor_off(n, cb, d / 2)) = codes;
+        uint2 codes;
+        const uint32_t sb = quant16(x, sk, &codes);
+        *reinterpret_cast<uint2*>(img + blob_kcodes(d) + fp4_kmajor_off(n, cb, d / 2)) = codes;
         const int kb = cb >> 2, k16 = cb & 3;
-        blob[blob_ksf(d) + (kb >> 1) * 512 + (n & 31) * 16 + ((n >> 5) + 2 * (kb & 1)) * 4 + k16] = (uint8_t)sb;
+        img[blob_ksf(d) + (kb >> 1) * 512 + (n & 31) * 16 + ((n >> 5) + 2 * (kb & 1)) * 4 + k16] = (uint8_t)sb;
       }
     }
-    // V^T: per (channel pair, 16-key block kb16); keys past Nkv are zero
+    // V^T: per (channel pair, 16-key block kb16)
     for (int it = threadIdx.x; it < (d / 2) * 4; it += blockDim.x) {
       const int cp = it % (d / 2), kb16 = it / (d / 2);
       float x0[16], x1[16];
@@ -271,10 +293,12 @@ __global__ void __launch_bounds__(kThreads) quant_kernel(Shape s, const uint16_t
         const int c = 2 * cp + e;
         uint2 codes;
         const uint32_t sb = quant16(e ? x1 : x0, sv, &codes);
-        *reinterpret_cast<uint2*>(blob + blob_vcodes(d) + fp4_kmajor_off(c, kb16, 32)) = codes;
-        blob[blob_vsf(d) + (c >> 7) * 512 + sf_atom_off(c & 127, kb16)] = (uint8_t)sb;
+        *reinterpret_cast<uint2*>(img + blob_vcodes(d) + fp4_kmajor_off(c, kb16, 32)) = codes;
+        img[blob_vsf(d) + (c >> 7) * 512 + sf_atom_off(c & 127, kb16)] = (uint8_t)sb;
       }
     }
+    __syncthreads();
+    store_image(ws.kv_blob + ((size_t)bh * T + t) * blob_bytes(d), img, blob_bytes(d));
     return;
   }
   // Q: one 128-row block of packed rows p = pos*G + g
@@ -282,7 +306,7 @@ __global__ void __launch_bounds__(kThreads) quant_kernel(Shape s, const uint16_t
   const int nblk = s.nblk(), G = s.G(), R = s.R();
   const int bh = qb / nblk, blk = qb % nblk;
   const int b = bh / s.Hkv, h = bh % s.Hkv;
-  uint8_t* qblob = ws.q_blob + ((size_t)bh * nblk + blk) * qblob_bytes(d);
+  uint8_t* img = smem;
   if (blk == 0)
     for (int g = threadIdx.x; g < G; g += blockDim.x) {
       const int hq = b * s.Hq + h * G + g;
@@ -306,9 +330,11 @@ __global__ void __launch_bounds__(kThreads) quant_kernel(Shape s, const uint16_t
       }
       sb = quant16(x, head_scale(__uint_as_float(ws.qamax[hq])), &codes);
     }
-    *reinterpret_cast<uint2*>(qblob + fp4_kmajor_off(p, cb, d / 2)) = codes;
-    qblob[qblob_sf(d) + (cb >> 2) * 512 + sf_atom_off(p, cb & 3)] = (uint8_t)sb;
+    *reinterpret_cast<uint2*>(img + fp4_kmajor_off(p, cb, d / 2)) = codes;
+    img[qblob_sf(d) + (cb >> 2) * 512 + sf_atom_off(p, cb & 3)] = (uint8_t)sb;
   }
+  __syncthreads();
+  store_image(ws.q_blob + ((size_t)bh * nblk + blk) * qblob_bytes(d), img, qblob_bytes(d));
 }
 
 }  // namespace
@@ -316,6 +342,7 @@ __global__ void __launch_bounds__(kThreads) quant_kernel(Shape s, const uint16_t
 cudaError_t launch_quantize(const Shape& s, const void* q, const void* k, const void* v, const Workspace& ws,
                             bool do_q, bool do_kv, cudaStream_t st) {
   const int BH = s.BH(), d = s.d, T = s.T();
+  int* err = device_error_word();
   cudaError_t e;
   if (do_kv) {
     if ((e = cudaMemsetAsync(ws.kmin, 0xFF, sizeof(uint32_t) * BH * d, st))) return e;
@@ -327,21 +354,26 @@ cudaError_t launch_quantize(const Shape& s, const void* q, const void* k, const 
   const int n_kv = do_kv ? BH * T : 0;
   const int q_rows = 64;
   const int n_q = do_q ? s.B * s.Hq * ((s.Nq + q_rows - 1) / q_rows) : 0;
-  const size_t sm1 = (size_t)kTile * d * 2;
+  const size_t sm1 = (size_t)kTile * d * 2 * 2;
+  if (sm1 > 48 * 1024 &&
+      (e = cudaFuncSetAttribute(stats_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm1)))
+    return e;
   if (n_kv + n_q > 0)
     stats_kernel<<<n_kv + n_q, kThreads, sm1, st>>>(s, (const uint16_t*)q, (const uint16_t*)k, (const uint16_t*)v, ws,
-                                                    n_kv, q_rows, do_kv);
+                                                    n_kv, q_rows, do_kv, err);
   if ((e = cudaGetLastError())) return e;
   if (do_kv) {
-    finalize_kernel<<<BH * (d / 32), kThreads, 0, st>>>(s, ws);
+    finalize_kernel<<<BH * (d / kFinChannels), kThreads, 0, st>>>(s, ws);
     if ((e = cudaGetLastError())) return e;
   }
   const int n_qb = do_q ? BH * s.nblk() : 0;
-  const size_t sm2 = (size_t)kTile * d * 2 * 2 + d * 4;
-  if (sm2 > 48 * 1024) cudaFuncSetAttribute(quant_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm2);
+  const size_t sm2 = (size_t)kTile * d * 2 * 2 + blob_bytes(d) + d * 4;
+  if (sm2 > 48 * 1024 &&
+      (e = cudaFuncSetAttribute(quant_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm2)))
+    return e;
   if (n_kv + n_qb > 0)
     quant_kernel<<<n_kv + n_qb, kThreads, sm2, st>>>(s, (const uint16_t*)q, (const uint16_t*)k, (const uint16_t*)v,
-                                                     ws, n_kv, do_kv);
+                                                     ws, n_kv, do_kv, err);
   return cudaGetLastError();
 }
 
