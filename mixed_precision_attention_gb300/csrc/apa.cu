@@ -89,6 +89,7 @@ size_t workspace_layout(const Shape& s, bool apa_mode, Workspace* ws, void* base
   w.state_ml = (float2*)take(BH * nblk * kBlockRows * 8);
   w.hot_list = (uint32_t*)take(BH * nblk * T * 4);
   w.hot_count = (uint32_t*)take(BH * nblk * 4);
+  w.v16 = (uint16_t*)take(BH * s.Nkv * d * 2);
   if (ws) *ws = w;
   return off;
 }

@@ -10,6 +10,7 @@
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <cstring>
 
 namespace apa {
 
@@ -79,6 +80,7 @@ struct Workspace {
   float* s_q;         // [B*Hq]
   uint8_t* kv_blob;   // [BH][T][blob_bytes(d)]
   uint8_t* q_blob;    // [BH][nblk][qblob_bytes(d)]
+  uint16_t* v16;      // [BH][Nkv][d] FP16 copy of V / v16_scale(max |v|) for pass 2, or null
   // pass 1 -> pass 2
   float* state_o;     // [BH][nblk*128][d]: pass-1 o (scaled by s_v)
   float2* state_ml;   // [BH][nblk*128]: pass-1 frame m and cold sum l
@@ -86,6 +88,23 @@ struct Workspace {
   uint32_t* hot_count;// [BH*nblk]
 };
 size_t workspace_layout(const Shape& s, bool apa_mode, Workspace* ws, void* base);
+
+// Power-of-two divisor that brings a head's V into FP16 range: 1 when max |v| is
+// at most 2^15, else 2^(e - 14) for max |v| in [2^e, 2^(e+1)).  Dividing by it is
+// exact, so the FP16 copy holds every bf16 value of V exactly except those below
+// 2^-17 times the divisor (FP16 subnormals), which round to a multiple of 2^-24.
+__host__ __device__ inline float v16_scale(float vamax) {
+  int e = 0;
+  if (vamax > 32768.f) {
+    uint32_t bits;
+    memcpy(&bits, &vamax, 4);
+    e = (int)((bits >> 23) & 0xFF) - 127 - 14;
+  }
+  uint32_t sb = (uint32_t)(127 + e) << 23;
+  float sc;
+  memcpy(&sc, &sb, 4);
+  return sc;
+}
 
 int* device_error_word();  // library-wide device error word (set by bounded waits)
 

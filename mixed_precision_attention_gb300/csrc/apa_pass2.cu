@@ -24,6 +24,7 @@
 // two BF16 terms, P = P_hi + P_lo (P_lo the BF16 rounding of the residual), so
 // the PV product and the row sum carry ~16 mantissa bits of P instead of 8.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "apa_internal.h"
 #include "tc.cuh"
@@ -40,6 +41,7 @@ struct P2Params {
   const float2* state_ml;     // pass-1 (m, l) [BH][nblk*128] or null
   const uint32_t* hot_list;   // [BH*nblk][T] or null (all visible tiles)
   const uint32_t* hot_count;  // [BH*nblk] or null
+  const uint32_t* vamax;      // [BH] max |v| (float bits): the FP16 V copy's scale, or null
   float* out;                 // [B,Hq,Nq,d]
   float* lse;                 // [B,Hq,Nq] or null
   int* err;
@@ -48,18 +50,21 @@ struct P2Params {
 constexpr int kThreads = 192;
 constexpr float kTau2 = 8.0f;  // pass-2 lazy rescale threshold (log2 units)
 
-template <int D>
+// kF16: P as one FP16 term against the FP16 copy of V; else P = P_hi + P_lo in
+// BF16 against V itself.
+template <int D, bool kF16>
 struct P2Cfg {
   static constexpr int NS = D >= 256 ? 2 : 3;
   static constexpr int kAtoms = D / 64;
   static constexpr int kQBytes = 128 * D * 2;
   static constexpr int kKVBytes = 64 * D * 2;  // one of K or V per stage
-  static constexpr int kPBytes = 128 * 64 * 2;  // one BF16 term of P
-  static constexpr int NP = D >= 256 ? 1 : 2;    // P buffers (each holds P_hi and P_lo)
+  static constexpr int kPBytes = 128 * 64 * 2;  // one 16-bit term of P
+  static constexpr int kPTerms = kF16 ? 1 : 2;
+  static constexpr int NP = D >= 256 ? 1 : 2;   // P buffers (each holds kPTerms terms)
   static constexpr int kQOff = 0;
   static constexpr int kStageOff = kQBytes;
   static constexpr int kPOff = kStageOff + NS * 2 * kKVBytes;
-  static constexpr int kSmem = kPOff + NP * 2 * kPBytes + 1024;  // + alignment slack
+  static constexpr int kSmem = kPOff + NP * kPTerms * kPBytes + 1024;  // + alignment slack
   static constexpr uint32_t kTmemCols = D + 128 <= 256 ? 256 : 512;
   static constexpr uint32_t kOCol = 0, kSCol = D;
 };
@@ -75,10 +80,10 @@ __device__ __forceinline__ void wait_bounded(uint32_t bar, uint32_t parity, int*
   }
 }
 
-template <int D>
+template <int D, bool kF16>
 __global__ void __launch_bounds__(kThreads, 1)
     pass2_kernel(const P2Params p, const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap) {
-  using C = P2Cfg<D>;
+  using C = P2Cfg<D, kF16>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ __align__(8) uint64_t bars[2 * C::NS + 9];
@@ -197,7 +202,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 5) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0 && n > 0) {
-      const uint32_t idS = idesc_bf16(128, 64, 0), idO = idesc_bf16(128, D, 1);
+      const uint32_t idS = idesc_bf16(128, 64, 0), idO = kF16 ? idesc_f16(128, D, 1) : idesc_bf16(128, D, 1);
       auto issue_s = [&](int i) -> bool {
         const int st = i % C::NS;
         if (!mbar_wait(kv_full(st), (i / C::NS) & 1, &abort_flag, p.err)) return false;
@@ -219,13 +224,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!(ok = mbar_wait(p_full(i & 1), (i >> 1) & 1, &abort_flag, p.err))) break;
         tc_fence_after();
         const uint32_t vaddr = sbase + C::kStageOff + (i % C::NS) * 2 * C::kKVBytes + C::kKVBytes;
-        const uint32_t paddr = sbase + C::kPOff + (i % C::NP) * 2 * C::kPBytes;
+        const uint32_t paddr = sbase + C::kPOff + (i % C::NP) * C::kPTerms * C::kPBytes;
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
           const uint64_t bd = smem_desc(vaddr + kk * 2048, 8192, 1024, kSwizzle128B);
           mma_bf16(tmem + C::kOCol, smem_desc(paddr + kk * 32, 16, 1024, kSwizzle128B), bd, idO,
                    (i > 0 || kk > 0) ? 1u : 0u);
-          mma_bf16(tmem + C::kOCol, smem_desc(paddr + C::kPBytes + kk * 32, 16, 1024, kSwizzle128B), bd, idO, 1u);
+          if (!kF16)
+            mma_bf16(tmem + C::kOCol, smem_desc(paddr + C::kPBytes + kk * 32, 16, 1024, kSwizzle128B), bd, idO, 1u);
         }
         mma_commit(pv_done(i & 1));
         mma_commit(kv_empty(i % C::NS));
@@ -254,12 +260,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(s_free(i & 1));
         if (i >= C::NP && !(ok = warp_wait(pv_done((i - C::NP) & 1), ((i - C::NP) >> 1) & 1))) break;
-        uint8_t* prow = smem + C::kPOff + (i % C::NP) * 2 * C::kPBytes + r * 128;
+        uint8_t* prow = smem + C::kPOff + (i % C::NP) * C::kPTerms * C::kPBytes + r * 128;
 #pragma unroll
         for (int ch = 0; ch < 8; ++ch) {
           const int sw = (ch ^ (r & 7)) << 4;  // same swizzled order as the computed rows: no bank conflicts
           *reinterpret_cast<uint4*>(prow + sw) = make_uint4(0u, 0u, 0u, 0u);
-          *reinterpret_cast<uint4*>(prow + C::kPBytes + sw) = make_uint4(0u, 0u, 0u, 0u);
+          if (!kF16) *reinterpret_cast<uint4*>(prow + C::kPBytes + sw) = make_uint4(0u, 0u, 0u, 0u);
         }
         fence_proxy_async_smem();
         __syncwarp();
@@ -292,7 +298,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // this P buffer is free once PV(i - NP) has completed
       if (i >= C::NP && !(ok = warp_wait(pv_done((i - C::NP) & 1), ((i - C::NP) >> 1) & 1))) break;
-      uint8_t* prow = smem + C::kPOff + (i % C::NP) * 2 * C::kPBytes + r * 128;
+      uint8_t* prow = smem + C::kPOff + (i % C::NP) * C::kPTerms * C::kPBytes + r * 128;
       float psum = 0.f;
 #pragma unroll
       for (int ch = 0; ch < 8; ++ch) {
@@ -301,17 +307,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int e = 0; e < 4; ++e) {
           const int j = 8 * ch + 2 * e;
           const float a0 = ex2_approx(sv[j] - m2), a1 = ex2_approx(sv[j + 1] - m2);
-          const __nv_bfloat162 h2 = __floats2bfloat162_rn(a0, a1);
-          const float2 hf = __bfloat1622float2(h2);
-          const __nv_bfloat162 l2v = __floats2bfloat162_rn(a0 - hf.x, a1 - hf.y);
-          const float2 lf = __bfloat1622float2(l2v);
-          psum += (hf.x + lf.x) + (hf.y + lf.y);
-          hi[e] = *reinterpret_cast<const uint32_t*>(&h2);
-          lo[e] = *reinterpret_cast<const uint32_t*>(&l2v);
+          if (kF16) {
+            // the row sum adds the FP16 values the tensor cores see
+            hi[e] = cvt_f16x2(a0, a1);
+            const float2 hf = __half22float2(*reinterpret_cast<const __half2*>(&hi[e]));
+            psum += hf.x + hf.y;
+          } else {
+            const __nv_bfloat162 h2 = __floats2bfloat162_rn(a0, a1);
+            const float2 hf = __bfloat1622float2(h2);
+            const __nv_bfloat162 l2v = __floats2bfloat162_rn(a0 - hf.x, a1 - hf.y);
+            const float2 lf = __bfloat1622float2(l2v);
+            psum += (hf.x + lf.x) + (hf.y + lf.y);
+            hi[e] = *reinterpret_cast<const uint32_t*>(&h2);
+            lo[e] = *reinterpret_cast<const uint32_t*>(&l2v);
+          }
         }
         const int sw = (ch ^ (r & 7)) << 4;
         *reinterpret_cast<uint4*>(prow + sw) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-        *reinterpret_cast<uint4*>(prow + C::kPBytes + sw) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        if (!kF16) *reinterpret_cast<uint4*>(prow + C::kPBytes + sw) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
       }
       l2 = l2 * f + psum;
       if (__any_sync(0xffffffffu, rescale)) {
@@ -354,6 +367,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float w1 = e1 == -INFINITY ? 0.f : exp2f(e1 - M), w2 = e2 == -INFINITY ? 0.f : exp2f(e2 - M);
       const float L = w1 * l1 + w2 * l2;
       const float invL = 1.f / L;
+      const float w2o = kF16 ? w2 * v16_scale(__uint_as_float(p.vamax[bh])) : w2;  // O carries V / scale
       float* orow = p.out + (((size_t)b * s.Hq + hq) * s.Nq + pos) * D;
 #pragma unroll 1
       for (int c0 = 0; c0 < D; c0 += 32) {
@@ -373,7 +387,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               const float a1 = st ? st[c0 + j + e] : 0.f;
-              rr[e] = (w1 * a1 + w2 * __uint_as_float(o[j + e])) * invL;
+              rr[e] = (w1 * a1 + w2o * __uint_as_float(o[j + e])) * invL;
             }
             *reinterpret_cast<float4*>(orow + c0 + j) = res;
           }
@@ -394,7 +408,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-bool make_kv_map(CUtensorMap* map, const void* base, const Shape& s) {
+bool make_kv_map(CUtensorMap* map, const void* base, const Shape& s, CUtensorMapDataType dtype) {
   using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                 const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                 CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
@@ -411,27 +425,36 @@ bool make_kv_map(CUtensorMap* map, const void* base, const Shape& s) {
   const cuuint64_t strides[2] = {(cuuint64_t)s.d * 2, (cuuint64_t)s.Nkv * s.d * 2};
   const cuuint32_t box[3] = {64, 64, 1};
   const cuuint32_t estr[3] = {1, 1, 1};
-  return encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+  return encode(map, dtype, 3, const_cast<void*>(base), dims, strides, box, estr,
                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D>
-cudaError_t launch_d(const P2Params& prm, const CUtensorMap& km, const CUtensorMap& vm, cudaStream_t st) {
-  const int smem = P2Cfg<D>::kSmem;
-  cudaError_t e = cudaFuncSetAttribute(pass2_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+template <int D, bool kF16>
+cudaError_t launch_dv(const P2Params& prm, const CUtensorMap& km, const CUtensorMap& vm, cudaStream_t st) {
+  const int smem = P2Cfg<D, kF16>::kSmem;
+  cudaError_t e = cudaFuncSetAttribute(pass2_kernel<D, kF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e) return e;
   const int grid = prm.s.BH() * prm.s.nblk();
-  pass2_kernel<D><<<grid, kThreads, smem, st>>>(prm, km, vm);
+  pass2_kernel<D, kF16><<<grid, kThreads, smem, st>>>(prm, km, vm);
   return cudaGetLastError();
+}
+template <int D>
+cudaError_t launch_d(const P2Params& prm, const CUtensorMap& km, const CUtensorMap& vm, cudaStream_t st) {
+  return prm.vamax ? launch_dv<D, true>(prm, km, vm, st) : launch_dv<D, false>(prm, km, vm, st);
 }
 
 }  // namespace
 
 cudaError_t launch_pass2(const Shape& s, const void* q, const void* k, const void* v, const Workspace* ws, float* out,
                          float* lse, cudaStream_t st) {
+  // with the FP16 copy of V (APA mode) P goes to the tensor cores as one FP16 term
+  const bool f16 = ws && ws->v16;
   CUtensorMap km, vm;
-  if (!make_kv_map(&km, k, s) || !make_kv_map(&vm, v, s)) return cudaErrorInvalidValue;
+  if (!make_kv_map(&km, k, s, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) ||
+      !make_kv_map(&vm, f16 ? (const void*)ws->v16 : v, s,
+                   f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16))
+    return cudaErrorInvalidValue;
   P2Params prm{};
   prm.s = s;
   prm.q = (const uint16_t*)q;
@@ -440,6 +463,7 @@ cudaError_t launch_pass2(const Shape& s, const void* q, const void* k, const voi
   prm.state_ml = ws ? ws->state_ml : nullptr;
   prm.hot_list = ws ? ws->hot_list : nullptr;
   prm.hot_count = ws ? ws->hot_count : nullptr;
+  prm.vamax = f16 ? ws->vamax : nullptr;
   prm.out = out;
   prm.lse = lse;
   prm.err = device_error_word();

@@ -297,6 +297,19 @@ __global__ void __launch_bounds__(kThreads) quant_kernel(Shape s, const uint16_t
         img[blob_vsf(d) + (c >> 7) * 512 + sf_atom_off(c & 127, kb16)] = (uint8_t)sb;
       }
     }
+    // FP16 copy of the tile's V rows for pass 2, divided by the head's power-of-two scale
+    if (ws.v16) {
+      const float inv = 1.f / v16_scale(__uint_as_float(ws.vamax[bh]));
+      uint4* dst = reinterpret_cast<uint4*>(ws.v16 + base);
+      for (int i = threadIdx.x; i < nk * d / 8; i += blockDim.x) {
+        const uint4 val = reinterpret_cast<const uint4*>(vs)[i];
+        const uint32_t w[4] = {val.x, val.y, val.z, val.w};
+        uint32_t o[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) o[e] = cvt_f16x2(bf16f(w[e] & 0xFFFF) * inv, bf16f(w[e] >> 16) * inv);
+        dst[i] = make_uint4(o[0], o[1], o[2], o[3]);
+      }
+    }
     __syncthreads();
     store_image(ws.kv_blob + ((size_t)bh * T + t) * blob_bytes(d), img, blob_bytes(d));
     return;

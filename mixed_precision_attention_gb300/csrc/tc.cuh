@@ -146,6 +146,22 @@ __host__ __device__ constexpr uint32_t idesc_bf16(uint32_t M, uint32_t N, uint32
          | ((N >> 3) << 17)   // N / 8
          | ((M >> 4) << 24);  // M / 16
 }
+// Instruction descriptor, kind::f16 with F16 A and B and FP32 accumulate.
+__host__ __device__ constexpr uint32_t idesc_f16(uint32_t M, uint32_t N, uint32_t b_mn) {
+  return (1u << 4)            // D format: F32
+         | (0u << 7)          // A format: F16
+         | (0u << 10)         // B format: F16
+         | (0u << 15)         // A K-major
+         | (b_mn << 16)       // B major-ness
+         | ((N >> 3) << 17)   // N / 8
+         | ((M >> 4) << 24);  // M / 16
+}
+// Two FP32 values -> packed FP16x2 (round to nearest even), lo in the low half.
+__device__ __forceinline__ uint32_t cvt_f16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
 // Instruction descriptor, kind::mxf4nvf4 (E2M1 x E2M1, UE4M3 scale per 16 along K).
 __host__ __device__ constexpr uint32_t idesc_nvf4(uint32_t M, uint32_t N) {
   return (1u << 7)            // A format: E2M1
