@@ -314,12 +314,14 @@ def run_gpu(args):
                         "peak_note": f"dense NVFP4 = {pk_kind} sustained bf16 x {FP4_PER_BF16:g} (nominal ratio)",
                         "flops_per_launch": work["F1"], "ms_per_launch": t_p1}
     p2_ach = work["F2"] / (t_p2 * 1e-3) / 1e12 if t_p2 > 0 else 0.0
-    q_bytes = (B * Hq * Nq * d + 2 * B * Hkv * Nkv * d) * (2 + 0.5625)
+    # bf16 Q, K, V read once; E2M1 codes + UE4M3 scales (0.5625 B per element) and
+    # the FP16 copy of V written
+    q_bytes = (B * Hq * Nq * d + 2 * B * Hkv * Nkv * d) * (2 + 0.5625) + B * Hkv * Nkv * d * 2
     line["stages"] = {
         "quantize": {"ms": t_q, "hbm_gbs": q_bytes / (t_q * 1e-3) / 1e9,
                      "hbm_frac": q_bytes / (t_q * 1e-3) / 1e9 / pk["hbm_gbs"]},
         "pass1": {"ms": t_p1, "tflops_fp4": p1_ach, "frac_fp4_peak": p1_ach / fp4_peak},
-        "pass2_merge": {"ms": t_p2, "tflops_bf16": p2_ach, "frac_bf16_peak": p2_ach / bf16_peak},
+        "pass2_merge": {"ms": t_p2, "tflops_16bit": p2_ach, "frac_bf16_peak": p2_ach / bf16_peak},
     }
     line["tensor_roofline_frac"] = (work["F1"] / fp4_peak + work["F2"] / bf16_peak) / 1e12 / (ms * 1e-3)
     line["hot_tile_frac"] = work["hot_frac"]

@@ -52,19 +52,30 @@ constexpr float kTau2 = 8.0f;  // pass-2 lazy rescale threshold (log2 units)
 
 // kF16: P as one FP16 term against the FP16 copy of V; else P = P_hi + P_lo in
 // BF16 against V itself.
+//
+// The barriers live at the end of the dynamic shared-memory window and there is
+// no static shared memory.  With kCtasPerSm = 2 (2 K/V stages, one P buffer,
+// 112 KB per CTA at d = 128) two CTAs would fit an SM with no alignment slack;
+// the kernel then checks that the window starts on a 1024-byte boundary (the
+// 128-byte swizzle needs it).  Measured on the 2048 x 122880 layer, two CTAs of
+// that shape were no faster than one CTA with 3 stages and 2 P buffers.
 template <int D, bool kF16>
 struct P2Cfg {
-  static constexpr int NS = D >= 256 ? 2 : 3;
+  static constexpr int kCtasPerSm = 1;
+  static constexpr int NS = kCtasPerSm == 2 ? 2 : (D >= 256 ? 2 : 3);
   static constexpr int kAtoms = D / 64;
   static constexpr int kQBytes = 128 * D * 2;
   static constexpr int kKVBytes = 64 * D * 2;  // one of K or V per stage
   static constexpr int kPBytes = 128 * 64 * 2;  // one 16-bit term of P
   static constexpr int kPTerms = kF16 ? 1 : 2;
-  static constexpr int NP = D >= 256 ? 1 : 2;   // P buffers (each holds kPTerms terms)
+  static constexpr int NP = kCtasPerSm == 2 ? 1 : (D >= 256 ? 1 : 2);  // P buffers (kPTerms terms each)
   static constexpr int kQOff = 0;
   static constexpr int kStageOff = kQBytes;
   static constexpr int kPOff = kStageOff + NS * 2 * kKVBytes;
-  static constexpr int kSmem = kPOff + NP * kPTerms * kPBytes + 1024;  // + alignment slack
+  static constexpr int kNumBars = 2 * NS + 9;
+  static constexpr int kBarOff = kPOff + NP * kPTerms * kPBytes;
+  static constexpr int kSlack = kCtasPerSm == 2 ? 0 : 1024;  // runtime alignment room
+  static constexpr int kSmem = kBarOff + kNumBars * 8 + 16 + kSlack;
   static constexpr uint32_t kTmemCols = D + 128 <= 256 ? 256 : 512;
   static constexpr uint32_t kOCol = 0, kSCol = D;
 };
@@ -81,14 +92,18 @@ __device__ __forceinline__ void wait_bounded(uint32_t bar, uint32_t parity, int*
 }
 
 template <int D, bool kF16>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, P2Cfg<D, kF16>::kCtasPerSm)
     pass2_kernel(const P2Params p, const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap) {
   using C = P2Cfg<D, kF16>;
-  extern __shared__ uint8_t smem_raw[];
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ __align__(8) uint64_t bars[2 * C::NS + 9];
-  __shared__ uint32_t tmem_slot;
-  __shared__ int abort_flag;
+  if (C::kSlack == 0 && smem != smem_raw) {  // no room to realign: refuse loudly
+    if (threadIdx.x == 0) atomicCAS(p.err, 0, APA_DEVERR_SMEM_ALIGN);
+    return;
+  }
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
+  uint32_t& tmem_slot = *reinterpret_cast<uint32_t*>(smem + C::kBarOff + C::kNumBars * 8);
+  int& abort_flag = *reinterpret_cast<int*>(smem + C::kBarOff + C::kNumBars * 8 + 4);
 
   const Shape& s = p.s;
   const int nblk = s.nblk(), BH = s.BH(), G = s.G(), R = s.R(), T = s.T(), off = s.off();
@@ -131,7 +146,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     abort_flag = 0;
-    for (int i = 0; i < 2 * C::NS + 9; ++i) {
+    for (int i = 0; i < C::kNumBars; ++i) {
       const bool per_warp = (i >= 2 * C::NS + 2 && i < 2 * C::NS + 6);  // s_free, p_full: one arrive per softmax warp
       mbar_init(bar0 + 8u * i, per_warp ? 4u : 1u);
     }
@@ -308,10 +323,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int j = 8 * ch + 2 * e;
           const float a0 = ex2_approx(sv[j] - m2), a1 = ex2_approx(sv[j + 1] - m2);
           if (kF16) {
-            // the row sum adds the FP16 values the tensor cores see
+            // the row sum adds the FP32 values; their FP16 roundings (relative error
+            // at most 2^-11 each) go to the tensor cores
             hi[e] = cvt_f16x2(a0, a1);
-            const float2 hf = __half22float2(*reinterpret_cast<const __half2*>(&hi[e]));
-            psum += hf.x + hf.y;
+            psum += a0 + a1;
           } else {
             const __nv_bfloat162 h2 = __floats2bfloat162_rn(a0, a1);
             const float2 hf = __bfloat1622float2(h2);

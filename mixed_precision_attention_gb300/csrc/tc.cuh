@@ -18,6 +18,7 @@
 // device error codes (written to the library's device error word)
 #define APA_DEVERR_TIMEOUT 1
 #define APA_DEVERR_BOUNDS 2
+#define APA_DEVERR_SMEM_ALIGN 3  // a kernel found its shared-memory window misaligned and did nothing
 
 namespace apa {
 
