@@ -844,31 +844,40 @@ __global__ void __launch_bounds__(P1MCfg<D, U>::kThreads, 1) pass1_multi_kernel(
             tmem_cp_32x128b_x4(tmem + C::kSFQ + 4 * ((D / 64) * u + a),
                                smem_desc(sbase + u * C::kQStride + qblob_sf(D) + 512 * a, 128, 128, 0));
       }
+      // K scales of tile i into TMEM buffer i % 2, once its blob has landed
+      auto load_sfk = [&](int i) -> bool {
+        const int st = i % C::NS;
+        if (!mbar_wait(blob_full(st), (i / C::NS) & 1, &abort_flag, p.err)) return false;
+        tc_fence_after();
+        const uint32_t blob = sbase + C::kStageOff + st * C::kBlob;
+#pragma unroll
+        for (int c = 0; c < sf_chunks(D); ++c)
+          tmem_cp_32x128b_x4(tmem + C::kSFK + C::kSfc * (i & 1) + 4 * c,
+                             smem_desc(blob + blob_ksf(D) + 512 * c, 128, 128, 0));
+        return true;
+      };
+      // operand descriptors of unit 0 / stage 0; the others differ only in the start
+      // address field (address >> 4, no carry out of it inside shared memory)
+      const uint64_t qd0 = smem_desc(sbase, 128, 4 * D, 0);
+      const uint64_t kd0 = smem_desc(sbase + C::kStageOff + blob_kcodes(D), 128, 4 * D, 0);
       for (int i = 0; ok && i < n; ++i) {
         const int st = i % C::NS;
-        const uint32_t blob = sbase + C::kStageOff + st * C::kBlob;
         const uint32_t sfk = tmem + C::kSFK + C::kSfc * (i & 1);
         for (int u = 0; ok && u < U; ++u) {
           // S(u, i) once the previous user of the S buffer has read it out
           if (u > 0) {
             if (!(ok = mbar_spin_wait(s_free(u - 1), i & 1, &abort_flag, p.err))) break;
           } else {
-            if (!(ok = mbar_wait(blob_full(st), (i / C::NS) & 1, &abort_flag, p.err))) break;
+            // the K scales of tile i: their buffer was last read by S(*, i-2)
+            if (!(ok = load_sfk(i))) break;
             if (i > 0 && !(ok = mbar_spin_wait(s_free(U - 1), (i - 1) & 1, &abort_flag, p.err))) break;
-            tc_fence_after();
-            // K scales of tile i; their buffer was last read by S(*, i-2), which the units have read out
-#pragma unroll
-            for (int c = 0; c < sf_chunks(D); ++c)
-              tmem_cp_32x128b_x4(sfk + 4 * c, smem_desc(blob + blob_ksf(D) + 512 * c, 128, 128, 0));
           }
           tc_fence_after();
 #pragma unroll
-          for (int kk = 0; kk < D / 64; ++kk) {
-            const uint64_t ad = smem_desc(sbase + u * C::kQStride + 256 * kk, 128, 4 * D, 0);
-            const uint64_t bd = smem_desc(blob + blob_kcodes(D) + 256 * kk, 128, 4 * D, 0);
-            mma_nvf4(tmem + C::kS, ad, bd, idS, tmem + C::kSFQ + 4 * ((D / 64) * u + kk),
+          for (int kk = 0; kk < D / 64; ++kk)
+            mma_nvf4(tmem + C::kS, qd0 + ((uint32_t)(u * C::kQStride + 256 * kk) >> 4),
+                     kd0 + ((uint32_t)(st * C::kBlob + 256 * kk) >> 4), idS, tmem + C::kSFQ + 4 * ((D / 64) * u + kk),
                      sfk + 4 * (kk >> 1) + 2 * (kk & 1), kk > 0);
-          }
           mma_commit(s_full(u));
         }
         if (ok) mma_commit(blob_empty(st));
