@@ -67,7 +67,7 @@ def visible_counts(w: synth.Workload):
 
 
 def algorithmic(w: synth.Workload, hot_mask):
-    """Algorithmic work: FP4 flops of pass 1, BF16 flops of pass 2, pair counts."""
+    """Algorithmic work: FP4 flops of pass 1, 16-bit flops of pass 2, pair counts."""
     vis = visible_counts(w)  # [ng, T]
     T = vis.shape[1]
     m = np.ascontiguousarray(hot_mask).view(np.uint32)
@@ -76,7 +76,7 @@ def algorithmic(w: synth.Workload, hot_mask):
     hot_pairs = int((bits * vis[None, None]).sum())
     cold_pairs = pairs - hot_pairs
     d = w.d
-    F1 = pairs * (2 * d + 32) + cold_pairs * 2 * d  # QK^T + ones-MMA on every pair, PV on cold pairs
+    F1 = pairs * 2 * d + cold_pairs * 2 * d  # QK^T on every pair, PV on cold pairs (row sums on CUDA cores)
     F2 = hot_pairs * 4 * d                         # exact QK^T and PV on hot pairs
     tiles_vis = int((vis > 0).sum()) * w.B * w.Hkv
     hot_tiles = int((bits & (vis > 0)[None, None]).sum())
