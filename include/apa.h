@@ -85,9 +85,12 @@ int apa_attention_ws(const void* q, const void* k, const void* v, int B, int Hq,
                      size_t workspace_bytes, cudaStream_t stream);
 
 /* apa_attention() on HOST buffers (page-locked memory recommended): copies q, k,
- * v to the device, runs, copies out (and lse / hot_mask when non-null) back, all
- * on `stream`, and synchronizes `stream` before returning.  Device memory is
- * allocated stream-ordered for the duration of the call. */
+ * v to the device, runs, copies out (and lse / hot_mask when non-null) back,
+ * and synchronizes `stream` before returning.  q and out travel on `stream`; K
+ * and V are copied in halves on two library-owned streams that `stream` waits
+ * for.  The device memory is one library-owned buffer per device, grown on
+ * demand and kept until the process exits; calls on the same device are
+ * serialized by a lock. */
 int apa_attention_host(const void* q, const void* k, const void* v, int B, int Hq, int Hkv, int Nq, int Nkv, int d,
                        int causal, float eps, float* out, float* lse, uint32_t* hot_mask, cudaStream_t stream);
 

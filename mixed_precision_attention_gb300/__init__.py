@@ -90,10 +90,13 @@ def attention(q, k, v, causal: bool = True, eps: float = 0.005, return_hot_mask:
     return out, lse, mask
 
 
-def attention_host(q, k, v, causal: bool = True, eps: float = 0.005, return_hot_mask: bool = False, stream=None):
+def attention_host(q, k, v, causal: bool = True, eps: float = 0.005, return_hot_mask: bool = False, stream=None,
+                   out=None, lse=None):
     """apa_attention_host: the same computation on HOST tensors (torch CPU, bf16,
     contiguous; pinned memory recommended).  Copies in, runs, copies out and
-    synchronizes the stream.  Returns CPU tensors (out, lse, hot_mask or None)."""
+    synchronizes the stream.  `out` [B,Hq,Nq,d] and `lse` [B,Hq,Nq] (fp32 CPU,
+    contiguous) may be passed in to reuse them; by default they are allocated in
+    pinned memory.  Returns CPU tensors (out, lse, hot_mask or None)."""
     import torch
     lib = _lib.load()
     for name, t in (("q", q), ("k", k), ("v", v)):
@@ -101,8 +104,13 @@ def attention_host(q, k, v, causal: bool = True, eps: float = 0.005, return_hot_
             raise ValueError(f"{name} must be a contiguous 4-D bf16 CPU tensor")
     B, Hq, Nq, d = q.shape
     Hkv, Nkv = k.shape[1], k.shape[2]
-    out = torch.empty((B, Hq, Nq, d), dtype=torch.float32, pin_memory=True)
-    lse = torch.empty((B, Hq, Nq), dtype=torch.float32, pin_memory=True)
+    for name, t, shape in (("out", out, (B, Hq, Nq, d)), ("lse", lse, (B, Hq, Nq))):
+        if t is not None and (t.dtype != torch.float32 or t.is_cuda or not t.is_contiguous() or tuple(t.shape) != shape):
+            raise ValueError(f"{name} must be a contiguous fp32 CPU tensor of shape {shape}")
+    if out is None:
+        out = torch.empty((B, Hq, Nq, d), dtype=torch.float32, pin_memory=True)
+    if lse is None:
+        lse = torch.empty((B, Hq, Nq), dtype=torch.float32, pin_memory=True)
     mask = torch.empty(hot_mask_shape(B, Hq, Hkv, Nq, Nkv), dtype=torch.int32) if return_hot_mask else None
     s = ctypes.c_void_p(stream.cuda_stream) if stream is not None else _stream(None)
     st = lib.apa_attention_host(_ptr(q), _ptr(k), _ptr(v), B, Hq, Hkv, Nq, Nkv, d, int(bool(causal)), float(eps),

@@ -47,6 +47,39 @@ int validate(const void* q, const void* k, const void* v, const float* out, int 
 
 }  // namespace
 
+// Device staging for apa_attention_host: one buffer per device, grown on demand
+// and kept for the process (cudaMalloc once instead of a stream-ordered
+// allocation that the pool hands back to the driver at every synchronize), and
+// two copy streams with fork/join events.
+HostStaging& host_staging() {
+  static HostStaging hs[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
+  return hs[dev];
+}
+uint8_t* HostStaging::reserve(size_t bytes) {
+  if (bytes <= cap) return buf;
+  if (buf) cudaFree(buf);  // synchronizes; the previous call has completed anyway
+  buf = nullptr;
+  cap = 0;
+  if (cudaMalloc((void**)&buf, bytes) != cudaSuccess) {
+    buf = nullptr;
+    return nullptr;
+  }
+  cap = bytes;
+  return buf;
+}
+bool HostStaging::streams_ready() {
+  if (ready) return true;
+  for (int i = 0; i < 2; ++i)
+    if (cudaStreamCreateWithFlags(&copy[i], cudaStreamNonBlocking) != cudaSuccess ||
+        cudaEventCreateWithFlags(&join[i], cudaEventDisableTiming) != cudaSuccess)
+      return false;
+  if (cudaEventCreateWithFlags(&fork, cudaEventDisableTiming) != cudaSuccess) return false;
+  ready = true;
+  return true;
+}
+
 int* device_error_word() {
   static int* addr[64] = {nullptr};
   int dev = 0;
@@ -207,13 +240,27 @@ int apa_attention_host(const void* q, const void* k, const void* v, int B, int H
   };
   const size_t oq = slot(nq * 2), ok = slot(nkv * 2), ov = slot(nkv * 2), oo = slot(nq * 4);
   const size_t ol = slot(lse ? (size_t)B * Hq * Nq * 4 : 0), om = slot(hot_mask ? nmask * 4 : 0), ow = slot(need);
-  uint8_t* dev = nullptr;
-  if (cudaMallocAsync((void**)&dev, off, stream) != cudaSuccess) return APA_ERR_NOMEM;
-  st = APA_OK;
-  if (cudaMemcpyAsync(dev + oq, q, nq * 2, cudaMemcpyHostToDevice, stream) != cudaSuccess ||
-      cudaMemcpyAsync(dev + ok, k, nkv * 2, cudaMemcpyHostToDevice, stream) != cudaSuccess ||
-      cudaMemcpyAsync(dev + ov, v, nkv * 2, cudaMemcpyHostToDevice, stream) != cudaSuccess)
-    st = APA_ERR_CUDA;
+  // one call at a time per device: the device buffer and the copy streams are the library's
+  apa::HostStaging& hs = apa::host_staging();
+  std::lock_guard<std::mutex> lk(hs.mu);
+  uint8_t* dev = hs.reserve(off);
+  if (!dev) return APA_ERR_NOMEM;
+  if (!hs.streams_ready()) return APA_ERR_CUDA;
+  // inputs: q on `stream`; K and V in halves on two more streams, so that several
+  // copy engines share the transfer; `stream` waits for both before computing
+  const size_t hk = nkv / 2;
+  bool okc = cudaEventRecord(hs.fork, stream) == cudaSuccess;
+  for (int i = 0; i < 2 && okc; ++i) okc = cudaStreamWaitEvent(hs.copy[i], hs.fork, 0) == cudaSuccess;
+  okc = okc && cudaMemcpyAsync(dev + oq, q, nq * 2, cudaMemcpyHostToDevice, stream) == cudaSuccess;
+  for (int i = 0; i < 2 && okc; ++i) {
+    const size_t e0 = i ? hk : 0, e1 = i ? nkv : hk;
+    okc = cudaMemcpyAsync(dev + ok + e0 * 2, (const uint8_t*)k + e0 * 2, (e1 - e0) * 2, cudaMemcpyHostToDevice,
+                          hs.copy[i]) == cudaSuccess &&
+          cudaMemcpyAsync(dev + ov + e0 * 2, (const uint8_t*)v + e0 * 2, (e1 - e0) * 2, cudaMemcpyHostToDevice,
+                          hs.copy[i]) == cudaSuccess &&
+          cudaEventRecord(hs.join[i], hs.copy[i]) == cudaSuccess && cudaStreamWaitEvent(stream, hs.join[i], 0) == cudaSuccess;
+  }
+  st = okc ? APA_OK : APA_ERR_CUDA;
   if (st == APA_OK)
     st = apa::run_attention(s, dev + oq, dev + ok, dev + ov, eps, (float*)(dev + oo), lse ? (float*)(dev + ol) : nullptr,
                             hot_mask ? (uint32_t*)(dev + om) : nullptr, need ? dev + ow : nullptr, stream);
@@ -224,7 +271,7 @@ int apa_attention_host(const void* q, const void* k, const void* v, int B, int H
     if (hot_mask && cudaMemcpyAsync(hot_mask, dev + om, nmask * 4, cudaMemcpyDeviceToHost, stream) != cudaSuccess)
       st = APA_ERR_CUDA;
   }
-  if (cudaFreeAsync(dev, stream) != cudaSuccess && st == APA_OK) st = APA_ERR_CUDA;
+  // the copy streams were joined into `stream`, so this also waits for them
   if (cudaStreamSynchronize(stream) != cudaSuccess && st == APA_OK) st = APA_ERR_CUDA;
   return st;
 }

@@ -11,6 +11,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cstring>
+#include <mutex>
 
 namespace apa {
 
@@ -107,6 +108,19 @@ __host__ __device__ inline float v16_scale(float vamax) {
 }
 
 int* device_error_word();  // library-wide device error word (set by bounded waits)
+
+// Per-device staging of the host-buffer entry point (apa.cu).
+struct HostStaging {
+  std::mutex mu;
+  uint8_t* buf = nullptr;
+  size_t cap = 0;
+  bool ready = false;
+  cudaStream_t copy[2] = {nullptr, nullptr};
+  cudaEvent_t fork = nullptr, join[2] = {nullptr, nullptr};
+  uint8_t* reserve(size_t bytes);  // buffer of at least `bytes`, or null
+  bool streams_ready();
+};
+HostStaging& host_staging();
 
 // ------------------------------------------------------------------ launchers
 cudaError_t launch_quantize(const Shape& s, const void* q, const void* k, const void* v, const Workspace& ws,
