@@ -13,12 +13,15 @@
 // block, no pass-1 state, uncentred logits.
 //
 // GB300 design: one CTA = one 128-row block of GQA-packed rows of one KV head
-// (tcgen05 M = 128), 6 warps:
+// (tcgen05 M = 128), 7 warps:
 //   warps 0-3  softmax, one thread per row (TMEM lane = row);
-//   warp 4     TMA producer: K and V tiles (64 keys x d, bf16, 128-byte swizzle)
-//              into an NS-stage ring;
-//   warp 5     TMEM owner and MMA issuer: S = Q K^T (kind::f16, K-major x K-major)
-//              into a double-buffered S in TMEM, O += P V (V MN-major) into O in TMEM.
+//   warp 4     TMA producer: K and V tiles (64 keys x d, 128-byte swizzle) into an
+//              NS-stage ring;
+//   warp 5     TMEM owner and S issuer: S = Q K^T (kind::f16, K-major x K-major)
+//              into a double-buffered S in TMEM;
+//   warp 6     PV issuer: O += P V (V MN-major) into O in TMEM.
+// A tcgen05.mma takes tens of cycles to issue, and one tile needs d/16 of them
+// for S and 4 (or 8) for PV: issued by one thread, they set the tile period.
 // The running max moves lazily (only when a score exceeds it by more than 8 in
 // log2 units), so O in TMEM is rarely rescaled.  P goes to the tensor cores as
 // two BF16 terms, P = P_hi + P_lo (P_lo the BF16 rounding of the residual), so
@@ -47,7 +50,10 @@ struct P2Params {
   int* err;
 };
 
-constexpr int kThreads = 192;
+constexpr int kThreads = 224;
+#ifndef APA_P2_STAGES_D128
+#define APA_P2_STAGES_D128 4  // K/V stages of the FP16 pass 2 at d = 128
+#endif
 constexpr float kTau2 = 8.0f;  // pass-2 lazy rescale threshold (log2 units)
 
 // kF16: P as one FP16 term against the FP16 copy of V; else P = P_hi + P_lo in
@@ -62,7 +68,7 @@ constexpr float kTau2 = 8.0f;  // pass-2 lazy rescale threshold (log2 units)
 template <int D, bool kF16>
 struct P2Cfg {
   static constexpr int kCtasPerSm = 1;
-  static constexpr int NS = kCtasPerSm == 2 ? 2 : (D >= 256 ? 2 : 3);
+  static constexpr int NS = kCtasPerSm == 2 ? 2 : (D >= 256 ? 2 : (kF16 && D == 128 ? APA_P2_STAGES_D128 : 3));
   static constexpr int kAtoms = D / 64;
   static constexpr int kQBytes = 128 * D * 2;
   static constexpr int kKVBytes = 64 * D * 2;  // one of K or V per stage
@@ -72,7 +78,7 @@ struct P2Cfg {
   static constexpr int kQOff = 0;
   static constexpr int kStageOff = kQBytes;
   static constexpr int kPOff = kStageOff + NS * 2 * kKVBytes;
-  static constexpr int kNumBars = 2 * NS + 9;
+  static constexpr int kNumBars = 2 * NS + 10;
   static constexpr int kBarOff = kPOff + NP * kPTerms * kPBytes;
   static constexpr int kSlack = kCtasPerSm == 2 ? 0 : 1024;  // runtime alignment room
   static constexpr int kSmem = kBarOff + kNumBars * 8 + 16 + kSlack;
@@ -89,6 +95,54 @@ __device__ __forceinline__ void wait_bounded(uint32_t bar, uint32_t parity, int*
       return;
     }
   }
+}
+
+// P of eight consecutive keys, 2^(x*c2 + nb), as four FP16x2 words (key 2k in the
+// low half of word k); the FP32 values are added into (s0, s1): even keys into s0,
+// odd keys into s1.  The affine step and the sums run as packed FP32 pairs.
+__device__ __forceinline__ void p8_f16(const float* x, float c2, float nb, uint32_t* h, float& s0, float& s1) {
+  asm("{\n.reg .b64 a0, a1, a2, a3, c, n, s, one;\n"
+      ".reg .f32 y0, y1, y2, y3, y4, y5, y6, y7;\n"
+      "mov.b64 c, {%14, %14};\n"
+      "mov.b64 n, {%15, %15};\n"
+      "mov.b64 one, {%16, %16};\n"
+      "mov.b64 a0, {%6, %7};\n"
+      "mov.b64 a1, {%8, %9};\n"
+      "mov.b64 a2, {%10, %11};\n"
+      "mov.b64 a3, {%12, %13};\n"
+      "fma.rn.f32x2 a0, a0, c, n;\n"
+      "fma.rn.f32x2 a1, a1, c, n;\n"
+      "fma.rn.f32x2 a2, a2, c, n;\n"
+      "fma.rn.f32x2 a3, a3, c, n;\n"
+      "mov.b64 {y0, y1}, a0;\n"
+      "mov.b64 {y2, y3}, a1;\n"
+      "mov.b64 {y4, y5}, a2;\n"
+      "mov.b64 {y6, y7}, a3;\n"
+      "ex2.approx.ftz.f32 y0, y0;\n"
+      "ex2.approx.ftz.f32 y1, y1;\n"
+      "ex2.approx.ftz.f32 y2, y2;\n"
+      "ex2.approx.ftz.f32 y3, y3;\n"
+      "ex2.approx.ftz.f32 y4, y4;\n"
+      "ex2.approx.ftz.f32 y5, y5;\n"
+      "ex2.approx.ftz.f32 y6, y6;\n"
+      "ex2.approx.ftz.f32 y7, y7;\n"
+      "cvt.rn.f16x2.f32 %0, y1, y0;\n"
+      "cvt.rn.f16x2.f32 %1, y3, y2;\n"
+      "cvt.rn.f16x2.f32 %2, y5, y4;\n"
+      "cvt.rn.f16x2.f32 %3, y7, y6;\n"
+      "mov.b64 s, {%4, %5};\n"
+      "mov.b64 a0, {y0, y1};\n"
+      "mov.b64 a1, {y2, y3};\n"
+      "mov.b64 a2, {y4, y5};\n"
+      "mov.b64 a3, {y6, y7};\n"
+      "fma.rn.f32x2 s, a0, one, s;\n"
+      "fma.rn.f32x2 s, a1, one, s;\n"
+      "fma.rn.f32x2 s, a2, one, s;\n"
+      "fma.rn.f32x2 s, a3, one, s;\n"
+      "mov.b64 {%4, %5}, s;\n}"
+      : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3]), "+f"(s0), "+f"(s1)
+      : "f"(x[0]), "f"(x[1]), "f"(x[2]), "f"(x[3]), "f"(x[4]), "f"(x[5]), "f"(x[6]), "f"(x[7]), "f"(c2), "f"(nb),
+        "f"(1.f));
 }
 
 template <int D, bool kF16>
@@ -121,9 +175,10 @@ __global__ void __launch_bounds__(kThreads, P2Cfg<D, kF16>::kCtasPerSm)
   auto s_free = [&](int b2) { return bar0 + 8u * (2 * C::NS + 2 + b2); };
   auto p_full = [&](int b2) { return bar0 + 8u * (2 * C::NS + 4 + b2); };
   auto pv_done = [&](int b2) { return bar0 + 8u * (2 * C::NS + 6 + b2); };
-  const uint32_t drain = bar0 + 8u * (2 * C::NS + 8);
+  const uint32_t drain = bar0 + 8u * (2 * C::NS + 8), drain_pv = bar0 + 8u * (2 * C::NS + 9);
   // every lane of a softmax warp waits; the warp proceeds only if all lanes succeeded
   auto warp_wait = [&](uint32_t bar, uint32_t parity) -> bool {
+    if (__all_sync(0xffffffffu, mbar_test_wait(bar, parity))) return true;  // already complete
     const bool okl = mbar_wait(bar, parity, &abort_flag, p.err);
     return __all_sync(0xffffffffu, okl);
   };
@@ -148,7 +203,8 @@ __global__ void __launch_bounds__(kThreads, P2Cfg<D, kF16>::kCtasPerSm)
     abort_flag = 0;
     for (int i = 0; i < C::kNumBars; ++i) {
       const bool per_warp = (i >= 2 * C::NS + 2 && i < 2 * C::NS + 6);  // s_free, p_full: one arrive per softmax warp
-      mbar_init(bar0 + 8u * i, per_warp ? 4u : 1u);
+      const bool kv_empty_bar = (i >= C::NS && i < 2 * C::NS);           // kv_empty: the S and the PV issuer
+      mbar_init(bar0 + 8u * i, per_warp ? 4u : (kv_empty_bar ? 2u : 1u));
     }
     fence_mbar_init();
   }
@@ -215,9 +271,9 @@ __global__ void __launch_bounds__(kThreads, P2Cfg<D, kF16>::kCtasPerSm)
       }
     }
   } else if (warp == 5) {
-    // ------------------------------------------------------------ MMA issuer
+    // ------------------------------------------------------------ S issuer
     if (lane == 0 && n > 0) {
-      const uint32_t idS = idesc_bf16(128, 64, 0), idO = kF16 ? idesc_f16(128, D, 1) : idesc_bf16(128, D, 1);
+      const uint32_t idS = idesc_bf16(128, 64, 0);
       auto issue_s = [&](int i) -> bool {
         const int st = i % C::NS;
         if (!mbar_wait(kv_full(st), (i / C::NS) & 1, &abort_flag, p.err)) return false;
@@ -231,12 +287,23 @@ __global__ void __launch_bounds__(kThreads, P2Cfg<D, kF16>::kCtasPerSm)
           mma_bf16(tmem + C::kSCol + 64 * (i & 1), ad, bd, idS, kk > 0);
         }
         mma_commit(s_full(i & 1));
+        mma_commit(kv_empty(st));  // this stage's K has been read
         return true;
       };
-      bool ok = issue_s(0);
+      for (int i = 0; i < n; ++i)
+        if (!issue_s(i)) break;
+      // drain: every tcgen05 op issued by this thread has completed before TMEM is freed
+      mma_commit(drain);
+      wait_bounded(drain, 0, p.err);
+    }
+  } else if (warp == 6) {
+    // ------------------------------------------------------------ PV issuer
+    if (lane == 0 && n > 0) {
+      const uint32_t idO = kF16 ? idesc_f16(128, D, 1) : idesc_bf16(128, D, 1);
+      bool ok = true;
       for (int i = 0; ok && i < n; ++i) {
-        if (i + 1 < n && !(ok = issue_s(i + 1))) break;
         if (!(ok = mbar_wait(p_full(i & 1), (i >> 1) & 1, &abort_flag, p.err))) break;
+        if (!(ok = mbar_wait(kv_full(i % C::NS), (i / C::NS) & 1, &abort_flag, p.err))) break;
         tc_fence_after();
         const uint32_t vaddr = sbase + C::kStageOff + (i % C::NS) * 2 * C::kKVBytes + C::kKVBytes;
         const uint32_t paddr = sbase + C::kPOff + (i % C::NP) * C::kPTerms * C::kPBytes;
@@ -249,11 +316,10 @@ __global__ void __launch_bounds__(kThreads, P2Cfg<D, kF16>::kCtasPerSm)
             mma_bf16(tmem + C::kOCol, smem_desc(paddr + C::kPBytes + kk * 32, 16, 1024, kSwizzle128B), bd, idO, 1u);
         }
         mma_commit(pv_done(i & 1));
-        mma_commit(kv_empty(i % C::NS));
+        mma_commit(kv_empty(i % C::NS));  // this stage's V has been read
       }
-      // drain: every tcgen05 op issued by this thread has completed before TMEM is freed
-      mma_commit(drain);
-      wait_bounded(drain, 0, p.err);
+      mma_commit(drain_pv);
+      wait_bounded(drain_pv, 0, p.err);
     }
   } else {
     // ------------------------------------------------------------ softmax (one thread per row)
@@ -263,9 +329,13 @@ __global__ void __launch_bounds__(kThreads, P2Cfg<D, kF16>::kCtasPerSm)
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
     float m2 = -INFINITY, l2 = 0.f;
     bool ok = true;
+    // the hot-list entry of the next tile is loaded one tile ahead, off the critical path
+    uint32_t gm_next = 0;
+    int t_next = n > 0 ? tile_of(0, gm_next) : 0;
     for (int i = 0; i < n; ++i) {
-      uint32_t gm;
-      const int t = tile_of(i, gm);
+      const uint32_t gm = gm_next;
+      const int t = t_next;
+      if (i + 1 < n) t_next = tile_of(i + 1, gm_next);
       if (!(ok = warp_wait(s_full(i & 1), (i >> 1) & 1))) break;
       const bool row_hot = row_valid && ((gm >> (r >> 4)) & 1u);
       const int j0 = t * kTile;
@@ -295,13 +365,27 @@ __global__ void __launch_bounds__(kThreads, P2Cfg<D, kF16>::kCtasPerSm)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(s_free(i & 1));
+      // raw scores.  Keys past a row's last visible one are masked to -inf only on
+      // the diagonal (0 < nvis < 64); a row with nothing visible here (cold group or
+      // beyond the diagonal) keeps its scores but takes no part: its maximum is -inf
+      // and its P bias -inf, so its P is exactly 0.
       float sv[64];
-      float c = -INFINITY;
 #pragma unroll
-      for (int j = 0; j < 64; ++j) {
-        sv[j] = j < nvis ? fmaf(__uint_as_float(raw[j]), c2, -shift) : -INFINITY;
-        c = fmaxf(c, sv[j]);
+      for (int j = 0; j < 64; ++j) sv[j] = __uint_as_float(raw[j]);
+      if (__any_sync(0xffffffffu, nvis > 0 && nvis < 64)) {
+#pragma unroll
+        for (int j = 0; j < 64; ++j)
+          if (j >= nvis) sv[j] = -INFINITY;
       }
+      // row maximum as a tree of 3-input maxima; the logit map x*c2 - shift is monotone
+      // (c2 > 0), so its maximum is the map of the raw maximum, rounded the same way
+      float g8[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        g8[k] = max3(max3(sv[8 * k], sv[8 * k + 1], sv[8 * k + 2]), max3(sv[8 * k + 3], sv[8 * k + 4], sv[8 * k + 5]),
+                     fmaxf(sv[8 * k + 6], sv[8 * k + 7]));
+      const float rmax = max3(max3(g8[0], g8[1], g8[2]), max3(g8[3], g8[4], g8[5]), fmaxf(g8[6], g8[7]));
+      const float c = (nvis <= 0 || rmax == -INFINITY) ? -INFINITY : fmaf(rmax, c2, -shift);
       float f = 1.f;
       bool rescale = false;
       if (c > m2 + kTau2 || (m2 == -INFINITY && c > -INFINITY)) {
@@ -314,34 +398,38 @@ __global__ void __launch_bounds__(kThreads, P2Cfg<D, kF16>::kCtasPerSm)
       // this P buffer is free once PV(i - NP) has completed
       if (i >= C::NP && !(ok = warp_wait(pv_done((i - C::NP) & 1), ((i - C::NP) >> 1) & 1))) break;
       uint8_t* prow = smem + C::kPOff + (i % C::NP) * C::kPTerms * C::kPBytes + r * 128;
-      float psum = 0.f;
+      // P = 2^(x*c2 - shift - m2), one bias per row; -inf for a row with nothing
+      // visible in this tile (finite scores times c2 plus -inf give 2^-inf = 0)
+      const float nb = (nvis <= 0 || m2 == -INFINITY) ? -INFINITY : -shift - m2;
+      float ps[4] = {0.f, 0.f, 0.f, 0.f};  // four partial row sums (short dependency chains)
 #pragma unroll
       for (int ch = 0; ch < 8; ++ch) {
         uint32_t hi[4], lo[4];
+        if (kF16) {
+          // the row sum adds the FP32 values; their FP16 roundings (relative error
+          // at most 2^-11 each) go to the tensor cores
+          p8_f16(sv + 8 * ch, c2, nb, hi, ps[ch & 1], ps[2 + (ch & 1)]);
+        } else {
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int j = 8 * ch + 2 * e;
-          const float a0 = ex2_approx(sv[j] - m2), a1 = ex2_approx(sv[j + 1] - m2);
-          if (kF16) {
-            // the row sum adds the FP32 values; their FP16 roundings (relative error
-            // at most 2^-11 each) go to the tensor cores
-            hi[e] = cvt_f16x2(a0, a1);
-            psum += a0 + a1;
-          } else {
+          const float a0 = ex2_approx(fmaf(sv[j], c2, nb)), a1 = ex2_approx(fmaf(sv[j + 1], c2, nb));
+          {
             const __nv_bfloat162 h2 = __floats2bfloat162_rn(a0, a1);
             const float2 hf = __bfloat1622float2(h2);
             const __nv_bfloat162 l2v = __floats2bfloat162_rn(a0 - hf.x, a1 - hf.y);
             const float2 lf = __bfloat1622float2(l2v);
-            psum += (hf.x + lf.x) + (hf.y + lf.y);
+            ps[e] += (hf.x + lf.x) + (hf.y + lf.y);
             hi[e] = *reinterpret_cast<const uint32_t*>(&h2);
             lo[e] = *reinterpret_cast<const uint32_t*>(&l2v);
           }
+        }
         }
         const int sw = (ch ^ (r & 7)) << 4;
         *reinterpret_cast<uint4*>(prow + sw) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
         if (!kF16) *reinterpret_cast<uint4*>(prow + C::kPBytes + sw) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
       }
-      l2 = l2 * f + psum;
+      l2 = l2 * f + ((ps[0] + ps[1]) + (ps[2] + ps[3]));
       if (__any_sync(0xffffffffu, rescale)) {
         // O must not be read before PV(i-1) has landed
         if (!(ok = warp_wait(pv_done((i - 1) & 1), ((i - 1) >> 1) & 1))) break;
