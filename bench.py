@@ -41,7 +41,7 @@ UNIT = "TFLOP/s"
 PAGE_APA_MS = 5.200  # the blog's APA time for this layer on an RTX 5090 (context)
 FP4_PER_BF16 = 13.5 / 2.25  # nominal dense FP4 : BF16 tensor ratio
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-KERNELS_PER_STEP = 5  # stats, finalize, quantize, pass 1, pass 2 (+merge)
+KERNELS_PER_STEP = 6  # stats, finalize, quantize, pass 1, pass-2 ranking, pass 2 (+merge)
 
 
 # ----------------------------------------------------------------------------- helpers

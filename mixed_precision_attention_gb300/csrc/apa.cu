@@ -122,6 +122,7 @@ size_t workspace_layout(const Shape& s, bool apa_mode, Workspace* ws, void* base
   w.state_ml = (float2*)take(BH * nblk * kBlockRows * 8);
   w.hot_list = (uint32_t*)take(BH * nblk * T * 4);
   w.hot_count = (uint32_t*)take(BH * nblk * 4);
+  w.p2_order = (uint32_t*)take(BH * nblk * 4);
   w.v16 = (uint16_t*)take(BH * s.Nkv * d * 2);
   if (ws) *ws = w;
   return off;
@@ -182,6 +183,7 @@ static int run_attention(const Shape& s, const void* q, const void* k, const voi
   if (launch_quantize(s, q, k, v, ws, true, true, stream) != cudaSuccess) return APA_ERR_CUDA;
   stage(1);
   if (launch_pass1(s, ws, eps, hot_mask, stream) != cudaSuccess) return APA_ERR_CUDA;
+  if (launch_pass2_order(s, ws, stream) != cudaSuccess) return APA_ERR_CUDA;
   stage(2);
   if (launch_pass2(s, q, k, v, &ws, out, lse, stream) != cudaSuccess) return APA_ERR_CUDA;
   stage(3);

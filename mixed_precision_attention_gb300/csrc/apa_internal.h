@@ -87,6 +87,7 @@ struct Workspace {
   float2* state_ml;   // [BH][nblk*128]: pass-1 frame m and cold sum l
   uint32_t* hot_list; // [BH*nblk][T]: tile | group mask << 16
   uint32_t* hot_count;// [BH*nblk]
+  uint32_t* p2_order; // [BH*nblk]: pass-2 work items (bh * nblk + blk), longest hot list first
 };
 size_t workspace_layout(const Shape& s, bool apa_mode, Workspace* ws, void* base);
 
@@ -129,5 +130,6 @@ cudaError_t launch_pass1(const Shape& s, const Workspace& ws, float eps, uint32_
 cudaError_t launch_pass2(const Shape& s, const void* q, const void* k, const void* v, const Workspace* ws,
                          float* out, float* lse, cudaStream_t st);
 cudaError_t launch_visible_mask(const Shape& s, uint32_t* hot_mask, cudaStream_t st);
+cudaError_t launch_pass2_order(const Shape& s, const Workspace& ws, cudaStream_t st);
 
 }  // namespace apa

@@ -44,6 +44,7 @@ struct P2Params {
   const float2* state_ml;     // pass-1 (m, l) [BH][nblk*128] or null
   const uint32_t* hot_list;   // [BH*nblk][T] or null (all visible tiles)
   const uint32_t* hot_count;  // [BH*nblk] or null
+  const uint32_t* order;      // [BH*nblk] work items, longest hot list first, or null
   const uint32_t* vamax;      // [BH] max |v| (float bits): the FP16 V copy's scale, or null
   float* out;                 // [B,Hq,Nq,d]
   float* lse;                 // [B,Hq,Nq] or null
@@ -161,8 +162,17 @@ __global__ void __launch_bounds__(kThreads, P2Cfg<D, kF16>::kCtasPerSm)
 
   const Shape& s = p.s;
   const int nblk = s.nblk(), BH = s.BH(), G = s.G(), R = s.R(), T = s.T(), off = s.off();
-  // heavy (late, causal) blocks first
-  const int bh = blockIdx.x % BH, blk = nblk - 1 - (int)(blockIdx.x / BH);
+  // longest hot lists first when ranked, else heavy (late, causal) blocks first:
+  // CTAs start in index order, so the longest work items start earliest
+  int bh, blk;
+  if (p.order) {
+    const int item = (int)p.order[blockIdx.x];
+    bh = item / nblk;
+    blk = item % nblk;
+  } else {
+    bh = blockIdx.x % BH;
+    blk = nblk - 1 - (int)(blockIdx.x / BH);
+  }
   const int b = bh / s.Hkv, h = bh % s.Hkv;
   const int p0 = blk * kBlockRows;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -547,7 +557,30 @@ cudaError_t launch_d(const P2Params& prm, const CUtensorMap& km, const CUtensorM
   return prm.vamax ? launch_dv<D, true>(prm, km, vm, st) : launch_dv<D, false>(prm, km, vm, st);
 }
 
+// Ranks the pass-2 work items by hot-list length, longest first (ties by index,
+// so the order is deterministic): one block, each thread counts the items that
+// precede its own.  Quadratic, so only for up to kMaxRanked items.
+constexpr int kMaxRanked = 4096;
+__global__ void __launch_bounds__(1024) rank_kernel(const uint32_t* __restrict__ count, int n, uint32_t* order) {
+  __shared__ uint32_t c[kMaxRanked];
+  for (int i = threadIdx.x; i < n; i += blockDim.x) c[i] = count[i];
+  __syncthreads();
+  for (int i = threadIdx.x; i < n; i += blockDim.x) {
+    const uint32_t ci = c[i];
+    int rank = 0;
+    for (int j = 0; j < n; ++j) rank += (c[j] > ci) || (c[j] == ci && j < i);
+    order[rank] = (uint32_t)i;
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_pass2_order(const Shape& s, const Workspace& ws, cudaStream_t st) {
+  const size_t n = (size_t)s.BH() * s.nblk();
+  if (n > (size_t)kMaxRanked) return cudaSuccess;  // pass 2 keeps the position order
+  rank_kernel<<<1, 1024, 0, st>>>(ws.hot_count, (int)n, ws.p2_order);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_pass2(const Shape& s, const void* q, const void* k, const void* v, const Workspace* ws, float* out,
                          float* lse, cudaStream_t st) {
@@ -566,6 +599,7 @@ cudaError_t launch_pass2(const Shape& s, const void* q, const void* k, const voi
   prm.state_ml = ws ? ws->state_ml : nullptr;
   prm.hot_list = ws ? ws->hot_list : nullptr;
   prm.hot_count = ws ? ws->hot_count : nullptr;
+  prm.order = ws && (size_t)s.BH() * s.nblk() <= kMaxRanked ? ws->p2_order : nullptr;
   prm.vamax = f16 ? ws->vamax : nullptr;
   prm.out = out;
   prm.lse = lse;
