@@ -86,10 +86,13 @@ int apa_attention_ws(const void* q, const void* k, const void* v, int B, int Hq,
 
 /* apa_attention() on HOST buffers (page-locked memory recommended): copies q, k,
  * v to the device, runs, copies out (and lse / hot_mask when non-null) back,
- * and synchronizes `stream` before returning.  q and out travel on `stream`; K
- * and V are copied in halves on two library-owned streams that `stream` waits
- * for.  The device memory is one library-owned buffer per device, grown on
- * demand and kept until the process exits; calls on the same device are
+ * and synchronizes `stream` before returning.  The results equal those of
+ * apa_attention().  Each (b, KV head) is an independent problem of the method,
+ * so the call pipelines them: one's inputs are copied (on a library-owned copy
+ * stream) while earlier ones compute (on up to 8 library-owned streams) and
+ * their results are copied back.  All of it is ordered after the work already
+ * on `stream`.  The device memory is one library-owned buffer per device, grown
+ * on demand and kept until the process exits; calls on the same device are
  * serialized by a lock. */
 int apa_attention_host(const void* q, const void* k, const void* v, int B, int Hq, int Hkv, int Nq, int Nkv, int d,
                        int causal, float eps, float* out, float* lse, uint32_t* hot_mask, cudaStream_t stream);

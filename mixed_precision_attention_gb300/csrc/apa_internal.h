@@ -11,7 +11,6 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cstring>
-#include <mutex>
 
 namespace apa {
 
@@ -110,23 +109,15 @@ __host__ __device__ inline float v16_scale(float vamax) {
 
 int* device_error_word();  // library-wide device error word (set by bounded waits)
 
-// Per-device staging of the host-buffer entry point (apa.cu).
-struct HostStaging {
-  std::mutex mu;
-  uint8_t* buf = nullptr;
-  size_t cap = 0;
-  bool ready = false;
-  cudaStream_t copy[2] = {nullptr, nullptr};
-  cudaEvent_t fork = nullptr, join[2] = {nullptr, nullptr};
-  uint8_t* reserve(size_t bytes);  // buffer of at least `bytes`, or null
-  bool streams_ready();
-};
-HostStaging& host_staging();
 
 // ------------------------------------------------------------------ launchers
 cudaError_t launch_quantize(const Shape& s, const void* q, const void* k, const void* v, const Workspace& ws,
                             bool do_q, bool do_kv, cudaStream_t st);
-cudaError_t launch_pass1(const Shape& s, const Workspace& ws, float eps, uint32_t* hot_mask, cudaStream_t st);
+// wide: one 128-row block per CTA (three times the CTAs, each on its own SM when
+// the GPU is otherwise idle, so a single problem finishes sooner) instead of
+// three blocks of one KV head per CTA (the faster choice for a full GPU)
+cudaError_t launch_pass1(const Shape& s, const Workspace& ws, float eps, uint32_t* hot_mask, bool wide,
+                         cudaStream_t st);
 cudaError_t launch_pass2(const Shape& s, const void* q, const void* k, const void* v, const Workspace* ws,
                          float* out, float* lse, cudaStream_t st);
 cudaError_t launch_visible_mask(const Shape& s, uint32_t* hot_mask, cudaStream_t st);

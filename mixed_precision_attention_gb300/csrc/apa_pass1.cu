@@ -1144,17 +1144,17 @@ bool single_unit() {
 }
 
 template <int D>
-cudaError_t launch_d(const P1Params& prm, cudaStream_t st) {
+cudaError_t launch_d(const P1Params& prm, bool wide, cudaStream_t st) {
   if (rowsum_by_mma()) return launch_dv<D, true>(prm, st);
   if constexpr (D <= 128) {
-    if (!single_unit()) return launch_multi<D, 3>(prm, st);
+    if (!wide && !single_unit()) return launch_multi<D, 3>(prm, st);
   }
   return launch_dv<D, false>(prm, st);
 }
 
 }  // namespace
 
-cudaError_t launch_pass1(const Shape& s, const Workspace& ws, float eps, uint32_t* hot_mask, cudaStream_t st) {
+cudaError_t launch_pass1(const Shape& s, const Workspace& ws, float eps, uint32_t* hot_mask, bool wide, cudaStream_t st) {
   P1Params prm{};
   prm.s = s;
   prm.kv_blob = ws.kv_blob;
@@ -1170,9 +1170,9 @@ cudaError_t launch_pass1(const Shape& s, const Workspace& ws, float eps, uint32_
   prm.hot_mask = hot_mask;
   prm.err = device_error_word();
   switch (s.d) {
-    case 64: return launch_d<64>(prm, st);
-    case 128: return launch_d<128>(prm, st);
-    case 256: return launch_d<256>(prm, st);
+    case 64: return launch_d<64>(prm, wide, st);
+    case 128: return launch_d<128>(prm, wide, st);
+    case 256: return launch_d<256>(prm, wide, st);
   }
   return cudaErrorInvalidValue;
 }
