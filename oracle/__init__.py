@@ -28,6 +28,7 @@ _lib = None
 
 QUANT_Q, QUANT_K, QUANT_V, QUANT_P = 1, 2, 4, 8
 QUANT_ALL = 15
+QUANT_Q2 = 16  # Q as two FP4 terms, Q1 + FP4(Q - Q1) (needs QUANT_Q)
 TILE = 64
 GROUP_ROWS = 16
 
@@ -62,7 +63,9 @@ def _load():
             lib.oracle_exact.restype = None
             lib.oracle_quantize_kv_head.argtypes = [P, P, i32, i32, P, P, P, P, P, P, P]
             lib.oracle_quantize_kv_head.restype = None
-            lib.oracle_quantize_q_head.argtypes = [P, i32, i32, P, P, P]
+            lib.oracle_quantize_q_head.argtypes = [P, i32, i32, P, P, P, P, P]
+            lib.oracle_quantize_residual_blocks.argtypes = [P, i64, f64, P, P, P, P]
+            lib.oracle_quantize_residual_blocks.restype = None
             lib.oracle_quantize_q_head.restype = None
             lib.oracle_apa.argtypes = [P, P, P, i32, i32, i32, i32, i32, i32, i32, f64, f64, f64, i32,
                                        P, i64, P, P, P, P, P]
@@ -160,21 +163,29 @@ def quantize_kv(k: np.ndarray, v: np.ndarray):
     return r
 
 
-def quantize_q(q: np.ndarray):
-    """NVFP4 codes of Q per (b, query head): codes [B,Hq,Nq,d], sf [B,Hq,Nq,d/16], s_q [B,Hq]."""
+def quantize_q(q: np.ndarray, residual: bool = False):
+    """NVFP4 codes of Q per (b, query head): codes [B,Hq,Nq,d], sf [B,Hq,Nq,d/16], s_q [B,Hq];
+    with residual=True also codes2 / sf2, the FP4 residual term Q - Q1 in the same head scale."""
     q = _u16(q)
     B, Hq, Nq, d = q.shape
     codes = np.empty((B, Hq, Nq, d), np.uint8)
     sf = np.empty((B, Hq, Nq, d // 16), np.uint8)
+    codes2 = np.empty_like(codes) if residual else None
+    sf2 = np.empty_like(sf) if residual else None
     s_q = np.empty((B, Hq))
     lib = _load()
     for b in range(B):
         for h in range(Hq):
             s = ctypes.c_double()
             lib.oracle_quantize_q_head(_ptr(np.ascontiguousarray(q[b, h])), Nq, d, _ptr(codes[b, h]),
-                                       _ptr(sf[b, h]), ctypes.byref(s))
+                                       _ptr(sf[b, h]), ctypes.byref(s),
+                                       _ptr(codes2[b, h]) if residual else None,
+                                       _ptr(sf2[b, h]) if residual else None)
             s_q[b, h] = s.value
-    return dict(codes=codes, sf=sf, s_q=s_q)
+    r = dict(codes=codes, sf=sf, s_q=s_q)
+    if residual:
+        r.update(codes2=codes2, sf2=sf2)
+    return r
 
 
 # ----------------------------------------------------------------- attention

@@ -132,6 +132,25 @@ void oracle_quantize_blocks(const float* x, int64_t nblk, double s, uint8_t* cod
   }
 }
 
+/* The FP4 residual of Q ("Second hunt": Q2 is the FP4 residual Q - Q1 in the
+ * same scale).  Reading taken: the same FP32 per-head scale s, block scales of
+ * their own, and the residual formed in FP32 in this order, per element:
+ *   q1 = E2M1(code1) * UE4M3(sb1)   (exact: at most 7 significant bits)
+ *   d1 = fp32(q1 * s),  r = fp32(x - d1);
+ * then r is quantized like any other 16-value block with scale s. */
+void oracle_quantize_residual_blocks(const float* x, int64_t nblk, double s, const uint8_t* codes1,
+                                     const uint8_t* sf1, uint8_t* codes2, uint8_t* sf2) {
+  float r[16];
+  for (int64_t b = 0; b < nblk; ++b) {
+    for (int i = 0; i < 16; ++i) {
+      double q1 = oracle_e2m1_value(codes1[b * 16 + i]) * oracle_ue4m3_value(sf1[b]);
+      double d1 = f32(q1 * s);
+      r[i] = (float)f32((double)x[b * 16 + i] - d1);
+    }
+    oracle_quantize_blocks(r, 1, s, codes2 + b * 16, sf2 + b);
+  }
+}
+
 /* Tiles per range of the key-mean sum. */
 #define MEAN_RANGE_TILES 64
 
@@ -236,6 +255,7 @@ void oracle_exact(const uint16_t* q, const uint16_t* k, const uint16_t* v, int B
 #define QUANT_K 2
 #define QUANT_V 4
 #define QUANT_P 8
+#define QUANT_Q2 16 /* Q as two FP4 terms, Q1 + FP4(Q - Q1) ("Second hunt"); needs QUANT_Q */
 
 typedef struct {
   double eps;         /* hot-test threshold; 0 = every visible tile hot, +inf = none */
@@ -276,8 +296,10 @@ void oracle_quantize_kv_head(const uint16_t* kh, const uint16_t* vh, int Nkv, in
   free(vt);
 }
 
-/* NVFP4 codes of one query head: codes [Nq][d], sf [Nq][d/16], *s_q. */
-void oracle_quantize_q_head(const uint16_t* qh, int Nq, int d, uint8_t* codes, uint8_t* sf, double* s_q) {
+/* NVFP4 codes of one query head: codes [Nq][d], sf [Nq][d/16], *s_q; with
+ * codes2 / sf2 non-null also the codes of the residual term (same layout). */
+void oracle_quantize_q_head(const uint16_t* qh, int Nq, int d, uint8_t* codes, uint8_t* sf, double* s_q,
+                            uint8_t* codes2, uint8_t* sf2) {
   float* x = (float*)malloc(sizeof(float) * (size_t)Nq * d);
   double amax = 0.0;
   for (int64_t e = 0; e < (int64_t)Nq * d; ++e) {
@@ -286,6 +308,7 @@ void oracle_quantize_q_head(const uint16_t* qh, int Nq, int d, uint8_t* codes, u
   }
   *s_q = oracle_head_scale(amax);
   oracle_quantize_blocks(x, (int64_t)Nq * d / 16, *s_q, codes, sf);
+  if (codes2 && sf2) oracle_quantize_residual_blocks(x, (int64_t)Nq * d / 16, *s_q, codes, sf, codes2, sf2);
   free(x);
 }
 
@@ -348,11 +371,15 @@ static void quantize_q_row(const uint16_t* qr, int d, double s_q, int quant, dou
     return;
   }
   float x[16];
-  uint8_t codes[16], sf;
+  uint8_t codes[16], sf, codes2[16], sf2;
   for (int b = 0; b < d / 16; ++b) {
     for (int i = 0; i < 16; ++i) x[i] = (float)oracle_bf16_to_double(qr[b * 16 + i]);
     oracle_quantize_blocks(x, 1, s_q, codes, &sf);
     for (int i = 0; i < 16; ++i) out[b * 16 + i] = oracle_e2m1_value(codes[i]) * oracle_ue4m3_value(sf);
+    if (quant & QUANT_Q2) {  /* both terms in units of s_q, accumulated against the same K */
+      oracle_quantize_residual_blocks(x, 1, s_q, codes, &sf, codes2, &sf2);
+      for (int i = 0; i < 16; ++i) out[b * 16 + i] += oracle_e2m1_value(codes2[i]) * oracle_ue4m3_value(sf2);
+    }
   }
 }
 
