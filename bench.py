@@ -264,9 +264,9 @@ def run_gpu(args):
     work = algorithmic(w, mask.cpu().numpy())
     flops_exact = w.flops_exact
 
-    def timed(eps, steps, warmup, ws_tensor, sample_clocks=False):
+    def timed(eps, steps, warmup, ws_tensor, sample_clocks=False, q_residual=False):
         for _ in range(warmup):
-            apa.attention(tq, tk, tv, causal=w.causal, eps=eps, workspace=ws_tensor)
+            apa.attention(tq, tk, tv, causal=w.causal, eps=eps, workspace=ws_tensor, q_residual=q_residual)
         torch.cuda.synchronize(dev)
         barrier()
         torch.cuda.synchronize(dev)
@@ -280,7 +280,7 @@ def run_gpu(args):
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         for _ in range(steps):
-            apa.attention(tq, tk, tv, causal=w.causal, eps=eps, workspace=ws_tensor)
+            apa.attention(tq, tk, tv, causal=w.causal, eps=eps, workspace=ws_tensor, q_residual=q_residual)
         e1.record(stream)
         torch.cuda.synchronize(dev)
         barrier()
@@ -335,6 +335,14 @@ def run_gpu(args):
         ms0 = max_over_ranks(ms0)
         line["eps0_all_bf16"] = {"ms_per_step": ms0, "tflops": world * flops_exact / (ms0 * 1e-3) / 1e12,
                                  "speedup_of_apa": ms0 / ms}
+        # the accuracy option: Q as two FP4 terms in pass 1 (one block per pass-1 CTA)
+        ws_q2 = torch.empty(apa.workspace_bytes(B, Hq, Hkv, Nq, Nkv, d, w.eps, q_residual=True),
+                            dtype=torch.uint8, device=dev)
+        msq2, stq2, _ = timed(w.eps, max(3, args.steps // 4), 3, ws_q2, q_residual=True)
+        del ws_q2
+        msq2 = max_over_ranks(msq2)
+        line["q_residual"] = {"ms_per_step": msq2, "tflops": world * flops_exact / (msq2 * 1e-3) / 1e12,
+                              "cost_vs_apa": msq2 / ms - 1.0, "stages_ms": stq2}
         # end to end through the host-buffer entry point: H2D of q, k, v from pinned
         # memory, the whole path, D2H of out and lse, every step
         hq, hk, hv = (synth.to_torch_bf16(a).pin_memory() for a in (q, k, v))

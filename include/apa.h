@@ -52,6 +52,10 @@ extern "C" {
 #define APA_ERR_DEVICE (-7)    /* a kernel recorded a device-side timeout (apa_check_error) */
 #define APA_ERR_ALIGN (-8)     /* q, k or v not 16-byte aligned */
 #define APA_ERR_SCRATCH (-9)   /* too large for the fixed scratch of apa_quantize_noalloc */
+#define APA_ERR_FLAGS (-10)    /* an unknown bit in `flags` */
+
+/* Options of the _ex entry points. */
+#define APA_FLAG_Q_RESIDUAL 1u /* Q as two FP4 terms in pass 1 (see apa_attention_ex) */
 
 /* Size of the fixed device scratch array behind apa_quantize_noalloc (16 MiB). */
 #define APA_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
@@ -84,6 +88,21 @@ int apa_attention_ws(const void* q, const void* k, const void* v, int B, int Hq,
                      int causal, float eps, float* out, float* lse, uint32_t* hot_mask, void* workspace,
                      size_t workspace_bytes, cudaStream_t stream);
 
+/* apa_attention() with options (APA_FLAG_*; unknown bits give APA_ERR_FLAGS):
+ *   APA_FLAG_Q_RESIDUAL  Q goes to pass 1 as two FP4 terms ("Second hunt" on the
+ *                        page): Q1 as before and Q2, the FP4 quantization of the
+ *                        residual Q - Q1 under the same FP32 head scale (block
+ *                        scales of its own; residual r = fp32(x - fp32(E2M1 *
+ *                        UE4M3 * s)) per element).  Both terms accumulate into
+ *                        the same S against the same K: twice the QK^T work of
+ *                        pass 1, which then runs one 128-row block per CTA.
+ * `workspace` of at least apa_workspace_bytes_ex() bytes (256-byte aligned), or
+ * null to have it allocated stream-ordered for the call. */
+int apa_attention_ex(const void* q, const void* k, const void* v, int B, int Hq, int Hkv, int Nq, int Nkv, int d,
+                     int causal, float eps, unsigned flags, float* out, float* lse, uint32_t* hot_mask,
+                     void* workspace, size_t workspace_bytes, cudaStream_t stream);
+size_t apa_workspace_bytes_ex(int B, int Hq, int Hkv, int Nq, int Nkv, int d, float eps, unsigned flags);
+
 /* apa_attention() on HOST buffers (page-locked memory recommended): copies q, k,
  * v to the device, runs, copies out (and lse / hot_mask when non-null) back,
  * and synchronizes `stream` before returning.  The results equal those of
@@ -111,6 +130,11 @@ int apa_quantize(const void* q, const void* k, const void* v, int B, int Hq, int
                  uint8_t* kv_blob, uint8_t* q_blob, float* mu, float* s_q, float* s_k, float* s_v,
                  cudaStream_t stream);
 size_t apa_kv_blob_bytes(int B, int Hkv, int Nkv, int d);
+/* apa_quantize() that also writes q2_blob (same layout as q_blob): the codes and
+ * scales of the FP4 residual term of Q (APA_FLAG_Q_RESIDUAL); q2_blob may be null. */
+int apa_quantize_ex(const void* q, const void* k, const void* v, int B, int Hq, int Hkv, int Nq, int Nkv, int d,
+                    uint8_t* kv_blob, uint8_t* q_blob, uint8_t* q2_blob, float* mu, float* s_q, float* s_k,
+                    float* s_v, cudaStream_t stream);
 
 /* apa_quantize() for callers that must not allocate device memory during the
  * call: engines that reserve the whole GPU for their own memory arena up front,

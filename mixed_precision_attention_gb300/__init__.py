@@ -19,8 +19,9 @@ from . import _lib
 from ._lib import ApaError, status_string
 
 __all__ = ["attention", "attention_host", "quantize", "quantize_noalloc", "workspace_bytes", "check_error", "ApaError",
-           "status_string", "hot_mask_shape", "TILE", "GROUP_ROWS", "BLOCK_ROWS"]
+           "status_string", "hot_mask_shape", "TILE", "GROUP_ROWS", "BLOCK_ROWS", "FLAG_Q_RESIDUAL"]
 
+FLAG_Q_RESIDUAL = 1  # APA_FLAG_Q_RESIDUAL: Q as two FP4 terms in pass 1
 TILE = 64          # keys per tile
 GROUP_ROWS = 16    # rows per hot-test group
 BLOCK_ROWS = 128   # GQA-packed rows per CTA
@@ -57,12 +58,13 @@ def _check_qkv(q, k, v):
     return B, Hq, k.shape[1], Nq, k.shape[2], d
 
 
-def workspace_bytes(B, Hq, Hkv, Nq, Nkv, d, eps):
-    return int(_lib.load().apa_workspace_bytes(B, Hq, Hkv, Nq, Nkv, d, float(eps)))
+def workspace_bytes(B, Hq, Hkv, Nq, Nkv, d, eps, q_residual: bool = False):
+    flags = FLAG_Q_RESIDUAL if q_residual else 0
+    return int(_lib.load().apa_workspace_bytes_ex(B, Hq, Hkv, Nq, Nkv, d, float(eps), flags))
 
 
 def attention(q, k, v, causal: bool = True, eps: float = 0.005, return_hot_mask: bool = False,
-              return_lse: bool = True, workspace=None):
+              return_lse: bool = True, workspace=None, q_residual: bool = False):
     """Adaptive-precision attention.
 
     q: [B, Hq, Nq, d] bf16; k, v: [B, Hkv, Nkv, d] bf16 (CUDA, contiguous).
@@ -72,6 +74,7 @@ def attention(q, k, v, causal: bool = True, eps: float = 0.005, return_hot_mask:
     hot_mask is int32 [B, Hkv, ceil(G*Nq/16), ceil(T/32)] holding uint32 bit
     words (bit t%32 of word t/32: tile t hot for that 16-row group).
     workspace: optional uint8 CUDA tensor of at least workspace_bytes(...) bytes.
+    q_residual: Q as two FP4 terms in pass 1 (apa_attention_ex, APA_FLAG_Q_RESIDUAL).
     """
     import torch
     lib = _lib.load()
@@ -80,13 +83,19 @@ def attention(q, k, v, causal: bool = True, eps: float = 0.005, return_hot_mask:
     out = torch.empty((B, Hq, Nq, d), dtype=torch.float32, device=dev)
     lse = torch.empty((B, Hq, Nq), dtype=torch.float32, device=dev) if return_lse else None
     mask = torch.empty(hot_mask_shape(B, Hq, Hkv, Nq, Nkv), dtype=torch.int32, device=dev) if return_hot_mask else None
-    need = workspace_bytes(B, Hq, Hkv, Nq, Nkv, d, eps)
+    need = workspace_bytes(B, Hq, Hkv, Nq, Nkv, d, eps, q_residual)
     if workspace is None and need:
         workspace = torch.empty(need, dtype=torch.uint8, device=dev)
     nbytes = 0 if workspace is None else workspace.numel()
-    st = lib.apa_attention_ws(_ptr(q), _ptr(k), _ptr(v), B, Hq, Hkv, Nq, Nkv, d, int(bool(causal)), float(eps),
-                              _ptr(out), _ptr(lse), _ptr(mask), _ptr(workspace), nbytes, _stream(dev))
-    _lib.check(st, "apa_attention_ws")
+    if q_residual:
+        st = lib.apa_attention_ex(_ptr(q), _ptr(k), _ptr(v), B, Hq, Hkv, Nq, Nkv, d, int(bool(causal)), float(eps),
+                                  FLAG_Q_RESIDUAL, _ptr(out), _ptr(lse), _ptr(mask), _ptr(workspace), nbytes,
+                                  _stream(dev))
+        _lib.check(st, "apa_attention_ex")
+    else:
+        st = lib.apa_attention_ws(_ptr(q), _ptr(k), _ptr(v), B, Hq, Hkv, Nq, Nkv, d, int(bool(causal)), float(eps),
+                                  _ptr(out), _ptr(lse), _ptr(mask), _ptr(workspace), nbytes, _stream(dev))
+        _lib.check(st, "apa_attention_ws")
     return out, lse, mask
 
 
@@ -119,9 +128,10 @@ def attention_host(q, k, v, causal: bool = True, eps: float = 0.005, return_hot_
     return out, lse, mask
 
 
-def quantize(q, k, v):
-    """The pass-1 NVFP4 operands (apa_quantize): dict of CUDA tensors
-    kv_blob, q_blob (uint8), mu [B,Hkv,d], s_q [B,Hq], s_k, s_v [B,Hkv] (fp32)."""
+def quantize(q, k, v, q_residual: bool = False):
+    """The pass-1 NVFP4 operands (apa_quantize_ex): dict of CUDA tensors
+    kv_blob, q_blob (uint8), mu [B,Hkv,d], s_q [B,Hq], s_k, s_v [B,Hkv] (fp32);
+    with q_residual also q2_blob (uint8, q_blob's layout), the FP4 residual of Q."""
     import torch
     lib = _lib.load()
     B, Hq, Hkv, Nq, Nkv, d = _check_qkv(q, k, v)
@@ -132,9 +142,12 @@ def quantize(q, k, v):
              s_q=torch.empty((B, Hq), dtype=torch.float32, device=dev),
              s_k=torch.empty((B, Hkv), dtype=torch.float32, device=dev),
              s_v=torch.empty((B, Hkv), dtype=torch.float32, device=dev))
-    st = lib.apa_quantize(_ptr(q), _ptr(k), _ptr(v), B, Hq, Hkv, Nq, Nkv, d, _ptr(r["kv_blob"]), _ptr(r["q_blob"]),
-                          _ptr(r["mu"]), _ptr(r["s_q"]), _ptr(r["s_k"]), _ptr(r["s_v"]), _stream(dev))
-    _lib.check(st, "apa_quantize")
+    if q_residual:
+        r["q2_blob"] = torch.empty_like(r["q_blob"])
+    st = lib.apa_quantize_ex(_ptr(q), _ptr(k), _ptr(v), B, Hq, Hkv, Nq, Nkv, d, _ptr(r["kv_blob"]),
+                             _ptr(r["q_blob"]), _ptr(r.get("q2_blob")), _ptr(r["mu"]), _ptr(r["s_q"]), _ptr(r["s_k"]),
+                             _ptr(r["s_v"]), _stream(dev))
+    _lib.check(st, "apa_quantize_ex")
     return r
 
 

@@ -47,7 +47,7 @@ int validate(const void* q, const void* k, const void* v, const float* out, int 
 
 }  // namespace
 
-// Per-device staging of the host-buffer entry point (apa.cu).
+// Per-device staging of the host-buffer entry point.
 constexpr int kHostLanes = 8;  // compute streams of the host-buffer entry point
 struct HostStaging {
   std::mutex mu;
@@ -109,7 +109,7 @@ int* device_error_word() {
   return addr[dev];
 }
 
-size_t workspace_layout(const Shape& s, bool apa_mode, Workspace* ws, void* base) {
+size_t workspace_layout(const Shape& s, bool apa_mode, Workspace* ws, void* base, unsigned flags) {
   Workspace w{};
   if (!apa_mode) {
     if (ws) *ws = w;
@@ -140,6 +140,7 @@ size_t workspace_layout(const Shape& s, bool apa_mode, Workspace* ws, void* base
   w.hot_list = (uint32_t*)take(BH * nblk * T * 4);
   w.hot_count = (uint32_t*)take(BH * nblk * 4);
   w.p2_order = (uint32_t*)take(BH * nblk * 4);
+  if (flags & APA_FLAG_Q_RESIDUAL) w.q2_blob = (uint8_t*)take(BH * nblk * qblob_bytes((int)d));
   w.v16 = (uint16_t*)take(BH * s.Nkv * d * 2);
   if (ws) *ws = w;
   return off;
@@ -176,7 +177,8 @@ size_t begin_call() {
 }  // namespace
 
 static int run_attention(const Shape& s, const void* q, const void* k, const void* v, float eps, float* out, float* lse,
-                         uint32_t* hot_mask, void* workspace, cudaStream_t stream, bool wide_pass1 = false) {
+                         uint32_t* hot_mask, void* workspace, cudaStream_t stream, bool wide_pass1 = false,
+                         unsigned flags = 0) {
   const size_t call = begin_call();
   auto stage = [&](int slot) {
     if (call != SIZE_MAX) cudaEventRecord(g_timing.ev[call * 4 + slot], stream);
@@ -191,7 +193,7 @@ static int run_attention(const Shape& s, const void* q, const void* k, const voi
     return st;
   }
   Workspace ws;
-  workspace_layout(s, true, &ws, workspace);
+  workspace_layout(s, true, &ws, workspace, flags);
   stage(0);
   if (hot_mask) {
     const size_t words = (size_t)s.BH() * s.ngroups() * ((s.T() + 31) / 32);
@@ -199,7 +201,7 @@ static int run_attention(const Shape& s, const void* q, const void* k, const voi
   }
   if (launch_quantize(s, q, k, v, ws, true, true, stream) != cudaSuccess) return APA_ERR_CUDA;
   stage(1);
-  if (launch_pass1(s, ws, eps, hot_mask, wide_pass1, stream) != cudaSuccess) return APA_ERR_CUDA;
+  if (launch_pass1(s, ws, eps, hot_mask, wide_pass1 || ws.q2_blob, stream) != cudaSuccess) return APA_ERR_CUDA;
   if (launch_pass2_order(s, ws, stream) != cudaSuccess) return APA_ERR_CUDA;
   stage(2);
   if (launch_pass2(s, q, k, v, &ws, out, lse, stream) != cudaSuccess) return APA_ERR_CUDA;
@@ -240,6 +242,28 @@ int apa_attention(const void* q, const void* k, const void* v, int B, int Hq, in
   if (need && cudaMallocAsync(&ws, need, stream) != cudaSuccess) return APA_ERR_NOMEM;
   st = apa::run_attention(s, q, k, v, eps, out, lse, hot_mask, ws, stream);
   if (ws && cudaFreeAsync(ws, stream) != cudaSuccess && st == APA_OK) st = APA_ERR_CUDA;
+  return st;
+}
+
+size_t apa_workspace_bytes_ex(int B, int Hq, int Hkv, int Nq, int Nkv, int d, float eps, unsigned flags) {
+  if (B < 1 || Hq < 1 || Hkv < 1 || Nq < 1 || Nkv < 1 || Hq % Hkv || (flags & ~APA_FLAG_Q_RESIDUAL)) return 0;
+  Shape s{B, Hq, Hkv, Nq, Nkv, d, 1};
+  return apa::workspace_layout(s, eps != 0.f, nullptr, nullptr, flags);
+}
+
+int apa_attention_ex(const void* q, const void* k, const void* v, int B, int Hq, int Hkv, int Nq, int Nkv, int d,
+                     int causal, float eps, unsigned flags, float* out, float* lse, uint32_t* hot_mask,
+                     void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  int st = apa::validate(q, k, v, out, B, Hq, Hkv, Nq, Nkv, d, causal, eps, true);
+  if (st) return st;
+  if (flags & ~APA_FLAG_Q_RESIDUAL) return APA_ERR_FLAGS;
+  Shape s{B, Hq, Hkv, Nq, Nkv, d, causal ? 1 : 0};
+  const size_t need = apa::workspace_layout(s, eps != 0.f, nullptr, nullptr, flags);
+  void* ws = workspace;
+  if (ws && (workspace_bytes < need || ((uintptr_t)ws & 255))) return APA_ERR_NOMEM;  // as apa_attention_ws
+  if (!ws && need && cudaMallocAsync(&ws, need, stream) != cudaSuccess) return APA_ERR_NOMEM;
+  st = apa::run_attention(s, q, k, v, eps, out, lse, hot_mask, ws, stream, false, flags);
+  if (!workspace && ws && cudaFreeAsync(ws, stream) != cudaSuccess && st == APA_OK) st = APA_ERR_CUDA;
   return st;
 }
 
@@ -325,6 +349,12 @@ size_t apa_q_blob_bytes(int B, int Hq, int Hkv, int Nq, int d) {
 int apa_quantize(const void* q, const void* k, const void* v, int B, int Hq, int Hkv, int Nq, int Nkv, int d,
                  uint8_t* kv_blob, uint8_t* q_blob, float* mu, float* s_q, float* s_k, float* s_v,
                  cudaStream_t stream) {
+  return apa_quantize_ex(q, k, v, B, Hq, Hkv, Nq, Nkv, d, kv_blob, q_blob, nullptr, mu, s_q, s_k, s_v, stream);
+}
+
+int apa_quantize_ex(const void* q, const void* k, const void* v, int B, int Hq, int Hkv, int Nq, int Nkv, int d,
+                    uint8_t* kv_blob, uint8_t* q_blob, uint8_t* q2_blob, float* mu, float* s_q, float* s_k,
+                    float* s_v, cudaStream_t stream) {
   int st = apa::validate(q, k, v, nullptr, B, Hq, Hkv, Nq, Nkv, d, 0, 1.f, false);
   if (st) return st;
   if (!kv_blob || !q_blob || !mu || !s_q || !s_k || !s_v) return APA_ERR_NULL;
@@ -354,6 +384,7 @@ int apa_quantize(const void* q, const void* k, const void* v, int B, int Hq, int
   ws.s_q = s_q;
   ws.kv_blob = kv_blob;
   ws.q_blob = q_blob;
+  ws.q2_blob = q2_blob;
   st = apa::launch_quantize(s, q, k, v, ws, true, true, stream) == cudaSuccess ? APA_OK : APA_ERR_CUDA;
   if (cudaFreeAsync(scratch, stream) != cudaSuccess && st == APA_OK) st = APA_ERR_CUDA;
   return st;
@@ -410,6 +441,7 @@ const char* apa_status_string(int status) {
     case APA_ERR_DEVICE: return "a kernel timed out waiting on the device";
     case APA_ERR_ALIGN: return "q, k and v must be 16-byte aligned";
     case APA_ERR_SCRATCH: return "problem too large for the fixed scratch of apa_quantize_noalloc";
+    case APA_ERR_FLAGS: return "unknown option flag";
   }
   return "unknown status";
 }

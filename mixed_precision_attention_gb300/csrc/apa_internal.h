@@ -80,6 +80,7 @@ struct Workspace {
   float* s_q;         // [B*Hq]
   uint8_t* kv_blob;   // [BH][T][blob_bytes(d)]
   uint8_t* q_blob;    // [BH][nblk][qblob_bytes(d)]
+  uint8_t* q2_blob;   // [BH][nblk][qblob_bytes(d)] the FP4 residual term of Q, or null
   uint16_t* v16;      // [BH][Nkv][d] FP16 copy of V / v16_scale(max |v|) for pass 2, or null
   // pass 1 -> pass 2
   float* state_o;     // [BH][nblk*128][d]: pass-1 o (scaled by s_v)
@@ -88,7 +89,8 @@ struct Workspace {
   uint32_t* hot_count;// [BH*nblk]
   uint32_t* p2_order; // [BH*nblk]: pass-2 work items (bh * nblk + blk), longest hot list first
 };
-size_t workspace_layout(const Shape& s, bool apa_mode, Workspace* ws, void* base);
+// flags: APA_FLAG_* of apa.h (APA_FLAG_Q_RESIDUAL adds the residual Q blob)
+size_t workspace_layout(const Shape& s, bool apa_mode, Workspace* ws, void* base, unsigned flags = 0);
 
 // Power-of-two divisor that brings a head's V into FP16 range: 1 when max |v| is
 // at most 2^15, else 2^(e - 14) for max |v| in [2^e, 2^(e+1)).  Dividing by it is

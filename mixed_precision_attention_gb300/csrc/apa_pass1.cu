@@ -49,6 +49,7 @@ struct P1Params {
   Shape s;
   const uint8_t* kv_blob;
   const uint8_t* q_blob;
+  const uint8_t* q2_blob;  // the FP4 residual term of Q, or null (one-block kernel only)
   const float* s_k;
   const float* s_v;
   const float* s_q;
@@ -77,10 +78,13 @@ struct P1Cfg {
   static constexpr int kOnesOff = kPOff + NP * 4096;    // 16 rows x 32 B of E2M1 1.0
   static constexpr int kOnesSfOff = kOnesOff + 512;     // 512-B scale atom of UE4M3 1.0
   static constexpr int kPsfOff = kOnesSfOff + 512;      // NP x 512-B scale atoms of P
-  static constexpr int kSmem = kPsfOff + NP * 512 + 128;
+  static constexpr int kQ2Off = (kPsfOff + NP * 512 + 1023) / 1024 * 1024;  // residual Q blob
+  static constexpr int kSmem = kQ2Off + kQBlob + 128;
   static constexpr uint32_t kTmemCols = D <= 128 ? 256 : 512;
   static constexpr uint32_t kSfc = 4 * sf_chunks(D);  // TMEM columns of one K or V scale set
-  static constexpr uint32_t kO = 0, kS = D, kL = D + 64, kSFQ = D + 80;
+  // kL: the ones-MMA row sums, or (register row sums) the scales of the residual Q term
+  static constexpr uint32_t kO = 0, kS = D, kL = D + 64, kSFQ = D + 80, kSFQ2 = kL;
+  static_assert(4 * (D / 64) <= 16, "residual Q scales fit the row-sum columns");
   static constexpr uint32_t kSFK = kSFQ + 4 * (D / 64);  // 3 buffers (tile % 3)
   static constexpr uint32_t kSFV = kSFK + 3 * kSfc;      // 3 buffers (tile % 3)
   static constexpr uint32_t kSFP = kSFV + 3 * kSfc;      // NP buffers (tile % NP)
@@ -252,8 +256,10 @@ __global__ void __launch_bounds__(kThreads, (D <= 128 ? 2 : 1)) pass1_kernel(con
     // ------------------------------------------------------------ bulk-copy producer
     if (lane == 0) {
       const uint8_t* qsrc = p.q_blob + ((size_t)bh * nblk + blk) * C::kQBlob;
-      mbar_arrive_expect_tx(q_full, C::kQBlob);
+      const bool q2 = !kOnesMma && p.q2_blob;
+      mbar_arrive_expect_tx(q_full, q2 ? 2 * C::kQBlob : C::kQBlob);
       bulk_g2s(sbase + C::kQOff, qsrc, C::kQBlob, q_full);
+      if (q2) bulk_g2s(sbase + C::kQ2Off, p.q2_blob + ((size_t)bh * nblk + blk) * C::kQBlob, C::kQBlob, q_full);
       int issued = 0;
       for (int i = 0; i < n; ++i) {
         const int st = i % C::NS;
@@ -280,6 +286,11 @@ __global__ void __launch_bounds__(kThreads, (D <= 128 ? 2 : 1)) pass1_kernel(con
 #pragma unroll
         for (int a = 0; a < D / 64; ++a)
           tmem_cp_32x128b_x4(tmem + C::kSFQ + 4 * a, smem_desc(sbase + C::kQOff + qblob_sf(D) + 512 * a, 128, 128, 0));
+        if (!kOnesMma && p.q2_blob)
+#pragma unroll
+          for (int a = 0; a < D / 64; ++a)
+            tmem_cp_32x128b_x4(tmem + C::kSFQ2 + 4 * a,
+                               smem_desc(sbase + C::kQ2Off + qblob_sf(D) + 512 * a, 128, 128, 0));
         tmem_cp_32x128b_x4(tmem + C::kSFO, smem_desc(sbase + C::kOnesSfOff, 128, 128, 0));
       }
       // S(i) into the single S buffer once tile i-1 has been read out of it
@@ -301,6 +312,15 @@ __global__ void __launch_bounds__(kThreads, (D <= 128 ? 2 : 1)) pass1_kernel(con
           const uint64_t ad = smem_desc(sbase + C::kQOff + 256 * kk, 128, 4 * D, 0);
           const uint64_t bd = smem_desc(blob + blob_kcodes(D) + 256 * kk, 128, 4 * D, 0);
           mma_nvf4(tmem + C::kS, ad, bd, idS, tmem + C::kSFQ + 4 * kk, sfk + 4 * (kk >> 1) + 2 * (kk & 1), kk > 0);
+        }
+        if (!kOnesMma && p.q2_blob) {
+          // the residual term of Q, accumulated into the same S against the same K
+#pragma unroll
+          for (int kk = 0; kk < D / 64; ++kk) {
+            const uint64_t ad = smem_desc(sbase + C::kQ2Off + 256 * kk, 128, 4 * D, 0);
+            const uint64_t bd = smem_desc(blob + blob_kcodes(D) + 256 * kk, 128, 4 * D, 0);
+            mma_nvf4(tmem + C::kS, ad, bd, idS, tmem + C::kSFQ2 + 4 * kk, sfk + 4 * (kk >> 1) + 2 * (kk & 1), 1);
+          }
         }
         mma_commit(s_full);
         return true;
@@ -1145,6 +1165,8 @@ bool single_unit() {
 
 template <int D>
 cudaError_t launch_d(const P1Params& prm, bool wide, cudaStream_t st) {
+  // the residual Q term lives in the one-block kernel with register row sums
+  if (prm.q2_blob) return launch_dv<D, false>(prm, st);
   if (rowsum_by_mma()) return launch_dv<D, true>(prm, st);
   if constexpr (D <= 128) {
     if (!wide && !single_unit()) return launch_multi<D, 3>(prm, st);
@@ -1159,6 +1181,7 @@ cudaError_t launch_pass1(const Shape& s, const Workspace& ws, float eps, uint32_
   prm.s = s;
   prm.kv_blob = ws.kv_blob;
   prm.q_blob = ws.q_blob;
+  prm.q2_blob = ws.q2_blob;
   prm.s_k = ws.s_k;
   prm.s_v = ws.s_v;
   prm.s_q = ws.s_q;

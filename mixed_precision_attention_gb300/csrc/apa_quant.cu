@@ -46,6 +46,12 @@ __device__ __forceinline__ float ue4m3_value(uint32_t code) {
   if (E == 0) return (float)m * 0.001953125f;  // m * 2^-9
   return __uint_as_float(((E + 120u) << 23) | (m << 20));
 }
+// Value of a 4-bit E2M1 code (sign in bit 3): 0, 0.5, 1, 1.5, 2, 3, 4, 6.
+__device__ __forceinline__ float e2m1_value(uint32_t c) {
+  const uint32_t m = c & 7u;
+  const float v = m < 4 ? 0.5f * (float)m : (float)(1u << ((m >> 1) - 1)) * (1.f + 0.5f * (float)(m & 1u));
+  return (c & 8u) ? -v : v;
+}
 __device__ __forceinline__ float head_scale(float amax) { return amax == 0.f ? 1.f : __fdiv_rn(amax, 2688.f); }
 
 // Quantizes 16 values with head scale s; returns the scale code, writes 8 code bytes.
@@ -320,6 +326,8 @@ __global__ void __launch_bounds__(kThreads) quant_kernel(Shape s, const uint16_t
   const int bh = qb / nblk, blk = qb % nblk;
   const int b = bh / s.Hkv, h = bh % s.Hkv;
   uint8_t* img = smem;
+  uint8_t* img2 = smem + qblob_bytes(d);  // the residual term, when asked for
+  const bool q2 = ws.q2_blob != nullptr;
   if (blk == 0)
     for (int g = threadIdx.x; g < G; g += blockDim.x) {
       const int hq = b * s.Hq + h * G + g;
@@ -328,8 +336,8 @@ __global__ void __launch_bounds__(kThreads) quant_kernel(Shape s, const uint16_t
   const int ncb = d / 16;
   for (int it = threadIdx.x; it < kBlockRows * ncb; it += blockDim.x) {
     const int p = it / ncb, cb = it % ncb, P = blk * kBlockRows + p;
-    uint2 codes = make_uint2(0u, 0u);
-    uint32_t sb = 0;
+    uint2 codes = make_uint2(0u, 0u), codes2 = make_uint2(0u, 0u);
+    uint32_t sb = 0, sb2 = 0;
     if (P < R) {
       const int g = P % G, pos = P / G, hq = b * s.Hq + h * G + g;
       const uint4* src = reinterpret_cast<const uint4*>(q + ((size_t)hq * s.Nq + pos) * d + cb * 16);
@@ -341,13 +349,31 @@ __global__ void __launch_bounds__(kThreads) quant_kernel(Shape s, const uint16_t
         x[2 * i] = bf16f(w[i] & 0xFFFF);
         x[2 * i + 1] = bf16f(w[i] >> 16);
       }
-      sb = quant16(x, head_scale(__uint_as_float(ws.qamax[hq])), &codes);
+      const float sq = head_scale(__uint_as_float(ws.qamax[hq]));
+      sb = quant16(x, sq, &codes);
+      if (q2) {
+        // the FP4 residual in the same head scale: r = fp32(x - fp32(E2M1 * UE4M3 * s))
+        // (the product of a code and a scale has at most 7 significant bits: exact)
+        const float sv1 = ue4m3_value(sb);
+        float r[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const uint32_t c = ((i < 8 ? codes.x >> (4 * i) : codes.y >> (4 * (i - 8)))) & 0xFu;
+          r[i] = __fsub_rn(x[i], __fmul_rn(e2m1_value(c) * sv1, sq));
+        }
+        sb2 = quant16(r, sq, &codes2);
+      }
     }
     *reinterpret_cast<uint2*>(img + fp4_kmajor_off(p, cb, d / 2)) = codes;
     img[qblob_sf(d) + (cb >> 2) * 512 + sf_atom_off(p, cb & 3)] = (uint8_t)sb;
+    if (q2) {
+      *reinterpret_cast<uint2*>(img2 + fp4_kmajor_off(p, cb, d / 2)) = codes2;
+      img2[qblob_sf(d) + (cb >> 2) * 512 + sf_atom_off(p, cb & 3)] = (uint8_t)sb2;
+    }
   }
   __syncthreads();
   store_image(ws.q_blob + ((size_t)bh * nblk + blk) * qblob_bytes(d), img, qblob_bytes(d));
+  if (q2) store_image(ws.q2_blob + ((size_t)bh * nblk + blk) * qblob_bytes(d), img2, qblob_bytes(d));
 }
 
 }  // namespace

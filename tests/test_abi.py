@@ -24,11 +24,11 @@ def test_exports_every_declared_symbol(lib):
 
 def test_status_strings(lib):
     seen = set()
-    for s in range(0, -9, -1):
+    for s in range(0, -11, -1):
         text = _lib.status_string(s)
         assert text and text != "unknown status"
         seen.add(text)
-    assert len(seen) == 9
+    assert len(seen) == 11
     assert _lib.status_string(-99) == "unknown status"
 
 
@@ -73,6 +73,20 @@ def test_workspace_too_small_is_rejected(lib):
     assert st == -6
     st = lib.apa_attention_ws(*OK_PTR, 1, 2, 1, 128, 512, 64, 1, 0.005, P(0x40000), None, None,
                               P(0x50010), need, None)  # not 256-byte aligned
+    assert st == -6
+
+
+def test_option_flags(lib):
+    # the residual-Q option needs one more Q blob; unknown bits are rejected before any work
+    base = lib.apa_workspace_bytes_ex(1, 2, 1, 128, 512, 64, 0.005, 0)
+    assert base == lib.apa_workspace_bytes(1, 2, 1, 128, 512, 64, 0.005)
+    q2 = lib.apa_workspace_bytes_ex(1, 2, 1, 128, 512, 64, 0.005, 1)
+    assert q2 >= base + lib.apa_q_blob_bytes(1, 2, 1, 128, 64)
+    assert lib.apa_workspace_bytes_ex(1, 2, 1, 128, 512, 64, 0.005, 2) == 0
+    st = lib.apa_attention_ex(*OK_PTR, 1, 2, 1, 128, 512, 64, 1, 0.005, 2, P(0x40000), None, None, None, 0, None)
+    assert st == -10
+    st = lib.apa_attention_ex(*OK_PTR, 1, 2, 1, 128, 512, 64, 1, 0.005, 1, P(0x40000), None, None,
+                              P(0x50000), q2 - 1, None)
     assert st == -6
 
 

@@ -147,3 +147,31 @@ def test_host_entry_point_reuses_buffers_and_grows():
         assert np.array_equal(out.numpy().astype(np.float64), dev[0])
         assert np.array_equal(lse.numpy().astype(np.float64), dev[1])
     torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("name", ["gqa3_ragged", "batch_ragged_d128", "d256", "long_tail"])
+@pytest.mark.parametrize("eps", [0.005, float("inf")])
+def test_q_residual_matches_two_term_emulation(name, eps):
+    """apa_attention_ex with APA_FLAG_Q_RESIDUAL against the oracle's two-term-Q
+    emulation, with the same bounds as the single-term path; the all-FP4 result
+    also moves closer to exact attention than the single-term one."""
+    import mixed_precision_attention_gb300 as apa
+    w, (q, k, v) = _inputs(name)
+    quant = oracle.QUANT_ALL | oracle.QUANT_Q2
+    ref = oracle.apa(q, k, v, eps=eps, quant=quant)
+    tq, tk, tv = (_gpu.to_dev(a) for a in (q, k, v))
+    o, l, m = apa.attention(tq, tk, tv, causal=True, eps=eps, return_hot_mask=True, q_residual=True)
+    apa.check_error()
+    out, lse = o.cpu().numpy().astype(np.float64), l.cpu().numpy().astype(np.float64)
+    assert np.abs(out - ref["out"]).max() <= 1e-2
+    assert _gpu.cosine(out, ref["out"]) >= 0.9999
+    assert np.abs(lse - ref["lse"]).max() <= 1e-2
+    T = (w.Nkv + 63) // 64
+    g_hot, o_hot = _gpu.hot_bits(m.cpu().numpy().view(np.uint32), T), _gpu.hot_bits(ref["hot_mask"], T)
+    ng = oracle.n_groups(w.Hq, w.Hkv, w.Nq)
+    vis = np.broadcast_to(_gpu.group_visible(w.Hq, w.Hkv, w.Nq, w.Nkv, True, ng, T), g_hot.shape)
+    assert (g_hot == o_hot)[vis].mean() >= 0.999
+    if np.isinf(eps):
+        ex, _ = oracle.exact(q, k, v)
+        one, _, _ = _gpu.run_apa(q, k, v, eps=eps)
+        assert np.linalg.norm(out - ex) < np.linalg.norm(one - ex)

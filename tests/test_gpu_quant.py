@@ -83,3 +83,20 @@ def test_quantizer_deterministic():
     a, b = _quant_gpu(q, k, v), _quant_gpu(q, k, v)
     for n in a:
         assert np.array_equal(a[n], b[n])
+
+
+@pytest.mark.parametrize("case", [CASES[1], CASES[2]])
+def test_q_residual_blob_bit_exact(case):
+    # the FP4 residual term of Q (Q2 = FP4(Q - Q1) under the same head scale)
+    import mixed_precision_attention_gb300 as apa
+    w = synth.small(sink_gain=4.0, **case)
+    q, k, v = synth.generate(w)
+    r = apa.quantize(_gpu.to_dev(q), _gpu.to_dev(k), _gpu.to_dev(v), q_residual=True)
+    apa.check_error()
+    oq = oracle.quantize_q(q, residual=True)
+    qc, qsf, _, _ = _gpu.decode_q_blob(r["q_blob"].cpu().numpy(), w.B, w.Hq, w.Hkv, w.Nq, w.d)
+    assert np.array_equal(qc, oq["codes"]) and np.array_equal(qsf, oq["sf"])
+    c2, s2, pad_c, pad_s = _gpu.decode_q_blob(r["q2_blob"].cpu().numpy(), w.B, w.Hq, w.Hkv, w.Nq, w.d)
+    assert np.array_equal(c2, oq["codes2"]) and np.array_equal(s2, oq["sf2"])
+    assert not pad_c.any() and not pad_s.any()
+    assert oq["sf2"].any()  # the residual is not trivially zero
