@@ -29,6 +29,7 @@ _lib = None
 QUANT_Q, QUANT_K, QUANT_V, QUANT_P = 1, 2, 4, 8
 QUANT_ALL = 15
 QUANT_Q2 = 16  # Q as two FP4 terms, Q1 + FP4(Q - Q1) (needs QUANT_Q)
+QUANT_LSE = 32  # least-squared-error block scales for Q, K and V
 TILE = 64
 GROUP_ROWS = 16
 
@@ -61,10 +62,12 @@ def _load():
             lib.oracle_merge.argtypes = [f64, f64, P, f64, f64, P, i32, P]; lib.oracle_merge.restype = f64
             lib.oracle_exact.argtypes = [P, P, P, i32, i32, i32, i32, i32, i32, i32, P, i64, P, P]
             lib.oracle_exact.restype = None
-            lib.oracle_quantize_kv_head.argtypes = [P, P, i32, i32, P, P, P, P, P, P, P]
+            lib.oracle_quantize_kv_head.argtypes = [P, P, i32, i32, P, P, P, P, P, P, P, i32]
             lib.oracle_quantize_kv_head.restype = None
-            lib.oracle_quantize_q_head.argtypes = [P, i32, i32, P, P, P, P, P]
-            lib.oracle_quantize_residual_blocks.argtypes = [P, i64, f64, P, P, P, P]
+            lib.oracle_quantize_q_head.argtypes = [P, i32, i32, P, P, P, P, P, i32]
+            lib.oracle_quantize_residual_blocks.argtypes = [P, i64, f64, P, P, P, P, i32]
+            lib.oracle_quantize_blocks_mode.argtypes = [P, i64, f64, P, P, i32]
+            lib.oracle_quantize_blocks_mode.restype = None
             lib.oracle_quantize_residual_blocks.restype = None
             lib.oracle_quantize_q_head.restype = None
             lib.oracle_apa.argtypes = [P, P, P, i32, i32, i32, i32, i32, i32, i32, f64, f64, f64, i32,
@@ -108,15 +111,16 @@ def head_scale(amax: float) -> float:
     return _load().oracle_head_scale(float(amax))
 
 
-def quantize_blocks(x: np.ndarray, s: float):
-    """Quantizes float32 values in blocks of 16 (last axis) with head scale s.
+def quantize_blocks(x: np.ndarray, s: float, lse: bool = False):
+    """Quantizes float32 values in blocks of 16 (last axis) with head scale s;
+    lse: least-squared-error block scales instead of the nearest ones.
 
     Returns (codes uint8 same shape as x, sf uint8 with the last axis / 16)."""
     x = np.ascontiguousarray(x, dtype=np.float32)
     assert x.shape[-1] % 16 == 0
     codes = np.empty(x.shape, dtype=np.uint8)
     sf = np.empty(x.shape[:-1] + (x.shape[-1] // 16,), dtype=np.uint8)
-    _load().oracle_quantize_blocks(_ptr(x), x.size // 16, float(s), _ptr(codes), _ptr(sf))
+    _load().oracle_quantize_blocks_mode(_ptr(x), x.size // 16, float(s), _ptr(codes), _ptr(sf), int(lse))
     return codes, sf
 
 
@@ -139,7 +143,7 @@ def merge(m1, l1, o1, m2, l2, o2):
 
 
 # ----------------------------------------------------------------- quantizer
-def quantize_kv(k: np.ndarray, v: np.ndarray):
+def quantize_kv(k: np.ndarray, v: np.ndarray, lse: bool = False):
     """NVFP4 codes of K (centred) and V^T for every (b, KV head).
 
     Returns dict with mu [B,Hkv,d] f32, kcodes [B,Hkv,Nkv,d] u8, ksf [B,Hkv,Nkv,d/16],
@@ -158,12 +162,12 @@ def quantize_kv(k: np.ndarray, v: np.ndarray):
             lib.oracle_quantize_kv_head(_ptr(np.ascontiguousarray(k[b, h])), _ptr(np.ascontiguousarray(v[b, h])),
                                         Nkv, d, _ptr(r["mu"][b, h]), _ptr(r["kcodes"][b, h]),
                                         _ptr(r["ksf"][b, h]), ctypes.byref(sk), _ptr(r["vcodes"][b, h]),
-                                        _ptr(r["vsf"][b, h]), ctypes.byref(sv))
+                                        _ptr(r["vsf"][b, h]), ctypes.byref(sv), int(lse))
             r["s_k"][b, h], r["s_v"][b, h] = sk.value, sv.value
     return r
 
 
-def quantize_q(q: np.ndarray, residual: bool = False):
+def quantize_q(q: np.ndarray, residual: bool = False, lse: bool = False):
     """NVFP4 codes of Q per (b, query head): codes [B,Hq,Nq,d], sf [B,Hq,Nq,d/16], s_q [B,Hq];
     with residual=True also codes2 / sf2, the FP4 residual term Q - Q1 in the same head scale."""
     q = _u16(q)
@@ -180,7 +184,7 @@ def quantize_q(q: np.ndarray, residual: bool = False):
             lib.oracle_quantize_q_head(_ptr(np.ascontiguousarray(q[b, h])), Nq, d, _ptr(codes[b, h]),
                                        _ptr(sf[b, h]), ctypes.byref(s),
                                        _ptr(codes2[b, h]) if residual else None,
-                                       _ptr(sf2[b, h]) if residual else None)
+                                       _ptr(sf2[b, h]) if residual else None, int(lse))
             s_q[b, h] = s.value
     r = dict(codes=codes, sf=sf, s_q=s_q)
     if residual:

@@ -113,7 +113,28 @@ double oracle_head_scale(double amax) {
  * Per block: a = max|x|; scale code sb = UE4M3(fp32(a / fp32(6 s)));
  * if sb == 0 every code is 0, else code = E2M1(fp32(x * fp32(1 / fp32(sb s)))).
  * Dequantized value = E2M1(code) * UE4M3(sb) * s. */
-void oracle_quantize_blocks(const float* x, int64_t nblk, double s, uint8_t* codes, uint8_t* sf) {
+/* E2M1 codes of one block under scale code sb; returns the FP32 sum of squared
+ * errors sum_i fp32(x_i - fp32(E2M1(code_i) * D))^2, accumulated in index order
+ * with every product and sum rounded to FP32 (D = fp32(UE4M3(sb) * s)). */
+static double block_codes(const float* xb, double s, int sb, uint8_t* codes) {
+  double D = f32(oracle_ue4m3_value(sb) * s);
+  double inv = f32(1.0 / D);
+  double err = 0.0;
+  for (int i = 0; i < 16; ++i) {
+    codes[i] = (uint8_t)oracle_e2m1_code(f32((double)xb[i] * inv));
+    double t = f32((double)xb[i] - f32(oracle_e2m1_value(codes[i]) * D));
+    err = f32(err + f32(t * t));
+  }
+  return err;
+}
+
+/* lse != 0: least-squared-error block scales (the APA page, "Second hunt": every
+ * block scale picked from a small set of candidates by least squared error
+ * instead of the nearest one).  Reading taken: the candidates are the nearest
+ * code sb and its neighbours sb - 1 and sb + 1 (within 1..126), tried in that
+ * order; a candidate replaces the current pick only with a strictly smaller
+ * error (block_codes).  An all-zero block keeps code 0. */
+void oracle_quantize_blocks_mode(const float* x, int64_t nblk, double s, uint8_t* codes, uint8_t* sf, int lse) {
   for (int64_t b = 0; b < nblk; ++b) {
     const float* xb = x + b * 16;
     double a = 0.0;
@@ -126,10 +147,24 @@ void oracle_quantize_blocks(const float* x, int64_t nblk, double s, uint8_t* cod
       for (int i = 0; i < 16; ++i) codes[b * 16 + i] = 0;
       continue;
     }
-    double D = f32(oracle_ue4m3_value(sb) * s);
-    double inv = f32(1.0 / D);
-    for (int i = 0; i < 16; ++i) codes[b * 16 + i] = (uint8_t)oracle_e2m1_code(f32((double)xb[i] * inv));
+    double best = block_codes(xb, s, sb, codes + b * 16);
+    if (!lse) continue;
+    const int cand[2] = {sb - 1, sb + 1};
+    for (int j = 0; j < 2; ++j) {
+      if (cand[j] < 1 || cand[j] > 0x7E) continue;
+      uint8_t c2[16];
+      double e = block_codes(xb, s, cand[j], c2);
+      if (e < best) {
+        best = e;
+        sf[b] = (uint8_t)cand[j];
+        memcpy(codes + b * 16, c2, 16);
+      }
+    }
   }
+}
+
+void oracle_quantize_blocks(const float* x, int64_t nblk, double s, uint8_t* codes, uint8_t* sf) {
+  oracle_quantize_blocks_mode(x, nblk, s, codes, sf, 0);
 }
 
 /* The FP4 residual of Q ("Second hunt": Q2 is the FP4 residual Q - Q1 in the
@@ -139,7 +174,7 @@ void oracle_quantize_blocks(const float* x, int64_t nblk, double s, uint8_t* cod
  *   d1 = fp32(q1 * s),  r = fp32(x - d1);
  * then r is quantized like any other 16-value block with scale s. */
 void oracle_quantize_residual_blocks(const float* x, int64_t nblk, double s, const uint8_t* codes1,
-                                     const uint8_t* sf1, uint8_t* codes2, uint8_t* sf2) {
+                                     const uint8_t* sf1, uint8_t* codes2, uint8_t* sf2, int lse) {
   float r[16];
   for (int64_t b = 0; b < nblk; ++b) {
     for (int i = 0; i < 16; ++i) {
@@ -147,7 +182,7 @@ void oracle_quantize_residual_blocks(const float* x, int64_t nblk, double s, con
       double d1 = f32(q1 * s);
       r[i] = (float)f32((double)x[b * 16 + i] - d1);
     }
-    oracle_quantize_blocks(r, 1, s, codes2 + b * 16, sf2 + b);
+    oracle_quantize_blocks_mode(r, 1, s, codes2 + b * 16, sf2 + b, lse);
   }
 }
 
@@ -256,6 +291,7 @@ void oracle_exact(const uint16_t* q, const uint16_t* k, const uint16_t* v, int B
 #define QUANT_V 4
 #define QUANT_P 8
 #define QUANT_Q2 16 /* Q as two FP4 terms, Q1 + FP4(Q - Q1) ("Second hunt"); needs QUANT_Q */
+#define QUANT_LSE 32 /* least-squared-error block scales for Q, K and V ("Second hunt") */
 
 typedef struct {
   double eps;         /* hot-test threshold; 0 = every visible tile hot, +inf = none */
@@ -273,7 +309,7 @@ typedef struct {
  *   vsf [d][Npad/16]  UE4M3 scale codes; *s_v the FP32 head scale. */
 void oracle_quantize_kv_head(const uint16_t* kh, const uint16_t* vh, int Nkv, int d, float* mu,
                              uint8_t* kcodes, uint8_t* ksf, double* s_k, uint8_t* vcodes, uint8_t* vsf,
-                             double* s_v) {
+                             double* s_v, int lse) {
   oracle_key_mean(kh, Nkv, d, mu);
   float* kc = (float*)malloc(sizeof(float) * (size_t)Nkv * d);
   double amax = 0.0;
@@ -282,7 +318,7 @@ void oracle_quantize_kv_head(const uint16_t* kh, const uint16_t* vh, int Nkv, in
     amax = fmax(amax, fabs((double)kc[e]));
   }
   *s_k = oracle_head_scale(amax);
-  oracle_quantize_blocks(kc, (int64_t)Nkv * d / 16, *s_k, kcodes, ksf);
+  oracle_quantize_blocks_mode(kc, (int64_t)Nkv * d / 16, *s_k, kcodes, ksf, lse);
   free(kc);
   int Npad = (Nkv + 15) / 16 * 16;
   amax = 0.0;
@@ -291,7 +327,7 @@ void oracle_quantize_kv_head(const uint16_t* kh, const uint16_t* vh, int Nkv, in
   float* vt = (float*)malloc(sizeof(float) * (size_t)Npad);
   for (int c = 0; c < d; ++c) {
     for (int j = 0; j < Npad; ++j) vt[j] = j < Nkv ? (float)oracle_bf16_to_double(vh[(int64_t)j * d + c]) : 0.0f;
-    oracle_quantize_blocks(vt, Npad / 16, *s_v, vcodes + (int64_t)c * Npad, vsf + (int64_t)c * (Npad / 16));
+    oracle_quantize_blocks_mode(vt, Npad / 16, *s_v, vcodes + (int64_t)c * Npad, vsf + (int64_t)c * (Npad / 16), lse);
   }
   free(vt);
 }
@@ -299,7 +335,7 @@ void oracle_quantize_kv_head(const uint16_t* kh, const uint16_t* vh, int Nkv, in
 /* NVFP4 codes of one query head: codes [Nq][d], sf [Nq][d/16], *s_q; with
  * codes2 / sf2 non-null also the codes of the residual term (same layout). */
 void oracle_quantize_q_head(const uint16_t* qh, int Nq, int d, uint8_t* codes, uint8_t* sf, double* s_q,
-                            uint8_t* codes2, uint8_t* sf2) {
+                            uint8_t* codes2, uint8_t* sf2, int lse) {
   float* x = (float*)malloc(sizeof(float) * (size_t)Nq * d);
   double amax = 0.0;
   for (int64_t e = 0; e < (int64_t)Nq * d; ++e) {
@@ -307,8 +343,8 @@ void oracle_quantize_q_head(const uint16_t* qh, int Nq, int d, uint8_t* codes, u
     amax = fmax(amax, fabs((double)x[e]));
   }
   *s_q = oracle_head_scale(amax);
-  oracle_quantize_blocks(x, (int64_t)Nq * d / 16, *s_q, codes, sf);
-  if (codes2 && sf2) oracle_quantize_residual_blocks(x, (int64_t)Nq * d / 16, *s_q, codes, sf, codes2, sf2);
+  oracle_quantize_blocks_mode(x, (int64_t)Nq * d / 16, *s_q, codes, sf, lse);
+  if (codes2 && sf2) oracle_quantize_residual_blocks(x, (int64_t)Nq * d / 16, *s_q, codes, sf, codes2, sf2, lse);
   free(x);
 }
 
@@ -332,7 +368,7 @@ static void prepare_head(const uint16_t* kh, const uint16_t* vh, int Nkv, int d,
   uint8_t* vcodes = (uint8_t*)malloc((size_t)Npad * d);
   uint8_t* vsf = (uint8_t*)malloc((size_t)Npad * d / 16);
   double s_k, s_v;
-  oracle_quantize_kv_head(kh, vh, Nkv, d, H->mu, kcodes, ksf, &s_k, vcodes, vsf, &s_v);
+  oracle_quantize_kv_head(kh, vh, Nkv, d, H->mu, kcodes, ksf, &s_k, vcodes, vsf, &s_v, (quant & QUANT_LSE) != 0);
   if (quant & QUANT_K) {
     H->s_k = s_k;
     for (int64_t e = 0; e < (int64_t)Nkv * d; ++e)
@@ -374,10 +410,11 @@ static void quantize_q_row(const uint16_t* qr, int d, double s_q, int quant, dou
   uint8_t codes[16], sf, codes2[16], sf2;
   for (int b = 0; b < d / 16; ++b) {
     for (int i = 0; i < 16; ++i) x[i] = (float)oracle_bf16_to_double(qr[b * 16 + i]);
-    oracle_quantize_blocks(x, 1, s_q, codes, &sf);
+    const int lse = (quant & QUANT_LSE) != 0;
+    oracle_quantize_blocks_mode(x, 1, s_q, codes, &sf, lse);
     for (int i = 0; i < 16; ++i) out[b * 16 + i] = oracle_e2m1_value(codes[i]) * oracle_ue4m3_value(sf);
     if (quant & QUANT_Q2) {  /* both terms in units of s_q, accumulated against the same K */
-      oracle_quantize_residual_blocks(x, 1, s_q, codes, &sf, codes2, &sf2);
+      oracle_quantize_residual_blocks(x, 1, s_q, codes, &sf, codes2, &sf2, lse);
       for (int i = 0; i < 16; ++i) out[b * 16 + i] += oracle_e2m1_value(codes2[i]) * oracle_ue4m3_value(sf2);
     }
   }

@@ -49,7 +49,7 @@ def test_representable_q_has_zero_residual():
     c2, f2 = np.zeros_like(c1), np.zeros_like(f1)
     lib = oracle._load()
     lib.oracle_quantize_residual_blocks(oracle._ptr(np.ascontiguousarray(xf)), xf.size // 16, s,
-                                        oracle._ptr(c1), oracle._ptr(f1), oracle._ptr(c2), oracle._ptr(f2))
+                                        oracle._ptr(c1), oracle._ptr(f1), oracle._ptr(c2), oracle._ptr(f2), 0)
     assert np.array_equal(_deq(c1, f1, s).astype(np.float32), xf)  # Q1 holds them up to the FP32 rounding
     assert not c2.any() and not f2.any()
 
