@@ -264,9 +264,10 @@ def run_gpu(args):
     work = algorithmic(w, mask.cpu().numpy())
     flops_exact = w.flops_exact
 
-    def timed(eps, steps, warmup, ws_tensor, sample_clocks=False, q_residual=False):
+    def timed(eps, steps, warmup, ws_tensor, sample_clocks=False, q_residual=False, lse_scales=False):
         for _ in range(warmup):
-            apa.attention(tq, tk, tv, causal=w.causal, eps=eps, workspace=ws_tensor, q_residual=q_residual)
+            apa.attention(tq, tk, tv, causal=w.causal, eps=eps, workspace=ws_tensor, q_residual=q_residual,
+                          lse_scales=lse_scales)
         torch.cuda.synchronize(dev)
         barrier()
         torch.cuda.synchronize(dev)
@@ -280,7 +281,8 @@ def run_gpu(args):
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         for _ in range(steps):
-            apa.attention(tq, tk, tv, causal=w.causal, eps=eps, workspace=ws_tensor, q_residual=q_residual)
+            apa.attention(tq, tk, tv, causal=w.causal, eps=eps, workspace=ws_tensor, q_residual=q_residual,
+                          lse_scales=lse_scales)
         e1.record(stream)
         torch.cuda.synchronize(dev)
         barrier()
@@ -343,6 +345,10 @@ def run_gpu(args):
         msq2 = max_over_ranks(msq2)
         line["q_residual"] = {"ms_per_step": msq2, "tflops": world * flops_exact / (msq2 * 1e-3) / 1e12,
                               "cost_vs_apa": msq2 / ms - 1.0, "stages_ms": stq2}
+        # the other accuracy option: least-squared-error block scales (quantizer only)
+        mslse, stlse, _ = timed(w.eps, max(3, args.steps // 4), 3, workspace, lse_scales=True)
+        mslse = max_over_ranks(mslse)
+        line["lse_scales"] = {"ms_per_step": mslse, "cost_vs_apa": mslse / ms - 1.0, "stages_ms": stlse}
         # end to end through the host-buffer entry point: H2D of q, k, v from pinned
         # memory, the whole path, D2H of out and lse, every step
         hq, hk, hv = (synth.to_torch_bf16(a).pin_memory() for a in (q, k, v))

@@ -56,6 +56,7 @@ extern "C" {
 
 /* Options of the _ex entry points. */
 #define APA_FLAG_Q_RESIDUAL 1u /* Q as two FP4 terms in pass 1 (see apa_attention_ex) */
+#define APA_FLAG_LSE_SCALES 2u /* least-squared-error block scales for Q, K, V (see apa_attention_ex) */
 
 /* Size of the fixed device scratch array behind apa_quantize_noalloc (16 MiB). */
 #define APA_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
@@ -96,6 +97,12 @@ int apa_attention_ws(const void* q, const void* k, const void* v, int B, int Hq,
  *                        UE4M3 * s)) per element).  Both terms accumulate into
  *                        the same S against the same K: twice the QK^T work of
  *                        pass 1, which then runs one 128-row block per CTA.
+ *   APA_FLAG_LSE_SCALES  every block scale of Q, K, V (and of the residual Q
+ *                        term) picked by least squared error instead of the
+ *                        nearest one ("Second hunt"): among the nearest UE4M3
+ *                        code and its two neighbours, tried in that order, the
+ *                        one whose FP32 sum of squared errors over the 16 values
+ *                        (in index order) is strictly smallest.
  * `workspace` of at least apa_workspace_bytes_ex() bytes (256-byte aligned), or
  * null to have it allocated stream-ordered for the call. */
 int apa_attention_ex(const void* q, const void* k, const void* v, int B, int Hq, int Hkv, int Nq, int Nkv, int d,
@@ -130,11 +137,13 @@ int apa_quantize(const void* q, const void* k, const void* v, int B, int Hq, int
                  uint8_t* kv_blob, uint8_t* q_blob, float* mu, float* s_q, float* s_k, float* s_v,
                  cudaStream_t stream);
 size_t apa_kv_blob_bytes(int B, int Hkv, int Nkv, int d);
-/* apa_quantize() that also writes q2_blob (same layout as q_blob): the codes and
- * scales of the FP4 residual term of Q (APA_FLAG_Q_RESIDUAL); q2_blob may be null. */
+/* apa_quantize() with options: q2_blob (nullable, q_blob's layout) receives the
+ * codes and scales of the FP4 residual term of Q (APA_FLAG_Q_RESIDUAL);
+ * APA_FLAG_LSE_SCALES picks every block scale by least squared error.  The flag
+ * APA_FLAG_Q_RESIDUAL is implied by a non-null q2_blob. */
 int apa_quantize_ex(const void* q, const void* k, const void* v, int B, int Hq, int Hkv, int Nq, int Nkv, int d,
-                    uint8_t* kv_blob, uint8_t* q_blob, uint8_t* q2_blob, float* mu, float* s_q, float* s_k,
-                    float* s_v, cudaStream_t stream);
+                    unsigned flags, uint8_t* kv_blob, uint8_t* q_blob, uint8_t* q2_blob, float* mu, float* s_q,
+                    float* s_k, float* s_v, cudaStream_t stream);
 
 /* apa_quantize() for callers that must not allocate device memory during the
  * call: engines that reserve the whole GPU for their own memory arena up front,

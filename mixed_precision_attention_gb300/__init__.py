@@ -19,9 +19,11 @@ from . import _lib
 from ._lib import ApaError, status_string
 
 __all__ = ["attention", "attention_host", "quantize", "quantize_noalloc", "workspace_bytes", "check_error", "ApaError",
-           "status_string", "hot_mask_shape", "TILE", "GROUP_ROWS", "BLOCK_ROWS", "FLAG_Q_RESIDUAL"]
+           "status_string", "hot_mask_shape", "TILE", "GROUP_ROWS", "BLOCK_ROWS", "FLAG_Q_RESIDUAL",
+           "FLAG_LSE_SCALES"]
 
 FLAG_Q_RESIDUAL = 1  # APA_FLAG_Q_RESIDUAL: Q as two FP4 terms in pass 1
+FLAG_LSE_SCALES = 2  # APA_FLAG_LSE_SCALES: least-squared-error block scales for Q, K, V
 TILE = 64          # keys per tile
 GROUP_ROWS = 16    # rows per hot-test group
 BLOCK_ROWS = 128   # GQA-packed rows per CTA
@@ -58,13 +60,17 @@ def _check_qkv(q, k, v):
     return B, Hq, k.shape[1], Nq, k.shape[2], d
 
 
+def _flags(q_residual=False, lse_scales=False):
+    return (FLAG_Q_RESIDUAL if q_residual else 0) | (FLAG_LSE_SCALES if lse_scales else 0)
+
+
 def workspace_bytes(B, Hq, Hkv, Nq, Nkv, d, eps, q_residual: bool = False):
-    flags = FLAG_Q_RESIDUAL if q_residual else 0
+    flags = _flags(q_residual)
     return int(_lib.load().apa_workspace_bytes_ex(B, Hq, Hkv, Nq, Nkv, d, float(eps), flags))
 
 
 def attention(q, k, v, causal: bool = True, eps: float = 0.005, return_hot_mask: bool = False,
-              return_lse: bool = True, workspace=None, q_residual: bool = False):
+              return_lse: bool = True, workspace=None, q_residual: bool = False, lse_scales: bool = False):
     """Adaptive-precision attention.
 
     q: [B, Hq, Nq, d] bf16; k, v: [B, Hkv, Nkv, d] bf16 (CUDA, contiguous).
@@ -75,6 +81,7 @@ def attention(q, k, v, causal: bool = True, eps: float = 0.005, return_hot_mask:
     words (bit t%32 of word t/32: tile t hot for that 16-row group).
     workspace: optional uint8 CUDA tensor of at least workspace_bytes(...) bytes.
     q_residual: Q as two FP4 terms in pass 1 (apa_attention_ex, APA_FLAG_Q_RESIDUAL).
+    lse_scales: least-squared-error block scales for Q, K, V (APA_FLAG_LSE_SCALES).
     """
     import torch
     lib = _lib.load()
@@ -87,10 +94,10 @@ def attention(q, k, v, causal: bool = True, eps: float = 0.005, return_hot_mask:
     if workspace is None and need:
         workspace = torch.empty(need, dtype=torch.uint8, device=dev)
     nbytes = 0 if workspace is None else workspace.numel()
-    if q_residual:
+    if q_residual or lse_scales:
         st = lib.apa_attention_ex(_ptr(q), _ptr(k), _ptr(v), B, Hq, Hkv, Nq, Nkv, d, int(bool(causal)), float(eps),
-                                  FLAG_Q_RESIDUAL, _ptr(out), _ptr(lse), _ptr(mask), _ptr(workspace), nbytes,
-                                  _stream(dev))
+                                  _flags(q_residual, lse_scales), _ptr(out), _ptr(lse), _ptr(mask), _ptr(workspace),
+                                  nbytes, _stream(dev))
         _lib.check(st, "apa_attention_ex")
     else:
         st = lib.apa_attention_ws(_ptr(q), _ptr(k), _ptr(v), B, Hq, Hkv, Nq, Nkv, d, int(bool(causal)), float(eps),
@@ -128,10 +135,11 @@ def attention_host(q, k, v, causal: bool = True, eps: float = 0.005, return_hot_
     return out, lse, mask
 
 
-def quantize(q, k, v, q_residual: bool = False):
+def quantize(q, k, v, q_residual: bool = False, lse_scales: bool = False):
     """The pass-1 NVFP4 operands (apa_quantize_ex): dict of CUDA tensors
     kv_blob, q_blob (uint8), mu [B,Hkv,d], s_q [B,Hq], s_k, s_v [B,Hkv] (fp32);
-    with q_residual also q2_blob (uint8, q_blob's layout), the FP4 residual of Q."""
+    with q_residual also q2_blob (uint8, q_blob's layout), the FP4 residual of Q;
+    lse_scales: least-squared-error block scales."""
     import torch
     lib = _lib.load()
     B, Hq, Hkv, Nq, Nkv, d = _check_qkv(q, k, v)
@@ -144,7 +152,8 @@ def quantize(q, k, v, q_residual: bool = False):
              s_v=torch.empty((B, Hkv), dtype=torch.float32, device=dev))
     if q_residual:
         r["q2_blob"] = torch.empty_like(r["q_blob"])
-    st = lib.apa_quantize_ex(_ptr(q), _ptr(k), _ptr(v), B, Hq, Hkv, Nq, Nkv, d, _ptr(r["kv_blob"]),
+    st = lib.apa_quantize_ex(_ptr(q), _ptr(k), _ptr(v), B, Hq, Hkv, Nq, Nkv, d, _flags(q_residual, lse_scales),
+                             _ptr(r["kv_blob"]),
                              _ptr(r["q_blob"]), _ptr(r.get("q2_blob")), _ptr(r["mu"]), _ptr(r["s_q"]), _ptr(r["s_k"]),
                              _ptr(r["s_v"]), _stream(dev))
     _lib.check(st, "apa_quantize_ex")

@@ -15,6 +15,7 @@ namespace {
 __device__ int g_device_error;  // set by bounded waits that gave up
 
 constexpr size_t kAlign = 256;
+constexpr unsigned kKnownFlags = APA_FLAG_Q_RESIDUAL | APA_FLAG_LSE_SCALES;
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 __global__ void visible_mask_kernel(Shape s, uint32_t* mask) {
@@ -199,7 +200,8 @@ static int run_attention(const Shape& s, const void* q, const void* k, const voi
     const size_t words = (size_t)s.BH() * s.ngroups() * ((s.T() + 31) / 32);
     if (cudaMemsetAsync(hot_mask, 0, words * 4, stream) != cudaSuccess) return APA_ERR_CUDA;
   }
-  if (launch_quantize(s, q, k, v, ws, true, true, stream) != cudaSuccess) return APA_ERR_CUDA;
+  if (launch_quantize(s, q, k, v, ws, true, true, stream, (flags & APA_FLAG_LSE_SCALES) != 0) != cudaSuccess)
+    return APA_ERR_CUDA;
   stage(1);
   if (launch_pass1(s, ws, eps, hot_mask, wide_pass1 || ws.q2_blob, stream) != cudaSuccess) return APA_ERR_CUDA;
   if (launch_pass2_order(s, ws, stream) != cudaSuccess) return APA_ERR_CUDA;
@@ -246,7 +248,7 @@ int apa_attention(const void* q, const void* k, const void* v, int B, int Hq, in
 }
 
 size_t apa_workspace_bytes_ex(int B, int Hq, int Hkv, int Nq, int Nkv, int d, float eps, unsigned flags) {
-  if (B < 1 || Hq < 1 || Hkv < 1 || Nq < 1 || Nkv < 1 || Hq % Hkv || (flags & ~APA_FLAG_Q_RESIDUAL)) return 0;
+  if (B < 1 || Hq < 1 || Hkv < 1 || Nq < 1 || Nkv < 1 || Hq % Hkv || (flags & ~apa::kKnownFlags)) return 0;
   Shape s{B, Hq, Hkv, Nq, Nkv, d, 1};
   return apa::workspace_layout(s, eps != 0.f, nullptr, nullptr, flags);
 }
@@ -256,7 +258,7 @@ int apa_attention_ex(const void* q, const void* k, const void* v, int B, int Hq,
                      void* workspace, size_t workspace_bytes, cudaStream_t stream) {
   int st = apa::validate(q, k, v, out, B, Hq, Hkv, Nq, Nkv, d, causal, eps, true);
   if (st) return st;
-  if (flags & ~APA_FLAG_Q_RESIDUAL) return APA_ERR_FLAGS;
+  if (flags & ~apa::kKnownFlags) return APA_ERR_FLAGS;
   Shape s{B, Hq, Hkv, Nq, Nkv, d, causal ? 1 : 0};
   const size_t need = apa::workspace_layout(s, eps != 0.f, nullptr, nullptr, flags);
   void* ws = workspace;
@@ -349,15 +351,16 @@ size_t apa_q_blob_bytes(int B, int Hq, int Hkv, int Nq, int d) {
 int apa_quantize(const void* q, const void* k, const void* v, int B, int Hq, int Hkv, int Nq, int Nkv, int d,
                  uint8_t* kv_blob, uint8_t* q_blob, float* mu, float* s_q, float* s_k, float* s_v,
                  cudaStream_t stream) {
-  return apa_quantize_ex(q, k, v, B, Hq, Hkv, Nq, Nkv, d, kv_blob, q_blob, nullptr, mu, s_q, s_k, s_v, stream);
+  return apa_quantize_ex(q, k, v, B, Hq, Hkv, Nq, Nkv, d, 0u, kv_blob, q_blob, nullptr, mu, s_q, s_k, s_v, stream);
 }
 
 int apa_quantize_ex(const void* q, const void* k, const void* v, int B, int Hq, int Hkv, int Nq, int Nkv, int d,
-                    uint8_t* kv_blob, uint8_t* q_blob, uint8_t* q2_blob, float* mu, float* s_q, float* s_k,
-                    float* s_v, cudaStream_t stream) {
+                    unsigned flags, uint8_t* kv_blob, uint8_t* q_blob, uint8_t* q2_blob, float* mu, float* s_q,
+                    float* s_k, float* s_v, cudaStream_t stream) {
   int st = apa::validate(q, k, v, nullptr, B, Hq, Hkv, Nq, Nkv, d, 0, 1.f, false);
   if (st) return st;
   if (!kv_blob || !q_blob || !mu || !s_q || !s_k || !s_v) return APA_ERR_NULL;
+  if (flags & ~apa::kKnownFlags) return APA_ERR_FLAGS;
   Shape s{B, Hq, Hkv, Nq, Nkv, d, 0};
   const size_t BH = s.BH(), T = s.T(), BHq = (size_t)B * Hq;
   // scratch: per-tile key sums and the min / max / amax words
@@ -385,7 +388,9 @@ int apa_quantize_ex(const void* q, const void* k, const void* v, int B, int Hq, 
   ws.kv_blob = kv_blob;
   ws.q_blob = q_blob;
   ws.q2_blob = q2_blob;
-  st = apa::launch_quantize(s, q, k, v, ws, true, true, stream) == cudaSuccess ? APA_OK : APA_ERR_CUDA;
+  st = apa::launch_quantize(s, q, k, v, ws, true, true, stream, (flags & APA_FLAG_LSE_SCALES) != 0) == cudaSuccess
+           ? APA_OK
+           : APA_ERR_CUDA;
   if (cudaFreeAsync(scratch, stream) != cudaSuccess && st == APA_OK) st = APA_ERR_CUDA;
   return st;
 }

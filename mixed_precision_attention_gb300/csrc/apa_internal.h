@@ -113,8 +113,9 @@ int* device_error_word();  // library-wide device error word (set by bounded wai
 
 
 // ------------------------------------------------------------------ launchers
+// lse: least-squared-error block scales (APA_FLAG_LSE_SCALES) instead of the nearest ones
 cudaError_t launch_quantize(const Shape& s, const void* q, const void* k, const void* v, const Workspace& ws,
-                            bool do_q, bool do_kv, cudaStream_t st);
+                            bool do_q, bool do_kv, cudaStream_t st, bool lse = false);
 // wide: one 128-row block per CTA (three times the CTAs, each on its own SM when
 // the GPU is otherwise idle, so a single problem finishes sooner) instead of
 // three blocks of one KV head per CTA (the faster choice for a full GPU)

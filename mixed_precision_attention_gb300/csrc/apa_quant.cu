@@ -76,6 +76,51 @@ __device__ __forceinline__ uint32_t quant16(const float* x, float s, uint2* code
   return sb;
 }
 
+// E2M1 codes of 16 values under scale code sb, and the FP32 sum of squared
+// errors sum_i fp32(x_i - fp32(E2M1(code_i) * D))^2 in index order.
+__device__ __forceinline__ float block_codes(const float* x, float s, uint32_t sb, uint2* codes) {
+  const float D = __fmul_rn(ue4m3_value(sb), s);
+  const float inv = __frcp_rn(D);
+  uint32_t w[2] = {0u, 0u};
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const uint32_t byte = cvt_e2m1x2(__fmul_rn(x[2 * i], inv), __fmul_rn(x[2 * i + 1], inv));
+    w[i >> 2] |= byte << (8 * (i & 3));
+  }
+  float err = 0.f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const uint32_t c = (w[i >> 3] >> (4 * (i & 7))) & 0xFu;
+    const float t = __fsub_rn(x[i], __fmul_rn(e2m1_value(c), D));
+    err = __fadd_rn(err, __fmul_rn(t, t));
+  }
+  *codes = make_uint2(w[0], w[1]);
+  return err;
+}
+
+// quant16 with, when lse is set, the block scale picked by least squared error
+// among the nearest code and its two neighbours (tried in that order; only a
+// strictly smaller error replaces the pick).
+__device__ __forceinline__ uint32_t quant16_mode(const float* x, float s, uint2* codes, bool lse) {
+  uint32_t sb = quant16(x, s, codes);
+  if (!lse || sb == 0) return sb;
+  const uint32_t nearest = sb;
+  float best = block_codes(x, s, nearest, codes);
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    const uint32_t c = j == 0 ? nearest - 1 : nearest + 1;
+    if (c < 1 || c > 0x7E) continue;
+    uint2 c2;
+    const float e = block_codes(x, s, c, &c2);
+    if (e < best) {
+      best = e;
+      sb = c;
+      *codes = c2;
+    }
+  }
+  return sb;
+}
+
 // One elected thread brings rows [j0, j0 + nk) of the K and V slices of a tile
 // into shared memory with two bulk copies (rows are 2d bytes, a multiple of 16;
 // the slices start on 16-byte boundaries).  Every thread then waits, bounded;
@@ -233,7 +278,7 @@ __device__ __forceinline__ void store_image(uint8_t* dst, const uint8_t* img, in
 __global__ void __launch_bounds__(kThreads) quant_kernel(Shape s, const uint16_t* __restrict__ q,
                                                           const uint16_t* __restrict__ k,
                                                           const uint16_t* __restrict__ v, Workspace ws,
-                                                          int n_kv_blocks, int do_kv, int* err) {
+                                                          int n_kv_blocks, int do_kv, int* err, int lse) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ __align__(8) uint64_t bar;
   const int d = s.d, T = s.T();
@@ -278,7 +323,7 @@ __global__ void __launch_bounds__(kThreads) quant_kernel(Shape s, const uint16_t
           x[2 * i + 1] = __fsub_rn(bf16f(w[i] >> 16), mu16[2 * i + 1]);
         }
         uint2 codes;
-        const uint32_t sb = quant16(x, sk, &codes);
+        const uint32_t sb = quant16_mode(x, sk, &codes, lse);
         *reinterpret_cast<uint2*>(img + blob_kcodes(d) + fp4_kmajor_off(n, cb, d / 2)) = codes;
         const int kb = cb >> 2, k16 = cb & 3;
         img[blob_ksf(d) + (kb >> 1) * 512 + (n & 31) * 16 + ((n >> 5) + 2 * (kb & 1)) * 4 + k16] = (uint8_t)sb;
@@ -298,7 +343,7 @@ __global__ void __launch_bounds__(kThreads) quant_kernel(Shape s, const uint16_t
       for (int e = 0; e < 2; ++e) {
         const int c = 2 * cp + e;
         uint2 codes;
-        const uint32_t sb = quant16(e ? x1 : x0, sv, &codes);
+        const uint32_t sb = quant16_mode(e ? x1 : x0, sv, &codes, lse);
         *reinterpret_cast<uint2*>(img + blob_vcodes(d) + fp4_kmajor_off(c, kb16, 32)) = codes;
         img[blob_vsf(d) + (c >> 7) * 512 + sf_atom_off(c & 127, kb16)] = (uint8_t)sb;
       }
@@ -350,7 +395,7 @@ __global__ void __launch_bounds__(kThreads) quant_kernel(Shape s, const uint16_t
         x[2 * i + 1] = bf16f(w[i] >> 16);
       }
       const float sq = head_scale(__uint_as_float(ws.qamax[hq]));
-      sb = quant16(x, sq, &codes);
+      sb = quant16_mode(x, sq, &codes, lse);
       if (q2) {
         // the FP4 residual in the same head scale: r = fp32(x - fp32(E2M1 * UE4M3 * s))
         // (the product of a code and a scale has at most 7 significant bits: exact)
@@ -361,7 +406,7 @@ __global__ void __launch_bounds__(kThreads) quant_kernel(Shape s, const uint16_t
           const uint32_t c = ((i < 8 ? codes.x >> (4 * i) : codes.y >> (4 * (i - 8)))) & 0xFu;
           r[i] = __fsub_rn(x[i], __fmul_rn(e2m1_value(c) * sv1, sq));
         }
-        sb2 = quant16(r, sq, &codes2);
+        sb2 = quant16_mode(r, sq, &codes2, lse);
       }
     }
     *reinterpret_cast<uint2*>(img + fp4_kmajor_off(p, cb, d / 2)) = codes;
@@ -379,7 +424,7 @@ __global__ void __launch_bounds__(kThreads) quant_kernel(Shape s, const uint16_t
 }  // namespace
 
 cudaError_t launch_quantize(const Shape& s, const void* q, const void* k, const void* v, const Workspace& ws,
-                            bool do_q, bool do_kv, cudaStream_t st) {
+                            bool do_q, bool do_kv, cudaStream_t st, bool lse) {
   const int BH = s.BH(), d = s.d, T = s.T();
   int* err = device_error_word();
   cudaError_t e;
@@ -412,7 +457,7 @@ cudaError_t launch_quantize(const Shape& s, const void* q, const void* k, const 
     return e;
   if (n_kv + n_qb > 0)
     quant_kernel<<<n_kv + n_qb, kThreads, sm2, st>>>(s, (const uint16_t*)q, (const uint16_t*)k, (const uint16_t*)v,
-                                                     ws, n_kv, do_kv, err);
+                                                     ws, n_kv, do_kv, err, lse ? 1 : 0);
   return cudaGetLastError();
 }
 

@@ -175,3 +175,27 @@ def test_q_residual_matches_two_term_emulation(name, eps):
         ex, _ = oracle.exact(q, k, v)
         one, _, _ = _gpu.run_apa(q, k, v, eps=eps)
         assert np.linalg.norm(out - ex) < np.linalg.norm(one - ex)
+
+
+@pytest.mark.parametrize("name", ["gqa3_ragged", "batch_ragged_d128", "d256"])
+@pytest.mark.parametrize("q_residual", [False, True])
+def test_lse_scales_match_emulation(name, q_residual):
+    """APA_FLAG_LSE_SCALES (with and without the residual Q term) against the
+    oracle's emulation with the same scale choice."""
+    import mixed_precision_attention_gb300 as apa
+    w, (q, k, v) = _inputs(name)
+    quant = oracle.QUANT_ALL | oracle.QUANT_LSE | (oracle.QUANT_Q2 if q_residual else 0)
+    ref = oracle.apa(q, k, v, eps=0.005, quant=quant)
+    tq, tk, tv = (_gpu.to_dev(a) for a in (q, k, v))
+    o, l, m = apa.attention(tq, tk, tv, causal=True, eps=0.005, return_hot_mask=True, q_residual=q_residual,
+                            lse_scales=True)
+    apa.check_error()
+    out, lse = o.cpu().numpy().astype(np.float64), l.cpu().numpy().astype(np.float64)
+    assert np.abs(out - ref["out"]).max() <= 1e-2
+    assert _gpu.cosine(out, ref["out"]) >= 0.9999
+    assert np.abs(lse - ref["lse"]).max() <= 1e-2
+    T = (w.Nkv + 63) // 64
+    g_hot, o_hot = _gpu.hot_bits(m.cpu().numpy().view(np.uint32), T), _gpu.hot_bits(ref["hot_mask"], T)
+    ng = oracle.n_groups(w.Hq, w.Hkv, w.Nq)
+    vis = np.broadcast_to(_gpu.group_visible(w.Hq, w.Hkv, w.Nq, w.Nkv, True, ng, T), g_hot.shape)
+    assert (g_hot == o_hot)[vis].mean() >= 0.999

@@ -100,3 +100,27 @@ def test_q_residual_blob_bit_exact(case):
     assert np.array_equal(c2, oq["codes2"]) and np.array_equal(s2, oq["sf2"])
     assert not pad_c.any() and not pad_s.any()
     assert oq["sf2"].any()  # the residual is not trivially zero
+
+
+@pytest.mark.parametrize("case", [CASES[0], CASES[1], CASES[2]])
+def test_lse_scales_bit_exact(case):
+    # least-squared-error block scales (APA_FLAG_LSE_SCALES) for K, V, Q and the residual Q
+    import mixed_precision_attention_gb300 as apa
+    w = synth.small(sink_gain=4.0, **case)
+    q, k, v = synth.generate(w)
+    B, Hq, Hkv, Nq, Nkv, d = w.B, w.Hq, w.Hkv, w.Nq, w.Nkv, w.d
+    r = apa.quantize(_gpu.to_dev(q), _gpu.to_dev(k), _gpu.to_dev(v), q_residual=True, lse_scales=True)
+    apa.check_error()
+    g = {n: t.cpu().numpy() for n, t in r.items()}
+    ok = oracle.quantize_kv(k, v, lse=True)
+    oq = oracle.quantize_q(q, residual=True, lse=True)
+    kc, ksf, vc, vsf = _gpu.decode_kv_blob(g["kv_blob"], B, Hkv, Nkv, d)
+    assert np.array_equal(kc[:, :, :Nkv], ok["kcodes"]) and np.array_equal(ksf[:, :, :Nkv], ok["ksf"])
+    Npad = ok["vcodes"].shape[-1]
+    assert np.array_equal(vc[..., :Npad], ok["vcodes"]) and np.array_equal(vsf[..., :Npad // 16], ok["vsf"])
+    qc, qsf, _, _ = _gpu.decode_q_blob(g["q_blob"], B, Hq, Hkv, Nq, d)
+    assert np.array_equal(qc, oq["codes"]) and np.array_equal(qsf, oq["sf"])
+    c2, s2, _, _ = _gpu.decode_q_blob(g["q2_blob"], B, Hq, Hkv, Nq, d)
+    assert np.array_equal(c2, oq["codes2"]) and np.array_equal(s2, oq["sf2"])
+    near = oracle.quantize_kv(k, v)
+    assert (near["ksf"] != ok["ksf"]).any()  # the choice is not just the nearest scale
