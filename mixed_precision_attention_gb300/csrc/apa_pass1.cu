@@ -608,17 +608,18 @@ __global__ void __launch_bounds__(kThreads, (D <= 128 ? 2 : 1)) pass1_kernel(con
         uint32_t sfw = 0x08080808u;  // 2^-6 where nothing is visible
         float ell = 0.f;             // l_t: exact sum of the quantized P of this row
         if (!empty) {
-          sfw = 0;
+          // the four group scales, clamped at 2^-6 (code 8), converted and decoded in pairs
+          float gs[4], scv[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) gs[k] = ex2_approx(fmaf(g[k], cs, -mt)) * (1.f / 6.f);
+          sfw = cvt_ue4m3x4_min(gs[0], gs[1], gs[2], gs[3], 8u);
+          ue4m3x4_values(sfw, scv);
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
-            uint32_t sc = cvt_ue4m3(ex2_approx(fmaf(g[k], cs, -mt)) * (1.f / 6.f));
-            sc = max(sc, 8u);  // clamp the group scale at 2^-6
-            sfw |= sc << (8 * k);
-            const float scv = ue4m3_value(sc);
-            const float nb = -(mt + lg2_approx(scv));
+            const float nb = -(mt + lg2_approx(scv[k]));
 #pragma unroll
             for (int w = 0; w < 2; ++w) pw[2 * k + w] = encode8(raw + 16 * k + 8 * w, cs, nb);
-            ell = fmaf((float)(code_sum2(pw[2 * k]) + code_sum2(pw[2 * k + 1])), 0.5f * scv, ell);
+            ell = fmaf((float)(code_sum2(pw[2 * k]) + code_sum2(pw[2 * k + 1])), 0.5f * scv[k], ell);
           }
         } else {
 #pragma unroll
@@ -1007,17 +1008,18 @@ __global__ void __launch_bounds__(P1MCfg<D, U>::kThreads, 1) pass1_multi_kernel(
       uint32_t sfw = 0x08080808u;  // 2^-6 where nothing is visible
       float ell = 0.f;             // l_t: exact sum of the quantized P of this row
       if (!empty) {
-        sfw = 0;
+        // the four group scales, clamped at 2^-6 (code 8), converted and decoded in pairs
+        float gs[4], scv[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) gs[k] = ex2_approx(fmaf(g[k], cs, -mt)) * (1.f / 6.f);
+        sfw = cvt_ue4m3x4_min(gs[0], gs[1], gs[2], gs[3], 8u);
+        ue4m3x4_values(sfw, scv);
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-          uint32_t sc = cvt_ue4m3(ex2_approx(fmaf(g[k], cs, -mt)) * (1.f / 6.f));
-          sc = max(sc, 8u);  // clamp the group scale at 2^-6
-          sfw |= sc << (8 * k);
-          const float scv = ue4m3_value(sc);
-          const float nb = -(mt + lg2_approx(scv));
+          const float nb = -(mt + lg2_approx(scv[k]));
 #pragma unroll
           for (int w = 0; w < 2; ++w) pw[2 * k + w] = encode8(raw + 16 * k + 8 * w, cs, nb);
-          ell = fmaf((float)(code_sum2(pw[2 * k]) + code_sum2(pw[2 * k + 1])), 0.5f * scv, ell);
+          ell = fmaf((float)(code_sum2(pw[2 * k]) + code_sum2(pw[2 * k + 1])), 0.5f * scv[k], ell);
         }
       } else {
 #pragma unroll

@@ -8,6 +8,7 @@
 // a kernel can unwind instead of spinning forever.
 #pragma once
 #include <cstdint>
+#include <cuda_fp16.h>
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -255,11 +256,12 @@ __device__ __forceinline__ void tmem_st_x16(uint32_t taddr, const uint32_t* r) {
 }
 
 // ------------------------------------------------------------------ converts
+// (pure arithmetic: not volatile, so the compiler may schedule them freely)
 // Two FP32 values -> one byte of two E2M1 codes (round to nearest even, saturating):
 // `lo` goes to bits 0-3, `hi` to bits 4-7.
 __device__ __forceinline__ uint32_t cvt_e2m1x2(float lo, float hi) {
   uint32_t r;
-  asm volatile(
+  asm(
       "{\n.reg .b8 t;\n"
       "cvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n"
       "cvt.u32.u8 %0, t;\n}"
@@ -270,12 +272,35 @@ __device__ __forceinline__ uint32_t cvt_e2m1x2(float lo, float hi) {
 // Non-negative FP32 -> UE4M3 code byte (round to nearest even, saturating at 448).
 __device__ __forceinline__ uint32_t cvt_ue4m3(float x) {
   uint16_t r;
-  asm volatile("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(0.0f), "f"(x));
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(0.0f), "f"(x));
   return r & 0xFFu;
+}
+// Four non-negative FP32 values -> four UE4M3 code bytes (x0 in the lowest), each
+// rounded to nearest even, saturating at 448 and clamped below at code `lo`
+// (byte-wise unsigned maximum).
+__device__ __forceinline__ uint32_t cvt_ue4m3x4_min(float x0, float x1, float x2, float x3, uint32_t lo) {
+  uint16_t a, b;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(a) : "f"(x1), "f"(x0));
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(b) : "f"(x3), "f"(x2));
+  const uint32_t w = (uint32_t)a | ((uint32_t)b << 16);
+  return __vmaxu4(w, lo * 0x01010101u);
+}
+// The values of four UE4M3 code bytes (codes < 0x80; E4M3 and UE4M3 agree there),
+// exactly, through FP16.
+__device__ __forceinline__ void ue4m3x4_values(uint32_t w, float* v) {
+  uint32_t h01, h23;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h01) : "h"((uint16_t)(w & 0xFFFFu)));
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h23) : "h"((uint16_t)(w >> 16)));
+  const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&h01));
+  const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&h23));
+  v[0] = a.x;
+  v[1] = a.y;
+  v[2] = b.x;
+  v[3] = b.y;
 }
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;
-  asm volatile("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
 __device__ __forceinline__ float max3(float a, float b, float c) {
