@@ -30,6 +30,7 @@ QUANT_Q, QUANT_K, QUANT_V, QUANT_P = 1, 2, 4, 8
 QUANT_ALL = 15
 QUANT_Q2 = 16  # Q as two FP4 terms, Q1 + FP4(Q - Q1) (needs QUANT_Q)
 QUANT_LSE = 32  # least-squared-error block scales for Q, K and V
+QUANT_VWEIGHT = 64  # value-norm-weighted hot test (not a quantization)
 TILE = 64
 GROUP_ROWS = 16
 
@@ -67,6 +68,8 @@ def _load():
             lib.oracle_quantize_q_head.argtypes = [P, i32, i32, P, P, P, P, P, i32]
             lib.oracle_quantize_residual_blocks.argtypes = [P, i64, f64, P, P, P, P, i32]
             lib.oracle_quantize_blocks_mode.argtypes = [P, i64, f64, P, P, i32]
+            lib.oracle_value_weights.argtypes = [P, i32, i32, P]
+            lib.oracle_value_weights.restype = None
             lib.oracle_quantize_blocks_mode.restype = None
             lib.oracle_quantize_residual_blocks.restype = None
             lib.oracle_quantize_q_head.restype = None
@@ -190,6 +193,19 @@ def quantize_q(q: np.ndarray, residual: bool = False, lse: bool = False):
     if residual:
         r.update(codes2=codes2, sf2=sf2)
     return r
+
+
+def value_weights(v: np.ndarray):
+    """Value-norm weight of every 64-key tile per (b, KV head): [B, Hkv, T] float32."""
+    v = _u16(v)
+    B, Hkv, Nkv, d = v.shape
+    T = (Nkv + TILE - 1) // TILE
+    w = np.empty((B, Hkv, T), np.float32)
+    lib = _load()
+    for b in range(B):
+        for h in range(Hkv):
+            lib.oracle_value_weights(_ptr(np.ascontiguousarray(v[b, h])), Nkv, d, _ptr(w[b, h]))
+    return w
 
 
 # ----------------------------------------------------------------- attention

@@ -292,6 +292,7 @@ void oracle_exact(const uint16_t* q, const uint16_t* k, const uint16_t* v, int B
 #define QUANT_P 8
 #define QUANT_Q2 16 /* Q as two FP4 terms, Q1 + FP4(Q - Q1) ("Second hunt"); needs QUANT_Q */
 #define QUANT_LSE 32 /* least-squared-error block scales for Q, K and V ("Second hunt") */
+#define QUANT_VWEIGHT 64 /* value-norm-weighted hot test ("Honest limits"); not a quantization */
 
 typedef struct {
   double eps;         /* hot-test threshold; 0 = every visible tile hot, +inf = none */
@@ -355,11 +356,58 @@ typedef struct {
   double* vq;  /* [Nkv][d] pass-1 V (dequantized without s_v when V is quantized) */
   double s_k, s_v;
   float* mu;   /* [d] key mean */
+  float* wv;   /* [T] value-norm weight of each tile (oracle_value_weights) */
 } head_ops;
+
+/* Value-norm weights of one KV head's tiles (the APA page, "Honest limits": the
+ * hot test bounds a cold tile's share of the softmax mass, not of the output; a
+ * test weighted by value norm would target the rows where they differ).  The
+ * page gives no formula; reading taken, with every step rounded to FP32:
+ *   n_j = sqrt(sum_c fp32(v_jc^2)), the sum in channel order;
+ *   a_t = max of n_j over the tile's keys;
+ *   nbar = mean of n_j over all keys: FP32 sums per tile in key order, FP64 sums
+ *          of those per range of 64 tiles and of the ranges, / Nkv, to FP32
+ *          (the key mean's order);
+ *   w_t = a_t / nbar (1 if nbar is 0).
+ * The weighted test is l_t * w_t * 2^(m~ - m) > eps * lambda; lambda stays the
+ * plain mass. */
+void oracle_value_weights(const uint16_t* vh, int Nkv, int d, float* w) {
+  int T = (Nkv + TILE - 1) / TILE;
+  float* amax = (float*)malloc(sizeof(float) * T);
+  float* tsum = (float*)malloc(sizeof(float) * T);
+  for (int t = 0; t < T; ++t) {
+    double a = 0.0, sum = 0.0;
+    int j1 = (t + 1) * TILE < Nkv ? (t + 1) * TILE : Nkv;
+    for (int j = t * TILE; j < j1; ++j) {
+      double acc = 0.0;
+      for (int c = 0; c < d; ++c) {
+        double x = oracle_bf16_to_double(vh[(int64_t)j * d + c]);
+        acc = f32(acc + f32(x * x));
+      }
+      double n = f32(sqrt(acc));
+      a = fmax(a, n);
+      sum = f32(sum + n);
+    }
+    amax[t] = (float)a;
+    tsum[t] = (float)sum;
+  }
+  double S = 0.0;
+  for (int t0 = 0; t0 < T; t0 += MEAN_RANGE_TILES) {
+    double Sr = 0.0;
+    for (int t = t0; t < t0 + MEAN_RANGE_TILES && t < T; ++t) Sr += (double)tsum[t];
+    S += Sr;
+  }
+  double nbar = f32(S / (double)Nkv);
+  for (int t = 0; t < T; ++t) w[t] = nbar == 0.0 ? 1.0f : (float)f32((double)amax[t] / nbar);
+  free(amax);
+  free(tsum);
+}
 
 static void prepare_head(const uint16_t* kh, const uint16_t* vh, int Nkv, int d, int quant, head_ops* H) {
   int T = (Nkv + TILE - 1) / TILE, Npad = (Nkv + 15) / 16 * 16;
   H->Nkv = Nkv; H->d = d; H->T = T;
+  H->wv = (float*)malloc(sizeof(float) * (size_t)T);
+  oracle_value_weights(vh, Nkv, d, H->wv);
   H->kq = (double*)malloc(sizeof(double) * (size_t)Nkv * d);
   H->vq = (double*)malloc(sizeof(double) * (size_t)Nkv * d);
   H->mu = (float*)malloc(sizeof(float) * (size_t)d);
@@ -392,7 +440,7 @@ static void prepare_head(const uint16_t* kh, const uint16_t* vh, int Nkv, int d,
   free(kcodes); free(ksf); free(vcodes); free(vsf);
 }
 
-static void free_head(head_ops* H) { free(H->kq); free(H->vq); free(H->mu); }
+static void free_head(head_ops* H) { free(H->kq); free(H->vq); free(H->mu); free(H->wv); }
 
 /* Q of one query head: per-head scale over the whole (b, h) slice, 16 channels per scale. */
 static double q_head_scale(const uint16_t* qh, int Nq, int d) {
@@ -539,8 +587,9 @@ static void apa_group(const uint16_t* q, const uint16_t* k, const uint16_t* v, i
       for (int r = 0; r < nr; ++r) {
         if (empty[r]) continue;
         if (P->eps == 0.0) { hot = 1; continue; }
-        if (m[r] == -INFINITY) { if (lt[r] > 0.0) hot = 1; continue; }
-        if (lt[r] * exp2(mt[r] - m[r]) > P->eps * lam[r]) hot = 1;
+        double w = (P->quant & QUANT_VWEIGHT) ? (double)H->wv[t] : 1.0;
+        if (m[r] == -INFINITY) { if (lt[r] * w > 0.0) hot = 1; continue; }
+        if (lt[r] * w * exp2(mt[r] - m[r]) > P->eps * lam[r]) hot = 1;
       }
     }
     if (hot) hot_tile[t] = 1.0;
