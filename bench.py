@@ -264,10 +264,11 @@ def run_gpu(args):
     work = algorithmic(w, mask.cpu().numpy())
     flops_exact = w.flops_exact
 
-    def timed(eps, steps, warmup, ws_tensor, sample_clocks=False, q_residual=False, lse_scales=False):
+    def timed(eps, steps, warmup, ws_tensor, sample_clocks=False, q_residual=False, lse_scales=False,
+              value_weighted=False):
         for _ in range(warmup):
             apa.attention(tq, tk, tv, causal=w.causal, eps=eps, workspace=ws_tensor, q_residual=q_residual,
-                          lse_scales=lse_scales)
+                          lse_scales=lse_scales, value_weighted=value_weighted)
         torch.cuda.synchronize(dev)
         barrier()
         torch.cuda.synchronize(dev)
@@ -282,7 +283,7 @@ def run_gpu(args):
         e0.record(stream)
         for _ in range(steps):
             apa.attention(tq, tk, tv, causal=w.causal, eps=eps, workspace=ws_tensor, q_residual=q_residual,
-                          lse_scales=lse_scales)
+                          lse_scales=lse_scales, value_weighted=value_weighted)
         e1.record(stream)
         torch.cuda.synchronize(dev)
         barrier()
@@ -349,6 +350,16 @@ def run_gpu(args):
         mslse, stlse, _ = timed(w.eps, max(3, args.steps // 4), 3, workspace, lse_scales=True)
         mslse = max_over_ranks(mslse)
         line["lse_scales"] = {"ms_per_step": mslse, "cost_vs_apa": mslse / ms - 1.0, "stages_ms": stlse}
+        # the hot test weighted by value norm: its own hot set, so its own pass-2 work
+        ws_vw = torch.empty(apa.workspace_bytes(B, Hq, Hkv, Nq, Nkv, d, w.eps, value_weighted=True),
+                            dtype=torch.uint8, device=dev)
+        _, _, mvw = apa.attention(tq, tk, tv, causal=w.causal, eps=w.eps, return_hot_mask=True, workspace=ws_vw,
+                                  value_weighted=True)
+        msvw, stvw, _ = timed(w.eps, max(3, args.steps // 4), 3, ws_vw, value_weighted=True)
+        del ws_vw
+        msvw = max_over_ranks(msvw)
+        line["value_weighted"] = {"ms_per_step": msvw, "cost_vs_apa": msvw / ms - 1.0, "stages_ms": stvw,
+                                  "hot_pair_frac": algorithmic(w, mvw.cpu().numpy())["hot_pair_frac"]}
         # end to end through the host-buffer entry point: H2D of q, k, v from pinned
         # memory, the whole path, D2H of out and lse, every step
         hq, hk, hv = (synth.to_torch_bf16(a).pin_memory() for a in (q, k, v))

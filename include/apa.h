@@ -57,6 +57,7 @@ extern "C" {
 /* Options of the _ex entry points. */
 #define APA_FLAG_Q_RESIDUAL 1u /* Q as two FP4 terms in pass 1 (see apa_attention_ex) */
 #define APA_FLAG_LSE_SCALES 2u /* least-squared-error block scales for Q, K, V (see apa_attention_ex) */
+#define APA_FLAG_VALUE_WEIGHTED 4u /* hot test weighted by value norm (see apa_attention_ex) */
 
 /* Size of the fixed device scratch array behind apa_quantize_noalloc (16 MiB). */
 #define APA_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
@@ -103,6 +104,17 @@ int apa_attention_ws(const void* q, const void* k, const void* v, int B, int Hq,
  *                        code and its two neighbours, tried in that order, the
  *                        one whose FP32 sum of squared errors over the 16 values
  *                        (in index order) is strictly smallest.
+ *   APA_FLAG_VALUE_WEIGHTED  the hot test weighted by value norm ("Honest
+ *                        limits" on the page: the plain test bounds a cold
+ *                        tile's share of the softmax mass, not of the output):
+ *                        tile t is hot iff some row has w_t * l_t > eps * lambda,
+ *                        w_t = (largest key value norm in the tile) / (mean key
+ *                        value norm of the head); norms are FP32 sums of FP32
+ *                        squares in channel order with a rounded square root,
+ *                        the mean follows the key mean's summation order.
+ *                        lambda stays the plain running sum.  A cold tile then
+ *                        moves each output row by at most eps times the mean
+ *                        value norm.  Costs 8 bytes of workspace per tile.
  * `workspace` of at least apa_workspace_bytes_ex() bytes (256-byte aligned), or
  * null to have it allocated stream-ordered for the call. */
 int apa_attention_ex(const void* q, const void* k, const void* v, int B, int Hq, int Hkv, int Nq, int Nkv, int d,
@@ -140,7 +152,8 @@ size_t apa_kv_blob_bytes(int B, int Hkv, int Nkv, int d);
 /* apa_quantize() with options: q2_blob (nullable, q_blob's layout) receives the
  * codes and scales of the FP4 residual term of Q (APA_FLAG_Q_RESIDUAL);
  * APA_FLAG_LSE_SCALES picks every block scale by least squared error.  The flag
- * APA_FLAG_Q_RESIDUAL is implied by a non-null q2_blob. */
+ * APA_FLAG_Q_RESIDUAL is implied by a non-null q2_blob; APA_FLAG_VALUE_WEIGHTED
+ * changes nothing here (the weights are not an operand). */
 int apa_quantize_ex(const void* q, const void* k, const void* v, int B, int Hq, int Hkv, int Nq, int Nkv, int d,
                     unsigned flags, uint8_t* kv_blob, uint8_t* q_blob, uint8_t* q2_blob, float* mu, float* s_q,
                     float* s_k, float* s_v, cudaStream_t stream);

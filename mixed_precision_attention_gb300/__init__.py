@@ -20,10 +20,11 @@ from ._lib import ApaError, status_string
 
 __all__ = ["attention", "attention_host", "quantize", "quantize_noalloc", "workspace_bytes", "check_error", "ApaError",
            "status_string", "hot_mask_shape", "TILE", "GROUP_ROWS", "BLOCK_ROWS", "FLAG_Q_RESIDUAL",
-           "FLAG_LSE_SCALES"]
+           "FLAG_LSE_SCALES", "FLAG_VALUE_WEIGHTED"]
 
 FLAG_Q_RESIDUAL = 1  # APA_FLAG_Q_RESIDUAL: Q as two FP4 terms in pass 1
 FLAG_LSE_SCALES = 2  # APA_FLAG_LSE_SCALES: least-squared-error block scales for Q, K, V
+FLAG_VALUE_WEIGHTED = 4  # APA_FLAG_VALUE_WEIGHTED: hot test weighted by value norm
 TILE = 64          # keys per tile
 GROUP_ROWS = 16    # rows per hot-test group
 BLOCK_ROWS = 128   # GQA-packed rows per CTA
@@ -60,17 +61,19 @@ def _check_qkv(q, k, v):
     return B, Hq, k.shape[1], Nq, k.shape[2], d
 
 
-def _flags(q_residual=False, lse_scales=False):
-    return (FLAG_Q_RESIDUAL if q_residual else 0) | (FLAG_LSE_SCALES if lse_scales else 0)
+def _flags(q_residual=False, lse_scales=False, value_weighted=False):
+    return ((FLAG_Q_RESIDUAL if q_residual else 0) | (FLAG_LSE_SCALES if lse_scales else 0)
+            | (FLAG_VALUE_WEIGHTED if value_weighted else 0))
 
 
-def workspace_bytes(B, Hq, Hkv, Nq, Nkv, d, eps, q_residual: bool = False):
-    flags = _flags(q_residual)
+def workspace_bytes(B, Hq, Hkv, Nq, Nkv, d, eps, q_residual: bool = False, value_weighted: bool = False):
+    flags = _flags(q_residual, value_weighted=value_weighted)
     return int(_lib.load().apa_workspace_bytes_ex(B, Hq, Hkv, Nq, Nkv, d, float(eps), flags))
 
 
 def attention(q, k, v, causal: bool = True, eps: float = 0.005, return_hot_mask: bool = False,
-              return_lse: bool = True, workspace=None, q_residual: bool = False, lse_scales: bool = False):
+              return_lse: bool = True, workspace=None, q_residual: bool = False, lse_scales: bool = False,
+              value_weighted: bool = False):
     """Adaptive-precision attention.
 
     q: [B, Hq, Nq, d] bf16; k, v: [B, Hkv, Nkv, d] bf16 (CUDA, contiguous).
@@ -82,6 +85,7 @@ def attention(q, k, v, causal: bool = True, eps: float = 0.005, return_hot_mask:
     workspace: optional uint8 CUDA tensor of at least workspace_bytes(...) bytes.
     q_residual: Q as two FP4 terms in pass 1 (apa_attention_ex, APA_FLAG_Q_RESIDUAL).
     lse_scales: least-squared-error block scales for Q, K, V (APA_FLAG_LSE_SCALES).
+    value_weighted: hot test weighted by the tile's value norm (APA_FLAG_VALUE_WEIGHTED).
     """
     import torch
     lib = _lib.load()
@@ -90,13 +94,14 @@ def attention(q, k, v, causal: bool = True, eps: float = 0.005, return_hot_mask:
     out = torch.empty((B, Hq, Nq, d), dtype=torch.float32, device=dev)
     lse = torch.empty((B, Hq, Nq), dtype=torch.float32, device=dev) if return_lse else None
     mask = torch.empty(hot_mask_shape(B, Hq, Hkv, Nq, Nkv), dtype=torch.int32, device=dev) if return_hot_mask else None
-    need = workspace_bytes(B, Hq, Hkv, Nq, Nkv, d, eps, q_residual)
+    need = workspace_bytes(B, Hq, Hkv, Nq, Nkv, d, eps, q_residual, value_weighted)
     if workspace is None and need:
         workspace = torch.empty(need, dtype=torch.uint8, device=dev)
     nbytes = 0 if workspace is None else workspace.numel()
-    if q_residual or lse_scales:
+    flags = _flags(q_residual, lse_scales, value_weighted)
+    if flags:
         st = lib.apa_attention_ex(_ptr(q), _ptr(k), _ptr(v), B, Hq, Hkv, Nq, Nkv, d, int(bool(causal)), float(eps),
-                                  _flags(q_residual, lse_scales), _ptr(out), _ptr(lse), _ptr(mask), _ptr(workspace),
+                                  flags, _ptr(out), _ptr(lse), _ptr(mask), _ptr(workspace),
                                   nbytes, _stream(dev))
         _lib.check(st, "apa_attention_ex")
     else:

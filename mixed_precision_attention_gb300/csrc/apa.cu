@@ -15,7 +15,7 @@ namespace {
 __device__ int g_device_error;  // set by bounded waits that gave up
 
 constexpr size_t kAlign = 256;
-constexpr unsigned kKnownFlags = APA_FLAG_Q_RESIDUAL | APA_FLAG_LSE_SCALES;
+constexpr unsigned kKnownFlags = APA_FLAG_Q_RESIDUAL | APA_FLAG_LSE_SCALES | APA_FLAG_VALUE_WEIGHTED;
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 __global__ void visible_mask_kernel(Shape s, uint32_t* mask) {
@@ -142,6 +142,10 @@ size_t workspace_layout(const Shape& s, bool apa_mode, Workspace* ws, void* base
   w.hot_count = (uint32_t*)take(BH * nblk * 4);
   w.p2_order = (uint32_t*)take(BH * nblk * 4);
   if (flags & APA_FLAG_Q_RESIDUAL) w.q2_blob = (uint8_t*)take(BH * nblk * qblob_bytes((int)d));
+  if (flags & APA_FLAG_VALUE_WEIGHTED) {
+    w.wv = (float*)take(BH * T * 4);
+    w.vtsum = (float*)take(BH * T * 4);
+  }
   w.v16 = (uint16_t*)take(BH * s.Nkv * d * 2);
   if (ws) *ws = w;
   return off;

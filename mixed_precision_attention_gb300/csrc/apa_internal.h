@@ -82,6 +82,9 @@ struct Workspace {
   uint8_t* q_blob;    // [BH][nblk][qblob_bytes(d)]
   uint8_t* q2_blob;   // [BH][nblk][qblob_bytes(d)] the FP4 residual term of Q, or null
   uint16_t* v16;      // [BH][Nkv][d] FP16 copy of V / v16_scale(max |v|) for pass 2, or null
+  float* wv;          // [BH][T] largest key value norm of each tile, then (after the key
+                      // mean) the tile's hot-test weight; null unless value-weighted
+  float* vtsum;       // [BH][T] FP32 sum of the tile's key value norms (with wv)
   // pass 1 -> pass 2
   float* state_o;     // [BH][nblk*128][d]: pass-1 o (scaled by s_v)
   float2* state_ml;   // [BH][nblk*128]: pass-1 frame m and cold sum l

@@ -7,7 +7,9 @@
 //      the exponent bias, so ex2 produces the quantized P;
 //   3. row sums l_t from the same P, via one extra MMA against an E2M1 ones tile;
 //   4. the hot test: if any of the group's 16 rows has l_t > eps * lambda, the
-//      tile is hot: set the mask bit, skip the PV product for the group;
+//      tile is hot: set the mask bit, skip the PV product for the group (with the
+//      value-weighted option the test is w_t * l_t > eps * lambda, w_t the tile's
+//      largest key value norm over the head's mean one, after "Honest limits");
 //   5. cold tiles accumulate o += P V in FP4, the cold row sum grows by l_t.
 // Tile order: tile 0 (the sink), then from the causal diagonal backwards
 // ("Tile order").  Frames: lazy maximum with tau = 4 ("Lazy maximum"); a hot
@@ -59,6 +61,7 @@ struct P1Params {
   uint32_t* hot_list;
   uint32_t* hot_count;
   uint32_t* hot_mask;  // may be null
+  const float* wv;     // [BH][T] value-norm weight of each tile in the hot test, or null (weight 1)
   int* err;
 };
 
@@ -479,19 +482,21 @@ __global__ void __launch_bounds__(kThreads, (D <= 128 ? 2 : 1)) pass1_kernel(con
     // keeps m, so lambda += l_t and, if cold, l += l_t: no exponentials, no rescale).
     auto judge = [&](int i, const Pending& pd, bool lifted) -> bool {
       const int t = tile_of(i);
+      const float wt = p.wv ? __ldg(p.wv + (size_t)bh * T + t) : 1.f;
       if (!warp_wait(l_full, i & 1)) return false;
       tc_fence_after();
       uint32_t lb;
       tmem_ld_x1(tmem + lane_base + C::kL, lb);
       tmem_wait_ld();
       const float ell = __uint_as_float(lb);
-      // hot test: l_t (in the committed frame) > eps * lambda; thr is -1 at eps = 0 (every
-      // visible tile hot) and NaN at eps = inf with lambda = 0 (never hot)
+      // hot test: w_t * l_t (in the committed frame) > eps * lambda; thr is -1 at eps = 0
+      // (every visible tile hot) and NaN at eps = inf with lambda = 0 (never hot)
       const float thr = eps == 0.f ? -1.f : eps * lam;
+      const float ellw = ell * wt;
       bool vote;
-      if (!lifted) vote = valid && !pd.empty && ell > thr;
+      if (!lifted) vote = valid && !pd.empty && ellw > thr;
       else vote = valid && !pd.empty && !eps_inf &&
-                  ((m == -INFINITY) ? (eps == 0.f || ell > 0.f) : (ell * ex2_approx(pd.mt - m) > thr));
+                  ((m == -INFINITY) ? (eps == 0.f || ellw > 0.f) : (ellw * ex2_approx(pd.mt - m) > thr));
       const uint32_t bal = __ballot_sync(0xffffffffu, vote);
       const bool hot_lo = (bal & 0x0000FFFFu) != 0, hot_hi = (bal & 0xFFFF0000u) != 0;
       const bool hot = lane < 16 ? hot_lo : hot_hi;
@@ -576,6 +581,7 @@ __global__ void __launch_bounds__(kThreads, (D <= 128 ? 2 : 1)) pass1_kernel(con
       for (int i = 0; ok && i < n; ++i) {
         const int t = tile_of(i), j0 = t * kTile;
         const int nvis = valid ? min(kTile, vis_last + 1 - j0) : 0;
+        const float wt = p.wv ? __ldg(p.wv + (size_t)bh * T + t) : 1.f;
         if (!(ok = warp_wait(s_full, i & 1))) break;
         tc_fence_after();
         uint32_t sr[64];
@@ -625,14 +631,15 @@ __global__ void __launch_bounds__(kThreads, (D <= 128 ? 2 : 1)) pass1_kernel(con
 #pragma unroll
           for (int w = 0; w < 8; ++w) pw[w] = 0u;
         }
-        // hot test: l_t (in the committed frame) > eps * lambda
+        // hot test: w_t * l_t (in the committed frame) > eps * lambda
         const bool lift = !empty && mt != m;
         const bool lifted = __any_sync(0xffffffffu, lift);
         const float thr = eps == 0.f ? -1.f : eps * lam;
+        const float ellw = ell * wt;
         bool vote;
-        if (!lifted) vote = valid && !empty && ell > thr;
+        if (!lifted) vote = valid && !empty && ellw > thr;
         else vote = valid && !empty && !eps_inf &&
-                    ((m == -INFINITY) ? (eps == 0.f || ell > 0.f) : (ell * ex2_approx(mt - m) > thr));
+                    ((m == -INFINITY) ? (eps == 0.f || ellw > 0.f) : (ellw * ex2_approx(mt - m) > thr));
         const uint32_t bal = __ballot_sync(0xffffffffu, vote);
         const bool hot_lo = (bal & 0x0000FFFFu) != 0, hot_hi = (bal & 0xFFFF0000u) != 0;
         const bool hot = lane < 16 ? hot_lo : hot_hi;
@@ -976,6 +983,7 @@ __global__ void __launch_bounds__(P1MCfg<D, U>::kThreads, 1) pass1_multi_kernel(
     for (int i = 0; ok && i < n; ++i) {
       const int t = tile_of(i), j0 = t * kTile;
       const int nvis = valid ? min(kTile, vis_last + 1 - j0) : 0;
+      const float wt = p.wv ? __ldg(p.wv + (size_t)bh * T + t) : 1.f;
       if (!(ok = warp_wait(s_full(u), i & 1))) break;
       tc_fence_after();
       uint32_t sr[64];
@@ -1025,14 +1033,15 @@ __global__ void __launch_bounds__(P1MCfg<D, U>::kThreads, 1) pass1_multi_kernel(
 #pragma unroll
         for (int w = 0; w < 8; ++w) pw[w] = 0u;
       }
-      // hot test: l_t (in the committed frame) > eps * lambda
+      // hot test: w_t * l_t (in the committed frame) > eps * lambda
       const bool lift = !empty && mt != m;
       const bool lifted = __any_sync(0xffffffffu, lift);
       const float thr = eps == 0.f ? -1.f : eps * lam;
+      const float ellw = ell * wt;
       bool vote;
-      if (!lifted) vote = valid && !empty && ell > thr;
+      if (!lifted) vote = valid && !empty && ellw > thr;
       else vote = valid && !empty && !eps_inf &&
-                  ((m == -INFINITY) ? (eps == 0.f || ell > 0.f) : (ell * ex2_approx(mt - m) > thr));
+                  ((m == -INFINITY) ? (eps == 0.f || ellw > 0.f) : (ellw * ex2_approx(mt - m) > thr));
       const uint32_t bal = __ballot_sync(0xffffffffu, vote);
       const bool hot_lo = (bal & 0x0000FFFFu) != 0, hot_hi = (bal & 0xFFFF0000u) != 0;
       const bool hot = lane < 16 ? hot_lo : hot_hi;
@@ -1193,6 +1202,7 @@ cudaError_t launch_pass1(const Shape& s, const Workspace& ws, float eps, uint32_
   prm.hot_list = ws.hot_list;
   prm.hot_count = ws.hot_count;
   prm.hot_mask = hot_mask;
+  prm.wv = ws.wv;
   prm.err = device_error_word();
   switch (s.d) {
     case 64: return launch_d<64>(prm, wide, st);

@@ -20,7 +20,11 @@
 //                    sums, per-channel min/max of K (atomics on an order-preserving
 //                    encoding: exact, so order-free), max |V|; Q rows: max |Q| per
 //                    query head.
-//   finalize_kernel  per (b, KV head, 8 channels): mu and the head's max |k - mu|.
+//                    With the value-weighted hot test also each key's value norm
+//                    and per tile their maximum and FP32 sum.
+//   finalize_kernel  per (b, KV head, 8 channels): mu and the head's max |k - mu|;
+//                    per (b, KV head), value-weighted: the mean key value norm and
+//                    the tiles' weights.
 //   quant_kernel     FP32 head scales from the maxima; K/V tiles (bulk-copied) ->
 //                    blobs and 128-row Q blocks (GQA-packed) -> Q blobs, each
 //                    assembled in shared memory and written with 16-byte stores.
@@ -204,8 +208,37 @@ __global__ void __launch_bounds__(kThreads) stats_kernel(Shape s, const uint16_t
       atomicMin(&ws.kmin[(size_t)bh * d + c], ord_enc(mn));
       atomicMax(&ws.kmax[(size_t)bh * d + c], ord_enc(mx));
     }
-    vm = block_max(vm, red);
+    // value norm of each key (value-weighted hot test): FP32 squares summed in channel
+    // order, correctly rounded square root; the last two warps, one key per thread
+    __shared__ float nrm[kTile];
+    const int jn = threadIdx.x - (kThreads - kTile);
+    if (ws.wv && jn >= 0 && jn < nk) {
+      const uint4* row = reinterpret_cast<const uint4*>(vs + jn * d);
+      float acc = 0.f;
+      for (int c8 = 0; c8 < d / 8; ++c8) {
+        const uint4 x = row[c8];
+        const uint32_t w4[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float lo = bf16f(w4[e] & 0xFFFF), hi = bf16f(w4[e] >> 16);
+          acc = __fadd_rn(acc, __fmul_rn(lo, lo));
+          acc = __fadd_rn(acc, __fmul_rn(hi, hi));
+        }
+      }
+      nrm[jn] = __fsqrt_rn(acc);
+    }
+    vm = block_max(vm, red);  // (its barriers also publish nrm)
     if (threadIdx.x == 0) atomicMax(&ws.vamax[bh], __float_as_uint(vm));
+    if (ws.wv && threadIdx.x == 32) {
+      // the tile's largest norm and its FP32 norm sum in key order
+      float a = 0.f, sum = 0.f;
+      for (int j = 0; j < nk; ++j) {
+        a = fmaxf(a, nrm[j]);
+        sum = __fadd_rn(sum, nrm[j]);
+      }
+      ws.wv[(size_t)bh * T + t] = a;
+      ws.vtsum[(size_t)bh * T + t] = sum;
+    }
     return;
   }
   // max |Q| over a chunk of rows of one query head
@@ -229,9 +262,41 @@ constexpr int kMeanRange = 64;
 constexpr int kRangesPerPass = 64;
 constexpr int kFinChannels = 8;
 
+// The head's mean key value norm in the key mean's order (FP64 sums of the FP32
+// tile sums per range of kMeanRange tiles, then of the ranges), rounded to FP32,
+// and each tile's weight = its largest norm / the mean (1 when the mean is 0).
+__device__ void value_weights(const Shape& s, const Workspace& ws, int bh) {
+  __shared__ double rs[kThreads];
+  __shared__ float nbar_s;
+  const int T = s.T(), nR = (T + kMeanRange - 1) / kMeanRange;
+  const float* ts = ws.vtsum + (size_t)bh * T;
+  double S = 0.0;
+  for (int r0 = 0; r0 < nR; r0 += kThreads) {
+    const int r = r0 + threadIdx.x;
+    if (r < nR) {
+      double Sr = 0.0;
+      for (int t = r * kMeanRange; t < min(T, (r + 1) * kMeanRange); ++t) Sr += (double)ts[t];
+      rs[threadIdx.x] = Sr;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0)
+      for (int i = 0; i < min(kThreads, nR - r0); ++i) S += rs[i];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) nbar_s = __double2float_rn(S / (double)s.Nkv);
+  __syncthreads();
+  const float nbar = nbar_s;
+  float* w = ws.wv + (size_t)bh * T;
+  for (int t = threadIdx.x; t < T; t += kThreads) w[t] = nbar == 0.f ? 1.f : __fdiv_rn(w[t], nbar);
+}
+
 __global__ void __launch_bounds__(kThreads) finalize_kernel(Shape s, Workspace ws) {
   __shared__ double rs[kRangesPerPass][kFinChannels];
   const int cblocks = s.d / kFinChannels;
+  if ((int)blockIdx.x >= s.BH() * cblocks) {  // one extra block per head when value-weighted
+    value_weights(s, ws, blockIdx.x - s.BH() * cblocks);
+    return;
+  }
   const int bh = blockIdx.x / cblocks, cl = threadIdx.x % kFinChannels, lane = threadIdx.x / kFinChannels;
   constexpr int kLanes = kThreads / kFinChannels;
   const int c = (blockIdx.x % cblocks) * kFinChannels + cl;
@@ -447,7 +512,7 @@ cudaError_t launch_quantize(const Shape& s, const void* q, const void* k, const 
                                                     n_kv, q_rows, do_kv, err);
   if ((e = cudaGetLastError())) return e;
   if (do_kv) {
-    finalize_kernel<<<BH * (d / kFinChannels), kThreads, 0, st>>>(s, ws);
+    finalize_kernel<<<BH * (d / kFinChannels) + (ws.wv ? BH : 0), kThreads, 0, st>>>(s, ws);
     if ((e = cudaGetLastError())) return e;
   }
   const int n_qb = do_q ? BH * s.nblk() : 0;

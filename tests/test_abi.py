@@ -83,12 +83,18 @@ def test_option_flags(lib):
     q2 = lib.apa_workspace_bytes_ex(1, 2, 1, 128, 512, 64, 0.005, 1)
     assert q2 >= base + lib.apa_q_blob_bytes(1, 2, 1, 128, 64)
     assert lib.apa_workspace_bytes_ex(1, 2, 1, 128, 512, 64, 0.005, 2) == base  # the scale choice needs no memory
-    assert lib.apa_workspace_bytes_ex(1, 2, 1, 128, 512, 64, 0.005, 4) == 0
-    st = lib.apa_attention_ex(*OK_PTR, 1, 2, 1, 128, 512, 64, 1, 0.005, 4, P(0x40000), None, None, None, 0, None)
+    # the value-weighted test keeps two floats per (b, KV head, tile): 8 tiles here
+    vw = lib.apa_workspace_bytes_ex(1, 2, 1, 128, 512, 64, 0.005, 4)
+    assert base + 2 * 8 * 4 <= vw <= base + 2 * 256
+    assert lib.apa_workspace_bytes_ex(1, 2, 1, 128, 512, 64, 0.005, 8) == 0
+    st = lib.apa_attention_ex(*OK_PTR, 1, 2, 1, 128, 512, 64, 1, 0.005, 8, P(0x40000), None, None, None, 0, None)
     assert st == -10
     z = P(0x60000)
-    st = lib.apa_quantize_ex(*OK_PTR, 1, 2, 1, 128, 512, 64, 4, z, z, None, z, z, z, z, None)
+    st = lib.apa_quantize_ex(*OK_PTR, 1, 2, 1, 128, 512, 64, 8, z, z, None, z, z, z, z, None)
     assert st == -10
+    st = lib.apa_attention_ex(*OK_PTR, 1, 2, 1, 128, 512, 64, 1, 0.005, 4, P(0x40000), None, None,
+                              P(0x50000), vw - 1, None)
+    assert st == -6
     st = lib.apa_attention_ex(*OK_PTR, 1, 2, 1, 128, 512, 64, 1, 0.005, 1, P(0x40000), None, None,
                               P(0x50000), q2 - 1, None)
     assert st == -6

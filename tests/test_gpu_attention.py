@@ -199,3 +199,69 @@ def test_lse_scales_match_emulation(name, q_residual):
     ng = oracle.n_groups(w.Hq, w.Hkv, w.Nq)
     vis = np.broadcast_to(_gpu.group_visible(w.Hq, w.Hkv, w.Nq, w.Nkv, True, ng, T), g_hot.shape)
     assert (g_hot == o_hot)[vis].mean() >= 0.999
+
+
+def _value_weighted_inputs(name):
+    # one tile of large-norm values and one of small-norm values, so that the weights
+    # span well above and below 1
+    w, (q, k, v) = _inputs(name)
+    vf = synth.bf16_bits_to_f32(v).copy()
+    T = (w.Nkv + 63) // 64
+    vf[:, :, (T // 3) * 64:(T // 3 + 1) * 64] *= 12.0
+    vf[:, :, (T // 2) * 64:(T // 2 + 1) * 64] *= 0.05
+    return w, (q, k, synth.f32_to_bf16_bits(vf))
+
+
+@pytest.mark.parametrize("name", ["gqa3_ragged", "batch_ragged_d128", "d256", "long_tail"])
+@pytest.mark.parametrize("q_residual", [False, True])
+def test_value_weighted_matches_emulation(name, q_residual):
+    """APA_FLAG_VALUE_WEIGHTED against the oracle's weighted hot test: outputs within
+    the usual bounds, masks agree, and every tile the GPU calls cold has w_t * l_t
+    below eps of the oracle's final row sum (w_t the oracle's weights)."""
+    import mixed_precision_attention_gb300 as apa
+    w, (q, k, v) = _value_weighted_inputs(name)
+    eps = 0.005
+    quant = oracle.QUANT_ALL | oracle.QUANT_VWEIGHT | (oracle.QUANT_Q2 if q_residual else 0)
+    ref = oracle.apa(q, k, v, eps=eps, quant=quant, diag=True)
+    tq, tk, tv = (_gpu.to_dev(a) for a in (q, k, v))
+    o, l, m = apa.attention(tq, tk, tv, causal=True, eps=eps, return_hot_mask=True, q_residual=q_residual,
+                            value_weighted=True)
+    apa.check_error()
+    out, lse = o.cpu().numpy().astype(np.float64), l.cpu().numpy().astype(np.float64)
+    assert np.abs(out - ref["out"]).max() <= 1e-2
+    assert _gpu.cosine(out, ref["out"]) >= 0.9999
+    assert np.abs(lse - ref["lse"]).max() <= 1e-2
+    T = (w.Nkv + 63) // 64
+    ng = oracle.n_groups(w.Hq, w.Hkv, w.Nq)
+    g_hot, o_hot = _gpu.hot_bits(m.cpu().numpy().view(np.uint32), T), _gpu.hot_bits(ref["hot_mask"], T)
+    vis = np.broadcast_to(_gpu.group_visible(w.Hq, w.Hkv, w.Nq, w.Nkv, True, ng, T), g_hot.shape)
+    assert not g_hot[~vis].any()
+    assert (g_hot == o_hot)[vis].mean() >= 0.999
+    wt = oracle.value_weights(v)  # [B, Hkv, T]
+    ell = ref["ell"].reshape(w.B, w.Hkv, ng, 16, T) * wt[:, :, None, None, :]
+    lam = ref["lam"].reshape(w.B, w.Hkv, ng, 16)
+    cold = vis & ~g_hot
+    ratio = np.where(np.isnan(ell), 0.0, ell) / np.where(np.isnan(lam), np.inf, np.maximum(lam, 1e-300))[..., None]
+    assert np.max(np.where(cold[..., None, :], ratio, 0.0)) <= eps * 1.02
+    # against the unweighted run: the large-norm tile is hot for at least as many groups,
+    # and the masks differ wherever the oracle's do
+    _, _, m0 = apa.attention(tq, tk, tv, causal=True, eps=eps, return_hot_mask=True, q_residual=q_residual)
+    h0 = _gpu.hot_bits(m0.cpu().numpy().view(np.uint32), T)
+    big = T // 3
+    assert g_hot[..., big].sum() >= h0[..., big].sum()
+    ref0 = oracle.apa(q, k, v, eps=eps, quant=quant & ~oracle.QUANT_VWEIGHT)
+    if not np.array_equal(ref0["hot_mask"], ref["hot_mask"]):
+        assert not np.array_equal(g_hot, h0)
+
+
+@pytest.mark.parametrize("eps", [0.0, float("inf")])
+def test_value_weighted_eps_limits_are_unchanged(eps):
+    # eps = 0 (all exact) and eps = inf (all FP4) do not depend on the weights
+    import mixed_precision_attention_gb300 as apa
+    w, (q, k, v) = _value_weighted_inputs("batch_ragged_d128")
+    tq, tk, tv = (_gpu.to_dev(a) for a in (q, k, v))
+    a = apa.attention(tq, tk, tv, causal=True, eps=eps, return_hot_mask=True)
+    b = apa.attention(tq, tk, tv, causal=True, eps=eps, return_hot_mask=True, value_weighted=True)
+    apa.check_error()
+    for x, y in zip(a, b):
+        assert np.array_equal(x.cpu().numpy(), y.cpu().numpy())
