@@ -142,6 +142,7 @@ size_t workspace_layout(const Shape& s, bool apa_mode, Workspace* ws, void* base
   w.hot_count = (uint32_t*)take(BH * nblk * 4);
   w.p2_order = (uint32_t*)take(BH * nblk * 4);
   if (flags & APA_FLAG_Q_RESIDUAL) w.q2_blob = (uint8_t*)take(BH * nblk * qblob_bytes((int)d));
+  w.kv_ready = (uint32_t*)take((BH * T + 1) * 4);
   if (flags & APA_FLAG_VALUE_WEIGHTED) {
     w.wv = (float*)take(BH * T * 4);
     w.vtsum = (float*)take(BH * T * 4);
@@ -183,7 +184,7 @@ size_t begin_call() {
 
 static int run_attention(const Shape& s, const void* q, const void* k, const void* v, float eps, float* out, float* lse,
                          uint32_t* hot_mask, void* workspace, cudaStream_t stream, bool wide_pass1 = false,
-                         unsigned flags = 0) {
+                         unsigned flags = 0, bool kv_in_pass1_ok = true) {
   const size_t call = begin_call();
   auto stage = [&](int slot) {
     if (call != SIZE_MAX) cudaEventRecord(g_timing.ev[call * 4 + slot], stream);
@@ -204,10 +205,16 @@ static int run_attention(const Shape& s, const void* q, const void* k, const voi
     const size_t words = (size_t)s.BH() * s.ngroups() * ((s.T() + 31) / 32);
     if (cudaMemsetAsync(hot_mask, 0, words * 4, stream) != cudaSuccess) return APA_ERR_CUDA;
   }
-  if (launch_quantize(s, q, k, v, ws, true, true, stream, (flags & APA_FLAG_LSE_SCALES) != 0) != cudaSuccess)
+  // The K/V tiles are quantized inside the pass-1 launch, on the SMs its CTAs
+  // leave free, when there are enough of those; the statistics and Q come first.
+  const bool lse_scales = (flags & APA_FLAG_LSE_SCALES) != 0, wide = wide_pass1 || ws.q2_blob;
+  const bool kv_in_pass1 = kv_in_pass1_ok && pass1_quantizes_kv(s, wide, ws.q2_blob != nullptr);
+  if (launch_quantize(s, q, k, v, ws, true, true, stream, lse_scales, kv_in_pass1) != cudaSuccess)
     return APA_ERR_CUDA;
   stage(1);
-  if (launch_pass1(s, ws, eps, hot_mask, wide_pass1 || ws.q2_blob, stream) != cudaSuccess) return APA_ERR_CUDA;
+  const KvSource src{k, v, lse_scales};
+  if (launch_pass1(s, ws, eps, hot_mask, wide, stream, kv_in_pass1 ? &src : nullptr) != cudaSuccess)
+    return APA_ERR_CUDA;
   if (launch_pass2_order(s, ws, stream) != cudaSuccess) return APA_ERR_CUDA;
   stage(2);
   if (launch_pass2(s, q, k, v, &ws, out, lse, stream) != cudaSuccess) return APA_ERR_CUDA;
@@ -326,7 +333,8 @@ int apa_attention_host(const void* q, const void* k, const void* v, int B, int H
       break;
     }
     st = apa::run_attention(sub, dq, dk, dv, eps, dout, dlse, dmask,
-                            need ? dev + ow + (j % L) * apa::align_up(need) : nullptr, ls, j >= wide_from);
+                            need ? dev + ow + (j % L) * apa::align_up(need) : nullptr, ls, j >= wide_from, 0,
+                            false);  // (sub-problems share the GPU: no whole-GPU cooperative launch)
     if (st != APA_OK) break;
     good = ok_(cudaMemcpyAsync(out + j * qh, dout, qh * 4, cudaMemcpyDeviceToHost, ls)) &&
            (!lse || ok_(cudaMemcpyAsync(lse + j * lh, dlse, lh * 4, cudaMemcpyDeviceToHost, ls))) &&

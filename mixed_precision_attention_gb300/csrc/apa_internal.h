@@ -85,6 +85,9 @@ struct Workspace {
   float* wv;          // [BH][T] largest key value norm of each tile, then (after the key
                       // mean) the tile's hot-test weight; null unless value-weighted
   float* vtsum;       // [BH][T] FP32 sum of the tile's key value norms (with wv)
+  uint32_t* kv_ready; // [BH*T + 1]: per tile 1 once its blob is written by the K/V
+                      // quantizer inside the pass-1 launch; the last word is that
+                      // quantizer's ticket counter
   // pass 1 -> pass 2
   float* state_o;     // [BH][nblk*128][d]: pass-1 o (scaled by s_v)
   float2* state_ml;   // [BH][nblk*128]: pass-1 frame m and cold sum l
@@ -116,14 +119,27 @@ int* device_error_word();  // library-wide device error word (set by bounded wai
 
 
 // ------------------------------------------------------------------ launchers
-// lse: least-squared-error block scales (APA_FLAG_LSE_SCALES) instead of the nearest ones
+// lse: least-squared-error block scales (APA_FLAG_LSE_SCALES) instead of the nearest ones.
+// kv_in_pass1: the K/V tiles are left to the quantizer inside the pass-1 launch
+// (launch_pass1 with a KvSource): this call then runs the statistics and the Q
+// blocks (which also publish the K/V head scales) and clears ws.kv_ready.
 cudaError_t launch_quantize(const Shape& s, const void* q, const void* k, const void* v, const Workspace& ws,
-                            bool do_q, bool do_kv, cudaStream_t st, bool lse = false);
+                            bool do_q, bool do_kv, cudaStream_t st, bool lse = false, bool kv_in_pass1 = false);
+// The raw K and V for the K/V quantizer that runs inside the pass-1 launch.
+struct KvSource {
+  const void* k;
+  const void* v;
+  bool lse;
+};
+// Whether the pass-1 launch for this problem can quantize the K/V tiles itself
+// (the three-block kernel, with at least 8 SMs left over for the quantizer).
+bool pass1_quantizes_kv(const Shape& s, bool wide, bool q_residual);
 // wide: one 128-row block per CTA (three times the CTAs, each on its own SM when
 // the GPU is otherwise idle, so a single problem finishes sooner) instead of
-// three blocks of one KV head per CTA (the faster choice for a full GPU)
+// three blocks of one KV head per CTA (the faster choice for a full GPU).
+// kv: quantize the K/V tiles inside this launch (pass1_quantizes_kv must hold).
 cudaError_t launch_pass1(const Shape& s, const Workspace& ws, float eps, uint32_t* hot_mask, bool wide,
-                         cudaStream_t st);
+                         cudaStream_t st, const KvSource* kv = nullptr);
 cudaError_t launch_pass2(const Shape& s, const void* q, const void* k, const void* v, const Workspace* ws,
                          float* out, float* lse, cudaStream_t st);
 cudaError_t launch_visible_mask(const Shape& s, uint32_t* hot_mask, cudaStream_t st);

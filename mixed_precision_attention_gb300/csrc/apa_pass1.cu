@@ -41,6 +41,7 @@
 #include <cstring>
 
 #include "apa_internal.h"
+#include "quant_tile.cuh"
 #include "tc.cuh"
 
 namespace apa {
@@ -63,6 +64,14 @@ struct P1Params {
   uint32_t* hot_mask;  // may be null
   const float* wv;     // [BH][T] value-norm weight of each tile in the hot test, or null (weight 1)
   int* err;
+  // K/V quantized inside this launch (three-block kernel): CTAs n_p1.. run the
+  // quantizer role; kv_ready null otherwise
+  uint32_t* kv_ready;  // [BH*T] tile flags, then the quantizer's ticket counter
+  const uint16_t* k_raw;
+  const uint16_t* v_raw;
+  Workspace ws;
+  int n_p1;
+  int lse_scales;
 };
 
 constexpr int kSoftWarps = 4;
@@ -105,11 +114,6 @@ __device__ __forceinline__ void wait_bounded(uint32_t bar, uint32_t parity, int*
   }
 }
 
-__device__ __forceinline__ float ue4m3_value(uint32_t code) {
-  const uint32_t E = code >> 3, m = code & 7;
-  if (E == 0) return (float)m * 0.001953125f;
-  return __uint_as_float(((E + 120u) << 23) | (m << 20));
-}
 __device__ __forceinline__ float lg2_approx(float x) {
   float y;
   asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -769,6 +773,11 @@ struct P1MCfg {
   static constexpr uint32_t kSFP = kSFV + 2 * kSfc;           // [U][2] buffers (tile % 2)
   static_assert(kSFP + 8 * U <= kTmemCols, "TMEM budget");
   static constexpr int kThreads = (4 * U + 3) * 32;
+  // thread groups of the K/V quantizer role (each a multiple of d/16 threads)
+  static constexpr int kQuantGroups = 3;
+  static_assert(kThreads % kQuantGroups == 0 && (kThreads / kQuantGroups) % (D / 16) == 0 &&
+                    kQuantGroups <= kQuantRoleGroups,
+                "quantizer groups");
 };
 
 template <int D, int U>
@@ -776,6 +785,15 @@ __global__ void __launch_bounds__(P1MCfg<D, U>::kThreads, 1) pass1_multi_kernel(
   using C = P1MCfg<D, U>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+  if (p.kv_ready && (int)blockIdx.x >= p.n_p1) {
+    // the K/V quantizer, in groups that each keep a tile in flight: the tiles in
+    // the order the pass-1 CTAs below visit them
+    constexpr int kGroup = C::kThreads / C::kQuantGroups;
+    const int g = threadIdx.x / kGroup;
+    quant_role(p.s, p.k_raw, p.v_raw, p.ws, p.kv_ready, p.kv_ready + (size_t)p.s.BH() * p.s.T(), p.lse_scales != 0,
+               smem + g * quant_role_smem(D), p.err, g, threadIdx.x % kGroup, kGroup);
+    return;
+  }
   // barriers: q_full, blob_full[NS], blob_empty[NS], s_full[U], s_free[U], p_full[U][2], pv_done[U][2],
   // drain_s, drain_pv
   constexpr int kBars = 1 + 2 * C::NS + 6 * U + 2;
@@ -845,10 +863,37 @@ __global__ void __launch_bounds__(P1MCfg<D, U>::kThreads, 1) pass1_multi_kernel(
         if (grp * U + u < nblk)
           bulk_g2s(sbase + u * C::kQStride, p.q_blob + ((size_t)bh * nblk + grp * U + u) * C::kQBlob, C::kQBlob,
                    q_full);
-      int issued = 0;
+      // With the K/V quantizer in this launch: waits until the blob of visiting
+      // position i is written; returns one past the last position of i..i+7 known
+      // written (flags read together), or -1 if the wait gave up.
+      auto await_blobs = [&](int i) -> int {
+        const uint32_t* rd = p.kv_ready + (size_t)bh * T;
+        const unsigned long long t0 = clock64();
+        while (true) {
+          uint32_t got = 0;
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            if (i + j < n && ld_relaxed_gpu(rd + tile_of(i + j)) != 0u) got |= 1u << j;
+          const int k = __ffs(~got) - 1;  // leading positions written
+          if (k > 0) {
+            __threadfence();             // acquire: the blob stores come before the flags
+            fence_proxy_async_global();  // and before the bulk copies that read them
+            return i + k;
+          }
+          if (*(volatile int*)&abort_flag) return -1;
+          if (clock64() - t0 > APA_WAIT_LIMIT_CYCLES) {
+            abort_flag = 1;
+            if (p.err) atomicCAS(p.err, 0, APA_DEVERR_TIMEOUT);
+            return -1;
+          }
+          __nanosleep(128);
+        }
+      };
+      int issued = 0, written = 0;
       for (int i = 0; i < n; ++i) {
         const int st = i % C::NS;
         if (i >= C::NS && !mbar_wait(blob_empty(st), ((i / C::NS) - 1) & 1, &abort_flag, p.err)) break;
+        if (p.kv_ready && i >= written && (written = await_blobs(i)) < 0) break;
         mbar_arrive_expect_tx(blob_full(st), C::kBlob);
         bulk_g2s(sbase + C::kStageOff + st * C::kBlob, p.kv_blob + ((size_t)bh * T + tile_of(i)) * C::kBlob,
                  C::kBlob, blob_full(st));
@@ -1135,14 +1180,48 @@ __global__ void __launch_bounds__(P1MCfg<D, U>::kThreads, 1) pass1_multi_kernel(
   }
 }
 
+// Shared memory of the three-block kernel when it also runs the K/V quantizer:
+// enough for either role, and more than half an SM's so that one CTA takes a
+// whole SM (its TMEM allocation is the SM's 512 columns).
+template <int D, int U>
+constexpr int multi_kv_smem() {
+  constexpr int a = P1MCfg<D, U>::kSmem, b = P1MCfg<D, U>::kQuantGroups * quant_role_smem(D) + 128,
+                half = 114 * 1024 + 1024;
+  return a > b ? (a > half ? a : half) : (b > half ? b : half);
+}
+
 template <int D, int U>
 cudaError_t launch_multi(const P1Params& prm, cudaStream_t st) {
   using C = P1MCfg<D, U>;
-  cudaError_t e = cudaFuncSetAttribute(pass1_multi_kernel<D, U>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+  const int n_p1 = prm.s.BH() * ((prm.s.nblk() + U - 1) / U);
+  if (!prm.kv_ready) {
+    cudaError_t e =
+        cudaFuncSetAttribute(pass1_multi_kernel<D, U>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+    if (e) return e;
+    pass1_multi_kernel<D, U><<<n_p1, C::kThreads, C::kSmem, st>>>(prm);
+    return cudaGetLastError();
+  }
+  // With the K/V quantizer: one CTA per SM, the pass-1 CTAs and a quantizer CTA on
+  // every other SM, launched cooperatively because the pass-1 CTAs wait for the
+  // quantizer's flags (all CTAs resident at once, so every wait ends).
+  const int smem = multi_kv_smem<D, U>();
+  cudaError_t e = cudaFuncSetAttribute(pass1_multi_kernel<D, U>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e) return e;
-  const int ngrp = (prm.s.nblk() + U - 1) / U;
-  pass1_multi_kernel<D, U><<<prm.s.BH() * ngrp, C::kThreads, C::kSmem, st>>>(prm);
-  return cudaGetLastError();
+  int dev = 0, sms = 0;
+  if ((e = cudaGetDevice(&dev)) || (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev))) return e;
+  P1Params prm2 = prm;
+  prm2.n_p1 = n_p1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)sms);
+  cfg.blockDim = dim3(C::kThreads);
+  cfg.dynamicSmemBytes = (size_t)smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, pass1_multi_kernel<D, U>, prm2);
 }
 
 template <int D, bool kOnesMma>
@@ -1176,6 +1255,12 @@ bool single_unit() {
 
 template <int D>
 cudaError_t launch_d(const P1Params& prm, bool wide, cudaStream_t st) {
+  if constexpr (D <= 128) {
+    // the K/V quantizer runs only inside the three-block kernel
+    if (prm.kv_ready) return launch_multi<D, 3>(prm, st);
+  } else {
+    if (prm.kv_ready) return cudaErrorInvalidValue;
+  }
   // the residual Q term lives in the one-block kernel with register row sums
   if (prm.q2_blob) return launch_dv<D, false>(prm, st);
   if (rowsum_by_mma()) return launch_dv<D, true>(prm, st);
@@ -1185,9 +1270,44 @@ cudaError_t launch_d(const P1Params& prm, bool wide, cudaStream_t st) {
   return launch_dv<D, false>(prm, st);
 }
 
+// APA_PASS1_QUANT_KV=0 keeps the K/V quantization in its own kernel (for comparison).
+bool kv_in_pass1_allowed() {
+  static const bool v = [] {
+    const char* e = getenv("APA_PASS1_QUANT_KV");
+    return !(e && strcmp(e, "0") == 0);
+  }();
+  return v;
+}
+
+template <int D>
+bool multi_quantizes_kv(const Shape& s) {
+  constexpr int U = 3;
+  using C = P1MCfg<D, U>;
+  int dev = 0, sms = 0, per_sm = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return false;
+  const int n_p1 = s.BH() * ((s.nblk() + U - 1) / U);
+  if (sms - n_p1 < 8) return false;
+  if (cudaFuncSetAttribute(pass1_multi_kernel<D, U>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           multi_kv_smem<D, U>()) != cudaSuccess ||
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, pass1_multi_kernel<D, U>, C::kThreads,
+                                                    multi_kv_smem<D, U>()) != cudaSuccess)
+    return false;
+  return per_sm == 1;
+}
+
 }  // namespace
 
-cudaError_t launch_pass1(const Shape& s, const Workspace& ws, float eps, uint32_t* hot_mask, bool wide, cudaStream_t st) {
+bool pass1_quantizes_kv(const Shape& s, bool wide, bool q_residual) {
+  if (wide || q_residual || rowsum_by_mma() || single_unit() || !kv_in_pass1_allowed()) return false;
+  if (s.d == 64) return multi_quantizes_kv<64>(s);
+  if (s.d == 128) return multi_quantizes_kv<128>(s);
+  return false;
+}
+
+cudaError_t launch_pass1(const Shape& s, const Workspace& ws, float eps, uint32_t* hot_mask, bool wide, cudaStream_t st,
+                         const KvSource* kv) {
   P1Params prm{};
   prm.s = s;
   prm.kv_blob = ws.kv_blob;
@@ -1203,6 +1323,13 @@ cudaError_t launch_pass1(const Shape& s, const Workspace& ws, float eps, uint32_
   prm.hot_count = ws.hot_count;
   prm.hot_mask = hot_mask;
   prm.wv = ws.wv;
+  if (kv) {
+    prm.kv_ready = ws.kv_ready;
+    prm.k_raw = static_cast<const uint16_t*>(kv->k);
+    prm.v_raw = static_cast<const uint16_t*>(kv->v);
+    prm.ws = ws;
+    prm.lse_scales = kv->lse ? 1 : 0;
+  }
   prm.err = device_error_word();
   switch (s.d) {
     case 64: return launch_d<64>(prm, wide, st);

@@ -28,7 +28,10 @@
 //   quant_kernel     FP32 head scales from the maxima; K/V tiles (bulk-copied) ->
 //                    blobs and 128-row Q blocks (GQA-packed) -> Q blobs, each
 //                    assembled in shared memory and written with 16-byte stores.
+//                    When pass 1 quantizes the K/V tiles inside its own launch
+//                    (quant_role in quant_tile.cuh), only the Q blocks run here.
 #include "apa_internal.h"
+#include "quant_tile.cuh"
 #include "tc.cuh"
 
 namespace apa {
@@ -44,87 +47,6 @@ __device__ __forceinline__ uint32_t ord_enc(float f) {
 __device__ __forceinline__ float ord_dec(uint32_t e) {
   return __uint_as_float((e & 0x80000000u) ? (e & 0x7FFFFFFFu) : ~e);
 }
-__device__ __forceinline__ float bf16f(uint16_t h) { return __uint_as_float((uint32_t)h << 16); }
-__device__ __forceinline__ float ue4m3_value(uint32_t code) {
-  uint32_t E = code >> 3, m = code & 7;
-  if (E == 0) return (float)m * 0.001953125f;  // m * 2^-9
-  return __uint_as_float(((E + 120u) << 23) | (m << 20));
-}
-// Value of a 4-bit E2M1 code (sign in bit 3): 0, 0.5, 1, 1.5, 2, 3, 4, 6.
-__device__ __forceinline__ float e2m1_value(uint32_t c) {
-  const uint32_t m = c & 7u;
-  const float v = m < 4 ? 0.5f * (float)m : (float)(1u << ((m >> 1) - 1)) * (1.f + 0.5f * (float)(m & 1u));
-  return (c & 8u) ? -v : v;
-}
-__device__ __forceinline__ float head_scale(float amax) { return amax == 0.f ? 1.f : __fdiv_rn(amax, 2688.f); }
-
-// Quantizes 16 values with head scale s; returns the scale code, writes 8 code bytes.
-__device__ __forceinline__ uint32_t quant16(const float* x, float s, uint2* codes) {
-  float a = 0.f;
-#pragma unroll
-  for (int i = 0; i < 16; ++i) a = fmaxf(a, fabsf(x[i]));
-  const float r = __fdiv_rn(a, __fmul_rn(6.f, s));
-  const uint32_t sb = cvt_ue4m3(r);
-  if (sb == 0) {
-    *codes = make_uint2(0u, 0u);
-    return 0;
-  }
-  const float inv = __frcp_rn(__fmul_rn(ue4m3_value(sb), s));
-  uint32_t w[2] = {0u, 0u};
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const uint32_t byte = cvt_e2m1x2(__fmul_rn(x[2 * i], inv), __fmul_rn(x[2 * i + 1], inv));
-    w[i >> 2] |= byte << (8 * (i & 3));
-  }
-  *codes = make_uint2(w[0], w[1]);
-  return sb;
-}
-
-// E2M1 codes of 16 values under scale code sb, and the FP32 sum of squared
-// errors sum_i fp32(x_i - fp32(E2M1(code_i) * D))^2 in index order.
-__device__ __forceinline__ float block_codes(const float* x, float s, uint32_t sb, uint2* codes) {
-  const float D = __fmul_rn(ue4m3_value(sb), s);
-  const float inv = __frcp_rn(D);
-  uint32_t w[2] = {0u, 0u};
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const uint32_t byte = cvt_e2m1x2(__fmul_rn(x[2 * i], inv), __fmul_rn(x[2 * i + 1], inv));
-    w[i >> 2] |= byte << (8 * (i & 3));
-  }
-  float err = 0.f;
-#pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    const uint32_t c = (w[i >> 3] >> (4 * (i & 7))) & 0xFu;
-    const float t = __fsub_rn(x[i], __fmul_rn(e2m1_value(c), D));
-    err = __fadd_rn(err, __fmul_rn(t, t));
-  }
-  *codes = make_uint2(w[0], w[1]);
-  return err;
-}
-
-// quant16 with, when lse is set, the block scale picked by least squared error
-// among the nearest code and its two neighbours (tried in that order; only a
-// strictly smaller error replaces the pick).
-__device__ __forceinline__ uint32_t quant16_mode(const float* x, float s, uint2* codes, bool lse) {
-  uint32_t sb = quant16(x, s, codes);
-  if (!lse || sb == 0) return sb;
-  const uint32_t nearest = sb;
-  float best = block_codes(x, s, nearest, codes);
-#pragma unroll
-  for (int j = 0; j < 2; ++j) {
-    const uint32_t c = j == 0 ? nearest - 1 : nearest + 1;
-    if (c < 1 || c > 0x7E) continue;
-    uint2 c2;
-    const float e = block_codes(x, s, c, &c2);
-    if (e < best) {
-      best = e;
-      sb = c;
-      *codes = c2;
-    }
-  }
-  return sb;
-}
-
 // One elected thread brings rows [j0, j0 + nk) of the K and V slices of a tile
 // into shared memory with two bulk copies (rows are 2d bytes, a multiple of 16;
 // the slices start on 16-byte boundaries).  Every thread then waits, bounded;
@@ -334,16 +256,11 @@ __global__ void __launch_bounds__(kThreads) finalize_kernel(Shape s, Workspace w
   }
 }
 
-// Copies a blob image from shared memory to global memory with 16-byte stores.
-__device__ __forceinline__ void store_image(uint8_t* dst, const uint8_t* img, int bytes) {
-  for (int i = threadIdx.x; i < bytes / 16; i += blockDim.x)
-    reinterpret_cast<uint4*>(dst)[i] = reinterpret_cast<const uint4*>(img)[i];
-}
-
 __global__ void __launch_bounds__(kThreads) quant_kernel(Shape s, const uint16_t* __restrict__ q,
                                                           const uint16_t* __restrict__ k,
                                                           const uint16_t* __restrict__ v, Workspace ws,
-                                                          int n_kv_blocks, int do_kv, int* err, int lse) {
+                                                          int n_kv_blocks, int do_kv, int* err, int lse,
+                                                          int kv_scales_from_q) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ __align__(8) uint64_t bar;
   const int d = s.d, T = s.T();
@@ -369,63 +286,7 @@ __global__ void __launch_bounds__(kThreads) quant_kernel(Shape s, const uint16_t
       ws.s_k[bh] = sk;
       ws.s_v[bh] = sv;
     }
-    const int ncb = d / 16;
-    // K: per (key n, 16-channel block cb), centred.  blockDim is a multiple of
-    // ncb, so each thread keeps one cb and its 16 means in registers.
-    {
-      const int cb = threadIdx.x % ncb;
-      float mu16[16];
-#pragma unroll
-      for (int i = 0; i < 16; ++i) mu16[i] = mus[cb * 16 + i];
-      for (int n = threadIdx.x / ncb; n < nk; n += blockDim.x / ncb) {
-        const uint4* src = reinterpret_cast<const uint4*>(ks + n * d + cb * 16);
-        const uint4 a0 = src[0], a1 = src[1];
-        const uint32_t w[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-        float x[16];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          x[2 * i] = __fsub_rn(bf16f(w[i] & 0xFFFF), mu16[2 * i]);
-          x[2 * i + 1] = __fsub_rn(bf16f(w[i] >> 16), mu16[2 * i + 1]);
-        }
-        uint2 codes;
-        const uint32_t sb = quant16_mode(x, sk, &codes, lse);
-        *reinterpret_cast<uint2*>(img + blob_kcodes(d) + fp4_kmajor_off(n, cb, d / 2)) = codes;
-        const int kb = cb >> 2, k16 = cb & 3;
-        img[blob_ksf(d) + (kb >> 1) * 512 + (n & 31) * 16 + ((n >> 5) + 2 * (kb & 1)) * 4 + k16] = (uint8_t)sb;
-      }
-    }
-    // V^T: per (channel pair, 16-key block kb16)
-    for (int it = threadIdx.x; it < (d / 2) * 4; it += blockDim.x) {
-      const int cp = it % (d / 2), kb16 = it / (d / 2);
-      float x0[16], x1[16];
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const uint32_t w = reinterpret_cast<const uint32_t*>(vs + (kb16 * 16 + i) * d)[cp];
-        x0[i] = bf16f(w & 0xFFFF);
-        x1[i] = bf16f(w >> 16);
-      }
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int c = 2 * cp + e;
-        uint2 codes;
-        const uint32_t sb = quant16_mode(e ? x1 : x0, sv, &codes, lse);
-        *reinterpret_cast<uint2*>(img + blob_vcodes(d) + fp4_kmajor_off(c, kb16, 32)) = codes;
-        img[blob_vsf(d) + (c >> 7) * 512 + sf_atom_off(c & 127, kb16)] = (uint8_t)sb;
-      }
-    }
-    // FP16 copy of the tile's V rows for pass 2, divided by the head's power-of-two scale
-    if (ws.v16) {
-      const float inv = 1.f / v16_scale(__uint_as_float(ws.vamax[bh]));
-      uint4* dst = reinterpret_cast<uint4*>(ws.v16 + base);
-      for (int i = threadIdx.x; i < nk * d / 8; i += blockDim.x) {
-        const uint4 val = reinterpret_cast<const uint4*>(vs)[i];
-        const uint32_t w[4] = {val.x, val.y, val.z, val.w};
-        uint32_t o[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) o[e] = cvt_f16x2(bf16f(w[e] & 0xFFFF) * inv, bf16f(w[e] >> 16) * inv);
-        dst[i] = make_uint4(o[0], o[1], o[2], o[3]);
-      }
-    }
+    quant_kv_tile(s, ws, bh, t, nk, ks, vs, mus, img, lse != 0, threadIdx.x, blockDim.x);
     __syncthreads();
     store_image(ws.kv_blob + ((size_t)bh * T + t) * blob_bytes(d), img, blob_bytes(d));
     return;
@@ -438,6 +299,12 @@ __global__ void __launch_bounds__(kThreads) quant_kernel(Shape s, const uint16_t
   uint8_t* img = smem;
   uint8_t* img2 = smem + qblob_bytes(d);  // the residual term, when asked for
   const bool q2 = ws.q2_blob != nullptr;
+  if (blk == 0 && kv_scales_from_q && threadIdx.x == 0) {
+    // the K/V tiles are quantized inside the pass-1 launch, which needs the head
+    // scales from its start: the Q blocks publish them
+    ws.s_k[bh] = head_scale(__uint_as_float(ws.kcamax[bh]));
+    ws.s_v[bh] = head_scale(__uint_as_float(ws.vamax[bh]));
+  }
   if (blk == 0)
     for (int g = threadIdx.x; g < G; g += blockDim.x) {
       const int hq = b * s.Hq + h * G + g;
@@ -489,7 +356,7 @@ __global__ void __launch_bounds__(kThreads) quant_kernel(Shape s, const uint16_t
 }  // namespace
 
 cudaError_t launch_quantize(const Shape& s, const void* q, const void* k, const void* v, const Workspace& ws,
-                            bool do_q, bool do_kv, cudaStream_t st, bool lse) {
+                            bool do_q, bool do_kv, cudaStream_t st, bool lse, bool kv_in_pass1) {
   const int BH = s.BH(), d = s.d, T = s.T();
   int* err = device_error_word();
   cudaError_t e;
@@ -500,6 +367,8 @@ cudaError_t launch_quantize(const Shape& s, const void* q, const void* k, const 
     if ((e = cudaMemsetAsync(ws.kcamax, 0x00, sizeof(uint32_t) * BH, st))) return e;
   }
   if (do_q && (e = cudaMemsetAsync(ws.qamax, 0x00, sizeof(uint32_t) * s.B * s.Hq, st))) return e;
+  if (kv_in_pass1 && (e = cudaMemsetAsync(ws.kv_ready, 0x00, sizeof(uint32_t) * ((size_t)BH * T + 1), st)))
+    return e;
   const int n_kv = do_kv ? BH * T : 0;
   const int q_rows = 64;
   const int n_q = do_q ? s.B * s.Hq * ((s.Nq + q_rows - 1) / q_rows) : 0;
@@ -516,13 +385,14 @@ cudaError_t launch_quantize(const Shape& s, const void* q, const void* k, const 
     if ((e = cudaGetLastError())) return e;
   }
   const int n_qb = do_q ? BH * s.nblk() : 0;
+  const int n_kvq = kv_in_pass1 ? 0 : n_kv;  // K/V blocks of the quantizer kernel
   const size_t sm2 = (size_t)kTile * d * 2 * 2 + blob_bytes(d) + d * 4;
   if (sm2 > 48 * 1024 &&
       (e = cudaFuncSetAttribute(quant_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm2)))
     return e;
-  if (n_kv + n_qb > 0)
-    quant_kernel<<<n_kv + n_qb, kThreads, sm2, st>>>(s, (const uint16_t*)q, (const uint16_t*)k, (const uint16_t*)v,
-                                                     ws, n_kv, do_kv, err, lse ? 1 : 0);
+  if (n_kvq + n_qb > 0)
+    quant_kernel<<<n_kvq + n_qb, kThreads, sm2, st>>>(s, (const uint16_t*)q, (const uint16_t*)k, (const uint16_t*)v,
+                                                      ws, n_kvq, n_kvq > 0, err, lse ? 1 : 0, kv_in_pass1 ? 1 : 0);
   return cudaGetLastError();
 }
 
