@@ -309,7 +309,7 @@ def run_gpu(args):
     fp4_peak = pk["bf16_tflops_sustained"] * FP4_PER_BF16
     bf16_peak = pk["bf16_tflops_sustained"]
     t_q, t_p1, t_p2 = stages
-    src = kernel_source_hash(["apa_pass1.cu", "tc.cuh", "apa_internal.h"])
+    src = kernel_source_hash(["apa_pass1.cu", "quant_tile.cuh", "tc.cuh", "apa_internal.h"])
     p1_ach = work["F1"] / (t_p1 * 1e-3) / 1e12
     traffic = profiled_traffic("pass1", src)
     line["roofline"] = {"kernel": "pass1 (tcgen05 kind::mxf4nvf4)", "bound": "tensor", "achieved": p1_ach,
