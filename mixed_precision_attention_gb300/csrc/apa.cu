@@ -210,7 +210,7 @@ static int run_attention(const Shape& s, const void* q, const void* k, const voi
   // The least-squared-error scales cost about three times the quantizer work, more
   // than those SMs keep up with, so that option keeps the quantizer kernel.
   const bool lse_scales = (flags & APA_FLAG_LSE_SCALES) != 0, wide = wide_pass1 || ws.q2_blob;
-  const bool kv_in_pass1 = kv_in_pass1_ok && !lse_scales && pass1_quantizes_kv(s, wide, ws.q2_blob != nullptr);
+  const bool kv_in_pass1 = kv_in_pass1_ok && !lse_scales && pass1_quantizes_kv(s, wide_pass1, ws.q2_blob != nullptr);
   if (launch_quantize(s, q, k, v, ws, true, true, stream, lse_scales, kv_in_pass1) != cudaSuccess)
     return APA_ERR_CUDA;
   stage(1);

@@ -93,6 +93,9 @@ struct P1Cfg {
   static constexpr int kQ2Off = (kPsfOff + NP * 512 + 1023) / 1024 * 1024;  // residual Q blob
   static constexpr int kSmem = kQ2Off + kQBlob + 128;
   static constexpr uint32_t kTmemCols = D <= 128 ? 256 : 512;
+  // the K/V quantizer role in this kernel: two groups of 96 threads, each with
+  // double-buffered loads, or single-buffered at d = 256 (shared memory)
+  static constexpr int kQuantGroups = 2, kQuantBufs = D >= 256 ? 1 : 2;
   static constexpr uint32_t kSfc = 4 * sf_chunks(D);  // TMEM columns of one K or V scale set
   // kL: the ones-MMA row sums, or (register row sums) the scales of the residual Q term
   static constexpr uint32_t kO = 0, kS = D, kL = D + 64, kSFQ = D + 80, kSFQ2 = kL;
@@ -182,6 +185,35 @@ __device__ __forceinline__ uint32_t code_sum2(uint32_t w) {
   return acc;
 }
 
+// With the K/V quantizer in the same launch (lane 0 of a producer warp): waits
+// until the blob of visiting position i is written; returns one past the last of
+// positions i..i+7 known written (their flags read together), or -1 if the wait
+// gave up (then *abort_flag is set and the timeout recorded in *err).
+template <typename TileOf>
+__device__ __forceinline__ int await_blobs(const uint32_t* rd, int i, int n, TileOf tile_of, int* abort_flag,
+                                           int* err) {
+  const unsigned long long t0 = clock64();
+  while (true) {
+    uint32_t got = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      if (i + j < n && ld_relaxed_gpu(rd + tile_of(i + j)) != 0u) got |= 1u << j;
+    const int k = __ffs(~got) - 1;  // leading positions written
+    if (k > 0) {
+      __threadfence();             // acquire: the blob stores come before the flags
+      fence_proxy_async_global();  // and before the bulk copies that read them
+      return i + k;
+    }
+    if (*(volatile int*)abort_flag) return -1;
+    if (clock64() - t0 > APA_WAIT_LIMIT_CYCLES) {
+      *(volatile int*)abort_flag = 1;
+      if (err) atomicCAS(err, 0, APA_DEVERR_TIMEOUT);
+      return -1;
+    }
+    __nanosleep(128);
+  }
+}
+
 // What a row keeps between encoding a tile and judging it.
 struct Pending {
   float c, mt;
@@ -200,6 +232,15 @@ __global__ void __launch_bounds__(kThreads, (D <= 128 ? 2 : 1)) pass1_kernel(con
   using C = P1Cfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+  if (!kOnesMma && p.kv_ready && (int)blockIdx.x >= p.n_p1) {
+    // the K/V quantizer, in groups that each keep a tile in flight: the tiles in
+    // the order the pass-1 CTAs below visit them
+    constexpr int kGroup = kThreads / C::kQuantGroups;
+    const int g = threadIdx.x / kGroup;
+    quant_role(p.s, p.k_raw, p.v_raw, p.ws, p.kv_ready, p.kv_ready + (size_t)p.s.BH() * p.s.T(), p.lse_scales != 0,
+               smem + g * quant_role_smem(D, C::kQuantBufs), p.err, g, threadIdx.x % kGroup, kGroup, C::kQuantBufs);
+    return;
+  }
   // barriers: q_full, blob_full[4], blob_empty[4], s_full, s_free, p_full[2], l_full, dec[2], pv_done[2], drain
   __shared__ __align__(8) uint64_t bars[19];
   __shared__ uint32_t tmem_slot;
@@ -267,10 +308,13 @@ __global__ void __launch_bounds__(kThreads, (D <= 128 ? 2 : 1)) pass1_kernel(con
       mbar_arrive_expect_tx(q_full, q2 ? 2 * C::kQBlob : C::kQBlob);
       bulk_g2s(sbase + C::kQOff, qsrc, C::kQBlob, q_full);
       if (q2) bulk_g2s(sbase + C::kQ2Off, p.q2_blob + ((size_t)bh * nblk + blk) * C::kQBlob, C::kQBlob, q_full);
-      int issued = 0;
+      int issued = 0, written = 0;
       for (int i = 0; i < n; ++i) {
         const int st = i % C::NS;
         if (i >= C::NS && !mbar_wait(blob_empty(st), ((i / C::NS) - 1) & 1, &abort_flag, p.err)) break;
+        if (!kOnesMma && p.kv_ready && i >= written &&
+            (written = await_blobs(p.kv_ready + (size_t)bh * T, i, n, tile_of, &abort_flag, p.err)) < 0)
+          break;
         const uint8_t* src = p.kv_blob + ((size_t)bh * T + tile_of(i)) * C::kBlob;
         mbar_arrive_expect_tx(blob_full(st), C::kBlob);
         bulk_g2s(sbase + C::kStageOff + st * C::kBlob, src, C::kBlob, blob_full(st));
@@ -791,7 +835,7 @@ __global__ void __launch_bounds__(P1MCfg<D, U>::kThreads, 1) pass1_multi_kernel(
     constexpr int kGroup = C::kThreads / C::kQuantGroups;
     const int g = threadIdx.x / kGroup;
     quant_role(p.s, p.k_raw, p.v_raw, p.ws, p.kv_ready, p.kv_ready + (size_t)p.s.BH() * p.s.T(), p.lse_scales != 0,
-               smem + g * quant_role_smem(D), p.err, g, threadIdx.x % kGroup, kGroup);
+               smem + g * quant_role_smem(D), p.err, g, threadIdx.x % kGroup, kGroup, 2);
     return;
   }
   // barriers: q_full, blob_full[NS], blob_empty[NS], s_full[U], s_free[U], p_full[U][2], pv_done[U][2],
@@ -863,37 +907,13 @@ __global__ void __launch_bounds__(P1MCfg<D, U>::kThreads, 1) pass1_multi_kernel(
         if (grp * U + u < nblk)
           bulk_g2s(sbase + u * C::kQStride, p.q_blob + ((size_t)bh * nblk + grp * U + u) * C::kQBlob, C::kQBlob,
                    q_full);
-      // With the K/V quantizer in this launch: waits until the blob of visiting
-      // position i is written; returns one past the last position of i..i+7 known
-      // written (flags read together), or -1 if the wait gave up.
-      auto await_blobs = [&](int i) -> int {
-        const uint32_t* rd = p.kv_ready + (size_t)bh * T;
-        const unsigned long long t0 = clock64();
-        while (true) {
-          uint32_t got = 0;
-#pragma unroll
-          for (int j = 0; j < 8; ++j)
-            if (i + j < n && ld_relaxed_gpu(rd + tile_of(i + j)) != 0u) got |= 1u << j;
-          const int k = __ffs(~got) - 1;  // leading positions written
-          if (k > 0) {
-            __threadfence();             // acquire: the blob stores come before the flags
-            fence_proxy_async_global();  // and before the bulk copies that read them
-            return i + k;
-          }
-          if (*(volatile int*)&abort_flag) return -1;
-          if (clock64() - t0 > APA_WAIT_LIMIT_CYCLES) {
-            abort_flag = 1;
-            if (p.err) atomicCAS(p.err, 0, APA_DEVERR_TIMEOUT);
-            return -1;
-          }
-          __nanosleep(128);
-        }
-      };
       int issued = 0, written = 0;
       for (int i = 0; i < n; ++i) {
         const int st = i % C::NS;
         if (i >= C::NS && !mbar_wait(blob_empty(st), ((i / C::NS) - 1) & 1, &abort_flag, p.err)) break;
-        if (p.kv_ready && i >= written && (written = await_blobs(i)) < 0) break;
+        if (p.kv_ready && i >= written &&
+            (written = await_blobs(p.kv_ready + (size_t)bh * T, i, n, tile_of, &abort_flag, p.err)) < 0)
+          break;
         mbar_arrive_expect_tx(blob_full(st), C::kBlob);
         bulk_g2s(sbase + C::kStageOff + st * C::kBlob, p.kv_blob + ((size_t)bh * T + tile_of(i)) * C::kBlob,
                  C::kBlob, blob_full(st));
@@ -1224,14 +1244,46 @@ cudaError_t launch_multi(const P1Params& prm, cudaStream_t st) {
   return cudaLaunchKernelEx(&cfg, pass1_multi_kernel<D, U>, prm2);
 }
 
+// Shared memory of the one-block kernel when it also runs the K/V quantizer:
+// enough for either role, and more than half an SM's (one CTA per SM).
+template <int D>
+constexpr int single_kv_smem() {
+  constexpr int a = P1Cfg<D>::kSmem, b = P1Cfg<D>::kQuantGroups * quant_role_smem(D, P1Cfg<D>::kQuantBufs) + 128,
+                half = 114 * 1024 + 1024;
+  return a > b ? (a > half ? a : half) : (b > half ? b : half);
+}
+
 template <int D, bool kOnesMma>
 cudaError_t launch_dv(const P1Params& prm, cudaStream_t st) {
-  const int smem = P1Cfg<D>::kSmem;
-  cudaError_t e =
-      cudaFuncSetAttribute(pass1_kernel<D, kOnesMma>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  const int n_p1 = prm.s.BH() * prm.s.nblk();
+  if (!prm.kv_ready) {
+    const int smem = P1Cfg<D>::kSmem;
+    cudaError_t e =
+        cudaFuncSetAttribute(pass1_kernel<D, kOnesMma>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e) return e;
+    pass1_kernel<D, kOnesMma><<<n_p1, kThreads, smem, st>>>(prm);
+    return cudaGetLastError();
+  }
+  if (kOnesMma) return cudaErrorInvalidValue;
+  // with the K/V quantizer: one CTA per SM, cooperative (see launch_multi)
+  const int smem = single_kv_smem<D>();
+  cudaError_t e = cudaFuncSetAttribute(pass1_kernel<D, kOnesMma>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e) return e;
-  pass1_kernel<D, kOnesMma><<<prm.s.BH() * prm.s.nblk(), kThreads, smem, st>>>(prm);
-  return cudaGetLastError();
+  int dev = 0, sms = 0;
+  if ((e = cudaGetDevice(&dev)) || (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev))) return e;
+  P1Params prm2 = prm;
+  prm2.n_p1 = n_p1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)sms);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = (size_t)smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, pass1_kernel<D, kOnesMma>, prm2);
 }
 
 // APA_PASS1_ROWSUM=mma selects the ones-MMA row sums (for comparison); the
@@ -1255,12 +1307,6 @@ bool single_unit() {
 
 template <int D>
 cudaError_t launch_d(const P1Params& prm, bool wide, cudaStream_t st) {
-  if constexpr (D <= 128) {
-    // the K/V quantizer runs only inside the three-block kernel
-    if (prm.kv_ready) return launch_multi<D, 3>(prm, st);
-  } else {
-    if (prm.kv_ready) return cudaErrorInvalidValue;
-  }
   // the residual Q term lives in the one-block kernel with register row sums
   if (prm.q2_blob) return launch_dv<D, false>(prm, st);
   if (rowsum_by_mma()) return launch_dv<D, true>(prm, st);
@@ -1277,6 +1323,22 @@ bool kv_in_pass1_allowed() {
     return !(e && strcmp(e, "0") == 0);
   }();
   return v;
+}
+
+template <int D>
+bool single_quantizes_kv(const Shape& s) {
+  int dev = 0, sms = 0, per_sm = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return false;
+  const int n_p1 = s.BH() * s.nblk();
+  if (sms - n_p1 < 8) return false;
+  if (cudaFuncSetAttribute(pass1_kernel<D, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, single_kv_smem<D>()) !=
+          cudaSuccess ||
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, pass1_kernel<D, false>, kThreads, single_kv_smem<D>()) !=
+          cudaSuccess)
+    return false;
+  return per_sm == 1;
 }
 
 template <int D>
@@ -1300,9 +1362,16 @@ bool multi_quantizes_kv(const Shape& s) {
 }  // namespace
 
 bool pass1_quantizes_kv(const Shape& s, bool wide, bool q_residual) {
-  if (wide || q_residual || rowsum_by_mma() || single_unit() || !kv_in_pass1_allowed()) return false;
-  if (s.d == 64) return multi_quantizes_kv<64>(s);
-  if (s.d == 128) return multi_quantizes_kv<128>(s);
+  // the same choice of kernel as launch_d; the wide form shares the GPU and the
+  // ones-MMA form has no room, so neither hosts the quantizer
+  if (wide || !kv_in_pass1_allowed()) return false;
+  if (!q_residual && rowsum_by_mma()) return false;
+  const bool one_block = q_residual || single_unit() || s.d > 128;
+  switch (s.d) {
+    case 64: return one_block ? single_quantizes_kv<64>(s) : multi_quantizes_kv<64>(s);
+    case 128: return one_block ? single_quantizes_kv<128>(s) : multi_quantizes_kv<128>(s);
+    case 256: return single_quantizes_kv<256>(s);
+  }
   return false;
 }
 

@@ -104,12 +104,15 @@ __device__ __forceinline__ void store_image(uint8_t* dst, const uint8_t* img, in
   store_image(dst, img, bytes, threadIdx.x, blockDim.x);
 }
 
-// Barrier over the nth threads of a group (named barrier id, 1..15); the _and
-// form also returns whether v held in every thread of the group.
-__device__ __forceinline__ void group_sync(int id, int nth) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nth) : "memory");
+// Barrier over the nth threads of a group (named barrier id, 1..4); the _and
+// form also returns whether v held in every thread of the group.  The ids are
+// immediates, so a kernel reserves only the barriers it can name.
+template <int kId>
+__device__ __forceinline__ void bar_sync_id(int nth) {
+  asm volatile("bar.sync %0, %1;" ::"n"(kId), "r"(nth) : "memory");
 }
-__device__ __forceinline__ bool group_sync_and(int id, int nth, bool v) {
+template <int kId>
+__device__ __forceinline__ bool bar_red_and_id(int nth, bool v) {
   uint32_t r;
   asm volatile(
       "{\n.reg .pred p, q;\n"
@@ -117,9 +120,25 @@ __device__ __forceinline__ bool group_sync_and(int id, int nth, bool v) {
       "bar.red.and.pred q, %2, %3, p;\n"
       "selp.u32 %0, 1, 0, q;\n}"
       : "=r"(r)
-      : "r"((uint32_t)v), "r"(id), "r"(nth)
+      : "r"((uint32_t)v), "n"(kId), "r"(nth)
       : "memory");
   return r != 0;
+}
+__device__ __forceinline__ void group_sync(int id, int nth) {
+  switch (id) {
+    case 1: bar_sync_id<1>(nth); break;
+    case 2: bar_sync_id<2>(nth); break;
+    case 3: bar_sync_id<3>(nth); break;
+    default: bar_sync_id<4>(nth); break;
+  }
+}
+__device__ __forceinline__ bool group_sync_and(int id, int nth, bool v) {
+  switch (id) {
+    case 1: return bar_red_and_id<1>(nth, v);
+    case 2: return bar_red_and_id<2>(nth, v);
+    case 3: return bar_red_and_id<3>(nth, v);
+    default: return bar_red_and_id<4>(nth, v);
+  }
 }
 
 // Quantizes the tile of keys [t*64, t*64 + nk) of head bh whose K and V rows are
@@ -193,9 +212,11 @@ __device__ __forceinline__ void quant_kv_tile(const Shape& s, const Workspace& w
   }
 }
 
-// Bytes of shared memory one group of the K/V quantizer role needs: two K/V tile
+// Bytes of shared memory one group of the K/V quantizer role needs: nbuf K/V tile
 // buffers, the blob image, the key mean and two mbarriers (a multiple of 16).
-__host__ __device__ constexpr int quant_role_smem(int d) { return 4 * kTile * d * 2 + blob_bytes(d) + d * 4 + 16; }
+__host__ __device__ constexpr int quant_role_smem(int d, int nbuf = 2) {
+  return nbuf * 2 * kTile * d * 2 + blob_bytes(d) + d * 4 + 16;
+}
 
 constexpr int kQuantRoleGroups = 4;  // at most, per block
 
@@ -206,20 +227,21 @@ constexpr int kQuantRoleGroups = 4;  // at most, per block
 // step, which is the order in which pass 1 visits the tiles ("Tile order": the
 // sink, then back from the causal diagonal).  It quantizes the tile, stores its
 // blob and FP16 V rows, and then publishes ready[bh * T + t] = 1 (release at GPU
-// scope) for pass 1 to wait on.  The K/V loads are double-buffered: the next
-// ticket's bulk copies fly while the group quantizes the current tile.  `smem`
-// (16-byte aligned) holds quant_role_smem(d) bytes of the group's own.  Returns
-// false if a wait gave up (the error word is set).
+// scope) for pass 1 to wait on.  With nbuf = 2 the K/V loads are double-buffered:
+// the next ticket's bulk copies fly while the group quantizes the current tile;
+// with nbuf = 1 they are issued once the tile is done.  `smem` (16-byte aligned)
+// holds quant_role_smem(d, nbuf) bytes of the group's own.  Returns false if a
+// wait gave up (the error word is set).
 __device__ __noinline__ bool quant_role(const Shape& s, const uint16_t* __restrict__ k,
                                         const uint16_t* __restrict__ v, const Workspace& ws, uint32_t* ready,
                                         uint32_t* ticket, bool lse, uint8_t* smem, int* err, int group, int tid,
-                                        int nth) {
+                                        int nth, int nbuf) {
   __shared__ int tk_all[kQuantRoleGroups][2];
   int* tk_s = tk_all[group];
   const int bid = 1 + group;
   const int d = s.d, T = s.T(), BH = s.BH(), total = BH * T;
   const int kvb = kTile * d * 2;  // bytes of one K or V tile
-  uint8_t* img = smem + 4 * kvb;
+  uint8_t* img = smem + 2 * nbuf * kvb;
   float* mus = reinterpret_cast<float*>(img + blob_bytes(d));
   const uint32_t bar0 = smem_u32(mus + d);
   if (tid == 0) {
@@ -262,7 +284,7 @@ __device__ __noinline__ bool quant_role(const Shape& s, const uint16_t* __restri
     if (tid == 0) {
       const int nx = (int)atomicAdd(ticket, 1u);
       tk_s[(j + 1) & 1] = nx;
-      if (nx < total) {
+      if (nx < total && nbuf == 2) {
         issue(nx, buf ^ 1);
         pending |= 1u << (buf ^ 1);
       }
@@ -295,9 +317,13 @@ __device__ __noinline__ bool quant_role(const Shape& s, const uint16_t* __restri
     if (tid == 0) {
       __threadfence();
       st_release_gpu(ready + (size_t)bh * T + t, 1u);
+      if (nbuf == 1 && nxt < total) {  // the only buffer is free again
+        issue(nxt, 0);
+        pending |= 1u;
+      }
     }
     cur = nxt;
-    buf ^= 1;
+    if (nbuf == 2) buf ^= 1;
   }
   if (!ok && tid == 0) {
     // let the copies in flight land before the block's shared memory goes away (bounded)
