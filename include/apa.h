@@ -76,7 +76,15 @@ extern "C" {
  *            holds query head h*G + g at position pos).  At eps = 0 every tile the
  *            group can see is marked.  Nullable.
  * The workspace is allocated stream-ordered on `stream` (cudaMallocAsync) and
- * released the same way.  Returns APA_OK or a negative status. */
+ * released the same way.  Returns APA_OK or a negative status.
+ * When the pass-1 CTAs leave at least 8 SMs free, the K/V tiles are quantized
+ * inside the pass-1 launch ("What else is in the box" on the page: quantization
+ * inside the launch): that kernel is then launched cooperatively with one block
+ * on every SM, so it starts once the whole GPU is free and holds it while it
+ * runs.  If the driver refuses that launch (fewer SMs available to the context
+ * than the device has), the call falls back to the separate quantizer kernel.
+ * The environment variable APA_PASS1_QUANT_KV=0 selects the separate kernel
+ * always.  The results are the same bits either way. */
 int apa_attention(const void* q, const void* k, const void* v, int B, int Hq, int Hkv, int Nq, int Nkv, int d,
                   int causal, float eps, float* out, float* lse, uint32_t* hot_mask, cudaStream_t stream);
 

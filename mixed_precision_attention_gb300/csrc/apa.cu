@@ -215,8 +215,16 @@ static int run_attention(const Shape& s, const void* q, const void* k, const voi
     return APA_ERR_CUDA;
   stage(1);
   const KvSource src{k, v, lse_scales};
-  if (launch_pass1(s, ws, eps, hot_mask, wide, stream, kv_in_pass1 ? &src : nullptr) != cudaSuccess)
-    return APA_ERR_CUDA;
+  cudaError_t e1 = launch_pass1(s, ws, eps, hot_mask, wide, stream, kv_in_pass1 ? &src : nullptr);
+  if (kv_in_pass1 && e1 == cudaErrorCooperativeLaunchTooLarge) {
+    // fewer SMs than the device reports are ours (a partitioned or shared GPU):
+    // quantize K/V with the separate kernel (recomputing the same statistics) and
+    // run pass 1 on its own
+    (void)cudaGetLastError();
+    if (launch_quantize(s, q, k, v, ws, false, true, stream, lse_scales) != cudaSuccess) return APA_ERR_CUDA;
+    e1 = launch_pass1(s, ws, eps, hot_mask, wide, stream);
+  }
+  if (e1 != cudaSuccess) return APA_ERR_CUDA;
   if (launch_pass2_order(s, ws, stream) != cudaSuccess) return APA_ERR_CUDA;
   stage(2);
   if (launch_pass2(s, q, k, v, &ws, out, lse, stream) != cudaSuccess) return APA_ERR_CUDA;
