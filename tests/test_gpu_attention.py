@@ -269,3 +269,25 @@ def test_value_weighted_eps_limits_are_unchanged(eps):
     apa.check_error()
     for x, y in zip(a, b):
         assert np.array_equal(x.cpu().numpy(), y.cpu().numpy())
+
+
+def test_in_launch_quantizer_with_few_spare_sms():
+    """48 KV heads x 3 groups of three 128-row blocks = 144 pass-1 CTAs: on a
+    152-SM part only 8 SMs quantize K/V inside the pass-1 launch, so pass 1 keeps
+    waiting on the quantizer's per-tile flags.  The result must equal, bit for bit,
+    the host entry point's, whose sub-problems use the separate quantizer kernel."""
+    import torch
+
+    import mixed_precision_attention_gb300 as apa
+    w = synth.small(B=1, Hq=48, Hkv=48, Nq=1152, Nkv=4096, d=128, n_outliers=2, sink_gain=4.0, seed=5)
+    q, k, v = synth.generate(w)
+    dev = _gpu.run_apa(q, k, v, eps=0.005)
+    hq, hk, hv = (synth.to_torch_bf16(a).pin_memory() for a in (q, k, v))
+    out, lse, mask = apa.attention_host(hq, hk, hv, causal=True, eps=0.005, return_hot_mask=True)
+    torch.cuda.synchronize()
+    assert np.array_equal(out.numpy().astype(np.float64), dev[0])
+    assert np.array_equal(lse.numpy().astype(np.float64), dev[1])
+    assert np.array_equal(mask.numpy().view(np.uint32), dev[2])
+    # and a sample of rows against the oracle's emulation
+    ref = oracle.apa(*(np.ascontiguousarray(a[:, :2]) for a in (q, k, v)), eps=0.005)
+    assert np.abs(dev[0][:, :2] - ref["out"]).max() <= 1e-2
