@@ -124,3 +124,46 @@ def test_lse_scales_bit_exact(case):
     assert np.array_equal(c2, oq["codes2"]) and np.array_equal(s2, oq["sf2"])
     near = oracle.quantize_kv(k, v)
     assert (near["ksf"] != ok["ksf"]).any()  # the choice is not just the nearest scale
+
+
+def test_e2m1_rounding_of_every_bf16_value_in_range():
+    """Every bf16 value x with |x| <= 6, signed zeros included, through the GPU
+    quantizer with head scale 1 and block scale 1 (a head maximum of 2688 and a 6
+    in every block), so each code is the plain E2M1 rounding of x: nearest of
+    0, 0.5, 1, 1.5, 2, 3, 4, 6, ties to the even code, sign kept.  Checked
+    against that rule written out here and against the oracle."""
+    pos = np.arange(0x0000, 0x40C1, dtype=np.uint16)          # +0 .. 6.0
+    vals = np.concatenate([pos, pos | np.uint16(0x8000)])   # and -0 .. -6.0
+    d = 128
+    nb = (len(vals) + 14) // 15                              # 15 values + one 6.0 per block
+    blocks = np.full((nb, 16), 0x40C0, np.uint16)
+    flat = blocks[:, 1:].reshape(-1)
+    flat[:len(vals)] = vals
+    flat[len(vals):] = 0x40C0
+    blocks[:, 1:] = flat.reshape(nb, 15)
+    rows = (nb * 16 + d - 1) // d
+    qrow = np.full(rows * d, 0x40C0, np.uint16)
+    qrow[:nb * 16] = blocks.reshape(-1)
+    q = np.zeros((1, 1, rows + 1, d), np.uint16)
+    q[0, 0, :rows] = qrow.reshape(rows, d)
+    q[0, 0, rows, 0] = synth.f32_to_bf16_bits(np.array([2688.0], np.float32))[0]  # head maximum: scale 1
+    kv = synth.f32_to_bf16_bits(np.ones((1, 1, 64, d), np.float32))
+    g = _quant_gpu(q, kv, kv)
+    assert g["s_q"][0, 0] == 1.0
+    qc, qsf, _, _ = _gpu.decode_q_blob(g["q_blob"], 1, 1, 1, rows + 1, d)
+    codes = qc[0, 0, :rows].reshape(-1)[:nb * 16].reshape(nb, 16)
+    assert (qsf[0, 0, :rows].reshape(-1)[:nb] == 0x38).all()   # UE4M3 1.0 for every test block
+    # the rule, independently
+    x = synth.bf16_bits_to_f32(vals).astype(np.float64)
+    grid = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+    dist = np.abs(np.abs(x)[:, None] - grid)
+    best = dist.min(1, keepdims=True)
+    cand = np.where(dist == best, np.arange(8), 99)
+    even = np.where((dist == best) & (np.arange(8) % 2 == 0), np.arange(8), 99).min(1)
+    idx = np.where(even < 99, even, cand.min(1))
+    want = idx | (np.signbit(x).astype(np.int64) << 3)
+    got = codes[:, 1:].reshape(-1)[:len(vals)]
+    assert np.array_equal(got.astype(np.int64), want)
+    # and the oracle agrees on the whole tensor
+    oq = oracle.quantize_q(q)
+    assert np.array_equal(qc, oq["codes"]) and np.array_equal(qsf, oq["sf"])
