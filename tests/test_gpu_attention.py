@@ -291,3 +291,34 @@ def test_in_launch_quantizer_with_few_spare_sms():
     # and a sample of rows against the oracle's emulation
     ref = oracle.apa(*(np.ascontiguousarray(a[:, :2]) for a in (q, k, v)), eps=0.005)
     assert np.abs(dev[0][:, :2] - ref["out"]).max() <= 1e-2
+
+
+def test_subnormal_block_scales_reach_the_tensor_cores():
+    """UE4M3 block scales below 2^-6 (E = 0: m * 2^-9) are decoded by the block-
+    scaled MMA as the oracle decodes them.  All-FP4 run (eps = inf), non-causal:
+    rows 0-9 attend almost only to key tile 1, whose V blocks have subnormal scales
+    (values 0.03 under a V head scale of 1); row 10 is a Q row with subnormal
+    scales whose scores decide where it looks.  Dropping those scales would zero
+    the rows' output, or spread row 10 evenly over all keys (channel 5 near 10.5)."""
+    rng = np.random.default_rng(3)
+    B, Hq, Hkv, Nq, Nkv, d = 1, 1, 1, 64, 256, 64
+    u = rng.standard_normal(d).astype(np.float32)
+    qf = (2.0 * u + 0.3 * rng.standard_normal((B, Hq, Nq, d))).astype(np.float32)
+    kf = (-8.0 * u + 0.3 * rng.standard_normal((B, Hkv, Nkv, d))).astype(np.float32)
+    kf[0, 0, 64:128] = 8.0 * u + 0.3 * rng.standard_normal((64, d))
+    vf = rng.standard_normal((B, Hkv, Nkv, d)).astype(np.float32)
+    vf[0, 0, 64:128] = 0.03 * np.sign(rng.standard_normal((64, d)))
+    vf[0, 0, 200, 5] = 2688.0
+    qf[0, 0, 10, :] = 0.03 * np.sign(u)
+    qf[0, 0, 11, :] = 0.0
+    qf[0, 0, 11, 0] = 2688.0
+    q, k, v = (synth.f32_to_bf16_bits(a) for a in (qf, kf, vf))
+    assert (oracle.quantize_kv(k, v)["vsf"][0, 0, :, 4:8] < 8).all()   # subnormal V scales in tile 1
+    assert (oracle.quantize_q(q)["sf"][0, 0, 10] < 8).all()             # and in Q row 10
+    ref = oracle.apa(q, k, v, causal=False, eps=np.inf)["out"][0, 0]
+    out, _, _ = _gpu.run_apa(q, k, v, causal=False, eps=np.inf)
+    got = out[0, 0]
+    assert np.abs(got - ref).max() <= 1e-2
+    for r in range(10):
+        assert abs(np.linalg.norm(got[r]) - np.linalg.norm(ref[r])) <= 0.05 * np.linalg.norm(ref[r])
+    assert abs(got[10, 5] - ref[10, 5]) <= 0.05 and ref[10, 5] < 2.0
