@@ -49,7 +49,7 @@ extern "C" {
 #define APA_ERR_HEAD_DIM (-4)  /* d not in {64, 128, 256} */
 #define APA_ERR_CUDA (-5)      /* a CUDA call or launch failed; cudaGetLastError() holds the cause */
 #define APA_ERR_NOMEM (-6)     /* the workspace could not be allocated, or the given one is too small */
-#define APA_ERR_DEVICE (-7)    /* a kernel recorded a device-side timeout (apa_check_error) */
+#define APA_ERR_DEVICE (-7)    /* a kernel recorded a device-side error: a timeout, or a bad block-table entry (apa_check_error) */
 #define APA_ERR_ALIGN (-8)     /* q, k or v not 16-byte aligned */
 #define APA_ERR_SCRATCH (-9)   /* too large for the fixed scratch of apa_quantize_noalloc */
 #define APA_ERR_FLAGS (-10)    /* an unknown bit in `flags` */
@@ -129,6 +129,22 @@ int apa_attention_ex(const void* q, const void* k, const void* v, int B, int Hq,
                      int causal, float eps, unsigned flags, float* out, float* lse, uint32_t* hot_mask,
                      void* workspace, size_t workspace_bytes, cudaStream_t stream);
 size_t apa_workspace_bytes_ex(int B, int Hq, int Hkv, int Nq, int Nkv, int d, float eps, unsigned flags);
+
+/* apa_attention() on a paged K/V cache.  Every (sequence, KV head) keeps its keys
+ * and values in pages of 64 keys (one key tile) drawn from one pool:
+ *   k_pages, v_pages  bf16 [num_pages][Hkv][64][d], contiguous, 16-byte aligned
+ *   block_table       int32 [B][max_pages] in device memory: entry t of sequence b
+ *                     is the page holding its keys 64t .. 64t+63;
+ *                     max_pages >= ceil(Nkv/64); num_pages * Hkv * 64 < 2^31
+ * (the blog, "What else is in the box": pass 2 reads through a block table; here
+ * every read of K and V does).  All sequences have Nkv keys and Nq queries, as
+ * in apa_attention.  Keys past Nkv in a sequence's last page are never used.  A
+ * table entry outside [0, num_pages) reads page 0 and is reported by
+ * apa_check_error as a bounds error (status APA_ERR_DEVICE).  The results are
+ * those of apa_attention on the same keys laid out contiguously, bit for bit. */
+int apa_attention_paged(const void* q, const void* k_pages, const void* v_pages, int num_pages,
+                        const int32_t* block_table, int max_pages, int B, int Hq, int Hkv, int Nq, int Nkv, int d,
+                        int causal, float eps, float* out, float* lse, uint32_t* hot_mask, cudaStream_t stream);
 
 /* apa_attention() on HOST buffers (page-locked memory recommended): copies q, k,
  * v to the device, runs, copies out (and lse / hot_mask when non-null) back,

@@ -18,7 +18,7 @@ import ctypes
 from . import _lib
 from ._lib import ApaError, status_string
 
-__all__ = ["attention", "attention_host", "quantize", "quantize_noalloc", "workspace_bytes", "check_error", "ApaError",
+__all__ = ["attention", "attention_paged", "attention_host", "quantize", "quantize_noalloc", "workspace_bytes", "check_error", "ApaError",
            "status_string", "hot_mask_shape", "TILE", "GROUP_ROWS", "BLOCK_ROWS", "FLAG_Q_RESIDUAL",
            "FLAG_LSE_SCALES", "FLAG_VALUE_WEIGHTED"]
 
@@ -108,6 +108,38 @@ def attention(q, k, v, causal: bool = True, eps: float = 0.005, return_hot_mask:
         st = lib.apa_attention_ws(_ptr(q), _ptr(k), _ptr(v), B, Hq, Hkv, Nq, Nkv, d, int(bool(causal)), float(eps),
                                   _ptr(out), _ptr(lse), _ptr(mask), _ptr(workspace), nbytes, _stream(dev))
         _lib.check(st, "apa_attention_ws")
+    return out, lse, mask
+
+
+def attention_paged(q, k_pages, v_pages, block_table, Nkv: int, causal: bool = True, eps: float = 0.005,
+                    return_hot_mask: bool = False, return_lse: bool = True):
+    """apa_attention_paged: attention over a paged K/V cache.
+
+    q: [B, Hq, Nq, d] bf16; k_pages, v_pages: [num_pages, Hkv, 64, d] bf16 (one page
+    = one 64-key tile of one sequence, all KV heads); block_table: int32 CUDA tensor
+    [B, max_pages], entry t of sequence b = the page holding its keys 64t..64t+63;
+    Nkv: keys per sequence.  Returns (out, lse or None, hot_mask or None) as attention()."""
+    import torch
+    lib = _lib.load()
+    for name, t in (("q", q), ("k_pages", k_pages), ("v_pages", v_pages)):
+        if not isinstance(t, torch.Tensor) or t.dtype != torch.bfloat16 or t.dim() != 4 or not t.is_cuda \
+                or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous 4-D bf16 CUDA tensor")
+    if k_pages.shape != v_pages.shape or k_pages.shape[2] != TILE or k_pages.shape[3] != q.shape[3]:
+        raise ValueError("k_pages and v_pages must be [num_pages, Hkv, 64, d] with q's d")
+    if (not isinstance(block_table, torch.Tensor) or block_table.dtype != torch.int32 or block_table.dim() != 2
+            or not block_table.is_cuda or not block_table.is_contiguous() or block_table.shape[0] != q.shape[0]):
+        raise ValueError("block_table must be a contiguous int32 CUDA tensor [B, max_pages]")
+    B, Hq, Nq, d = q.shape
+    num_pages, Hkv = k_pages.shape[0], k_pages.shape[1]
+    dev = q.device
+    out = torch.empty((B, Hq, Nq, d), dtype=torch.float32, device=dev)
+    lse = torch.empty((B, Hq, Nq), dtype=torch.float32, device=dev) if return_lse else None
+    mask = torch.empty(hot_mask_shape(B, Hq, Hkv, Nq, Nkv), dtype=torch.int32, device=dev) if return_hot_mask else None
+    st = lib.apa_attention_paged(_ptr(q), _ptr(k_pages), _ptr(v_pages), num_pages, _ptr(block_table),
+                                 block_table.shape[1], B, Hq, Hkv, Nq, int(Nkv), d, int(bool(causal)), float(eps),
+                                 _ptr(out), _ptr(lse), _ptr(mask), _stream(dev))
+    _lib.check(st, "apa_attention_paged")
     return out, lse, mask
 
 

@@ -22,6 +22,7 @@ _SIGS = {
     "apa_attention": (I, [P, P, P, I, I, I, I, I, I, I, F, P, P, P, P]),
     "apa_attention_ws": (I, [P, P, P, I, I, I, I, I, I, I, F, P, P, P, P, SZ, P]),
     "apa_attention_host": (I, [P, P, P, I, I, I, I, I, I, I, F, P, P, P, P]),
+    "apa_attention_paged": (I, [P, P, P, I, P, I, I, I, I, I, I, I, I, F, P, P, P, P]),
     "apa_workspace_bytes": (SZ, [I, I, I, I, I, I, F]),
     "apa_attention_ex": (I, [P, P, P, I, I, I, I, I, I, I, F, ctypes.c_uint, P, P, P, P, SZ, P]),
     "apa_workspace_bytes_ex": (SZ, [I, I, I, I, I, I, F, ctypes.c_uint]),

@@ -268,6 +268,27 @@ int apa_attention(const void* q, const void* k, const void* v, int B, int Hq, in
   return st;
 }
 
+int apa_attention_paged(const void* q, const void* k_pages, const void* v_pages, int num_pages,
+                        const int32_t* block_table, int max_pages, int B, int Hq, int Hkv, int Nq, int Nkv, int d,
+                        int causal, float eps, float* out, float* lse, uint32_t* hot_mask, cudaStream_t stream) {
+  int st = apa::validate(q, k_pages, v_pages, out, B, Hq, Hkv, Nq, Nkv, d, causal, eps, true);
+  if (st) return st;
+  if (!block_table) return APA_ERR_NULL;
+  if (num_pages < 1 || max_pages < (Nkv + apa::kTile - 1) / apa::kTile ||
+      (long long)num_pages * Hkv * apa::kTile > (1ll << 31))
+    return APA_ERR_SHAPE;
+  Shape s{B, Hq, Hkv, Nq, Nkv, d, causal ? 1 : 0};
+  s.pages = block_table;
+  s.max_pages = max_pages;
+  s.num_pages = num_pages;
+  const size_t need = apa::workspace_layout(s, eps != 0.f, nullptr, nullptr);
+  void* ws = nullptr;
+  if (need && cudaMallocAsync(&ws, need, stream) != cudaSuccess) return APA_ERR_NOMEM;
+  st = apa::run_attention(s, q, k_pages, v_pages, eps, out, lse, hot_mask, ws, stream);
+  if (ws && cudaFreeAsync(ws, stream) != cudaSuccess && st == APA_OK) st = APA_ERR_CUDA;
+  return st;
+}
+
 size_t apa_workspace_bytes_ex(int B, int Hq, int Hkv, int Nq, int Nkv, int d, float eps, unsigned flags) {
   if (B < 1 || Hq < 1 || Hkv < 1 || Nq < 1 || Nkv < 1 || Hq % Hkv || (flags & ~apa::kKnownFlags)) return 0;
   Shape s{B, Hq, Hkv, Nq, Nkv, d, 1};
@@ -465,7 +486,7 @@ const char* apa_status_string(int status) {
     case APA_ERR_HEAD_DIM: return "head dimension must be 64, 128 or 256";
     case APA_ERR_CUDA: return "CUDA error (see cudaGetLastError)";
     case APA_ERR_NOMEM: return "workspace allocation failed or workspace too small";
-    case APA_ERR_DEVICE: return "a kernel timed out waiting on the device";
+    case APA_ERR_DEVICE: return "a kernel recorded a device-side error (a wait timed out, or a block-table entry was outside the page pool)";
     case APA_ERR_ALIGN: return "q, k and v must be 16-byte aligned";
     case APA_ERR_SCRATCH: return "problem too large for the fixed scratch of apa_quantize_noalloc";
     case APA_ERR_FLAGS: return "unknown option flag";

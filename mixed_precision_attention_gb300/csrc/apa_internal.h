@@ -23,6 +23,11 @@ constexpr float kLog2e = 1.4426950408889634f;
 
 struct Shape {
   int B, Hq, Hkv, Nq, Nkv, d, causal;
+  // Paged K/V (null: contiguous [B][Hkv][Nkv][d]): a pool of num_pages pages of
+  // kTile keys, [page][Hkv][kTile][d], and a block table [B][max_pages] whose
+  // entry t is the page holding keys kTile*t .. kTile*t + kTile-1 of sequence b.
+  const int32_t* pages = nullptr;
+  int max_pages = 0, num_pages = 0;
   __host__ __device__ int G() const { return Hq / Hkv; }
   __host__ __device__ int R() const { return G() * Nq; }
   __host__ __device__ int T() const { return (Nkv + kTile - 1) / kTile; }
@@ -116,6 +121,25 @@ __host__ __device__ inline float v16_scale(float vamax) {
 }
 
 int* device_error_word();  // library-wide device error word (set by bounded waits)
+
+#ifdef __CUDACC__
+// The page of key tile t of head (b, h) in a paged K/V pool; an entry outside the
+// pool reads page 0 and records APA_DEVERR_BOUNDS (2) in *err.
+__device__ __forceinline__ int kv_page(const Shape& s, int b, int t, int* err) {
+  int pg = s.pages[(size_t)b * s.max_pages + t];
+  if (pg < 0 || pg >= s.num_pages) {
+    if (err) atomicCAS(err, 0, 2);
+    pg = 0;
+  }
+  return pg;
+}
+// Element offset, in K or V, of the first key of tile t of head bh.
+__device__ __forceinline__ size_t kv_tile_offset(const Shape& s, int bh, int t, int* err) {
+  if (!s.pages) return ((size_t)bh * s.Nkv + (size_t)t * kTile) * s.d;
+  const int b = bh / s.Hkv, h = bh % s.Hkv;
+  return (((size_t)kv_page(s, b, t, err) * s.Hkv + h) * kTile) * s.d;
+}
+#endif
 
 
 // ------------------------------------------------------------------ launchers

@@ -267,12 +267,23 @@ __global__ void __launch_bounds__(kThreads, P2Cfg<D, kF16>::kCtasPerSm)
         if (i >= C::NS && !mbar_wait(kv_empty(st), ((i / C::NS) - 1) & 1, &abort_flag, p.err)) break;
         uint32_t gm;
         const int t = tile_of(i, gm);
+        // contiguous maps: (channel, key, b * Hkv + h); paged maps: (channel, key in
+        // page, page * Hkv + h).  The FP16 copy of V is contiguous in either case.
+        int ky = t * kTile, kz = bh, vy = ky, vz = bh;
+        if (s.pages) {
+          ky = 0;
+          kz = kv_page(s, b, t, p.err) * s.Hkv + h;
+          if (!kF16) {
+            vy = 0;
+            vz = kz;
+          }
+        }
         mbar_arrive_expect_tx(kv_full(st), 2 * C::kKVBytes);
         const uint32_t kdst = sbase + C::kStageOff + st * 2 * C::kKVBytes;
 #pragma unroll
         for (int a = 0; a < C::kAtoms; ++a) {
-          tma_load_3d(kdst + a * 8192, &kmap, a * 64, t * kTile, bh, kv_full(st));
-          tma_load_3d(kdst + C::kKVBytes + a * 8192, &vmap, a * 64, t * kTile, bh, kv_full(st));
+          tma_load_3d(kdst + a * 8192, &kmap, a * 64, ky, kz, kv_full(st));
+          tma_load_3d(kdst + C::kKVBytes + a * 8192, &vmap, a * 64, vy, vz, kv_full(st));
         }
         issued = i + 1;
       }
@@ -287,6 +298,22 @@ __global__ void __launch_bounds__(kThreads, P2Cfg<D, kF16>::kCtasPerSm)
       auto issue_s = [&](int i) -> bool {
         const int st = i % C::NS;
         if (!mbar_wait(kv_full(st), (i / C::NS) & 1, &abort_flag, p.err)) return false;
+        uint32_t gm_unused;
+        if (s.pages && (s.Nkv % kTile) != 0 && tile_of(i, gm_unused) == T - 1) {
+          // paged pool: the keys past Nkv in a sequence's last page hold whatever the
+          // pool holds there (possibly NaN or Inf).  Masked scores and a zero P do not
+          // keep those out of an MMA, so the rows are zeroed here, before any MMA
+          // reads this stage: K always, V when it comes from the pool too.
+          const int nk = s.Nkv - (T - 1) * kTile, rows = kTile - nk;
+          uint8_t* kst = smem + C::kStageOff + st * 2 * C::kKVBytes;
+          for (int part = 0; part < (kF16 ? 1 : 2); ++part)
+            for (int x = 0; x < rows * C::kAtoms * 8; ++x) {
+              const int rest = x >> 3, rr = nk + rest % rows, atom = rest / rows;
+              *reinterpret_cast<uint4*>(kst + part * C::kKVBytes + atom * 8192 + rr * 128 + (x & 7) * 16) =
+                  make_uint4(0u, 0u, 0u, 0u);
+            }
+          fence_proxy_async_smem();
+        }
         if (i >= 2 && !mbar_wait(s_free(i & 1), ((i >> 1) - 1) & 1, &abort_flag, p.err)) return false;
         tc_fence_after();
         const uint32_t kaddr = sbase + C::kStageOff + st * 2 * C::kKVBytes;
@@ -521,7 +548,8 @@ __global__ void __launch_bounds__(kThreads, P2Cfg<D, kF16>::kCtasPerSm)
   }
 }
 
-bool make_kv_map(CUtensorMap* map, const void* base, const Shape& s, CUtensorMapDataType dtype) {
+// paged: the pool [num_pages][Hkv][64][d] as (channel, key in page, page * Hkv + h)
+bool make_kv_map(CUtensorMap* map, const void* base, const Shape& s, CUtensorMapDataType dtype, bool paged) {
   using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                 const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                 CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
@@ -534,8 +562,10 @@ bool make_kv_map(CUtensorMap* map, const void* base, const Shape& s, CUtensorMap
       return false;
     encode = reinterpret_cast<EncodeFn>(fn);
   }
-  const cuuint64_t dims[3] = {(cuuint64_t)s.d, (cuuint64_t)s.Nkv, (cuuint64_t)s.BH()};
-  const cuuint64_t strides[2] = {(cuuint64_t)s.d * 2, (cuuint64_t)s.Nkv * s.d * 2};
+  const cuuint64_t rows = paged ? (cuuint64_t)kTile : (cuuint64_t)s.Nkv;
+  const cuuint64_t planes = paged ? (cuuint64_t)s.num_pages * s.Hkv : (cuuint64_t)s.BH();
+  const cuuint64_t dims[3] = {(cuuint64_t)s.d, rows, planes};
+  const cuuint64_t strides[2] = {(cuuint64_t)s.d * 2, rows * s.d * 2};
   const cuuint32_t box[3] = {64, 64, 1};
   const cuuint32_t estr[3] = {1, 1, 1};
   return encode(map, dtype, 3, const_cast<void*>(base), dims, strides, box, estr,
@@ -587,9 +617,9 @@ cudaError_t launch_pass2(const Shape& s, const void* q, const void* k, const voi
   // with the FP16 copy of V (APA mode) P goes to the tensor cores as one FP16 term
   const bool f16 = ws && ws->v16;
   CUtensorMap km, vm;
-  if (!make_kv_map(&km, k, s, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) ||
+  if (!make_kv_map(&km, k, s, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, s.pages != nullptr) ||
       !make_kv_map(&vm, f16 ? (const void*)ws->v16 : v, s,
-                   f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16))
+                   f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, s.pages && !f16))
     return cudaErrorInvalidValue;
   P2Params prm{};
   prm.s = s;

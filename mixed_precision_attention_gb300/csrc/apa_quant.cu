@@ -109,7 +109,7 @@ __global__ void __launch_bounds__(kThreads) stats_kernel(Shape s, const uint16_t
   if (do_kv && (int)blockIdx.x < n_kv_blocks) {
     const int bh = blockIdx.x / T, t = blockIdx.x % T;
     const int j0 = t * kTile, nk = min(kTile, s.Nkv - j0);
-    const size_t base = ((size_t)bh * s.Nkv + j0) * d;
+    const size_t base = kv_tile_offset(s, bh, t, err);
     uint16_t* ks = reinterpret_cast<uint16_t*>(smem);
     uint16_t* vs = ks + kTile * d;
     if (!load_kv_tile(ks, vs, k + base, v + base, nk, d, &bar, err)) return;
@@ -271,7 +271,7 @@ __global__ void __launch_bounds__(kThreads) quant_kernel(Shape s, const uint16_t
     uint16_t* vs = ks + kTile * d;
     uint8_t* img = reinterpret_cast<uint8_t*>(vs + kTile * d);  // the blob, assembled here
     float* mus = reinterpret_cast<float*>(img + blob_bytes(d));
-    const size_t base = ((size_t)bh * s.Nkv + j0) * d;
+    const size_t base = kv_tile_offset(s, bh, t, err);
     // keys past Nkv quantize as zero V; the image starts zeroed (padding included)
     for (int i = threadIdx.x; i < (kTile - nk) * d / 8; i += blockDim.x)
       reinterpret_cast<uint4*>(vs + nk * d)[i] = make_uint4(0u, 0u, 0u, 0u);

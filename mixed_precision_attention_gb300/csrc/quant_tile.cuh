@@ -261,7 +261,7 @@ __device__ __noinline__ bool quant_role(const Shape& s, const uint16_t* __restri
     int bh;
     const int t = tile_of(tk, &bh);
     const int nk = min(kTile, s.Nkv - t * kTile);
-    const size_t base = ((size_t)bh * s.Nkv + (size_t)t * kTile) * d;
+    const size_t base = kv_tile_offset(s, bh, t, err);
     const uint32_t bytes = (uint32_t)nk * d * 2, bar = bar0 + 8u * buf;
     const uint32_t dst = smem_u32(smem + 2 * kvb * buf);
     fence_proxy_async_smem();  // the group's earlier accesses of this buffer come first

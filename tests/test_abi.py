@@ -116,3 +116,15 @@ def test_noalloc_quantizer_rejects_oversized_problems(lib):
     assert _lib.status_string(-9) != "unknown status"
     assert lib.apa_quantize_noalloc_scratch_bytes(1, 24, 8, 122880, 128) <= 16 * 2 ** 20
     assert lib.apa_quantize_noalloc(*OK_PTR, 1, 2, 1, 128, 512, 64, None, z, z, z, z, z, None) == -1
+
+
+def test_paged_argument_errors(lib):
+    # rejected on the host before anything is enqueued
+    z = P(0x70000)
+    # a null block table
+    assert lib.apa_attention_paged(*OK_PTR, 10, None, 8, 1, 2, 1, 128, 512, 64, 1, 0.005, z, None, None, None) == -1
+    # max_pages below ceil(Nkv / 64), and an empty pool
+    assert lib.apa_attention_paged(*OK_PTR, 10, z, 7, 1, 2, 1, 128, 512, 64, 1, 0.005, z, None, None, None) == -2
+    assert lib.apa_attention_paged(*OK_PTR, 0, z, 8, 1, 2, 1, 128, 512, 64, 1, 0.005, z, None, None, None) == -2
+    # the usual shape checks still apply
+    assert lib.apa_attention_paged(*OK_PTR, 10, z, 8, 1, 3, 2, 128, 512, 64, 1, 0.005, z, None, None, None) == -2
