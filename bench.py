@@ -167,6 +167,33 @@ def dist_setup():
         int(os.environ.get("LOCAL_RANK", "0"))
 
 
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world, device):
+    """The largest x over all ranks (every rank gets it); x itself on one rank."""
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def rank_layer_seed(w: synth.Workload, rank: int) -> int:
+    """Each rank runs its own layer (weak scaling): the workload's seed plus the rank."""
+    return w.seed + rank
+
+
+def whole_job_tflops(world: int, flops_per_rank: float, ms_max: float) -> float:
+    """Throughput of the whole job: every rank's work over the slowest rank's time."""
+    return world * flops_per_rank / (ms_max * 1e-3) / 1e12
+
+
 def cpu_sample(w: synth.Workload, q, k, v, heads=(0,), groups_per_head=16, seed=0):
     """The oracle's APA emulation on a bounded sample: `groups_per_head` 16-row
     groups spread over the rows of each listed KV head.  Returns (seconds, flops
@@ -242,21 +269,10 @@ def run_gpu(args):
     lib = _lib.load()
 
     w = synth.WORKLOADS[WORKLOAD]
-    q, k, v = synth.generate(w, seed=w.seed + rank)  # each rank: its own layer
+    q, k, v = synth.generate(w, seed=rank_layer_seed(w, rank))  # each rank: its own layer
     tq, tk, tv = (synth.to_torch_bf16(a, dev) for a in (q, k, v))
     B, Hq, Hkv, Nq, Nkv, d = w.B, w.Hq, w.Hkv, w.Nq, w.Nkv, w.d
     workspace = torch.empty(apa.workspace_bytes(B, Hq, Hkv, Nq, Nkv, d, w.eps), dtype=torch.uint8, device=dev)
-
-    def barrier():
-        if world > 1:
-            torch.distributed.barrier()
-
-    def max_over_ranks(x):
-        if world == 1:
-            return x
-        t = torch.tensor([x], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        return float(t.item())
 
     # one untimed call with the hot mask: the algorithmic work of this layer
     _, _, mask = apa.attention(tq, tk, tv, causal=w.causal, eps=w.eps, return_hot_mask=True, workspace=workspace)
@@ -270,7 +286,7 @@ def run_gpu(args):
             apa.attention(tq, tk, tv, causal=w.causal, eps=eps, workspace=ws_tensor, q_residual=q_residual,
                           lse_scales=lse_scales, value_weighted=value_weighted)
         torch.cuda.synchronize(dev)
-        barrier()
+        barrier(world)
         torch.cuda.synchronize(dev)
         clk = None
         if sample_clocks:
@@ -286,7 +302,7 @@ def run_gpu(args):
                           lse_scales=lse_scales, value_weighted=value_weighted)
         e1.record(stream)
         torch.cuda.synchronize(dev)
-        barrier()
+        barrier(world)
         torch.cuda.synchronize(dev)
         ms3 = (ctypes.c_float * 3)()
         calls = ctypes.c_int()
@@ -297,8 +313,8 @@ def run_gpu(args):
         return e0.elapsed_time(e1) / steps, [x / max(1, calls.value) for x in ms3], clocks
 
     ms, stages, clocks = timed(w.eps, args.steps, args.warmup, workspace, sample_clocks=True)
-    ms = max_over_ranks(ms)
-    value = world * flops_exact / (ms * 1e-3) / 1e12
+    ms = max_over_ranks(ms, world, dev)
+    value = whole_job_tflops(world, flops_exact, ms)
 
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
@@ -335,20 +351,20 @@ def run_gpu(args):
     if not args.skip_extras:
         # the same library at eps = 0: every visible tile exact in BF16 (no workspace needed)
         ms0, _, _ = timed(0.0, max(3, args.steps // 4), 3, None)
-        ms0 = max_over_ranks(ms0)
-        line["eps0_all_bf16"] = {"ms_per_step": ms0, "tflops": world * flops_exact / (ms0 * 1e-3) / 1e12,
+        ms0 = max_over_ranks(ms0, world, dev)
+        line["eps0_all_bf16"] = {"ms_per_step": ms0, "tflops": whole_job_tflops(world, flops_exact, ms0),
                                  "speedup_of_apa": ms0 / ms}
         # the accuracy option: Q as two FP4 terms in pass 1 (one block per pass-1 CTA)
         ws_q2 = torch.empty(apa.workspace_bytes(B, Hq, Hkv, Nq, Nkv, d, w.eps, q_residual=True),
                             dtype=torch.uint8, device=dev)
         msq2, stq2, _ = timed(w.eps, max(3, args.steps // 4), 3, ws_q2, q_residual=True)
         del ws_q2
-        msq2 = max_over_ranks(msq2)
-        line["q_residual"] = {"ms_per_step": msq2, "tflops": world * flops_exact / (msq2 * 1e-3) / 1e12,
+        msq2 = max_over_ranks(msq2, world, dev)
+        line["q_residual"] = {"ms_per_step": msq2, "tflops": whole_job_tflops(world, flops_exact, msq2),
                               "cost_vs_apa": msq2 / ms - 1.0, "stages_ms": stq2}
         # the other accuracy option: least-squared-error block scales (quantizer only)
         mslse, stlse, _ = timed(w.eps, max(3, args.steps // 4), 3, workspace, lse_scales=True)
-        mslse = max_over_ranks(mslse)
+        mslse = max_over_ranks(mslse, world, dev)
         line["lse_scales"] = {"ms_per_step": mslse, "cost_vs_apa": mslse / ms - 1.0, "stages_ms": stlse}
         # the hot test weighted by value norm: its own hot set, so its own pass-2 work
         ws_vw = torch.empty(apa.workspace_bytes(B, Hq, Hkv, Nq, Nkv, d, w.eps, value_weighted=True),
@@ -357,7 +373,7 @@ def run_gpu(args):
                                   value_weighted=True)
         msvw, stvw, _ = timed(w.eps, max(3, args.steps // 4), 3, ws_vw, value_weighted=True)
         del ws_vw
-        msvw = max_over_ranks(msvw)
+        msvw = max_over_ranks(msvw, world, dev)
         line["value_weighted"] = {"ms_per_step": msvw, "cost_vs_apa": msvw / ms - 1.0, "stages_ms": stvw,
                                   "hot_pair_frac": algorithmic(w, mvw.cpu().numpy())["hot_pair_frac"]}
         # end to end through the host-buffer entry point: H2D of q, k, v from pinned
@@ -365,12 +381,12 @@ def run_gpu(args):
         hq, hk, hv = (synth.to_torch_bf16(a).pin_memory() for a in (q, k, v))
         hout, hlse, _ = apa.attention_host(hq, hk, hv, causal=w.causal, eps=w.eps)  # pinned outputs, reused
         n_e2e = max(3, min(args.steps, 10))
-        barrier()
+        barrier(world)
         t0 = time.perf_counter()
         for _ in range(n_e2e):
             apa.attention_host(hq, hk, hv, causal=w.causal, eps=w.eps, out=hout, lse=hlse)
-        e2e_ms = max_over_ranks((time.perf_counter() - t0) * 1e3 / n_e2e)
-        line["e2e"] = {"value": world * flops_exact / (e2e_ms * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": e2e_ms,
+        e2e_ms = max_over_ranks((time.perf_counter() - t0) * 1e3 / n_e2e, world, dev)
+        line["e2e"] = {"value": whole_job_tflops(world, flops_exact, e2e_ms), "unit": UNIT, "ms_per_step": e2e_ms,
                        "h2d_bytes_per_step": q.nbytes + k.nbytes + v.nbytes,
                        "d2h_bytes_per_step": B * Hq * Nq * d * 4 + B * Hq * Nq * 4}
         if rank == 0 and world == 1:
