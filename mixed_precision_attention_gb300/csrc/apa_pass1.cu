@@ -37,6 +37,13 @@
 // At d <= 128 a CTA holds 256 TMEM columns and ~55 KB of shared memory, so two
 // CTAs share an SM.  (Two threads per row, swapping group maxima, was measured
 // slower: the per-warp waits and exchanges outweighed the halved encode.)
+//
+// K/V quantization inside the launch ("What else is in the box": the next
+// segment is quantized inside the launch).  When the pass-1 CTAs leave at least
+// 8 SMs free, either kernel below is launched cooperatively with one CTA on
+// every SM; the CTAs past the pass-1 ones run the K/V quantizer (quant_role in
+// quant_tile.cuh), which publishes a flag per tile in pass 1's visiting order,
+// and the producer waits (bounded) for a tile's flag before loading its blob.
 #include <cstdlib>
 #include <cstring>
 

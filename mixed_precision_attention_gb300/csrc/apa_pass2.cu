@@ -23,9 +23,15 @@
 // A tcgen05.mma takes tens of cycles to issue, and one tile needs d/16 of them
 // for S and 4 (or 8) for PV: issued by one thread, they set the tile period.
 // The running max moves lazily (only when a score exceeds it by more than 8 in
-// log2 units), so O in TMEM is rarely rescaled.  P goes to the tensor cores as
-// two BF16 terms, P = P_hi + P_lo (P_lo the BF16 rounding of the residual), so
-// the PV product and the row sum carry ~16 mantissa bits of P instead of 8.
+// log2 units), so O in TMEM is rarely rescaled.  In APA mode P goes to the tensor
+// cores as one FP16 term against the quantizer's FP16 copy of V (V divided by a
+// power of two per head); in the all-exact mode (eps = 0: no quantizer, no FP16
+// copy) as two BF16 terms, P = P_hi + P_lo (P_lo the BF16 rounding of the
+// residual), against V itself, so the PV product and the row sum carry ~16
+// mantissa bits of P instead of 8.
+// K, and V in the all-exact mode, may come from a paged pool through a block
+// table: the tensor maps then span the pool, and the rows past Nkv of the last
+// page are zeroed in shared memory before any MMA reads them.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
