@@ -322,3 +322,54 @@ def test_subnormal_block_scales_reach_the_tensor_cores():
     for r in range(10):
         assert abs(np.linalg.norm(got[r]) - np.linalg.norm(ref[r])) <= 0.05 * np.linalg.norm(ref[r])
     assert abs(got[10, 5] - ref[10, 5]) <= 0.05 and ref[10, 5] < 2.0
+
+
+EDGE = {
+    "one_query_one_key": dict(B=1, Hq=1, Hkv=1, Nq=1, Nkv=1, d=64, n_outliers=0),
+    "one_query_ragged": dict(B=1, Hq=2, Hkv=1, Nq=1, Nkv=130, d=128, n_outliers=1),
+    "no_gqa": dict(B=2, Hq=4, Hkv=4, Nq=70, Nkv=300, d=64, n_outliers=2),
+    "gqa32": dict(B=1, Hq=32, Hkv=1, Nq=20, Nkv=900, d=128, n_outliers=2),
+}
+
+
+@pytest.mark.parametrize("name", list(EDGE))
+@pytest.mark.parametrize("eps", [0.0, 0.005, float("inf")])
+@pytest.mark.parametrize("causal", [True, False])
+def test_edge_shapes(name, eps, causal):
+    """Degenerate and extreme shapes: one query and one key, one query over a ragged
+    three-tile context, one query head per KV head, 32 query heads on one KV head."""
+    w = synth.small(causal=causal, sink_gain=4.0, **EDGE[name])
+    q, k, v = synth.generate(w)
+    out, lse, mask = _gpu.run_apa(q, k, v, causal=causal, eps=eps)
+    if eps == 0:
+        ex, ex_lse = oracle.exact(q, k, v, causal=causal)
+        assert np.abs(out - ex).max() <= 4e-3 and np.abs(lse - ex_lse).max() <= 1e-3
+        return
+    ref = oracle.apa(q, k, v, causal=causal, eps=eps)
+    assert np.abs(out - ref["out"]).max() <= 1e-2
+    assert np.abs(lse - ref["lse"]).max() <= 1e-2
+    if np.isinf(eps):
+        assert not mask.any()
+
+
+@pytest.mark.parametrize("name", ["gqa3_ragged", "batch_ragged_d128"])
+def test_all_options_together(name):
+    """Q as two FP4 terms, least-squared-error scales and the value-weighted test
+    in one call, against the oracle's emulation with the same three choices."""
+    import mixed_precision_attention_gb300 as apa
+    w, (q, k, v) = _inputs(name)
+    quant = oracle.QUANT_ALL | oracle.QUANT_Q2 | oracle.QUANT_LSE | oracle.QUANT_VWEIGHT
+    ref = oracle.apa(q, k, v, eps=0.005, quant=quant)
+    tq, tk, tv = (_gpu.to_dev(a) for a in (q, k, v))
+    o, l, m = apa.attention(tq, tk, tv, causal=True, eps=0.005, return_hot_mask=True, q_residual=True,
+                            lse_scales=True, value_weighted=True)
+    apa.check_error()
+    out, lse = o.cpu().numpy().astype(np.float64), l.cpu().numpy().astype(np.float64)
+    assert np.abs(out - ref["out"]).max() <= 1e-2
+    assert _gpu.cosine(out, ref["out"]) >= 0.9999
+    assert np.abs(lse - ref["lse"]).max() <= 1e-2
+    T = (w.Nkv + 63) // 64
+    g_hot, o_hot = _gpu.hot_bits(m.cpu().numpy().view(np.uint32), T), _gpu.hot_bits(ref["hot_mask"], T)
+    ng = oracle.n_groups(w.Hq, w.Hkv, w.Nq)
+    vis = np.broadcast_to(_gpu.group_visible(w.Hq, w.Hkv, w.Nq, w.Nkv, True, ng, T), g_hot.shape)
+    assert (g_hot == o_hot)[vis].mean() >= 0.999
