@@ -32,6 +32,7 @@
 // K, and V in the all-exact mode, may come from a paged pool through a block
 // table: the tensor maps then span the pool, and the rows past Nkv of the last
 // page are zeroed in shared memory before any MMA reads them.
+#include <cstring>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -554,6 +555,408 @@ __global__ void __launch_bounds__(kThreads, P2Cfg<D, kF16>::kCtasPerSm)
   }
 }
 
+// Barrier over the two softmax warp groups (named barrier 1, 256 threads), also
+// returning whether v held in all of them.
+__device__ __forceinline__ bool dual_sync_and(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n.reg .pred p, q;\n"
+      "setp.ne.u32 p, %1, 0;\n"
+      "bar.red.and.pred q, 1, 256, p;\n"
+      "selp.u32 %0, 1, 0, q;\n}"
+      : "=r"(r)
+      : "r"((uint32_t)v)
+      : "memory");
+  return r != 0;
+}
+
+// ----------------------------------------------------------------------------
+// Pass 2 in APA mode (FP16 P.V, d <= 128) with two softmax warp groups on one
+// 128-row block: group u takes the hot-list entries i with i % 2 == u, with its
+// own online softmax (m, l) and its own O accumulator in TMEM, so the two
+// groups' per-tile latencies overlap.  At the end the pass-1 state and the two
+// groups' states are merged, always in that order.  TMEM: two O accumulators and
+// a double-buffered S per group (512 columns).
+#ifndef APA_P2D_STAGES
+#define APA_P2D_STAGES 5  // K/V stages of the two-group pass 2
+#endif
+#ifndef APA_P2D_PBUFS
+#define APA_P2D_PBUFS 1  // P buffers per group of the two-group pass 2
+#endif
+template <int D>
+struct P2DualCfg {
+  static constexpr int NS = APA_P2D_STAGES;  // K/V stages
+  static constexpr int NP = APA_P2D_PBUFS;   // P buffers per group
+  static constexpr int kAtoms = D / 64;
+  static constexpr int kQBytes = 128 * D * 2;
+  static constexpr int kKVBytes = 64 * D * 2;
+  static constexpr int kPBytes = 128 * 64 * 2;
+  static constexpr int kQOff = 0;
+  static constexpr int kStageOff = kQBytes;
+  static constexpr int kPOff = kStageOff + NS * 2 * kKVBytes;  // [2][NP] P
+  static constexpr int kMlOff = kPOff + 2 * NP * kPBytes;      // group 1's (m, l) per row for the merge
+  static constexpr int kNumBars = 2 * NS + 16 + 2;
+  static constexpr int kBarOff = kMlOff + 128 * 8;
+  static constexpr int kSmem = kBarOff + kNumBars * 8 + 16 + 1024;
+  static_assert(kSmem <= 232448, "shared memory");
+  static_assert(NP <= 2, "pv_done slots");
+  static constexpr uint32_t kTmemCols = 512;
+  static constexpr uint32_t kSBase = 2 * D;  // S(u, b) at kSBase + 128 u + 64 b; O(u) at D u
+  static constexpr int kThreads = 11 * 32;
+  static_assert(kSBase + 256 <= kTmemCols, "TMEM budget");
+};
+
+template <int D>
+__global__ void __launch_bounds__(P2DualCfg<D>::kThreads, 1)
+    pass2_dual_kernel(const P2Params p, const __grid_constant__ CUtensorMap kmap,
+                      const __grid_constant__ CUtensorMap vmap) {
+  using C = P2DualCfg<D>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
+  uint32_t& tmem_slot = *reinterpret_cast<uint32_t*>(smem + C::kBarOff + C::kNumBars * 8);
+  int& abort_flag = *reinterpret_cast<int*>(smem + C::kBarOff + C::kNumBars * 8 + 4);
+  float2* ml1 = reinterpret_cast<float2*>(smem + C::kMlOff);
+
+  const Shape& s = p.s;
+  const int nblk = s.nblk(), BH = s.BH(), G = s.G(), R = s.R(), T = s.T(), off = s.off();
+  int bh, blk;
+  if (p.order) {
+    const int item = (int)p.order[blockIdx.x];
+    bh = item / nblk;
+    blk = item % nblk;
+  } else {
+    bh = blockIdx.x % BH;
+    blk = nblk - 1 - (int)(blockIdx.x / BH);
+  }
+  const int b = bh / s.Hkv, h = bh % s.Hkv;
+  const int p0 = blk * kBlockRows;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int kProd = 8, kMmaS = 9, kMmaPV = 10;
+
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t bar0 = smem_u32(bars);
+  auto kv_full = [&](int st) { return bar0 + 8u * st; };
+  auto kv_empty = [&](int st) { return bar0 + 8u * (C::NS + st); };
+  auto s_full = [&](int u, int b2) { return bar0 + 8u * (2 * C::NS + 8 * u + b2); };
+  auto s_free = [&](int u, int b2) { return bar0 + 8u * (2 * C::NS + 8 * u + 2 + b2); };
+  auto p_full = [&](int u, int b2) { return bar0 + 8u * (2 * C::NS + 8 * u + 4 + b2); };
+  auto pv_done = [&](int u, int b2) { return bar0 + 8u * (2 * C::NS + 8 * u + 6 + b2); };
+  const uint32_t drain = bar0 + 8u * (2 * C::NS + 16), drain_pv = bar0 + 8u * (2 * C::NS + 17);
+  auto warp_wait = [&](uint32_t bar, uint32_t parity) -> bool {
+    if (__all_sync(0xffffffffu, mbar_test_wait(bar, parity))) return true;
+    const bool okl = mbar_wait(bar, parity, &abort_flag, p.err);
+    return __all_sync(0xffffffffu, okl);
+  };
+
+  const int n = (int)p.hot_count[(size_t)bh * nblk + blk];
+  const uint32_t* list = p.hot_list + ((size_t)bh * nblk + blk) * T;
+
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    for (int i = 0; i < C::kNumBars; ++i) {
+      uint32_t count = 1;
+      if (i >= C::NS && i < 2 * C::NS) count = 2;  // kv_empty: the S and the PV issuer
+      const int j = i - 2 * C::NS;
+      if (j >= 0 && j < 16 && (j & 7) >= 2 && (j & 7) < 6) count = 4;  // s_free, p_full: the group's four warps
+      mbar_init(bar0 + 8u * i, count);
+    }
+    fence_mbar_init();
+  }
+  if (warp == kMmaS) {
+    tmem_alloc(smem_u32(&tmem_slot), C::kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == kProd && lane == 0) {
+    prefetch_tmap(&kmap);
+    prefetch_tmap(&vmap);
+  }
+
+  // ---- softmax-thread setup: the Q row (group 0 stores it, 128-byte swizzle), q.mu (both groups)
+  const int u = warp >> 2, qw = warp & 3;  // softmax warps 0-7: group u, quarter qw
+  const int r = qw * 32 + lane;            // row within the block
+  const int P = p0 + r;
+  const bool row_valid = warp < 8 && P < R;
+  const int pos = row_valid ? P / G : 0;
+  const int hq = h * G + (row_valid ? P % G : 0);
+  float qmu = 0.f;
+  if (warp < 8) {
+    const uint4* src = reinterpret_cast<const uint4*>(p.q + (((size_t)b * s.Hq + hq) * s.Nq + pos) * D);
+    const float* mu = p.mu + (size_t)bh * D;
+#pragma unroll 4
+    for (int j = 0; j < D / 8; ++j) {
+      uint4 val = row_valid ? src[j] : make_uint4(0u, 0u, 0u, 0u);
+      const int atom = j >> 3, chunk = j & 7;
+      if (u == 0)
+        *reinterpret_cast<uint4*>(smem + C::kQOff + atom * 16384 + r * 128 + ((chunk ^ (r & 7)) << 4)) = val;
+      const uint32_t w[4] = {val.x, val.y, val.z, val.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        qmu = fmaf(__uint_as_float(w[e] << 16), mu[j * 8 + 2 * e], qmu);
+        qmu = fmaf(__uint_as_float(w[e] & 0xFFFF0000u), mu[j * 8 + 2 * e + 1], qmu);
+      }
+    }
+    fence_proxy_async_smem();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+
+  if (warp == kProd) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int issued = 0;
+      for (int i = 0; i < n; ++i) {
+        const int st = i % C::NS;
+        if (i >= C::NS && !mbar_wait(kv_empty(st), ((i / C::NS) - 1) & 1, &abort_flag, p.err)) break;
+        const int t = (int)(list[i] & 0xFFFFu);
+        int ky = t * kTile, kz = bh;
+        if (s.pages) {
+          ky = 0;
+          kz = kv_page(s, b, t, p.err) * s.Hkv + h;
+        }
+        mbar_arrive_expect_tx(kv_full(st), 2 * C::kKVBytes);
+        const uint32_t kdst = sbase + C::kStageOff + st * 2 * C::kKVBytes;
+#pragma unroll
+        for (int a = 0; a < C::kAtoms; ++a) {
+          tma_load_3d(kdst + a * 8192, &kmap, a * 64, ky, kz, kv_full(st));
+          tma_load_3d(kdst + C::kKVBytes + a * 8192, &vmap, a * 64, t * kTile, bh, kv_full(st));
+        }
+        issued = i + 1;
+      }
+      if (abort_flag) {  // let copies in flight land before the CTA exits
+        for (int i = max(0, issued - C::NS); i < issued; ++i) wait_bounded(kv_full(i % C::NS), (i / C::NS) & 1, p.err);
+      }
+    }
+  } else if (warp == kMmaS) {
+    // ------------------------------------------------------------ S issuer: tile i into group i % 2's S
+    if (lane == 0 && n > 0) {
+      const uint32_t idS = idesc_bf16(128, 64, 0);
+      bool ok = true;
+      for (int i = 0; ok && i < n; ++i) {
+        const int st = i % C::NS, v = i & 1, j = i >> 1, b2 = j & 1;
+        if (!(ok = mbar_wait(kv_full(st), (i / C::NS) & 1, &abort_flag, p.err))) break;
+        if (s.pages && (s.Nkv % kTile) != 0 && (int)(list[i] & 0xFFFFu) == T - 1) {
+          // paged pool: zero the K rows past Nkv of the last page before the MMA reads them
+          const int nk = s.Nkv - (T - 1) * kTile, rows = kTile - nk;
+          uint8_t* kst = smem + C::kStageOff + st * 2 * C::kKVBytes;
+          for (int x = 0; x < rows * C::kAtoms * 8; ++x) {
+            const int rest = x >> 3, rr = nk + rest % rows, atom = rest / rows;
+            *reinterpret_cast<uint4*>(kst + atom * 8192 + rr * 128 + (x & 7) * 16) = make_uint4(0u, 0u, 0u, 0u);
+          }
+          fence_proxy_async_smem();
+        }
+        if (j >= 2 && !(ok = mbar_wait(s_free(v, b2), ((j >> 1) - 1) & 1, &abort_flag, p.err))) break;
+        tc_fence_after();
+        const uint32_t kaddr = sbase + C::kStageOff + st * 2 * C::kKVBytes;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint64_t ad = smem_desc(sbase + C::kQOff + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024, kSwizzle128B);
+          const uint64_t bd = smem_desc(kaddr + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024, kSwizzle128B);
+          mma_bf16(tmem + C::kSBase + 128 * v + 64 * b2, ad, bd, idS, kk > 0);
+        }
+        mma_commit(s_full(v, b2));
+        mma_commit(kv_empty(st));  // this stage's K has been read
+      }
+      mma_commit(drain);
+      wait_bounded(drain, 0, p.err);
+    }
+  } else if (warp == kMmaPV) {
+    // ------------------------------------------------------------ PV issuer: tile i into group i % 2's O
+    if (lane == 0 && n > 0) {
+      const uint32_t idO = idesc_f16(128, D, 1);
+      bool ok = true;
+      for (int i = 0; ok && i < n; ++i) {
+        const int st = i % C::NS, v = i & 1, j = i >> 1, b2 = j & 1;
+        if (!(ok = mbar_wait(p_full(v, b2), (j >> 1) & 1, &abort_flag, p.err))) break;
+        if (!(ok = mbar_wait(kv_full(st), (i / C::NS) & 1, &abort_flag, p.err))) break;
+        tc_fence_after();
+        const uint32_t vaddr = sbase + C::kStageOff + st * 2 * C::kKVBytes + C::kKVBytes;
+        const uint32_t paddr = sbase + C::kPOff + (v * C::NP + j % C::NP) * C::kPBytes;
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          const uint64_t bd = smem_desc(vaddr + kk * 2048, 8192, 1024, kSwizzle128B);
+          mma_bf16(tmem + (uint32_t)(D * v), smem_desc(paddr + kk * 32, 16, 1024, kSwizzle128B), bd, idO,
+                   (j > 0 || kk > 0) ? 1u : 0u);
+        }
+        mma_commit(pv_done(v, b2));
+        mma_commit(kv_empty(st));  // this stage's V has been read
+      }
+      mma_commit(drain_pv);
+      wait_bounded(drain_pv, 0, p.err);
+    }
+  } else {
+    // ------------------------------------------------------------ softmax: group u, one thread per row
+    const int nu = (n - u + 1) / 2;  // this group's tiles: entries u, u+2, ...
+    const uint32_t tO = (uint32_t)(D * u), tS = C::kSBase + 128u * u;
+    const float c2 = kLog2e * rsqrtf((float)D);
+    const float shift = qmu * c2;
+    const int vis_last = s.causal ? pos + off : s.Nkv - 1;  // last visible key of this row
+    const uint32_t lane_base = (uint32_t)(qw * 32) << 16;
+    float m2 = -INFINITY, l2 = 0.f;
+    bool ok = true;
+    uint32_t e_next = nu > 0 ? list[u] : 0u;
+    for (int j = 0; j < nu; ++j) {
+      const uint32_t gm = e_next >> 16;
+      const int t = (int)(e_next & 0xFFFFu);
+      if (j + 1 < nu) e_next = list[2 * (j + 1) + u];
+      if (!(ok = warp_wait(s_full(u, j & 1), (j >> 1) & 1))) break;
+      const bool row_hot = row_valid && ((gm >> (r >> 4)) & 1u);
+      const int j0 = t * kTile;
+      const int nvis = row_hot ? min(kTile, vis_last + 1 - j0) : 0;  // keys j0 .. j0+nvis-1 visible
+      uint8_t* prow = smem + C::kPOff + (u * C::NP + j % C::NP) * C::kPBytes + r * 128;
+      if (!__any_sync(0xffffffffu, nvis > 0)) {
+        // neither of this warp's two groups of rows takes part in this tile: its P rows are zero
+        __syncwarp();
+        if (lane == 0) mbar_arrive(s_free(u, j & 1));
+        if (j >= C::NP && !(ok = warp_wait(pv_done(u, (j - C::NP) & 1), ((j - C::NP) >> 1) & 1))) break;
+#pragma unroll
+        for (int ch = 0; ch < 8; ++ch)
+          *reinterpret_cast<uint4*>(prow + ((ch ^ (r & 7)) << 4)) = make_uint4(0u, 0u, 0u, 0u);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(p_full(u, j & 1));
+        continue;
+      }
+      tc_fence_after();
+      uint32_t raw[64];
+      tmem_ld_x32(tmem + lane_base + tS + 64 * (j & 1), raw);
+      tmem_ld_x32(tmem + lane_base + tS + 64 * (j & 1) + 32, raw + 32);
+      tmem_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(s_free(u, j & 1));
+      float sv[64];
+#pragma unroll
+      for (int x = 0; x < 64; ++x) sv[x] = __uint_as_float(raw[x]);
+      if (__any_sync(0xffffffffu, nvis > 0 && nvis < 64)) {
+#pragma unroll
+        for (int x = 0; x < 64; ++x)
+          if (x >= nvis) sv[x] = -INFINITY;
+      }
+      float g8[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        g8[k] = max3(max3(sv[8 * k], sv[8 * k + 1], sv[8 * k + 2]), max3(sv[8 * k + 3], sv[8 * k + 4], sv[8 * k + 5]),
+                     fmaxf(sv[8 * k + 6], sv[8 * k + 7]));
+      const float rmax = max3(max3(g8[0], g8[1], g8[2]), max3(g8[3], g8[4], g8[5]), fmaxf(g8[6], g8[7]));
+      const float c = (nvis <= 0 || rmax == -INFINITY) ? -INFINITY : fmaf(rmax, c2, -shift);
+      float f = 1.f;
+      bool rescale = false;
+      if (c > m2 + kTau2 || (m2 == -INFINITY && c > -INFINITY)) {
+        if (l2 > 0.f) {
+          f = ex2_approx(m2 - c);
+          rescale = true;
+        }
+        m2 = c;
+      }
+      // this P buffer is free once PV(u, j - NP) has completed
+      if (j >= C::NP && !(ok = warp_wait(pv_done(u, (j - C::NP) & 1), ((j - C::NP) >> 1) & 1))) break;
+      const float nb = (nvis <= 0 || m2 == -INFINITY) ? -INFINITY : -shift - m2;
+      float ps[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int ch = 0; ch < 8; ++ch) {
+        uint32_t hi[4];
+        p8_f16(sv + 8 * ch, c2, nb, hi, ps[ch & 1], ps[2 + (ch & 1)]);
+        *reinterpret_cast<uint4*>(prow + ((ch ^ (r & 7)) << 4)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+      }
+      l2 = l2 * f + ((ps[0] + ps[1]) + (ps[2] + ps[3]));
+      if (__any_sync(0xffffffffu, rescale)) {
+        // O(u) must not be read before PV(u, j-1) has landed
+        if (!(ok = warp_wait(pv_done(u, (j - 1) & 1), ((j - 1) >> 1) & 1))) break;
+        tc_fence_after();
+#pragma unroll 1
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          uint32_t o[32];
+          tmem_ld_x32(tmem + lane_base + tO + c0, o);
+          tmem_wait_ld();
+#pragma unroll
+          for (int x = 0; x < 32; ++x) o[x] = __float_as_uint(__uint_as_float(o[x]) * f);
+          tmem_st_x16(tmem + lane_base + tO + c0, o);
+          tmem_st_x16(tmem + lane_base + tO + c0 + 16, o + 16);
+        }
+        tmem_wait_st();
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(p_full(u, j & 1));
+    }
+    // ---- epilogue: group 1 hands over (m, l); group 0 merges pass 1, group 0, group 1
+    if (ok && nu > 0) ok = warp_wait(pv_done(u, (nu - 1) & 1), ((nu - 1) >> 1) & 1);
+    tc_fence_after();
+    if (u == 1) ml1[r] = make_float2(m2, l2);
+    bool all_ok = dual_sync_and(ok);
+    const int n1 = n / 2;  // group 1's tiles
+    if (u == 0 && all_ok && n1 > 0)  // group 1's O is complete (waited here too, bounded)
+      all_ok = warp_wait(pv_done(1, (n1 - 1) & 1), ((n1 - 1) >> 1) & 1);
+    tc_fence_after();
+    if (u == 0 && all_ok) {
+      float m1 = -INFINITY, l1 = 0.f;
+      const float* st = p.state_o + ((size_t)bh * nblk * kBlockRows + P) * D;
+      if (row_valid) {
+        const float2 ml = p.state_ml[(size_t)bh * nblk * kBlockRows + P];
+        m1 = ml.x;
+        l1 = ml.y;
+      }
+      const float2 mlb = ml1[r];
+      const float mA = m2, lA = l2, mB = mlb.x, lB = mlb.y;
+      const float e1 = l1 > 0.f ? m1 : -INFINITY, eA = lA > 0.f ? mA : -INFINITY, eB = lB > 0.f ? mB : -INFINITY;
+      const float M = fmaxf(e1, fmaxf(eA, eB));
+      const float w1 = e1 == -INFINITY ? 0.f : exp2f(e1 - M), wA = eA == -INFINITY ? 0.f : exp2f(eA - M),
+                  wB = eB == -INFINITY ? 0.f : exp2f(eB - M);
+      const float L = (w1 * l1 + wA * lA) + wB * lB;
+      const float invL = 1.f / L;
+      const float vsc = v16_scale(__uint_as_float(p.vamax[bh]));  // O carries V / scale
+      const float wAo = wA * vsc, wBo = wB * vsc;
+      float* orow = p.out + (((size_t)b * s.Hq + hq) * s.Nq + pos) * D;
+#pragma unroll 1
+      for (int c0 = 0; c0 < D; c0 += 32) {
+        uint32_t oa[32], ob[32];
+        if (nu > 0) {
+          tmem_ld_x32(tmem + lane_base + 0 + c0, oa);
+        }
+        if (n1 > 0) {
+          tmem_ld_x32(tmem + lane_base + (uint32_t)D + c0, ob);
+        }
+        tmem_wait_ld();
+        if (nu == 0) {
+#pragma unroll
+          for (int x = 0; x < 32; ++x) oa[x] = 0u;
+        }
+        if (n1 == 0) {
+#pragma unroll
+          for (int x = 0; x < 32; ++x) ob[x] = 0u;
+        }
+        if (row_valid) {
+#pragma unroll
+          for (int x = 0; x < 32; x += 4) {
+            float4 res;
+            float* rr = &res.x;
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              rr[e] = ((w1 * st[c0 + x + e] + wAo * __uint_as_float(oa[x + e])) + wBo * __uint_as_float(ob[x + e])) *
+                      invL;
+            *reinterpret_cast<float4*>(orow + c0 + x) = res;
+          }
+        }
+      }
+      if (row_valid && p.lse) {
+        const float lg = M + log2f(L);
+        p.lse[((size_t)b * s.Hq + hq) * s.Nq + pos] = 0.6931471805599453f * lg + qmu * rsqrtf((float)D);
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaS) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
 // paged: the pool [num_pages][Hkv][64][d] as (channel, key in page, page * Hkv + h)
 bool make_kv_map(CUtensorMap* map, const void* base, const Shape& s, CUtensorMapDataType dtype, bool paged) {
   using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -588,8 +991,26 @@ cudaError_t launch_dv(const P2Params& prm, const CUtensorMap& km, const CUtensor
   pass2_kernel<D, kF16><<<grid, kThreads, smem, st>>>(prm, km, vm);
   return cudaGetLastError();
 }
+// APA_PASS2_DUAL=0 keeps one softmax warp group per block in APA mode (for comparison).
+bool dual_allowed() {
+  static const bool v = [] {
+    const char* e = getenv("APA_PASS2_DUAL");
+    return !(e && strcmp(e, "0") == 0);
+  }();
+  return v;
+}
+
 template <int D>
 cudaError_t launch_d(const P2Params& prm, const CUtensorMap& km, const CUtensorMap& vm, cudaStream_t st) {
+  if constexpr (D <= 128) {
+    if (prm.vamax && dual_allowed()) {
+      const int smem = P2DualCfg<D>::kSmem;
+      cudaError_t e = cudaFuncSetAttribute(pass2_dual_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+      if (e) return e;
+      pass2_dual_kernel<D><<<prm.s.BH() * prm.s.nblk(), P2DualCfg<D>::kThreads, smem, st>>>(prm, km, vm);
+      return cudaGetLastError();
+    }
+  }
   return prm.vamax ? launch_dv<D, true>(prm, km, vm, st) : launch_dv<D, false>(prm, km, vm, st);
 }
 
