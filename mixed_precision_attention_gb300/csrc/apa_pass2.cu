@@ -32,6 +32,15 @@
 // K, and V in the all-exact mode, may come from a paged pool through a block
 // table: the tensor maps then span the pool, and the rows past Nkv of the last
 // page are zeroed in shared memory before any MMA reads them.
+//
+// In APA mode at d <= 128 a second kernel (pass2_dual_kernel) runs instead: two
+// softmax warp groups per block take alternate entries of the hot list, each
+// with its own (m, l), its own O in TMEM and its own double-buffered S, so one
+// group's exp/convert/store of P overlaps the other's S and PV MMAs; 11 warps,
+// 5 K/V stages, one P buffer per group.  The block's final state is the merge of
+// the pass-1 state, group 0's and group 1's, in that order.  The per-row work is
+// the same as the one-group kernel's; only the tile-to-accumulator assignment
+// (and so the rounding order of the merge) differs.
 #include <cstring>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
