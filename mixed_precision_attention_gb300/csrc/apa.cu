@@ -8,6 +8,13 @@
 #include "../../include/apa.h"
 #include "apa_internal.h"
 
+#ifndef APA_HOST_LANE_PRIORITY
+#define APA_HOST_LANE_PRIORITY 1  // later compute lanes of apa_attention_host at higher stream priority
+#endif
+#ifndef APA_HOST_WIDE_EIGHTHS
+#define APA_HOST_WIDE_EIGHTHS 2  // eighths of the sub-problems of apa_attention_host run in the wide form
+#endif
+
 namespace apa {
 
 namespace {
@@ -90,10 +97,17 @@ bool HostStaging::streams_ready() {
       cudaEventCreateWithFlags(&fork, cudaEventDisableTiming) != cudaSuccess ||
       cudaEventCreateWithFlags(&arrived, cudaEventDisableTiming) != cudaSuccess)
     return false;
-  for (int i = 0; i < kHostLanes; ++i)
-    if (cudaStreamCreateWithFlags(&lane[i], cudaStreamNonBlocking) != cudaSuccess ||
+  // Later lanes take later sub-problems, which arrive last and so set the end of the
+  // call: their thread blocks go first whenever the GPU's SMs are all taken.
+  int least = 0, greatest = 0;
+  if (!APA_HOST_LANE_PRIORITY || cudaDeviceGetStreamPriorityRange(&least, &greatest) != cudaSuccess)
+    least = greatest = 0;
+  for (int i = 0; i < kHostLanes; ++i) {
+    const int prio = least + (greatest - least) * i / (kHostLanes - 1);
+    if (cudaStreamCreateWithPriority(&lane[i], cudaStreamNonBlocking, prio) != cudaSuccess ||
         cudaEventCreateWithFlags(&join[i], cudaEventDisableTiming) != cudaSuccess)
       return false;
+  }
   ready = true;
   return true;
 }
@@ -327,9 +341,10 @@ int apa_attention_host(const void* q, const void* k, const void* v, int B, int H
   const size_t need = apa::workspace_layout(sub, eps != 0.f, nullptr, nullptr);
   const int L = BH < apa::kHostLanes ? BH : apa::kHostLanes;
   // The last sub-problems to arrive finish sooner with one block per pass-1 CTA,
-  // spread over the SMs the earlier ones leave free (the last 3/8: the best of
-  // the splits measured on the 8-head 2048 x 122880 layer, 4.9 against 5.1 ms).
-  const int wide_from = BH - (3 * BH) / 8;
+  // spread over the SMs the earlier ones leave free; with the lanes' stream
+  // priorities the last 2/8 was the best split measured on the 8-head
+  // 2048 x 122880 layer (4.73 ms, against 5.0 for 3/8 and 5.15 for none).
+  const int wide_from = BH - (APA_HOST_WIDE_EIGHTHS * BH) / 8;
   size_t off = 0;
   auto slot = [&](size_t bytes) {
     const size_t o = off;

@@ -22,6 +22,9 @@ SHAPES = {
     "tiny": dict(B=1, Hq=2, Hkv=1, Nq=128, Nkv=512, d=64, n_outliers=0),
     "gqa3_ragged": dict(B=1, Hq=3, Hkv=1, Nq=45, Nkv=1000, d=64, n_outliers=2),
     "batch_ragged_d128": dict(B=2, Hq=8, Hkv=2, Nq=100, Nkv=1100, d=128, n_outliers=4),
+    # four sub-problems on the host path, the last in the wide form (one block per
+    # pass-1 CTA), with an odd number (3) of 128-row blocks
+    "host_wide_odd": dict(B=1, Hq=12, Hkv=4, Nq=120, Nkv=900, d=128, n_outliers=2),
     "d256": dict(B=1, Hq=4, Hkv=2, Nq=64, Nkv=700, d=256, n_outliers=4),
     "long_tail": dict(B=1, Hq=4, Hkv=1, Nq=64, Nkv=16384, d=128, n_outliers=4),
     "single_tile": dict(B=1, Hq=2, Hkv=1, Nq=40, Nkv=64, d=64, n_outliers=0),
@@ -115,11 +118,12 @@ def test_deterministic_reruns():
         assert np.array_equal(x, y)
 
 
-@pytest.mark.parametrize("name", ["batch_ragged_d128", "d256", "gqa3_ragged"])
+@pytest.mark.parametrize("name", ["batch_ragged_d128", "d256", "gqa3_ragged", "host_wide_odd"])
 def test_host_entry_point_matches_device(name):
     # the device call quantizes K/V inside the pass-1 launch (three-block kernel at
     # d <= 128, one-block kernel at d = 256); the host call's sub-problems use the
-    # separate quantizer kernel: the results agree bit for bit
+    # separate quantizer kernel, and its last ones one block per pass-1 CTA: the
+    # results agree bit for bit
     import torch
 
     import mixed_precision_attention_gb300 as apa
