@@ -151,8 +151,9 @@ int apa_attention_paged(const void* q, const void* k_pages, const void* v_pages,
  * and synchronizes `stream` before returning.  The results equal those of
  * apa_attention().  Each (b, KV head) is an independent problem of the method,
  * so the call pipelines them: one's inputs are copied (on a library-owned copy
- * stream) while earlier ones compute (on up to 8 library-owned streams) and
- * their results are copied back.  All of it is ordered after the work already
+ * stream) while earlier ones compute (on up to 8 library-owned streams, created
+ * at rising priority so that the sub-problems that arrive last are dispatched
+ * first) and their results are copied back.  All of it is ordered after the work already
  * on `stream`.  The device memory is one library-owned buffer per device, grown
  * on demand and kept until the process exits; calls on the same device are
  * serialized by a lock. */
