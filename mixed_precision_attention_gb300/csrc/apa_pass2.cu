@@ -592,6 +592,9 @@ __device__ __forceinline__ bool dual_sync_and(bool v) {
 #ifndef APA_P2D_PBUFS
 #define APA_P2D_PBUFS 1  // P buffers per group of the two-group pass 2
 #endif
+#ifndef APA_P2D_SISSUERS
+#define APA_P2D_SISSUERS 2  // S-issuing warps of the two-group pass 2: one per group, or one for both
+#endif
 template <int D>
 struct P2DualCfg {
   static constexpr int NS = APA_P2D_STAGES;  // K/V stages
@@ -604,14 +607,16 @@ struct P2DualCfg {
   static constexpr int kStageOff = kQBytes;
   static constexpr int kPOff = kStageOff + NS * 2 * kKVBytes;  // [2][NP] P
   static constexpr int kMlOff = kPOff + 2 * NP * kPBytes;      // group 1's (m, l) per row for the merge
-  static constexpr int kNumBars = 2 * NS + 16 + 2;
+  static constexpr int kSIssuers = APA_P2D_SISSUERS;
+  static_assert(kSIssuers == 1 || kSIssuers == 2, "S issuers");
+  static constexpr int kNumBars = 2 * NS + 16 + 1 + kSIssuers;
   static constexpr int kBarOff = kMlOff + 128 * 8;
   static constexpr int kSmem = kBarOff + kNumBars * 8 + 16 + 1024;
   static_assert(kSmem <= 232448, "shared memory");
   static_assert(NP <= 2, "pv_done slots");
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kSBase = 2 * D;  // S(u, b) at kSBase + 128 u + 64 b; O(u) at D u
-  static constexpr int kThreads = 11 * 32;
+  static constexpr int kThreads = (10 + kSIssuers) * 32;
   static_assert(kSBase + 256 <= kTmemCols, "TMEM budget");
 };
 
@@ -641,7 +646,9 @@ __global__ void __launch_bounds__(P2DualCfg<D>::kThreads, 1)
   const int b = bh / s.Hkv, h = bh % s.Hkv;
   const int p0 = blk * kBlockRows;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int kProd = 8, kMmaS = 9, kMmaPV = 10;
+  // warps 0-7 softmax, 8 TMA producer, 9 S issuer (group 0's tiles, or all of them
+  // with one S issuer), 10 PV issuer, 11 S issuer of group 1's tiles
+  const int kProd = 8, kMmaS = 9, kMmaPV = 10, kMmaS1 = 11;
 
   const uint32_t sbase = smem_u32(smem);
   const uint32_t bar0 = smem_u32(bars);
@@ -651,7 +658,8 @@ __global__ void __launch_bounds__(P2DualCfg<D>::kThreads, 1)
   auto s_free = [&](int u, int b2) { return bar0 + 8u * (2 * C::NS + 8 * u + 2 + b2); };
   auto p_full = [&](int u, int b2) { return bar0 + 8u * (2 * C::NS + 8 * u + 4 + b2); };
   auto pv_done = [&](int u, int b2) { return bar0 + 8u * (2 * C::NS + 8 * u + 6 + b2); };
-  const uint32_t drain = bar0 + 8u * (2 * C::NS + 16), drain_pv = bar0 + 8u * (2 * C::NS + 17);
+  const uint32_t drain_pv = bar0 + 8u * (2 * C::NS + 16);
+  auto drain_s = [&](int x) { return bar0 + 8u * (2 * C::NS + 17 + x); };  // per S issuer
   auto warp_wait = [&](uint32_t bar, uint32_t parity) -> bool {
     if (__all_sync(0xffffffffu, mbar_test_wait(bar, parity))) return true;
     const bool okl = mbar_wait(bar, parity, &abort_flag, p.err);
@@ -738,12 +746,13 @@ __global__ void __launch_bounds__(P2DualCfg<D>::kThreads, 1)
         for (int i = max(0, issued - C::NS); i < issued; ++i) wait_bounded(kv_full(i % C::NS), (i / C::NS) & 1, p.err);
       }
     }
-  } else if (warp == kMmaS) {
-    // ------------------------------------------------------------ S issuer: tile i into group i % 2's S
-    if (lane == 0 && n > 0) {
+  } else if (warp == kMmaS || (C::kSIssuers == 2 && warp == kMmaS1)) {
+    // ------------------------------------------------------------ S issuer(s): tile i into group i % 2's S
+    const int sx = warp == kMmaS ? 0 : 1;  // with two S issuers, issuer x takes the entries i % 2 == x
+    if (lane == 0 && n > sx) {
       const uint32_t idS = idesc_bf16(128, 64, 0);
       bool ok = true;
-      for (int i = 0; ok && i < n; ++i) {
+      for (int i = sx; ok && i < n; i += C::kSIssuers) {
         const int st = i % C::NS, v = i & 1, j = i >> 1, b2 = j & 1;
         if (!(ok = mbar_wait(kv_full(st), (i / C::NS) & 1, &abort_flag, p.err))) break;
         if (s.pages && (s.Nkv % kTile) != 0 && (int)(list[i] & 0xFFFFu) == T - 1) {
@@ -768,8 +777,8 @@ __global__ void __launch_bounds__(P2DualCfg<D>::kThreads, 1)
         mma_commit(s_full(v, b2));
         mma_commit(kv_empty(st));  // this stage's K has been read
       }
-      mma_commit(drain);
-      wait_bounded(drain, 0, p.err);
+      mma_commit(drain_s(sx));
+      wait_bounded(drain_s(sx), 0, p.err);
     }
   } else if (warp == kMmaPV) {
     // ------------------------------------------------------------ PV issuer: tile i into group i % 2's O
