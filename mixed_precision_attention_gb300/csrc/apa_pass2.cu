@@ -587,13 +587,13 @@ __device__ __forceinline__ bool dual_sync_and(bool v) {
 // groups' states are merged, always in that order.  TMEM: two O accumulators and
 // a double-buffered S per group (512 columns).
 #ifndef APA_P2D_STAGES
-#define APA_P2D_STAGES 5  // K/V stages of the two-group pass 2
+#define APA_P2D_STAGES 5  // K/V stages of the two-group pass 2 (even with two S issuers)
 #endif
 #ifndef APA_P2D_PBUFS
 #define APA_P2D_PBUFS 1  // P buffers per group of the two-group pass 2
 #endif
 #ifndef APA_P2D_SISSUERS
-#define APA_P2D_SISSUERS 2  // S-issuing warps of the two-group pass 2: one per group, or one for both
+#define APA_P2D_SISSUERS 1  // S-issuing warps of the two-group pass 2: one for both groups, or one per group
 #endif
 template <int D>
 struct P2DualCfg {
@@ -609,6 +609,13 @@ struct P2DualCfg {
   static constexpr int kMlOff = kPOff + 2 * NP * kPBytes;      // group 1's (m, l) per row for the merge
   static constexpr int kSIssuers = APA_P2D_SISSUERS;
   static_assert(kSIssuers == 1 || kSIssuers == 2, "S issuers");
+  // Two S issuers each wait on the K/V arrivals of their own entries (i % 2).  With
+  // NS even, entry i's stage i % NS is only ever used by entries of the same parity,
+  // so each issuer sees every phase of its stages in order.  With NS odd, a stage's
+  // previous use would be the other issuer's; a parity wait made one phase early (the
+  // previous load still landing, since loads can land out of order) would pass on the
+  // phase before it.
+  static_assert(kSIssuers == 1 || NS % 2 == 0, "two S issuers need an even stage count");
   static constexpr int kNumBars = 2 * NS + 16 + 1 + kSIssuers;
   static constexpr int kBarOff = kMlOff + 128 * 8;
   static constexpr int kSmem = kBarOff + kNumBars * 8 + 16 + 1024;
@@ -754,6 +761,8 @@ __global__ void __launch_bounds__(P2DualCfg<D>::kThreads, 1)
       bool ok = true;
       for (int i = sx; ok && i < n; i += C::kSIssuers) {
         const int st = i % C::NS, v = i & 1, j = i >> 1, b2 = j & 1;
+        // With two S issuers NS is even, so every use of stage st is this issuer's and
+        // it waits on the stage's phases in order (see P2DualCfg).
         if (!(ok = mbar_wait(kv_full(st), (i / C::NS) & 1, &abort_flag, p.err))) break;
         if (s.pages && (s.Nkv % kTile) != 0 && (int)(list[i] & 0xFFFFu) == T - 1) {
           // paged pool: zero the K rows past Nkv of the last page before the MMA reads them
