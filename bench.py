@@ -80,8 +80,19 @@ def algorithmic(w: synth.Workload, hot_mask):
     F2 = hot_pairs * 4 * d                         # exact QK^T and PV on hot pairs
     tiles_vis = int((vis > 0).sum()) * w.B * w.Hkv
     hot_tiles = int((bits & (vis > 0)[None, None]).sum())
+    # pass 2 walks, per 128-row block (8 groups), the union of its groups' hot tiles
+    ng = vis.shape[0]
+    nb = (ng + 7) // 8
+    gb = np.zeros(bits.shape[:2] + (nb * 8, T), bool)
+    gb[:, :, :ng] = bits & (vis > 0)[None, None]
+    union = gb.reshape(bits.shape[:2] + (nb, 8, T)).any(3)
+    vb = np.zeros((nb * 8, T), bool)
+    vb[:ng] = vis > 0
+    block_tiles_vis = int(vb.reshape(nb, 8, T).any(1).sum()) * w.B * w.Hkv
+    block_tiles_hot = int(union.sum())
     return dict(pairs=pairs, hot_pairs=hot_pairs, cold_pairs=cold_pairs, F1=F1, F2=F2,
-                hot_frac=hot_tiles / max(1, tiles_vis), hot_pair_frac=hot_pairs / max(1, pairs))
+                hot_frac=hot_tiles / max(1, tiles_vis), hot_pair_frac=hot_pairs / max(1, pairs),
+                block_tiles_hot=block_tiles_hot, block_tiles_vis=block_tiles_vis)
 
 
 def kernel_source_hash(files):
@@ -345,6 +356,10 @@ def run_gpu(args):
     line["tensor_roofline_frac"] = (work["F1"] / fp4_peak + work["F2"] / bf16_peak) / 1e12 / (ms * 1e-3)
     line["hot_tile_frac"] = work["hot_frac"]
     line["hot_pair_frac"] = work["hot_pair_frac"]
+    # what pass 2 computes: 128 x 64 (row, key) slots per block-tile in the union
+    line["pass2_union"] = {"block_tiles": work["block_tiles_hot"],
+                           "frac_of_visible_block_tiles": work["block_tiles_hot"] / max(1, work["block_tiles_vis"]),
+                           "pair_slots_per_hot_pair": work["block_tiles_hot"] * 128 * 64 / max(1, work["hot_pairs"])}
     line["peaks"] = {"source": pk_kind, **pk}
     line["clocks"] = clocks
 
