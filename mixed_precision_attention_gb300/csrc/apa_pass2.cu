@@ -36,8 +36,9 @@
 // In APA mode at d <= 128 a second kernel (pass2_dual_kernel) runs instead: two
 // softmax warp groups per block take alternate entries of the hot list, each
 // with its own (m, l), its own O in TMEM and its own double-buffered S, so one
-// group's exp/convert/store of P overlaps the other's S and PV MMAs; 11 warps,
-// 5 K/V stages, one P buffer per group.  The block's final state is the merge of
+// group's exp/convert/store of P overlaps the other's S and PV MMAs.  13 warps:
+// eight softmax, a TMA producer each for K (6-stage ring) and V (4 stages), an S
+// issuer per group and one PV issuer; one P buffer per group.  The block's final state is the merge of
 // the pass-1 state, group 0's and group 1's, in that order.  The per-row work is
 // the same as the one-group kernel's; only the tile-to-accumulator assignment
 // (and so the rounding order of the merge) differs.
@@ -586,44 +587,51 @@ __device__ __forceinline__ bool dual_sync_and(bool v) {
 // groups' per-tile latencies overlap.  At the end the pass-1 state and the two
 // groups' states are merged, always in that order.  TMEM: two O accumulators and
 // a double-buffered S per group (512 columns).
-#ifndef APA_P2D_STAGES
-#define APA_P2D_STAGES 5  // K/V stages of the two-group pass 2 (even with two S issuers)
+//
+// K and V travel in rings of their own, each filled by its own TMA warp: S(i)
+// then waits only for the K ring to free a stage (S(i - NSK) done), not for the
+// P.V product of an older tile, so the S MMAs run up to NSK tiles ahead.  Each
+// group has its own S-issuing warp; the PV warp serves both groups in list order.
+#ifndef APA_P2D_KSTAGES
+#define APA_P2D_KSTAGES 6  // K stages of the two-group pass 2 (even: see P2DualCfg)
+#endif
+#ifndef APA_P2D_VSTAGES
+#define APA_P2D_VSTAGES 4  // V stages of the two-group pass 2
 #endif
 #ifndef APA_P2D_PBUFS
 #define APA_P2D_PBUFS 1  // P buffers per group of the two-group pass 2
 #endif
-#ifndef APA_P2D_SISSUERS
-#define APA_P2D_SISSUERS 1  // S-issuing warps of the two-group pass 2: one for both groups, or one per group
-#endif
 template <int D>
 struct P2DualCfg {
-  static constexpr int NS = APA_P2D_STAGES;  // K/V stages
+  static constexpr int NS = APA_P2D_KSTAGES;   // K stages
+  static constexpr int NSV = APA_P2D_VSTAGES;  // V stages
   static constexpr int NP = APA_P2D_PBUFS;   // P buffers per group
   static constexpr int kAtoms = D / 64;
   static constexpr int kQBytes = 128 * D * 2;
   static constexpr int kKVBytes = 64 * D * 2;
   static constexpr int kPBytes = 128 * 64 * 2;
   static constexpr int kQOff = 0;
-  static constexpr int kStageOff = kQBytes;
-  static constexpr int kPOff = kStageOff + NS * 2 * kKVBytes;  // [2][NP] P
+  static constexpr int kKOff = kQBytes;
+  static constexpr int kVOff = kKOff + NS * kKVBytes;
+  static constexpr int kPOff = kVOff + NSV * kKVBytes;  // [2][NP] P
   static constexpr int kMlOff = kPOff + 2 * NP * kPBytes;      // group 1's (m, l) per row for the merge
-  static constexpr int kSIssuers = APA_P2D_SISSUERS;
-  static_assert(kSIssuers == 1 || kSIssuers == 2, "S issuers");
-  // Two S issuers each wait on the K/V arrivals of their own entries (i % 2).  With
-  // NS even, entry i's stage i % NS is only ever used by entries of the same parity,
-  // so each issuer sees every phase of its stages in order.  With NS odd, a stage's
-  // previous use would be the other issuer's; a parity wait made one phase early (the
-  // previous load still landing, since loads can land out of order) would pass on the
-  // phase before it.
-  static_assert(kSIssuers == 1 || NS % 2 == 0, "two S issuers need an even stage count");
-  static constexpr int kNumBars = 2 * NS + 16 + 1 + kSIssuers;
+  static constexpr int kSIssuers = 2;  // S-issuing warps: one per group
+  // The two S issuers each wait on the K arrivals of their own entries (i % 2).  With
+  // NS even, entry i's K stage i % NS is only ever used by entries of the same
+  // parity, so each issuer sees every phase of its stages in order.  With NS odd, a
+  // stage's previous use would be the other issuer's; a parity wait made one phase
+  // early (the previous load still landing, since loads can land out of order) would
+  // pass on the phase before it.
+  static_assert(NS % 2 == 0, "two S issuers need an even K stage count");
+  static constexpr int kB0 = 2 * NS + 2 * NSV;
+  static constexpr int kNumBars = kB0 + 16 + 1 + kSIssuers;
   static constexpr int kBarOff = kMlOff + 128 * 8;
   static constexpr int kSmem = kBarOff + kNumBars * 8 + 16 + 1024;
   static_assert(kSmem <= 232448, "shared memory");
   static_assert(NP <= 2, "pv_done slots");
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kSBase = 2 * D;  // S(u, b) at kSBase + 128 u + 64 b; O(u) at D u
-  static constexpr int kThreads = (10 + kSIssuers) * 32;
+  static constexpr int kThreads = 13 * 32;
   static_assert(kSBase + 256 <= kTmemCols, "TMEM budget");
 };
 
@@ -653,20 +661,22 @@ __global__ void __launch_bounds__(P2DualCfg<D>::kThreads, 1)
   const int b = bh / s.Hkv, h = bh % s.Hkv;
   const int p0 = blk * kBlockRows;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // warps 0-7 softmax, 8 TMA producer, 9 S issuer (group 0's tiles, or all of them
-  // with one S issuer), 10 PV issuer, 11 S issuer of group 1's tiles
-  const int kProd = 8, kMmaS = 9, kMmaPV = 10, kMmaS1 = 11;
+  // warps 0-7 softmax, 8 TMA producer of K, 9 S issuer of group 0's tiles, 10 PV
+  // issuer, 11 S issuer of group 1's tiles, 12 TMA producer of V
+  const int kProd = 8, kMmaS = 9, kMmaPV = 10, kMmaS1 = 11, kProdV = 12;
 
   const uint32_t sbase = smem_u32(smem);
   const uint32_t bar0 = smem_u32(bars);
-  auto kv_full = [&](int st) { return bar0 + 8u * st; };
-  auto kv_empty = [&](int st) { return bar0 + 8u * (C::NS + st); };
-  auto s_full = [&](int u, int b2) { return bar0 + 8u * (2 * C::NS + 8 * u + b2); };
-  auto s_free = [&](int u, int b2) { return bar0 + 8u * (2 * C::NS + 8 * u + 2 + b2); };
-  auto p_full = [&](int u, int b2) { return bar0 + 8u * (2 * C::NS + 8 * u + 4 + b2); };
-  auto pv_done = [&](int u, int b2) { return bar0 + 8u * (2 * C::NS + 8 * u + 6 + b2); };
-  const uint32_t drain_pv = bar0 + 8u * (2 * C::NS + 16);
-  auto drain_s = [&](int x) { return bar0 + 8u * (2 * C::NS + 17 + x); };  // per S issuer
+  auto k_full = [&](int st) { return bar0 + 8u * st; };
+  auto k_empty = [&](int st) { return bar0 + 8u * (C::NS + st); };
+  auto v_full = [&](int st) { return bar0 + 8u * (2 * C::NS + st); };
+  auto v_empty = [&](int st) { return bar0 + 8u * (2 * C::NS + C::NSV + st); };
+  auto s_full = [&](int u, int b2) { return bar0 + 8u * (C::kB0 + 8 * u + b2); };
+  auto s_free = [&](int u, int b2) { return bar0 + 8u * (C::kB0 + 8 * u + 2 + b2); };
+  auto p_full = [&](int u, int b2) { return bar0 + 8u * (C::kB0 + 8 * u + 4 + b2); };
+  auto pv_done = [&](int u, int b2) { return bar0 + 8u * (C::kB0 + 8 * u + 6 + b2); };
+  const uint32_t drain_pv = bar0 + 8u * (C::kB0 + 16);
+  auto drain_s = [&](int x) { return bar0 + 8u * (C::kB0 + 17 + x); };  // per S issuer
   auto warp_wait = [&](uint32_t bar, uint32_t parity) -> bool {
     if (__all_sync(0xffffffffu, mbar_test_wait(bar, parity))) return true;
     const bool okl = mbar_wait(bar, parity, &abort_flag, p.err);
@@ -680,8 +690,7 @@ __global__ void __launch_bounds__(P2DualCfg<D>::kThreads, 1)
     abort_flag = 0;
     for (int i = 0; i < C::kNumBars; ++i) {
       uint32_t count = 1;
-      if (i >= C::NS && i < 2 * C::NS) count = 2;  // kv_empty: the S and the PV issuer
-      const int j = i - 2 * C::NS;
+      const int j = i - C::kB0;
       if (j >= 0 && j < 16 && (j & 7) >= 2 && (j & 7) < 6) count = 4;  // s_free, p_full: the group's four warps
       mbar_init(bar0 + 8u * i, count);
     }
@@ -728,46 +737,61 @@ __global__ void __launch_bounds__(P2DualCfg<D>::kThreads, 1)
   const uint32_t tmem = tmem_slot;
 
   if (warp == kProd) {
-    // ------------------------------------------------------------ TMA producer
+    // ------------------------------------------------------------ TMA producer of K
     if (lane == 0) {
       int issued = 0;
       for (int i = 0; i < n; ++i) {
         const int st = i % C::NS;
-        if (i >= C::NS && !mbar_wait(kv_empty(st), ((i / C::NS) - 1) & 1, &abort_flag, p.err)) break;
+        if (i >= C::NS && !mbar_wait(k_empty(st), ((i / C::NS) - 1) & 1, &abort_flag, p.err)) break;
         const int t = (int)(list[i] & 0xFFFFu);
         int ky = t * kTile, kz = bh;
         if (s.pages) {
           ky = 0;
           kz = kv_page(s, b, t, p.err) * s.Hkv + h;
         }
-        mbar_arrive_expect_tx(kv_full(st), 2 * C::kKVBytes);
-        const uint32_t kdst = sbase + C::kStageOff + st * 2 * C::kKVBytes;
+        mbar_arrive_expect_tx(k_full(st), C::kKVBytes);
+        const uint32_t kdst = sbase + C::kKOff + st * C::kKVBytes;
 #pragma unroll
-        for (int a = 0; a < C::kAtoms; ++a) {
-          tma_load_3d(kdst + a * 8192, &kmap, a * 64, ky, kz, kv_full(st));
-          tma_load_3d(kdst + C::kKVBytes + a * 8192, &vmap, a * 64, t * kTile, bh, kv_full(st));
-        }
+        for (int a = 0; a < C::kAtoms; ++a) tma_load_3d(kdst + a * 8192, &kmap, a * 64, ky, kz, k_full(st));
         issued = i + 1;
       }
       if (abort_flag) {  // let copies in flight land before the CTA exits
-        for (int i = max(0, issued - C::NS); i < issued; ++i) wait_bounded(kv_full(i % C::NS), (i / C::NS) & 1, p.err);
+        for (int i = max(0, issued - C::NS); i < issued; ++i) wait_bounded(k_full(i % C::NS), (i / C::NS) & 1, p.err);
       }
     }
-  } else if (warp == kMmaS || (C::kSIssuers == 2 && warp == kMmaS1)) {
-    // ------------------------------------------------------------ S issuer(s): tile i into group i % 2's S
-    const int sx = warp == kMmaS ? 0 : 1;  // with two S issuers, issuer x takes the entries i % 2 == x
+  } else if (warp == kProdV) {
+    // ------------------------------------------------------------ TMA producer of V
+    if (lane == 0) {
+      int issued = 0;
+      for (int i = 0; i < n; ++i) {
+        const int st = i % C::NSV;
+        if (i >= C::NSV && !mbar_wait(v_empty(st), ((i / C::NSV) - 1) & 1, &abort_flag, p.err)) break;
+        const int t = (int)(list[i] & 0xFFFFu);
+        mbar_arrive_expect_tx(v_full(st), C::kKVBytes);
+        const uint32_t vdst = sbase + C::kVOff + st * C::kKVBytes;
+#pragma unroll
+        for (int a = 0; a < C::kAtoms; ++a) tma_load_3d(vdst + a * 8192, &vmap, a * 64, t * kTile, bh, v_full(st));
+        issued = i + 1;
+      }
+      if (abort_flag) {
+        for (int i = max(0, issued - C::NSV); i < issued; ++i) wait_bounded(v_full(i % C::NSV), (i / C::NSV) & 1, p.err);
+      }
+    }
+  } else if (warp == kMmaS || warp == kMmaS1) {
+    // ------------------------------------------------------------ S issuers: tile i into group i % 2's S
+    const int sx = warp == kMmaS ? 0 : 1;  // issuer x takes the entries i % 2 == x
     if (lane == 0 && n > sx) {
       const uint32_t idS = idesc_bf16(128, 64, 0);
       bool ok = true;
       for (int i = sx; ok && i < n; i += C::kSIssuers) {
         const int st = i % C::NS, v = i & 1, j = i >> 1, b2 = j & 1;
-        // With two S issuers NS is even, so every use of stage st is this issuer's and
-        // it waits on the stage's phases in order (see P2DualCfg).
-        if (!(ok = mbar_wait(kv_full(st), (i / C::NS) & 1, &abort_flag, p.err))) break;
+        // NS is even, so every use of K stage st is this issuer's and it waits on the
+        // stage's phases in order (see P2DualCfg).
+        if (!(ok = mbar_wait(k_full(st), (i / C::NS) & 1, &abort_flag, p.err))) break;
         if (s.pages && (s.Nkv % kTile) != 0 && (int)(list[i] & 0xFFFFu) == T - 1) {
           // paged pool: zero the K rows past Nkv of the last page before the MMA reads them
           const int nk = s.Nkv - (T - 1) * kTile, rows = kTile - nk;
-          uint8_t* kst = smem + C::kStageOff + st * 2 * C::kKVBytes;
+          uint8_t* kst = smem + C::kKOff + st * C::kKVBytes;
           for (int x = 0; x < rows * C::kAtoms * 8; ++x) {
             const int rest = x >> 3, rr = nk + rest % rows, atom = rest / rows;
             *reinterpret_cast<uint4*>(kst + atom * 8192 + rr * 128 + (x & 7) * 16) = make_uint4(0u, 0u, 0u, 0u);
@@ -776,7 +800,7 @@ __global__ void __launch_bounds__(P2DualCfg<D>::kThreads, 1)
         }
         if (j >= 2 && !(ok = mbar_wait(s_free(v, b2), ((j >> 1) - 1) & 1, &abort_flag, p.err))) break;
         tc_fence_after();
-        const uint32_t kaddr = sbase + C::kStageOff + st * 2 * C::kKVBytes;
+        const uint32_t kaddr = sbase + C::kKOff + st * C::kKVBytes;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint64_t ad = smem_desc(sbase + C::kQOff + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024, kSwizzle128B);
@@ -784,7 +808,7 @@ __global__ void __launch_bounds__(P2DualCfg<D>::kThreads, 1)
           mma_bf16(tmem + C::kSBase + 128 * v + 64 * b2, ad, bd, idS, kk > 0);
         }
         mma_commit(s_full(v, b2));
-        mma_commit(kv_empty(st));  // this stage's K has been read
+        mma_commit(k_empty(st));  // this stage's K has been read
       }
       mma_commit(drain_s(sx));
       wait_bounded(drain_s(sx), 0, p.err);
@@ -795,11 +819,11 @@ __global__ void __launch_bounds__(P2DualCfg<D>::kThreads, 1)
       const uint32_t idO = idesc_f16(128, D, 1);
       bool ok = true;
       for (int i = 0; ok && i < n; ++i) {
-        const int st = i % C::NS, v = i & 1, j = i >> 1, b2 = j & 1;
+        const int st = i % C::NSV, v = i & 1, j = i >> 1, b2 = j & 1;
         if (!(ok = mbar_wait(p_full(v, b2), (j >> 1) & 1, &abort_flag, p.err))) break;
-        if (!(ok = mbar_wait(kv_full(st), (i / C::NS) & 1, &abort_flag, p.err))) break;
+        if (!(ok = mbar_wait(v_full(st), (i / C::NSV) & 1, &abort_flag, p.err))) break;
         tc_fence_after();
-        const uint32_t vaddr = sbase + C::kStageOff + st * 2 * C::kKVBytes + C::kKVBytes;
+        const uint32_t vaddr = sbase + C::kVOff + st * C::kKVBytes;
         const uint32_t paddr = sbase + C::kPOff + (v * C::NP + j % C::NP) * C::kPBytes;
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
@@ -808,7 +832,7 @@ __global__ void __launch_bounds__(P2DualCfg<D>::kThreads, 1)
                    (j > 0 || kk > 0) ? 1u : 0u);
         }
         mma_commit(pv_done(v, b2));
-        mma_commit(kv_empty(st));  // this stage's V has been read
+        mma_commit(v_empty(st));  // this stage's V has been read
       }
       mma_commit(drain_pv);
       wait_bounded(drain_pv, 0, p.err);
