@@ -1,0 +1,204 @@
+"""The barrier protocol of the two-group pass-2 kernel (pass2_dual_kernel), run as a
+model under random schedules on the CPU.
+
+Actors: a TMA producer per ring, the S issuers, the PV issuer and the two softmax
+groups, each a generator that waits on mbarriers by parity, arrives on them, and
+issues asynchronous work.  TMA loads may complete in any order; the MMAs of one
+issuing thread complete in issue order (tcgen05.commit tracks all of that thread's
+earlier MMAs).  An mbarrier parity wait passes when the barrier's completed-phase
+count has the other parity, exactly as in hardware, so a wait made a phase early
+or two phases late passes on the wrong phase.  The checks:
+  - every wait that passes lands on the phase it means (completed count = phase + 1);
+  - every MMA reads the shared-memory stage, S slot or P buffer holding its entry;
+  - every schedule ends (no deadlock).
+The layout the kernel uses (K ring of 6 stages owned by one S issuer per group, a V
+ring of 4) must pass every schedule; a shared K/V ring of 5 stages with two S
+issuers must be caught: there consecutive uses of a stage alternate between the
+issuers, and one of them can wait a phase early while the stage's previous load is
+still landing."""
+import random
+
+import pytest
+
+
+class Bar:
+    def __init__(self, count):
+        self.count, self.pending, self.done = count, 0, 0
+
+    def arrive(self):
+        self.pending += 1
+        if self.pending == self.count:
+            self.pending, self.done = 0, self.done + 1
+
+
+class Violation(Exception):
+    pass
+
+
+def run(n, nsk, nsv, s_issuers, split, seed, pbuf_wait=True):
+    """One random schedule of one block with n hot-list entries.  split=False: one
+    ring of nsk stages holding K and V (one producer); True: a K ring (nsk) and a V
+    ring (nsv), a producer each.  pbuf_wait=False drops the groups' wait for the P
+    buffer (a planted mistake).  Raises Violation on a wrong phase or stage."""
+    rng = random.Random(seed)
+    bars = {}
+
+    def bar(name, count=1):
+        if name not in bars:
+            bars[name] = Bar(count)
+        return bars[name]
+
+    kst = {}    # K stage -> entry whose K has landed there (None while loading)
+    vst = {}
+    sslot = {}  # (group, slot) -> entry whose S is there
+    pbuf = {}   # group -> entry whose P is there
+    inflight = []  # (order key or None, callback): None = may complete in any order
+
+    def wait(name, phase, count=1):
+        b = bar(name, count)
+        while b.done % 2 == phase % 2:  # hardware parity test: passes once parity differs
+            yield None
+        if b.done != phase + 1:
+            raise Violation(f"wait on {name} for phase {phase} passed at {b.done} completed phases")
+
+    kring, vring = ("k", "v") if split else ("kv", "kv")
+    nsv_ = nsv if split else nsk
+
+    def producer(ring, ns, store):
+        for i in range(n):
+            st = i % ns
+            if i >= ns:
+                yield from wait((ring + "_empty", st), i // ns - 1, 1 if split else 2)
+            store[st] = None
+
+            def land(st=st, i=i):
+                store[st] = i
+                bar((ring + "_full", st)).arrive()
+            inflight.append((None, land))
+            yield None
+
+    def s_issuer(x):
+        for i in range(x, n, s_issuers):
+            st, v, j = i % nsk, i & 1, i >> 1
+            b2 = j & 1
+            yield from wait((kring + "_full", st), i // nsk)
+            if kst.get(st) != i:
+                raise Violation(f"S({i}) issued on K stage {st} holding {kst.get(st)}")
+            if j >= 2:
+                yield from wait(("s_free", v, b2), (j >> 1) - 1, 1)
+
+            def done(i=i, st=st, v=v, b2=b2):
+                if kst.get(st) != i:
+                    raise Violation(f"S({i}) read K stage {st} holding {kst.get(st)}")
+                sslot[(v, b2)] = i
+                bar(("s_full", v, b2)).arrive()
+                bar((kring + "_empty", st), 1 if split else 2).arrive()
+            inflight.append((("s", x), done))
+            yield None
+
+    def pv_issuer():
+        for i in range(n):
+            st, v, j = i % nsv_, i & 1, i >> 1
+            b2 = j & 1
+            yield from wait(("p_full", v, b2), j >> 1, 1)
+            yield from wait((vring + "_full", st), i // nsv_)
+            if vst.get(st) != i or pbuf.get(v) != i:
+                raise Violation(f"PV({i}) issued on V {vst.get(st)} / P {pbuf.get(v)}")
+
+            def done(i=i, st=st, v=v, b2=b2):
+                if vst.get(st) != i or pbuf.get(v) != i:
+                    raise Violation(f"PV({i}) read V {vst.get(st)} / P {pbuf.get(v)}")
+                bar(("pv_done", v, b2)).arrive()
+                bar((vring + "_empty", st), 1 if split else 2).arrive()
+            inflight.append((("pv",), done))
+            yield None
+
+    def group(v):
+        nu = (n - v + 1) // 2
+        for j in range(nu):
+            i = 2 * j + v
+            yield from wait(("s_full", v, j & 1), j >> 1)
+            if sslot.get((v, j & 1)) != i:
+                raise Violation(f"group {v} read S slot holding {sslot.get((v, j & 1))} for {i}")
+            bar(("s_free", v, j & 1), 1).arrive()
+            yield None
+            if j >= 1 and pbuf_wait:  # one P buffer: PV of the group's previous entry has read it
+                yield from wait(("pv_done", v, (j - 1) & 1), (j - 1) >> 1)
+            pbuf[v] = i
+            bar(("p_full", v, j & 1), 1).arrive()
+            yield None
+        if v == 0:  # the merge waits for both groups' last P.V
+            for u in (0, 1):
+                nl = (n - u + 1) // 2
+                if nl:
+                    yield from wait(("pv_done", u, (nl - 1) & 1), (nl - 1) >> 1)
+
+    actors = [producer(kring, nsk, kst)]
+    if split:
+        actors.append(producer(vring, nsv, vst))
+    actors += [s_issuer(x) for x in range(s_issuers)] + [pv_issuer(), group(0), group(1)]
+    if not split:
+        vst = kst  # one ring: V lands with K
+    live = list(actors)
+    for _ in range(200000):
+        if not live and not inflight:
+            return
+        # in-order completion per issuing thread: only the oldest op of each key
+        heads, seen = [], set()
+        for k, (key, cb) in enumerate(inflight):
+            if key is None or key not in seen:
+                heads.append(k)
+                if key is not None:
+                    seen.add(key)
+        choices = [("a", a) for a in live] + [("c", k) for k in heads]
+        kind, what = rng.choice(choices)
+        if kind == "c":
+            inflight.pop(what)[1]()
+            continue
+        try:
+            next(what)
+        except StopIteration:
+            live.remove(what)
+    raise Violation("no progress: deadlock")
+
+
+@pytest.mark.parametrize("n", [0, 1, 2, 3, 5, 8, 13, 24])
+def test_kept_layout_is_safe_under_random_schedules(n):
+    # K ring of 6 (each S issuer owns three stages), V ring of 4
+    for seed in range(60):
+        run(n, nsk=6, nsv=4, s_issuers=2, split=True, seed=seed)
+
+
+@pytest.mark.parametrize("nsk,nsv", [(2, 1), (4, 2), (8, 3)])
+def test_other_even_k_rings_are_safe(nsk, nsv):
+    for seed in range(40):
+        run(17, nsk=nsk, nsv=nsv, s_issuers=2, split=True, seed=seed)
+
+
+def test_first_form_one_ring_one_s_issuer_is_safe():
+    for seed in range(60):
+        run(17, nsk=5, nsv=5, s_issuers=1, split=False, seed=seed)
+
+
+def test_two_s_issuers_over_an_odd_shared_ring_are_caught():
+    """The layout whose timing was withdrawn: some schedule makes an issuer pass a
+    wait on the phase before the one it means."""
+    caught = 0
+    for seed in range(400):
+        try:
+            run(24, nsk=5, nsv=5, s_issuers=2, split=False, seed=seed)
+        except Violation:
+            caught += 1
+    assert caught > 0
+
+
+def test_planted_mistake_is_caught():
+    """The checker itself: a group that writes its next P without waiting for the
+    P.V of its previous one overwrites a buffer still to be read."""
+    caught = 0
+    for seed in range(200):
+        try:
+            run(12, nsk=6, nsv=4, s_issuers=2, split=True, seed=seed, pbuf_wait=False)
+        except Violation:
+            caught += 1
+    assert caught > 0
