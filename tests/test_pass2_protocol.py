@@ -15,7 +15,8 @@ The layout the kernel uses (K ring of 6 stages owned by one S issuer per group, 
 ring of 4) must pass every schedule; a shared K/V ring of 5 stages with two S
 issuers must be caught: there consecutive uses of a stage alternate between the
 issuers, and one of them can wait a phase early while the stage's previous load is
-still landing."""
+still landing.  Each run draws a speed per actor and a completion rate for copies
+and for MMAs, so that lagging issuers and long-running MMAs occur."""
 import random
 
 import pytest
@@ -140,7 +141,11 @@ def run(n, nsk, nsv, s_issuers, split, seed, pbuf_wait=True):
     if not split:
         vst = kst  # one ring: V lands with K
     live = list(actors)
-    for _ in range(200000):
+    # each run draws a speed per actor and a completion rate for copies and for MMAs,
+    # over two decades, so that lagging issuers and long-running MMAs both occur
+    speed = {id(a): 10 ** rng.uniform(-2, 0) for a in live}
+    rate = {"copy": 10 ** rng.uniform(-2, 0), "mma": 10 ** rng.uniform(-2, 0)}
+    for _ in range(400000):
         if not live and not inflight:
             return
         # in-order completion per issuing thread: only the oldest op of each key
@@ -151,7 +156,8 @@ def run(n, nsk, nsv, s_issuers, split, seed, pbuf_wait=True):
                 if key is not None:
                     seen.add(key)
         choices = [("a", a) for a in live] + [("c", k) for k in heads]
-        kind, what = rng.choice(choices)
+        weights = [speed[id(a)] for a in live] + [rate["copy" if inflight[k][0] is None else "mma"] for k in heads]
+        kind, what = rng.choices(choices, weights)[0]
         if kind == "c":
             inflight.pop(what)[1]()
             continue
