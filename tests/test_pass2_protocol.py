@@ -1,5 +1,5 @@
-"""The barrier protocol of the two-group pass-2 kernel (pass2_dual_kernel), run as a
-model under random schedules on the CPU.
+"""The barrier protocols of the pass-2 kernels (pass2_dual_kernel with two softmax
+groups, pass2_kernel with one), run as models under random schedules on the CPU.
 
 Actors: a TMA producer per ring, the S issuers, the PV issuer and the two softmax
 groups, each a generator that waits on mbarriers by parity, arrives on them, and
@@ -10,6 +10,7 @@ count has the other parity, exactly as in hardware, so a wait made a phase early
 or two phases late passes on the wrong phase.  The checks:
   - every wait that passes lands on the phase it means (completed count = phase + 1);
   - every MMA reads the shared-memory stage, S slot or P buffer holding its entry;
+  - O is rescaled, or merged, only with none of its group's P.V in flight;
   - every schedule ends (no deadlock).
 The layout the kernel uses (K ring of 6 stages owned by one S issuer per group, a V
 ring of 4) must pass every schedule; a shared K/V ring of 5 stages with two S
@@ -36,11 +37,13 @@ class Violation(Exception):
     pass
 
 
-def run(n, nsk, nsv, s_issuers, split, seed, pbuf_wait=True):
+def run(n, nsk, nsv, s_issuers, split, seed, pbuf_wait=True, groups=2, np_=1):
     """One random schedule of one block with n hot-list entries.  split=False: one
     ring of nsk stages holding K and V (one producer); True: a K ring (nsk) and a V
     ring (nsv), a producer each.  pbuf_wait=False drops the groups' wait for the P
-    buffer (a planted mistake).  Raises Violation on a wrong phase or stage."""
+    buffer (a planted mistake).  groups=1 with one S issuer and one ring is the
+    one-group kernel (pass2_kernel); np_ is the number of P buffers per group.
+    Raises Violation on a wrong phase or stage."""
     rng = random.Random(seed)
     bars = {}
 
@@ -52,7 +55,8 @@ def run(n, nsk, nsv, s_issuers, split, seed, pbuf_wait=True):
     kst = {}    # K stage -> entry whose K has landed there (None while loading)
     vst = {}
     sslot = {}  # (group, slot) -> entry whose S is there
-    pbuf = {}   # group -> entry whose P is there
+    pbuf = {}   # (group, buffer) -> entry whose P is there
+    pv_inflight = [0, 0]
     inflight = []  # (order key or None, callback): None = may complete in any order
 
     def wait(name, phase, count=1):
@@ -80,7 +84,7 @@ def run(n, nsk, nsv, s_issuers, split, seed, pbuf_wait=True):
 
     def s_issuer(x):
         for i in range(x, n, s_issuers):
-            st, v, j = i % nsk, i & 1, i >> 1
+            st, v, j = i % nsk, i % groups, i // groups
             b2 = j & 1
             yield from wait((kring + "_full", st), i // nsk)
             if kst.get(st) != i:
@@ -99,45 +103,55 @@ def run(n, nsk, nsv, s_issuers, split, seed, pbuf_wait=True):
 
     def pv_issuer():
         for i in range(n):
-            st, v, j = i % nsv_, i & 1, i >> 1
-            b2 = j & 1
+            st, v, j = i % nsv_, i % groups, i // groups
+            b2, pb = j & 1, (i // groups) % np_
             yield from wait(("p_full", v, b2), j >> 1, 1)
             yield from wait((vring + "_full", st), i // nsv_)
-            if vst.get(st) != i or pbuf.get(v) != i:
-                raise Violation(f"PV({i}) issued on V {vst.get(st)} / P {pbuf.get(v)}")
+            if vst.get(st) != i or pbuf.get((v, pb)) != i:
+                raise Violation(f"PV({i}) issued on V {vst.get(st)} / P {pbuf.get((v, pb))}")
+            pv_inflight[v] += 1
 
-            def done(i=i, st=st, v=v, b2=b2):
-                if vst.get(st) != i or pbuf.get(v) != i:
-                    raise Violation(f"PV({i}) read V {vst.get(st)} / P {pbuf.get(v)}")
+            def done(i=i, st=st, v=v, b2=b2, pb=pb):
+                if vst.get(st) != i or pbuf.get((v, pb)) != i:
+                    raise Violation(f"PV({i}) read V {vst.get(st)} / P {pbuf.get((v, pb))}")
+                pv_inflight[v] -= 1
                 bar(("pv_done", v, b2)).arrive()
                 bar((vring + "_empty", st), 1 if split else 2).arrive()
             inflight.append((("pv",), done))
             yield None
 
+    def count(v):
+        return (n - v + groups - 1) // groups
+
     def group(v):
-        nu = (n - v + 1) // 2
-        for j in range(nu):
-            i = 2 * j + v
+        for j in range(count(v)):
+            i = groups * j + v
             yield from wait(("s_full", v, j & 1), j >> 1)
             if sslot.get((v, j & 1)) != i:
                 raise Violation(f"group {v} read S slot holding {sslot.get((v, j & 1))} for {i}")
             bar(("s_free", v, j & 1), 1).arrive()
             yield None
-            if j >= 1 and pbuf_wait:  # one P buffer: PV of the group's previous entry has read it
+            if j >= np_ and pbuf_wait:  # P buffer j % np_: P.V of entry j - np_ has read it
+                yield from wait(("pv_done", v, (j - np_) & 1), (j - np_) >> 1)
+            if j >= 1 and rng.random() < 0.3:  # the running maximum moved: rescale O
                 yield from wait(("pv_done", v, (j - 1) & 1), (j - 1) >> 1)
-            pbuf[v] = i
+                if pv_inflight[v]:
+                    raise Violation(f"group {v} rescaled O with a P.V in flight at entry {i}")
+            pbuf[(v, j % np_)] = i
             bar(("p_full", v, j & 1), 1).arrive()
             yield None
-        if v == 0:  # the merge waits for both groups' last P.V
-            for u in (0, 1):
-                nl = (n - u + 1) // 2
+        if v == 0:  # the merge waits for every group's last P.V
+            for u in range(groups):
+                nl = count(u)
                 if nl:
                     yield from wait(("pv_done", u, (nl - 1) & 1), (nl - 1) >> 1)
+                    if pv_inflight[u]:
+                        raise Violation(f"merge with a P.V of group {u} in flight")
 
     actors = [producer(kring, nsk, kst)]
     if split:
         actors.append(producer(vring, nsv, vst))
-    actors += [s_issuer(x) for x in range(s_issuers)] + [pv_issuer(), group(0), group(1)]
+    actors += [s_issuer(x) for x in range(s_issuers)] + [pv_issuer()] + [group(v) for v in range(groups)]
     if not split:
         vst = kst  # one ring: V lands with K
     live = list(actors)
@@ -205,6 +219,25 @@ def test_planted_mistake_is_caught():
     for seed in range(200):
         try:
             run(12, nsk=6, nsv=4, s_issuers=2, split=True, seed=seed, pbuf_wait=False)
+        except Violation:
+            caught += 1
+    assert caught > 0
+
+
+@pytest.mark.parametrize("ns,np_", [(4, 2), (3, 2), (2, 1), (4, 1)])
+def test_one_group_kernel_is_safe(ns, np_):
+    """pass2_kernel: one softmax group, one S issuer, one K/V ring (4 stages with
+    two P buffers in APA mode at d = 128, 3 or 2 elsewhere)."""
+    for n in (1, 2, 7, 15):
+        for seed in range(25):
+            run(n, nsk=ns, nsv=ns, s_issuers=1, split=False, seed=seed, groups=1, np_=np_)
+
+
+def test_one_group_planted_mistake_is_caught():
+    caught = 0
+    for seed in range(200):
+        try:
+            run(12, nsk=4, nsv=4, s_issuers=1, split=False, seed=seed, groups=1, np_=2, pbuf_wait=False)
         except Violation:
             caught += 1
     assert caught > 0
