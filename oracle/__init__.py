@@ -74,7 +74,9 @@ def _load():
             lib.oracle_quantize_residual_blocks.restype = None
             lib.oracle_quantize_q_head.restype = None
             lib.oracle_apa.argtypes = [P, P, P, i32, i32, i32, i32, i32, i32, i32, f64, f64, f64, i32,
-                                       P, i64, P, P, P, P, P]
+                                       P, i64, P, P, P, P, P, P]
+            lib.oracle_p_tile.argtypes = [P, f64, f64, i32, P, P, P, P]
+            lib.oracle_p_tile.restype = f64
             lib.oracle_apa.restype = i32
             lib.oracle_num_threads.argtypes = []; lib.oracle_num_threads.restype = i32
             _lib = lib
@@ -229,7 +231,27 @@ def n_groups(Hq, Hkv, Nq):
     return ((Hq // Hkv) * Nq + GROUP_ROWS - 1) // GROUP_ROWS
 
 
-def apa(q, k, v, causal=True, eps=0.005, tau=4.0, cold_offset=32.0, quant=QUANT_ALL, units=None,
+TAU = 4.0           # lazy-maximum threshold, log2 units ("Lazy maximum")
+COLD_OFFSET = 32.0  # a hot tile lifts the frame at most to c - 32 ("The bug", the decoupled cold frame)
+
+
+def p_tile(s, m, tau=TAU, quantize=True):
+    """P of one row over one 64-key tile, encoded in FP4 as pass 1 does.
+
+    s: 64 scores in log2 units (-inf = not visible); m: the row's frame before
+    the tile.  Returns dict(c=tile max, mt=frame P is computed in, sc=[4] group
+    scales, p=[64] dequantized P, ell=sum of p)."""
+    s = np.ascontiguousarray(s, dtype=np.float64)
+    assert s.shape == (TILE,)
+    c, mt = ctypes.c_double(), ctypes.c_double()
+    sc = np.empty(TILE // 16)
+    p = np.empty(TILE)
+    ell = _load().oracle_p_tile(_ptr(s), float(m), float(tau), int(quantize), ctypes.byref(c), ctypes.byref(mt),
+                                _ptr(sc), _ptr(p))
+    return dict(c=c.value, mt=mt.value, sc=sc, p=p, ell=ell)
+
+
+def apa(q, k, v, causal=True, eps=0.005, tau=TAU, cold_offset=COLD_OFFSET, quant=QUANT_ALL, units=None,
         diag=False):
     """APA emulation (pass 1, hot test, exact pass 2, merge) in FP64.
 
@@ -237,7 +259,9 @@ def apa(q, k, v, causal=True, eps=0.005, tau=4.0, cold_offset=32.0, quant=QUANT_
     Returns dict(out, lse, hot_mask[, ell, lam]); rows of groups not asked for are NaN.
     hot_mask: uint32 [B, Hkv, ceil(R/16), ceil(T/32)], bit t%32 of word t/32.
     ell [n, 16, T]: each row's FP4 tile sum in the row's final frame (NaN = unseen);
-    lam [n, 16]: final running sum lambda."""
+    lam [n, 16]: final running sum lambda;
+    frame [n, 16, T, 3]: per row and tile seen, the tile maximum c, the frame m~
+    its P was computed in, and the row's frame after the tile (NaN = unseen)."""
     q, k, v = _u16(q), _u16(k), _u16(v)
     B, Hq, Nq, d = q.shape
     Hkv, Nkv = k.shape[1], k.shape[2]
@@ -250,14 +274,15 @@ def apa(q, k, v, causal=True, eps=0.005, tau=4.0, cold_offset=32.0, quant=QUANT_
     nu = B * Hkv * ng if u is None else len(u)
     ell = np.full((nu, GROUP_ROWS, T), np.nan) if diag else None
     lam = np.full((nu, GROUP_ROWS), np.nan) if diag else None
+    frame = np.full((nu, GROUP_ROWS, T, 3), np.nan) if diag else None
     rc = _load().oracle_apa(_ptr(q), _ptr(k), _ptr(v), B, Hq, Hkv, Nq, Nkv, d, int(causal), float(eps),
                             float(tau), float(cold_offset), int(quant), _ptr(u), 0 if u is None else len(u),
-                            _ptr(out), _ptr(lse), _ptr(hot), _ptr(ell), _ptr(lam))
+                            _ptr(out), _ptr(lse), _ptr(hot), _ptr(ell), _ptr(lam), _ptr(frame))
     if rc != 0:
         raise ValueError("unsupported shape for the oracle")
     r = dict(out=out, lse=lse, hot_mask=hot)
     if diag:
-        r["ell"], r["lam"] = ell, lam
+        r["ell"], r["lam"], r["frame"] = ell, lam, frame
     return r
 
 

@@ -468,10 +468,63 @@ static void quantize_q_row(const uint16_t* qr, int d, double s_q, int quant, dou
   }
 }
 
-/* The largest UE4M3-representable scale and the clamp of the P group scale
- * ("The bug: a sink that drowned the tail": the exponent is clamped at -6 so
- * the scale stays a normal UE4M3 value). */
+/* The clamp of the P group scale ("The bug: a sink that drowned the tail":
+ * the scale exponent is clamped at -6, so the scale stays a normal UE4M3
+ * value; 2^-6 is the smallest one). */
 #define P_SCALE_MIN 0.015625
+
+/* P of one row over one 64-key tile, encoded directly in FP4 (blog, "Pass 1:
+ * FP4 everywhere, with a hot test", step 2: each 16-key group gets its own
+ * scale, folded into the exponent bias; "Lazy maximum": tau = 4; "Second
+ * hunt": the group scales are UE4M3, so each group maximum lands near 6; "The
+ * bug": the scale exponent is clamped at -6).
+ *   s[64]   the row's scores in log2 units, -inf where the key is not visible;
+ *   m       the row's frame before this tile (-inf before its first tile);
+ *   c       the tile maximum (out); mt the frame P is computed in (out):
+ *           c if c > m + tau else m  (an empty tile keeps m);
+ *   sc[4]   per 16-key group k: UE4M3_RN(2^(g_k - mt) / 6), at least 2^-6,
+ *           g_k the group maximum (2^-6 for a group with nothing visible);
+ *   p[64]   sc_k * E2M1_RN(2^(s - mt) / sc_k), 0 where masked; with quant_p = 0
+ *           the exact 2^(s - mt) instead (the emulation's P switch).
+ * Returns l_t, the sum of p in index order (the tile's FP4 row sum, step 3). */
+double oracle_p_tile(const double* s, double m, double tau, int quant_p, double* c_out, double* mt_out,
+                     double* sc, double* p) {
+  double g[TILE / 16], c = -INFINITY;
+  for (int kg = 0; kg < TILE / 16; ++kg) {
+    g[kg] = -INFINITY;
+    for (int jj = kg * 16; jj < kg * 16 + 16; ++jj)
+      if (s[jj] > g[kg]) g[kg] = s[jj];
+    c = fmax(c, g[kg]);
+  }
+  *c_out = c;
+  if (c == -INFINITY) {
+    *mt_out = m;
+    for (int kg = 0; kg < TILE / 16; ++kg) sc[kg] = P_SCALE_MIN;
+    for (int jj = 0; jj < TILE; ++jj) p[jj] = 0.0;
+    return 0.0;
+  }
+  double mtl = (c > m + tau) ? c : m;
+  *mt_out = mtl;
+  double sum = 0.0;
+  for (int kg = 0; kg < TILE / 16; ++kg) {
+    double sck = P_SCALE_MIN;
+    if (g[kg] != -INFINITY) {
+      sck = oracle_ue4m3_value(oracle_ue4m3_code(exp2(g[kg] - mtl) / 6.0));
+      if (sck < P_SCALE_MIN) sck = P_SCALE_MIN;
+    }
+    sc[kg] = sck;
+    for (int jj = kg * 16; jj < kg * 16 + 16; ++jj) {
+      double pj = 0.0;
+      if (s[jj] != -INFINITY) {
+        double x = exp2(s[jj] - mtl);
+        pj = quant_p ? sck * oracle_e2m1_value(oracle_e2m1_code(x / sck)) : x;
+      }
+      p[jj] = pj;
+      sum += pj;
+    }
+  }
+  return sum;
+}
 
 /* Emulates pass 1, pass 2 and the merge for one 16-row group of one KV head.
  *
@@ -499,11 +552,15 @@ static void quantize_q_row(const uint16_t* qr, int d, double s_q, int quant, dou
  * diag_ell: optional [16][T]: l_t of each row expressed in the row's final
  *           frame (NaN where the row sees nothing of the tile).
  * diag_lam: optional [16]: final lambda (in the final frame).
+ * diag_frame: optional [16][T][3]: per row and tile it sees, the tile maximum
+ *           c, the frame m~ its P was computed in and the frame after the
+ *           commit (NaN where the row sees nothing of the tile).
  */
 static void apa_group(const uint16_t* q, const uint16_t* k, const uint16_t* v, int b, int hk, int grp,
                       int B, int Hq, int Hkv, int Nq, int Nkv, int d, int causal,
                       const oracle_apa_params* P, const head_ops* H, const double* s_q_heads,
-                      double* out, double* lse, uint32_t* hot_mask, double* diag_ell, double* diag_lam) {
+                      double* out, double* lse, uint32_t* hot_mask, double* diag_ell, double* diag_lam,
+                      double* diag_frame) {
   (void)B;
   int G = Hq / Hkv, R = G * Nq, T = H->T, off = Nkv - Nq;
   int nwords = (T + 31) / 32;
@@ -523,7 +580,7 @@ static void apa_group(const uint16_t* q, const uint16_t* k, const uint16_t* v, i
   double m[GROUP_ROWS], lam[GROUP_ROWS], l[GROUP_ROWS], cs[GROUP_ROWS];
   int pos[GROUP_ROWS], hq[GROUP_ROWS], lastv[GROUP_ROWS];
   double s[GROUP_ROWS][TILE], pv[GROUP_ROWS][TILE];
-  double mt[GROUP_ROWS], lt[GROUP_ROWS];
+  double mt[GROUP_ROWS], lt[GROUP_ROWS], ct[GROUP_ROWS];
   int empty[GROUP_ROWS];
 
   int tmax = 0;
@@ -546,39 +603,16 @@ static void apa_group(const uint16_t* q, const uint16_t* k, const uint16_t* v, i
     int j0 = t * TILE;
     /* scores, frame candidate, P and l_t per row */
     for (int r = 0; r < nr; ++r) {
-      double c = -INFINITY, g[TILE / 16];
-      for (int kg = 0; kg < TILE / 16; ++kg) g[kg] = -INFINITY;
       for (int jj = 0; jj < TILE; ++jj) {
         int j = j0 + jj;
         if (j >= Nkv || j > lastv[r]) { s[r][jj] = -INFINITY; continue; }
         double dot = 0.0;
         for (int ch = 0; ch < d; ++ch) dot += qq[r * d + ch] * H->kq[(int64_t)j * d + ch];
         s[r][jj] = dot * cs[r];
-        if (s[r][jj] > g[jj / 16]) g[jj / 16] = s[r][jj];
       }
-      for (int kg = 0; kg < TILE / 16; ++kg) c = fmax(c, g[kg]);
-      empty[r] = (c == -INFINITY);
-      if (empty[r]) { lt[r] = 0.0; mt[r] = m[r]; continue; }
-      double mtl = (c > m[r] + P->tau) ? c : m[r];
-      mt[r] = mtl;
-      double sum = 0.0;
-      for (int kg = 0; kg < TILE / 16; ++kg) {
-        double sc = P_SCALE_MIN;
-        if (g[kg] != -INFINITY) {
-          sc = oracle_ue4m3_value(oracle_ue4m3_code(exp2(g[kg] - mtl) / 6.0));
-          if (sc < P_SCALE_MIN) sc = P_SCALE_MIN;
-        }
-        for (int jj = kg * 16; jj < kg * 16 + 16; ++jj) {
-          double p = 0.0;
-          if (s[r][jj] != -INFINITY) {
-            double x = exp2(s[r][jj] - mtl);
-            p = (P->quant & QUANT_P) ? sc * oracle_e2m1_value(oracle_e2m1_code(x / sc)) : x;
-          }
-          pv[r][jj] = p;
-          sum += p;
-        }
-      }
-      lt[r] = sum;
+      double sc[TILE / 16];
+      lt[r] = oracle_p_tile(s[r], m[r], P->tau, (P->quant & QUANT_P) != 0, &ct[r], &mt[r], sc, pv[r]);
+      empty[r] = (ct[r] == -INFINITY);
     }
     /* the hot test: one verdict for the group.  eps = 0 is the all-exact run:
      * every tile the group can see is hot, even one whose FP4 mass rounds to 0. */
@@ -598,8 +632,7 @@ static void apa_group(const uint16_t* q, const uint16_t* k, const uint16_t* v, i
       if (empty[r]) continue;
       ell[r * T + t] = lt[r];
       frame[r * T + t] = mt[r];
-      double mn, c = -INFINITY;
-      for (int jj = 0; jj < TILE; ++jj) c = fmax(c, s[r][jj]);
+      double mn, c = ct[r];
       if (hot) {
         mn = fmax(m[r], c - P->cold_offset);
         double f = m[r] == -INFINITY ? 0.0 : exp2(m[r] - mn);
@@ -619,6 +652,10 @@ static void apa_group(const uint16_t* q, const uint16_t* k, const uint16_t* v, i
         }
       }
       m[r] = mn;
+      if (diag_frame) {
+        double* fr = diag_frame + ((int64_t)r * T + t) * 3;
+        fr[0] = c; fr[1] = mt[r]; fr[2] = mn;
+      }
     }
   }
 
@@ -680,12 +717,13 @@ static void apa_group(const uint16_t* q, const uint16_t* k, const uint16_t* v, i
  * units: optional [nunits][3] (b, hkv, group); NULL = every group.
  * out [B,Hq,Nq,d], lse [B,Hq,Nq]: written for the rows of the listed groups.
  * hot_mask [B,Hkv,ceil(R/16),ceil(T/32)]: written for the listed groups.
- * diag_ell [nunits][16][T], diag_lam [nunits][16]: optional diagnostics.
+ * diag_ell [nunits][16][T], diag_lam [nunits][16], diag_frame [nunits][16][T][3]:
+ * optional diagnostics (see apa_group).
  * Returns 0, or -1 on an unsupported shape. */
 int oracle_apa(const uint16_t* q, const uint16_t* k, const uint16_t* v, int B, int Hq, int Hkv, int Nq,
                int Nkv, int d, int causal, double eps, double tau, double cold_offset, int quant,
                const int32_t* units, int64_t nunits, double* out, double* lse, uint32_t* hot_mask,
-               double* diag_ell, double* diag_lam) {
+               double* diag_ell, double* diag_lam, double* diag_frame) {
   if (Hq % Hkv || Nkv < Nq || d % 64 || Nq <= 0) return -1;
   oracle_apa_params P = {eps, tau, cold_offset, quant};
   int G = Hq / Hkv, R = G * Nq, T = (Nkv + TILE - 1) / TILE;
@@ -718,7 +756,8 @@ int oracle_apa(const uint16_t* q, const uint16_t* k, const uint16_t* v, int B, i
       done[u] = 1;
       apa_group(q, k, v, b, hk, units[3 * u + 2], B, Hq, Hkv, Nq, Nkv, d, causal, &P, &H, sq, out, lse,
                 hot_mask, diag_ell ? diag_ell + u * GROUP_ROWS * T : NULL,
-                diag_lam ? diag_lam + u * GROUP_ROWS : NULL);
+                diag_lam ? diag_lam + u * GROUP_ROWS : NULL,
+                diag_frame ? diag_frame + u * GROUP_ROWS * T * 3 : NULL);
     }
     free_head(&H);
   }
