@@ -58,6 +58,7 @@ extern "C" {
 #define APA_FLAG_Q_RESIDUAL 1u /* Q as two FP4 terms in pass 1 (see apa_attention_ex) */
 #define APA_FLAG_LSE_SCALES 2u /* least-squared-error block scales for Q, K, V (see apa_attention_ex) */
 #define APA_FLAG_VALUE_WEIGHTED 4u /* hot test weighted by value norm (see apa_attention_ex) */
+#define APA_FLAG_ROWSUM_MMA 8u /* pass-1 tile row sums from an MMA against an E2M1 ones tile (see apa_attention_ex) */
 
 /* Size of the fixed device scratch array behind apa_quantize_noalloc (16 MiB). */
 #define APA_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
@@ -66,8 +67,10 @@ extern "C" {
  *   q        bf16 [B, Hq, Nq, d], contiguous
  *   k, v     bf16 [B, Hkv, Nkv, d], contiguous
  *   causal   0: every key visible; else tail-aligned causal mask
- *   eps      hot-test threshold.  0 runs every visible tile exactly (the all-BF16
- *            path, pass 2 only); +inf makes every tile cold (all-FP4 pass 1).
+ *   eps      hot-test threshold.  0 runs every visible tile exactly (the all-exact
+ *            path: pass 2 only, Q K^T in BF16, P.V with P rounded once to FP16
+ *            against an FP16 copy of V, FP32 accumulation); +inf makes every tile
+ *            cold (all-FP4 pass 1).
  *   out      fp32 [B, Hq, Nq, d] (required)
  *   lse      fp32 [B, Hq, Nq], natural-log log-sum-exp of the scaled scores (nullable)
  *   hot_mask uint32 [B, Hkv, ceil(G*Nq/16), ceil(T/32)] with G = Hq/Hkv and
@@ -83,12 +86,14 @@ extern "C" {
  * on every SM, so it starts once the whole GPU is free and holds it while it
  * runs.  If the driver refuses that launch (fewer SMs available to the context
  * than the device has), the call falls back to the separate quantizer kernel.
- * The environment variable APA_PASS1_QUANT_KV=0 selects the separate kernel
- * always.  The results are the same bits either way. */
+ * The results are the same bits either way. */
 int apa_attention(const void* q, const void* k, const void* v, int B, int Hq, int Hkv, int Nq, int Nkv, int d,
                   int causal, float eps, float* out, float* lse, uint32_t* hot_mask, cudaStream_t stream);
 
-/* Bytes of device workspace apa_attention_ws() needs for this problem (0 at eps = 0). */
+/* Bytes of device workspace apa_attention_ws() needs for this problem.  At
+ * eps = 0 that is the FP16 copy of V ([B][Hkv][Nkv][d] FP16, V divided by a
+ * power of two per head only when max |v| > 2^15, so exact for every bf16 value
+ * above the FP16 subnormals) and the heads' maxima of |v|. */
 size_t apa_workspace_bytes(int B, int Hq, int Hkv, int Nq, int Nkv, int d, float eps);
 
 /* apa_attention() with a caller-provided device workspace of at least
@@ -123,6 +128,14 @@ int apa_attention_ws(const void* q, const void* k, const void* v, int B, int Hq,
  *                        lambda stays the plain running sum.  A cold tile then
  *                        moves each output row by at most eps times the mean
  *                        value norm.  Costs 8 bytes of workspace per tile.
+ *   APA_FLAG_ROWSUM_MMA  the tile row sums l_t of pass 1 from one extra MMA of
+ *                        the E2M1 P against an E2M1 ones tile ("Pass 1", step 3
+ *                        on the page), instead of the default: each row's thread
+ *                        sums its own E2M1 codes exactly in registers.  Both are
+ *                        the exact sum of the quantized P; the MMA form runs one
+ *                        128-row block per pass-1 CTA with the separate K/V
+ *                        quantizer.  Not combinable with APA_FLAG_Q_RESIDUAL
+ *                        (APA_ERR_FLAGS): both need the same TMEM columns.
  * `workspace` of at least apa_workspace_bytes_ex() bytes (256-byte aligned), or
  * null to have it allocated stream-ordered for the call. */
 int apa_attention_ex(const void* q, const void* k, const void* v, int B, int Hq, int Hkv, int Nq, int Nkv, int d,
@@ -159,6 +172,18 @@ int apa_attention_paged(const void* q, const void* k_pages, const void* v_pages,
  * serialized by a lock. */
 int apa_attention_host(const void* q, const void* k, const void* v, int B, int Hq, int Hkv, int Nq, int Nkv, int d,
                        int causal, float eps, float* out, float* lse, uint32_t* hot_mask, cudaStream_t stream);
+
+/* Where, inside a caller's workspace, an eps > 0 call of apa_attention_ws() or
+ * apa_attention_ex() (with these flags) leaves the pass-1 NVFP4 operands: byte
+ * offsets of the K/V tile blobs, the Q blobs, the key mean and the FP32 head
+ * scales, in the layouts apa_quantize() writes them.  They hold the call's
+ * operands once the call has completed, until the workspace is used again; that
+ * holds whether the K/V tiles were quantized by the separate kernel or inside
+ * the pass-1 launch.  A measurement and testing aid, not needed to use the
+ * library.  Returns APA_OK; APA_ERR_EPS for eps <= 0 (the all-exact path
+ * quantizes nothing), or the argument errors of apa_attention_ex(). */
+int apa_workspace_operands(int B, int Hq, int Hkv, int Nq, int Nkv, int d, float eps, unsigned flags,
+                           size_t* kv_blob, size_t* q_blob, size_t* mu, size_t* s_q, size_t* s_k, size_t* s_v);
 
 /* The pass-1 NVFP4 operands on their own (blog, "Pass 1" and "Mean-centred K"):
  *   kv_blob  uint8 [B*Hkv][T][apa_kv_blob_bytes / (B*Hkv*T)]: per 64-key tile the

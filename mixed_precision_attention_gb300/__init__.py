@@ -18,13 +18,15 @@ import ctypes
 from . import _lib
 from ._lib import ApaError, status_string
 
-__all__ = ["attention", "attention_paged", "attention_host", "quantize", "quantize_noalloc", "workspace_bytes", "check_error", "ApaError",
+__all__ = ["attention", "attention_paged", "attention_host", "quantize", "quantize_noalloc", "workspace_bytes",
+           "workspace_operands", "check_error", "ApaError",
            "status_string", "hot_mask_shape", "TILE", "GROUP_ROWS", "BLOCK_ROWS", "FLAG_Q_RESIDUAL",
-           "FLAG_LSE_SCALES", "FLAG_VALUE_WEIGHTED"]
+           "FLAG_LSE_SCALES", "FLAG_VALUE_WEIGHTED", "FLAG_ROWSUM_MMA"]
 
 FLAG_Q_RESIDUAL = 1  # APA_FLAG_Q_RESIDUAL: Q as two FP4 terms in pass 1
 FLAG_LSE_SCALES = 2  # APA_FLAG_LSE_SCALES: least-squared-error block scales for Q, K, V
 FLAG_VALUE_WEIGHTED = 4  # APA_FLAG_VALUE_WEIGHTED: hot test weighted by value norm
+FLAG_ROWSUM_MMA = 8  # APA_FLAG_ROWSUM_MMA: pass-1 row sums from an MMA against an E2M1 ones tile
 TILE = 64          # keys per tile
 GROUP_ROWS = 16    # rows per hot-test group
 BLOCK_ROWS = 128   # GQA-packed rows per CTA
@@ -61,9 +63,9 @@ def _check_qkv(q, k, v):
     return B, Hq, k.shape[1], Nq, k.shape[2], d
 
 
-def _flags(q_residual=False, lse_scales=False, value_weighted=False):
+def _flags(q_residual=False, lse_scales=False, value_weighted=False, rowsum_mma=False):
     return ((FLAG_Q_RESIDUAL if q_residual else 0) | (FLAG_LSE_SCALES if lse_scales else 0)
-            | (FLAG_VALUE_WEIGHTED if value_weighted else 0))
+            | (FLAG_VALUE_WEIGHTED if value_weighted else 0) | (FLAG_ROWSUM_MMA if rowsum_mma else 0))
 
 
 def workspace_bytes(B, Hq, Hkv, Nq, Nkv, d, eps, q_residual: bool = False, value_weighted: bool = False):
@@ -71,9 +73,23 @@ def workspace_bytes(B, Hq, Hkv, Nq, Nkv, d, eps, q_residual: bool = False, value
     return int(_lib.load().apa_workspace_bytes_ex(B, Hq, Hkv, Nq, Nkv, d, float(eps), flags))
 
 
+def workspace_operands(B, Hq, Hkv, Nq, Nkv, d, eps, q_residual: bool = False, value_weighted: bool = False,
+                       rowsum_mma: bool = False):
+    """apa_workspace_operands: byte offsets, inside the workspace of an eps > 0
+    call with these options, of the pass-1 operands the call leaves there.
+    Returns dict(kv_blob, q_blob, mu, s_q, s_k, s_v) of offsets."""
+    lib = _lib.load()
+    offs = [ctypes.c_size_t() for _ in range(6)]
+    st = lib.apa_workspace_operands(B, Hq, Hkv, Nq, Nkv, d, float(eps),
+                                    _flags(q_residual, value_weighted=value_weighted, rowsum_mma=rowsum_mma),
+                                    *[ctypes.byref(o) for o in offs])
+    _lib.check(st, "apa_workspace_operands")
+    return dict(zip(("kv_blob", "q_blob", "mu", "s_q", "s_k", "s_v"), (o.value for o in offs)))
+
+
 def attention(q, k, v, causal: bool = True, eps: float = 0.005, return_hot_mask: bool = False,
               return_lse: bool = True, workspace=None, q_residual: bool = False, lse_scales: bool = False,
-              value_weighted: bool = False):
+              value_weighted: bool = False, rowsum_mma: bool = False):
     """Adaptive-precision attention.
 
     q: [B, Hq, Nq, d] bf16; k, v: [B, Hkv, Nkv, d] bf16 (CUDA, contiguous).
@@ -86,6 +102,7 @@ def attention(q, k, v, causal: bool = True, eps: float = 0.005, return_hot_mask:
     q_residual: Q as two FP4 terms in pass 1 (apa_attention_ex, APA_FLAG_Q_RESIDUAL).
     lse_scales: least-squared-error block scales for Q, K, V (APA_FLAG_LSE_SCALES).
     value_weighted: hot test weighted by the tile's value norm (APA_FLAG_VALUE_WEIGHTED).
+    rowsum_mma: pass-1 tile row sums from an MMA against an E2M1 ones tile (APA_FLAG_ROWSUM_MMA).
     """
     import torch
     lib = _lib.load()
@@ -98,7 +115,7 @@ def attention(q, k, v, causal: bool = True, eps: float = 0.005, return_hot_mask:
     if workspace is None and need:
         workspace = torch.empty(need, dtype=torch.uint8, device=dev)
     nbytes = 0 if workspace is None else workspace.numel()
-    flags = _flags(q_residual, lse_scales, value_weighted)
+    flags = _flags(q_residual, lse_scales, value_weighted, rowsum_mma)
     if flags:
         st = lib.apa_attention_ex(_ptr(q), _ptr(k), _ptr(v), B, Hq, Hkv, Nq, Nkv, d, int(bool(causal)), float(eps),
                                   flags, _ptr(out), _ptr(lse), _ptr(mask), _ptr(workspace),

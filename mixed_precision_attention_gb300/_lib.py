@@ -26,6 +26,7 @@ _SIGS = {
     "apa_workspace_bytes": (SZ, [I, I, I, I, I, I, F]),
     "apa_attention_ex": (I, [P, P, P, I, I, I, I, I, I, I, F, ctypes.c_uint, P, P, P, P, SZ, P]),
     "apa_workspace_bytes_ex": (SZ, [I, I, I, I, I, I, F, ctypes.c_uint]),
+    "apa_workspace_operands": (I, [I, I, I, I, I, I, F, ctypes.c_uint, P, P, P, P, P, P]),
     "apa_quantize_ex": (I, [P, P, P, I, I, I, I, I, I, ctypes.c_uint, P, P, P, P, P, P, P, P]),
     "apa_quantize": (I, [P, P, P, I, I, I, I, I, I, P, P, P, P, P, P, P]),
     "apa_quantize_noalloc": (I, [P, P, P, I, I, I, I, I, I, P, P, P, P, P, P, P]),

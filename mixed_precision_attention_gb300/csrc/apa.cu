@@ -22,7 +22,8 @@ namespace {
 __device__ int g_device_error;  // set by bounded waits that gave up
 
 constexpr size_t kAlign = 256;
-constexpr unsigned kKnownFlags = APA_FLAG_Q_RESIDUAL | APA_FLAG_LSE_SCALES | APA_FLAG_VALUE_WEIGHTED;
+constexpr unsigned kKnownFlags =
+    APA_FLAG_Q_RESIDUAL | APA_FLAG_LSE_SCALES | APA_FLAG_VALUE_WEIGHTED | APA_FLAG_ROWSUM_MMA;
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 __global__ void visible_mask_kernel(Shape s, uint32_t* mask) {
@@ -126,10 +127,6 @@ int* device_error_word() {
 
 size_t workspace_layout(const Shape& s, bool apa_mode, Workspace* ws, void* base, unsigned flags) {
   Workspace w{};
-  if (!apa_mode) {
-    if (ws) *ws = w;
-    return 0;
-  }
   const size_t BH = s.BH(), T = s.T(), d = s.d, nblk = s.nblk(), BHq = (size_t)s.B * s.Hq;
   size_t off = 0;
   uint8_t* b = static_cast<uint8_t*>(base);
@@ -138,6 +135,12 @@ size_t workspace_layout(const Shape& s, bool apa_mode, Workspace* ws, void* base
     off += align_up(bytes);
     return p;
   };
+  if (!apa_mode) {  // the all-exact path: the FP16 copy of V for its P.V product
+    w.vamax = (uint32_t*)take(BH * 4);
+    w.v16 = (uint16_t*)take(BH * s.Nkv * d * 2);
+    if (ws) *ws = w;
+    return off;
+  }
   w.ksum = (float*)take(BH * T * d * 4);
   w.kmin = (uint32_t*)take(BH * d * 4);
   w.kmax = (uint32_t*)take(BH * d * 4);
@@ -203,16 +206,19 @@ static int run_attention(const Shape& s, const void* q, const void* k, const voi
   auto stage = [&](int slot) {
     if (call != SIZE_MAX) cudaEventRecord(g_timing.ev[call * 4 + slot], stream);
   };
+  Workspace ws;
   if (eps == 0.f) {
+    // all exact: the FP16 copy of V, then pass 2 over every visible tile
+    workspace_layout(s, false, &ws, workspace, flags);
     stage(0);
+    if (launch_v16(s, v, ws, stream) != cudaSuccess) return APA_ERR_CUDA;
     stage(1);
     if (hot_mask && launch_visible_mask(s, hot_mask, stream) != cudaSuccess) return APA_ERR_CUDA;
     stage(2);
-    const int st = launch_pass2(s, q, k, v, nullptr, out, lse, stream) == cudaSuccess ? APA_OK : APA_ERR_CUDA;
+    const int st = launch_pass2(s, q, k, v, &ws, out, lse, stream) == cudaSuccess ? APA_OK : APA_ERR_CUDA;
     stage(3);
     return st;
   }
-  Workspace ws;
   workspace_layout(s, true, &ws, workspace, flags);
   stage(0);
   if (hot_mask) {
@@ -224,19 +230,21 @@ static int run_attention(const Shape& s, const void* q, const void* k, const voi
   // The least-squared-error scales cost about three times the quantizer work, more
   // than those SMs keep up with, so that option keeps the quantizer kernel.
   const bool lse_scales = (flags & APA_FLAG_LSE_SCALES) != 0, wide = wide_pass1 || ws.q2_blob;
-  const bool kv_in_pass1 = kv_in_pass1_ok && !lse_scales && pass1_quantizes_kv(s, wide_pass1, ws.q2_blob != nullptr);
+  const bool rowsum_mma = (flags & APA_FLAG_ROWSUM_MMA) != 0;
+  const bool kv_in_pass1 =
+      kv_in_pass1_ok && !lse_scales && pass1_quantizes_kv(s, wide_pass1, ws.q2_blob != nullptr, rowsum_mma);
   if (launch_quantize(s, q, k, v, ws, true, true, stream, lse_scales, kv_in_pass1) != cudaSuccess)
     return APA_ERR_CUDA;
   stage(1);
   const KvSource src{k, v, lse_scales};
-  cudaError_t e1 = launch_pass1(s, ws, eps, hot_mask, wide, stream, kv_in_pass1 ? &src : nullptr);
+  cudaError_t e1 = launch_pass1(s, ws, eps, hot_mask, wide, stream, kv_in_pass1 ? &src : nullptr, rowsum_mma);
   if (kv_in_pass1 && e1 == cudaErrorCooperativeLaunchTooLarge) {
     // fewer SMs than the device reports are ours (a partitioned or shared GPU):
     // quantize K/V with the separate kernel (recomputing the same statistics) and
     // run pass 1 on its own
     (void)cudaGetLastError();
     if (launch_quantize(s, q, k, v, ws, false, true, stream, lse_scales) != cudaSuccess) return APA_ERR_CUDA;
-    e1 = launch_pass1(s, ws, eps, hot_mask, wide, stream);
+    e1 = launch_pass1(s, ws, eps, hot_mask, wide, stream, nullptr, rowsum_mma);
   }
   if (e1 != cudaSuccess) return APA_ERR_CUDA;
   if (launch_pass2_order(s, ws, stream) != cudaSuccess) return APA_ERR_CUDA;
@@ -315,6 +323,8 @@ int apa_attention_ex(const void* q, const void* k, const void* v, int B, int Hq,
   int st = apa::validate(q, k, v, out, B, Hq, Hkv, Nq, Nkv, d, causal, eps, true);
   if (st) return st;
   if (flags & ~apa::kKnownFlags) return APA_ERR_FLAGS;
+  // the ones-MMA row sums and the residual Q term both need the same TMEM columns
+  if ((flags & APA_FLAG_ROWSUM_MMA) && (flags & APA_FLAG_Q_RESIDUAL)) return APA_ERR_FLAGS;
   Shape s{B, Hq, Hkv, Nq, Nkv, d, causal ? 1 : 0};
   const size_t need = apa::workspace_layout(s, eps != 0.f, nullptr, nullptr, flags);
   void* ws = workspace;
@@ -393,6 +403,26 @@ int apa_attention_host(const void* q, const void* k, const void* v, int B, int H
       if (st == APA_OK) st = APA_ERR_CUDA;
   if (cudaStreamSynchronize(stream) != cudaSuccess && st == APA_OK) st = APA_ERR_CUDA;
   return st;
+}
+
+int apa_workspace_operands(int B, int Hq, int Hkv, int Nq, int Nkv, int d, float eps, unsigned flags,
+                           size_t* kv_blob, size_t* q_blob, size_t* mu, size_t* s_q, size_t* s_k, size_t* s_v) {
+  if (!kv_blob || !q_blob || !mu || !s_q || !s_k || !s_v) return APA_ERR_NULL;
+  if (B < 1 || Hq < 1 || Hkv < 1 || Nq < 1 || Nkv < 1 || Hq % Hkv) return APA_ERR_SHAPE;
+  if (d != 64 && d != 128 && d != 256) return APA_ERR_HEAD_DIM;
+  if (std::isnan(eps) || eps <= 0.f) return APA_ERR_EPS;  // the all-exact path quantizes nothing
+  if (flags & ~apa::kKnownFlags) return APA_ERR_FLAGS;
+  Shape s{B, Hq, Hkv, Nq, Nkv, d, 1};
+  apa::Workspace w;
+  apa::workspace_layout(s, true, &w, reinterpret_cast<void*>(uintptr_t(4096)), flags);
+  auto off = [](const void* p) { return (size_t)(reinterpret_cast<uintptr_t>(p) - 4096); };
+  *kv_blob = off(w.kv_blob);
+  *q_blob = off(w.q_blob);
+  *mu = off(w.mu);
+  *s_q = off(w.s_q);
+  *s_k = off(w.s_k);
+  *s_v = off(w.s_v);
+  return APA_OK;
 }
 
 size_t apa_kv_blob_bytes(int B, int Hkv, int Nkv, int d) {
@@ -497,7 +527,7 @@ const char* apa_status_string(int status) {
     case APA_OK: return "ok";
     case APA_ERR_NULL: return "a required pointer is null";
     case APA_ERR_SHAPE: return "invalid shape (B, Hq, Hkv, Nq, Nkv; Hq % Hkv; causal needs Nkv >= Nq)";
-    case APA_ERR_EPS: return "eps must be >= 0 and not NaN";
+    case APA_ERR_EPS: return "eps must be >= 0 and not NaN (> 0 where pass-1 operands are asked for)";
     case APA_ERR_HEAD_DIM: return "head dimension must be 64, 128 or 256";
     case APA_ERR_CUDA: return "CUDA error (see cudaGetLastError)";
     case APA_ERR_NOMEM: return "workspace allocation failed or workspace too small";

@@ -100,6 +100,7 @@ struct Workspace {
   uint32_t* hot_count;// [BH*nblk]
   uint32_t* p2_order; // [BH*nblk]: pass-2 work items (bh * nblk + blk), longest hot list first
 };
+// apa_mode false (eps = 0): only the FP16 copy of V and the head maxima of V.
 // flags: APA_FLAG_* of apa.h (APA_FLAG_Q_RESIDUAL adds the residual Q blob)
 size_t workspace_layout(const Shape& s, bool apa_mode, Workspace* ws, void* base, unsigned flags = 0);
 
@@ -157,15 +158,19 @@ struct KvSource {
 };
 // Whether the pass-1 launch for this problem can quantize the K/V tiles itself
 // (the three-block kernel, with at least 8 SMs left over for the quantizer).
-bool pass1_quantizes_kv(const Shape& s, bool wide, bool q_residual);
+bool pass1_quantizes_kv(const Shape& s, bool wide, bool q_residual, bool rowsum_mma);
 // wide: one 128-row block per CTA (three times the CTAs, each on its own SM when
 // the GPU is otherwise idle, so a single problem finishes sooner) instead of
 // three blocks of one KV head per CTA (the faster choice for a full GPU).
 // kv: quantize the K/V tiles inside this launch (pass1_quantizes_kv must hold).
+// rowsum_mma: tile row sums from an MMA against an E2M1 ones tile (APA_FLAG_ROWSUM_MMA).
 cudaError_t launch_pass1(const Shape& s, const Workspace& ws, float eps, uint32_t* hot_mask, bool wide,
-                         cudaStream_t st, const KvSource* kv = nullptr);
+                         cudaStream_t st, const KvSource* kv = nullptr, bool rowsum_mma = false);
 cudaError_t launch_pass2(const Shape& s, const void* q, const void* k, const void* v, const Workspace* ws,
                          float* out, float* lse, cudaStream_t st);
+// The all-exact path's FP16 copy of V (ws.v16, with the head maxima in ws.vamax):
+// V divided by v16_scale(max |v|) per head, the copy the quantizer writes in APA mode.
+cudaError_t launch_v16(const Shape& s, const void* v, const Workspace& ws, cudaStream_t st);
 cudaError_t launch_visible_mask(const Shape& s, uint32_t* hot_mask, cudaStream_t st);
 cudaError_t launch_pass2_order(const Shape& s, const Workspace& ws, cudaStream_t st);
 

@@ -5,7 +5,10 @@
 //   1. S = Q K^T on the FP4 tensor cores, causal mask applied;
 //   2. P directly in FP4: each 16-key group gets its own scale, folded into
 //      the exponent bias, so ex2 produces the quantized P;
-//   3. row sums l_t from the same P, via one extra MMA against an E2M1 ones tile;
+//   3. row sums l_t of the same quantized P: by default each row's thread sums
+//      its own E2M1 codes exactly in registers (a byte-permute table and dp4a);
+//      with APA_FLAG_ROWSUM_MMA by one extra MMA against an E2M1 ones tile, the
+//      blog's form.  Both give the exact sum of the quantized P;
 //   4. the hot test: if any of the group's 16 rows has l_t > eps * lambda, the
 //      tile is hot: set the mask bit, skip the PV product for the group (with the
 //      value-weighted option the test is w_t * l_t > eps * lambda, w_t the tile's
@@ -18,25 +21,22 @@
 // hunt") clamped at 2^-6 ("The bug").  lambda is the running FP4 sum over every
 // tile judged so far, hot ones included ("Cold verdicts are safe").
 //
-// GB300 design: one CTA = one 128-row block of GQA-packed rows of one KV head.
-//   warps 0-3  one thread per row (TMEM lane = row): group maxima, frame, P
-//              encode (ex2 + cvt.e2m1x2), P to shared memory, P scales to TMEM
-//              (tcgen05.st), hot vote (ballot over the 16 lanes of a group),
-//              frame / lambda / l commit, O rescale when the frame moves;
-//   warp 4     bulk-copy producer: the Q blob, then one 72*d-byte NVFP4 blob per
-//              tile (K codes, V^T codes and both scale sets) into a 4-stage ring;
-//   warp 5     TMEM owner and MMA issuer (tcgen05.mma kind::mxf4nvf4,
-//              scale_vec::4X): S (M128 N64), ones (M128 N16), PV (M128 N=d), the
-//              scale copies (tcgen05.cp), and the block's hot-tile list.
-// Software pipelining: the P encoding of tile t+1 depends on the verdict of
-// tile t only through the frame, and only when tile t lifts it (c > m + tau);
-// otherwise m and the lambda update are the same whether t is hot or cold.  So
-// while the ones-MMA of tile t is in flight the softmax warps already encode
-// tile t+1, and judge tile t afterwards; a warp whose rows lifted the frame at
-// tile t judges it first.  The issuer runs S(t+2), PV(t), ones(t+1) in that order.
-// At d <= 128 a CTA holds 256 TMEM columns and ~55 KB of shared memory, so two
-// CTAs share an SM.  (Two threads per row, swapping group maxima, was measured
-// slower: the per-warp waits and exchanges outweighed the halved encode.)
+// Two kernels, one thread per row (TMEM lane = row) in both:
+//   pass1_multi_kernel<D, U>  (the default at d <= 128): U = 3 blocks of 128
+//              GQA-packed rows of one KV head per CTA, one CTA per SM.  TMEM holds
+//              the three O accumulators and one S buffer the units take in turn.
+//              Warps: 4 per unit (softmax), a bulk-copy producer, an S issuer and
+//              a PV issuer that also writes the hot lists (see its own comment).
+//   pass1_kernel<D, kOnesMma>  one block per CTA: d = 256, the residual-Q option,
+//              the ones-MMA row sums, and the "wide" form of the host entry point.
+//              Warps 0-3 softmax; warp 4 the bulk-copy producer (the Q blob, then
+//              one 72*d-byte NVFP4 blob per tile into a 4-stage ring); warp 5 the
+//              TMEM owner and MMA issuer (S, ones, PV, the scale copies, hot list).
+//              With the ones-MMA row sums the softmax warps encode tile t+1 while
+//              the row sums of tile t are in flight, and judge tile t afterwards
+//              (tile t+1's P depends on tile t's verdict only through the frame,
+//              and only when tile t lifts it); a warp whose rows lifted the frame
+//              at tile t judges it first.  The issuer runs S(t+2), PV(t), ones(t+1).
 //
 // K/V quantization inside the launch ("What else is in the box": the next
 // segment is quantized inside the launch).  When the pass-1 CTAs leave at least
@@ -44,8 +44,6 @@
 // every SM; the CTAs past the pass-1 ones run the K/V quantizer (quant_role in
 // quant_tile.cuh), which publishes a flag per tile in pass 1's visiting order,
 // and the producer waits (bounded) for a tile's flag before loading its blob.
-#include <cstdlib>
-#include <cstring>
 
 #include "apa_internal.h"
 #include "quant_tile.cuh"
@@ -1293,43 +1291,17 @@ cudaError_t launch_dv(const P1Params& prm, cudaStream_t st) {
   return cudaLaunchKernelEx(&cfg, pass1_kernel<D, kOnesMma>, prm2);
 }
 
-// APA_PASS1_ROWSUM=mma selects the ones-MMA row sums (for comparison); the
-// default sums each row's quantized P in registers.
-bool rowsum_by_mma() {
-  static const bool v = [] {
-    const char* e = getenv("APA_PASS1_ROWSUM");
-    return e && strcmp(e, "mma") == 0;
-  }();
-  return v;
-}
-
-// APA_PASS1_UNITS=1 selects the one-block-per-CTA kernel at d <= 128 (for comparison).
-bool single_unit() {
-  static const bool v = [] {
-    const char* e = getenv("APA_PASS1_UNITS");
-    return e && strcmp(e, "1") == 0;
-  }();
-  return v;
-}
-
+// rowsum_mma: the ones-MMA row sums (one-block kernel); the default sums each
+// row's quantized P in registers.
 template <int D>
-cudaError_t launch_d(const P1Params& prm, bool wide, cudaStream_t st) {
+cudaError_t launch_d(const P1Params& prm, bool wide, bool rowsum_mma, cudaStream_t st) {
   // the residual Q term lives in the one-block kernel with register row sums
   if (prm.q2_blob) return launch_dv<D, false>(prm, st);
-  if (rowsum_by_mma()) return launch_dv<D, true>(prm, st);
+  if (rowsum_mma) return launch_dv<D, true>(prm, st);
   if constexpr (D <= 128) {
-    if (!wide && !single_unit()) return launch_multi<D, 3>(prm, st);
+    if (!wide) return launch_multi<D, 3>(prm, st);
   }
   return launch_dv<D, false>(prm, st);
-}
-
-// APA_PASS1_QUANT_KV=0 keeps the K/V quantization in its own kernel (for comparison).
-bool kv_in_pass1_allowed() {
-  static const bool v = [] {
-    const char* e = getenv("APA_PASS1_QUANT_KV");
-    return !(e && strcmp(e, "0") == 0);
-  }();
-  return v;
 }
 
 template <int D>
@@ -1368,12 +1340,11 @@ bool multi_quantizes_kv(const Shape& s) {
 
 }  // namespace
 
-bool pass1_quantizes_kv(const Shape& s, bool wide, bool q_residual) {
+bool pass1_quantizes_kv(const Shape& s, bool wide, bool q_residual, bool rowsum_mma) {
   // the same choice of kernel as launch_d; the wide form shares the GPU and the
   // ones-MMA form has no room, so neither hosts the quantizer
-  if (wide || !kv_in_pass1_allowed()) return false;
-  if (!q_residual && rowsum_by_mma()) return false;
-  const bool one_block = q_residual || single_unit() || s.d > 128;
+  if (wide || rowsum_mma) return false;
+  const bool one_block = q_residual || s.d > 128;
   switch (s.d) {
     case 64: return one_block ? single_quantizes_kv<64>(s) : multi_quantizes_kv<64>(s);
     case 128: return one_block ? single_quantizes_kv<128>(s) : multi_quantizes_kv<128>(s);
@@ -1383,7 +1354,7 @@ bool pass1_quantizes_kv(const Shape& s, bool wide, bool q_residual) {
 }
 
 cudaError_t launch_pass1(const Shape& s, const Workspace& ws, float eps, uint32_t* hot_mask, bool wide, cudaStream_t st,
-                         const KvSource* kv) {
+                         const KvSource* kv, bool rowsum_mma) {
   P1Params prm{};
   prm.s = s;
   prm.kv_blob = ws.kv_blob;
@@ -1408,9 +1379,9 @@ cudaError_t launch_pass1(const Shape& s, const Workspace& ws, float eps, uint32_
   }
   prm.err = device_error_word();
   switch (s.d) {
-    case 64: return launch_d<64>(prm, wide, st);
-    case 128: return launch_d<128>(prm, wide, st);
-    case 256: return launch_d<256>(prm, wide, st);
+    case 64: return launch_d<64>(prm, wide, rowsum_mma, st);
+    case 128: return launch_d<128>(prm, wide, rowsum_mma, st);
+    case 256: return launch_d<256>(prm, wide, rowsum_mma, st);
   }
   return cudaErrorInvalidValue;
 }

@@ -9,8 +9,8 @@
 // same per-channel key mean as pass 1 (q.k - q.mu), so both states share one
 // frame; the natural-log LSE adds q.mu/sqrt(d) back.
 //
-// With eps = 0 the same kernel is the all-exact path: every visible tile of the
-// block, no pass-1 state, uncentred logits.
+// With eps = 0 the same kernels are the all-exact path: every visible tile of
+// the block, no pass-1 state, uncentred logits.
 //
 // GB300 design: one CTA = one 128-row block of GQA-packed rows of one KV head
 // (tcgen05 M = 128), 7 warps:
@@ -23,17 +23,16 @@
 // A tcgen05.mma takes tens of cycles to issue, and one tile needs d/16 of them
 // for S and 4 (or 8) for PV: issued by one thread, they set the tile period.
 // The running max moves lazily (only when a score exceeds it by more than 8 in
-// log2 units), so O in TMEM is rarely rescaled.  In APA mode P goes to the tensor
-// cores as one FP16 term against the quantizer's FP16 copy of V (V divided by a
-// power of two per head); in the all-exact mode (eps = 0: no quantizer, no FP16
-// copy) as two BF16 terms, P = P_hi + P_lo (P_lo the BF16 rounding of the
-// residual), against V itself, so the PV product and the row sum carry ~16
-// mantissa bits of P instead of 8.
-// K, and V in the all-exact mode, may come from a paged pool through a block
-// table: the tensor maps then span the pool, and the rows past Nkv of the last
-// page are zeroed in shared memory before any MMA reads them.
+// log2 units), so O in TMEM is rarely rescaled.  P goes to the tensor cores as
+// one FP16 term (relative rounding error at most 2^-11) against an FP16 copy of
+// V (V divided by a power of two per head, exact for every bf16 value above the
+// FP16 subnormals), which the quantizer writes in APA mode and a conversion
+// pass writes in the all-exact mode.
+// K may come from a paged pool through a block table: its tensor map then spans
+// the pool, and the rows past Nkv of the last page are zeroed in shared memory
+// before any MMA reads them.
 //
-// In APA mode at d <= 128 a second kernel (pass2_dual_kernel) runs instead: two
+// At d <= 128 a second kernel (pass2_dual_kernel) runs instead: two
 // softmax warp groups per block take alternate entries of the hot list, each
 // with its own (m, l), its own O in TMEM and its own double-buffered S, so one
 // group's exp/convert/store of P overlaps the other's S and PV MMAs.  13 warps:
@@ -43,7 +42,6 @@
 // the same as the one-group kernel's; only the tile-to-accumulator assignment
 // (and so the rounding order of the merge) differs.
 #include <cstring>
-#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
 #include "apa_internal.h"
@@ -74,30 +72,26 @@ constexpr int kThreads = 224;
 #endif
 constexpr float kTau2 = 8.0f;  // pass-2 lazy rescale threshold (log2 units)
 
-// kF16: P as one FP16 term against the FP16 copy of V; else P = P_hi + P_lo in
-// BF16 against V itself.
-//
 // The barriers live at the end of the dynamic shared-memory window and there is
 // no static shared memory.  With kCtasPerSm = 2 (2 K/V stages, one P buffer,
 // 112 KB per CTA at d = 128) two CTAs would fit an SM with no alignment slack;
 // the kernel then checks that the window starts on a 1024-byte boundary (the
 // 128-byte swizzle needs it).  Measured on the 2048 x 122880 layer, two CTAs of
 // that shape were no faster than one CTA with 3 stages and 2 P buffers.
-template <int D, bool kF16>
+template <int D>
 struct P2Cfg {
   static constexpr int kCtasPerSm = 1;
-  static constexpr int NS = kCtasPerSm == 2 ? 2 : (D >= 256 ? 2 : (kF16 && D == 128 ? APA_P2_STAGES_D128 : 3));
+  static constexpr int NS = kCtasPerSm == 2 ? 2 : (D >= 256 ? 2 : (D == 128 ? APA_P2_STAGES_D128 : 3));
   static constexpr int kAtoms = D / 64;
   static constexpr int kQBytes = 128 * D * 2;
   static constexpr int kKVBytes = 64 * D * 2;  // one of K or V per stage
   static constexpr int kPBytes = 128 * 64 * 2;  // one 16-bit term of P
-  static constexpr int kPTerms = kF16 ? 1 : 2;
-  static constexpr int NP = kCtasPerSm == 2 ? 1 : (D >= 256 ? 1 : 2);  // P buffers (kPTerms terms each)
+  static constexpr int NP = kCtasPerSm == 2 ? 1 : (D >= 256 ? 1 : 2);  // P buffers
   static constexpr int kQOff = 0;
   static constexpr int kStageOff = kQBytes;
   static constexpr int kPOff = kStageOff + NS * 2 * kKVBytes;
   static constexpr int kNumBars = 2 * NS + 10;
-  static constexpr int kBarOff = kPOff + NP * kPTerms * kPBytes;
+  static constexpr int kBarOff = kPOff + NP * kPBytes;
   static constexpr int kSlack = kCtasPerSm == 2 ? 0 : 1024;  // runtime alignment room
   static constexpr int kSmem = kBarOff + kNumBars * 8 + 16 + kSlack;
   static constexpr uint32_t kTmemCols = D + 128 <= 256 ? 256 : 512;
@@ -163,10 +157,10 @@ __device__ __forceinline__ void p8_f16(const float* x, float c2, float nb, uint3
         "f"(1.f));
 }
 
-template <int D, bool kF16>
-__global__ void __launch_bounds__(kThreads, P2Cfg<D, kF16>::kCtasPerSm)
+template <int D>
+__global__ void __launch_bounds__(kThreads, P2Cfg<D>::kCtasPerSm)
     pass2_kernel(const P2Params p, const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap) {
-  using C = P2Cfg<D, kF16>;
+  using C = P2Cfg<D>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   if (C::kSlack == 0 && smem != smem_raw) {  // no room to realign: refuse loudly
@@ -286,14 +280,11 @@ __global__ void __launch_bounds__(kThreads, P2Cfg<D, kF16>::kCtasPerSm)
         const int t = tile_of(i, gm);
         // contiguous maps: (channel, key, b * Hkv + h); paged maps: (channel, key in
         // page, page * Hkv + h).  The FP16 copy of V is contiguous in either case.
-        int ky = t * kTile, kz = bh, vy = ky, vz = bh;
+        int ky = t * kTile, kz = bh;
+        const int vy = ky, vz = bh;
         if (s.pages) {
           ky = 0;
           kz = kv_page(s, b, t, p.err) * s.Hkv + h;
-          if (!kF16) {
-            vy = 0;
-            vz = kz;
-          }
         }
         mbar_arrive_expect_tx(kv_full(st), 2 * C::kKVBytes);
         const uint32_t kdst = sbase + C::kStageOff + st * 2 * C::kKVBytes;
@@ -319,16 +310,14 @@ __global__ void __launch_bounds__(kThreads, P2Cfg<D, kF16>::kCtasPerSm)
         if (s.pages && (s.Nkv % kTile) != 0 && tile_of(i, gm_unused) == T - 1) {
           // paged pool: the keys past Nkv in a sequence's last page hold whatever the
           // pool holds there (possibly NaN or Inf).  Masked scores and a zero P do not
-          // keep those out of an MMA, so the rows are zeroed here, before any MMA
-          // reads this stage: K always, V when it comes from the pool too.
+          // keep those out of an MMA, so the K rows are zeroed here, before any MMA
+          // reads this stage (V comes from the contiguous FP16 copy).
           const int nk = s.Nkv - (T - 1) * kTile, rows = kTile - nk;
           uint8_t* kst = smem + C::kStageOff + st * 2 * C::kKVBytes;
-          for (int part = 0; part < (kF16 ? 1 : 2); ++part)
-            for (int x = 0; x < rows * C::kAtoms * 8; ++x) {
-              const int rest = x >> 3, rr = nk + rest % rows, atom = rest / rows;
-              *reinterpret_cast<uint4*>(kst + part * C::kKVBytes + atom * 8192 + rr * 128 + (x & 7) * 16) =
-                  make_uint4(0u, 0u, 0u, 0u);
-            }
+          for (int x = 0; x < rows * C::kAtoms * 8; ++x) {
+            const int rest = x >> 3, rr = nk + rest % rows, atom = rest / rows;
+            *reinterpret_cast<uint4*>(kst + atom * 8192 + rr * 128 + (x & 7) * 16) = make_uint4(0u, 0u, 0u, 0u);
+          }
           fence_proxy_async_smem();
         }
         if (i >= 2 && !mbar_wait(s_free(i & 1), ((i >> 1) - 1) & 1, &abort_flag, p.err)) return false;
@@ -353,21 +342,19 @@ __global__ void __launch_bounds__(kThreads, P2Cfg<D, kF16>::kCtasPerSm)
   } else if (warp == 6) {
     // ------------------------------------------------------------ PV issuer
     if (lane == 0 && n > 0) {
-      const uint32_t idO = kF16 ? idesc_f16(128, D, 1) : idesc_bf16(128, D, 1);
+      const uint32_t idO = idesc_f16(128, D, 1);
       bool ok = true;
       for (int i = 0; ok && i < n; ++i) {
         if (!(ok = mbar_wait(p_full(i & 1), (i >> 1) & 1, &abort_flag, p.err))) break;
         if (!(ok = mbar_wait(kv_full(i % C::NS), (i / C::NS) & 1, &abort_flag, p.err))) break;
         tc_fence_after();
         const uint32_t vaddr = sbase + C::kStageOff + (i % C::NS) * 2 * C::kKVBytes + C::kKVBytes;
-        const uint32_t paddr = sbase + C::kPOff + (i % C::NP) * C::kPTerms * C::kPBytes;
+        const uint32_t paddr = sbase + C::kPOff + (i % C::NP) * C::kPBytes;
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
           const uint64_t bd = smem_desc(vaddr + kk * 2048, 8192, 1024, kSwizzle128B);
           mma_bf16(tmem + C::kOCol, smem_desc(paddr + kk * 32, 16, 1024, kSwizzle128B), bd, idO,
                    (i > 0 || kk > 0) ? 1u : 0u);
-          if (!kF16)
-            mma_bf16(tmem + C::kOCol, smem_desc(paddr + C::kPBytes + kk * 32, 16, 1024, kSwizzle128B), bd, idO, 1u);
         }
         mma_commit(pv_done(i & 1));
         mma_commit(kv_empty(i % C::NS));  // this stage's V has been read
@@ -399,12 +386,11 @@ __global__ void __launch_bounds__(kThreads, P2Cfg<D, kF16>::kCtasPerSm)
         __syncwarp();
         if (lane == 0) mbar_arrive(s_free(i & 1));
         if (i >= C::NP && !(ok = warp_wait(pv_done((i - C::NP) & 1), ((i - C::NP) >> 1) & 1))) break;
-        uint8_t* prow = smem + C::kPOff + (i % C::NP) * C::kPTerms * C::kPBytes + r * 128;
+        uint8_t* prow = smem + C::kPOff + (i % C::NP) * C::kPBytes + r * 128;
 #pragma unroll
         for (int ch = 0; ch < 8; ++ch) {
           const int sw = (ch ^ (r & 7)) << 4;  // same swizzled order as the computed rows: no bank conflicts
           *reinterpret_cast<uint4*>(prow + sw) = make_uint4(0u, 0u, 0u, 0u);
-          if (!kF16) *reinterpret_cast<uint4*>(prow + C::kPBytes + sw) = make_uint4(0u, 0u, 0u, 0u);
         }
         fence_proxy_async_smem();
         __syncwarp();
@@ -451,37 +437,18 @@ __global__ void __launch_bounds__(kThreads, P2Cfg<D, kF16>::kCtasPerSm)
       }
       // this P buffer is free once PV(i - NP) has completed
       if (i >= C::NP && !(ok = warp_wait(pv_done((i - C::NP) & 1), ((i - C::NP) >> 1) & 1))) break;
-      uint8_t* prow = smem + C::kPOff + (i % C::NP) * C::kPTerms * C::kPBytes + r * 128;
+      uint8_t* prow = smem + C::kPOff + (i % C::NP) * C::kPBytes + r * 128;
       // P = 2^(x*c2 - shift - m2), one bias per row; -inf for a row with nothing
       // visible in this tile (finite scores times c2 plus -inf give 2^-inf = 0)
       const float nb = (nvis <= 0 || m2 == -INFINITY) ? -INFINITY : -shift - m2;
       float ps[4] = {0.f, 0.f, 0.f, 0.f};  // four partial row sums (short dependency chains)
 #pragma unroll
       for (int ch = 0; ch < 8; ++ch) {
-        uint32_t hi[4], lo[4];
-        if (kF16) {
-          // the row sum adds the FP32 values; their FP16 roundings (relative error
-          // at most 2^-11 each) go to the tensor cores
-          p8_f16(sv + 8 * ch, c2, nb, hi, ps[ch & 1], ps[2 + (ch & 1)]);
-        } else {
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int j = 8 * ch + 2 * e;
-          const float a0 = ex2_approx(fmaf(sv[j], c2, nb)), a1 = ex2_approx(fmaf(sv[j + 1], c2, nb));
-          {
-            const __nv_bfloat162 h2 = __floats2bfloat162_rn(a0, a1);
-            const float2 hf = __bfloat1622float2(h2);
-            const __nv_bfloat162 l2v = __floats2bfloat162_rn(a0 - hf.x, a1 - hf.y);
-            const float2 lf = __bfloat1622float2(l2v);
-            ps[e] += (hf.x + lf.x) + (hf.y + lf.y);
-            hi[e] = *reinterpret_cast<const uint32_t*>(&h2);
-            lo[e] = *reinterpret_cast<const uint32_t*>(&l2v);
-          }
-        }
-        }
-        const int sw = (ch ^ (r & 7)) << 4;
-        *reinterpret_cast<uint4*>(prow + sw) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-        if (!kF16) *reinterpret_cast<uint4*>(prow + C::kPBytes + sw) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        // the row sum adds the FP32 values; their FP16 roundings (relative error
+        // at most 2^-11 each) go to the tensor cores
+        uint32_t hi[4];
+        p8_f16(sv + 8 * ch, c2, nb, hi, ps[ch & 1], ps[2 + (ch & 1)]);
+        *reinterpret_cast<uint4*>(prow + ((ch ^ (r & 7)) << 4)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
       }
       l2 = l2 * f + ((ps[0] + ps[1]) + (ps[2] + ps[3]));
       if (__any_sync(0xffffffffu, rescale)) {
@@ -524,7 +491,7 @@ __global__ void __launch_bounds__(kThreads, P2Cfg<D, kF16>::kCtasPerSm)
       const float w1 = e1 == -INFINITY ? 0.f : exp2f(e1 - M), w2 = e2 == -INFINITY ? 0.f : exp2f(e2 - M);
       const float L = w1 * l1 + w2 * l2;
       const float invL = 1.f / L;
-      const float w2o = kF16 ? w2 * v16_scale(__uint_as_float(p.vamax[bh])) : w2;  // O carries V / scale
+      const float w2o = w2 * v16_scale(__uint_as_float(p.vamax[bh]));  // O carries V / scale
       float* orow = p.out + (((size_t)b * s.Hq + hq) * s.Nq + pos) * D;
 #pragma unroll 1
       for (int c0 = 0; c0 < D; c0 += 32) {
@@ -683,8 +650,16 @@ __global__ void __launch_bounds__(P2DualCfg<D>::kThreads, 1)
     return __all_sync(0xffffffffu, okl);
   };
 
-  const int n = (int)p.hot_count[(size_t)bh * nblk + blk];
-  const uint32_t* list = p.hot_list + ((size_t)bh * nblk + blk) * T;
+  // the block's tiles: its hot list (APA mode), or every tile it sees in the order
+  // 0, t_hi, ..., 1 with all eight row groups taking part (all-exact mode)
+  const bool apa_mode = p.hot_list != nullptr;
+  const int last_row = min(R, p0 + kBlockRows) - 1;
+  const int t_hi = s.causal ? min(T - 1, (last_row / G + off) / kTile) : T - 1;
+  const int n = apa_mode ? (int)p.hot_count[(size_t)bh * nblk + blk] : t_hi + 1;
+  const uint32_t* list = apa_mode ? p.hot_list + ((size_t)bh * nblk + blk) * T : nullptr;
+  auto entry = [&](int i) -> uint32_t {
+    return apa_mode ? list[i] : ((uint32_t)(i == 0 ? 0 : t_hi + 1 - i) | (0xFFu << 16));
+  };
 
   if (threadIdx.x == 0) {
     abort_flag = 0;
@@ -715,18 +690,20 @@ __global__ void __launch_bounds__(P2DualCfg<D>::kThreads, 1)
   float qmu = 0.f;
   if (warp < 8) {
     const uint4* src = reinterpret_cast<const uint4*>(p.q + (((size_t)b * s.Hq + hq) * s.Nq + pos) * D);
-    const float* mu = p.mu + (size_t)bh * D;
+    const float* mu = p.mu ? p.mu + (size_t)bh * D : nullptr;  // null: uncentred logits
 #pragma unroll 4
     for (int j = 0; j < D / 8; ++j) {
       uint4 val = row_valid ? src[j] : make_uint4(0u, 0u, 0u, 0u);
       const int atom = j >> 3, chunk = j & 7;
       if (u == 0)
         *reinterpret_cast<uint4*>(smem + C::kQOff + atom * 16384 + r * 128 + ((chunk ^ (r & 7)) << 4)) = val;
-      const uint32_t w[4] = {val.x, val.y, val.z, val.w};
+      if (mu) {
+        const uint32_t w[4] = {val.x, val.y, val.z, val.w};
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        qmu = fmaf(__uint_as_float(w[e] << 16), mu[j * 8 + 2 * e], qmu);
-        qmu = fmaf(__uint_as_float(w[e] & 0xFFFF0000u), mu[j * 8 + 2 * e + 1], qmu);
+        for (int e = 0; e < 4; ++e) {
+          qmu = fmaf(__uint_as_float(w[e] << 16), mu[j * 8 + 2 * e], qmu);
+          qmu = fmaf(__uint_as_float(w[e] & 0xFFFF0000u), mu[j * 8 + 2 * e + 1], qmu);
+        }
       }
     }
     fence_proxy_async_smem();
@@ -743,7 +720,7 @@ __global__ void __launch_bounds__(P2DualCfg<D>::kThreads, 1)
       for (int i = 0; i < n; ++i) {
         const int st = i % C::NS;
         if (i >= C::NS && !mbar_wait(k_empty(st), ((i / C::NS) - 1) & 1, &abort_flag, p.err)) break;
-        const int t = (int)(list[i] & 0xFFFFu);
+        const int t = (int)(entry(i) & 0xFFFFu);
         int ky = t * kTile, kz = bh;
         if (s.pages) {
           ky = 0;
@@ -766,7 +743,7 @@ __global__ void __launch_bounds__(P2DualCfg<D>::kThreads, 1)
       for (int i = 0; i < n; ++i) {
         const int st = i % C::NSV;
         if (i >= C::NSV && !mbar_wait(v_empty(st), ((i / C::NSV) - 1) & 1, &abort_flag, p.err)) break;
-        const int t = (int)(list[i] & 0xFFFFu);
+        const int t = (int)(entry(i) & 0xFFFFu);
         mbar_arrive_expect_tx(v_full(st), C::kKVBytes);
         const uint32_t vdst = sbase + C::kVOff + st * C::kKVBytes;
 #pragma unroll
@@ -788,7 +765,7 @@ __global__ void __launch_bounds__(P2DualCfg<D>::kThreads, 1)
         // NS is even, so every use of K stage st is this issuer's and it waits on the
         // stage's phases in order (see P2DualCfg).
         if (!(ok = mbar_wait(k_full(st), (i / C::NS) & 1, &abort_flag, p.err))) break;
-        if (s.pages && (s.Nkv % kTile) != 0 && (int)(list[i] & 0xFFFFu) == T - 1) {
+        if (s.pages && (s.Nkv % kTile) != 0 && (int)(entry(i) & 0xFFFFu) == T - 1) {
           // paged pool: zero the K rows past Nkv of the last page before the MMA reads them
           const int nk = s.Nkv - (T - 1) * kTile, rows = kTile - nk;
           uint8_t* kst = smem + C::kKOff + st * C::kKVBytes;
@@ -847,11 +824,11 @@ __global__ void __launch_bounds__(P2DualCfg<D>::kThreads, 1)
     const uint32_t lane_base = (uint32_t)(qw * 32) << 16;
     float m2 = -INFINITY, l2 = 0.f;
     bool ok = true;
-    uint32_t e_next = nu > 0 ? list[u] : 0u;
+    uint32_t e_next = nu > 0 ? entry(u) : 0u;
     for (int j = 0; j < nu; ++j) {
       const uint32_t gm = e_next >> 16;
       const int t = (int)(e_next & 0xFFFFu);
-      if (j + 1 < nu) e_next = list[2 * (j + 1) + u];
+      if (j + 1 < nu) e_next = entry(2 * (j + 1) + u);
       if (!(ok = warp_wait(s_full(u, j & 1), (j >> 1) & 1))) break;
       const bool row_hot = row_valid && ((gm >> (r >> 4)) & 1u);
       const int j0 = t * kTile;
@@ -944,9 +921,10 @@ __global__ void __launch_bounds__(P2DualCfg<D>::kThreads, 1)
       all_ok = warp_wait(pv_done(1, (n1 - 1) & 1), ((n1 - 1) >> 1) & 1);
     tc_fence_after();
     if (u == 0 && all_ok) {
+      // the pass-1 state (none in the all-exact mode), then the two groups' states
       float m1 = -INFINITY, l1 = 0.f;
-      const float* st = p.state_o + ((size_t)bh * nblk * kBlockRows + P) * D;
-      if (row_valid) {
+      const float* st = p.state_o ? p.state_o + ((size_t)bh * nblk * kBlockRows + P) * D : nullptr;
+      if (row_valid && p.state_ml) {
         const float2 ml = p.state_ml[(size_t)bh * nblk * kBlockRows + P];
         m1 = ml.x;
         l1 = ml.y;
@@ -986,9 +964,10 @@ __global__ void __launch_bounds__(P2DualCfg<D>::kThreads, 1)
             float4 res;
             float* rr = &res.x;
 #pragma unroll
-            for (int e = 0; e < 4; ++e)
-              rr[e] = ((w1 * st[c0 + x + e] + wAo * __uint_as_float(oa[x + e])) + wBo * __uint_as_float(ob[x + e])) *
-                      invL;
+            for (int e = 0; e < 4; ++e) {
+              const float a1 = st ? st[c0 + x + e] : 0.f;
+              rr[e] = ((w1 * a1 + wAo * __uint_as_float(oa[x + e])) + wBo * __uint_as_float(ob[x + e])) * invL;
+            }
             *reinterpret_cast<float4*>(orow + c0 + x) = res;
           }
         }
@@ -1033,36 +1012,22 @@ bool make_kv_map(CUtensorMap* map, const void* base, const Shape& s, CUtensorMap
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D, bool kF16>
-cudaError_t launch_dv(const P2Params& prm, const CUtensorMap& km, const CUtensorMap& vm, cudaStream_t st) {
-  const int smem = P2Cfg<D, kF16>::kSmem;
-  cudaError_t e = cudaFuncSetAttribute(pass2_kernel<D, kF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (e) return e;
-  const int grid = prm.s.BH() * prm.s.nblk();
-  pass2_kernel<D, kF16><<<grid, kThreads, smem, st>>>(prm, km, vm);
-  return cudaGetLastError();
-}
-// APA_PASS2_DUAL=0 keeps one softmax warp group per block in APA mode (for comparison).
-bool dual_allowed() {
-  static const bool v = [] {
-    const char* e = getenv("APA_PASS2_DUAL");
-    return !(e && strcmp(e, "0") == 0);
-  }();
-  return v;
-}
-
+// Two softmax groups per block at d <= 128; at d = 256 their two O accumulators
+// would take all 512 TMEM columns, so one group.
 template <int D>
 cudaError_t launch_d(const P2Params& prm, const CUtensorMap& km, const CUtensorMap& vm, cudaStream_t st) {
+  const int grid = prm.s.BH() * prm.s.nblk();
+  cudaError_t e;
   if constexpr (D <= 128) {
-    if (prm.vamax && dual_allowed()) {
-      const int smem = P2DualCfg<D>::kSmem;
-      cudaError_t e = cudaFuncSetAttribute(pass2_dual_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-      if (e) return e;
-      pass2_dual_kernel<D><<<prm.s.BH() * prm.s.nblk(), P2DualCfg<D>::kThreads, smem, st>>>(prm, km, vm);
-      return cudaGetLastError();
-    }
+    const int smem = P2DualCfg<D>::kSmem;
+    if ((e = cudaFuncSetAttribute(pass2_dual_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem))) return e;
+    pass2_dual_kernel<D><<<grid, P2DualCfg<D>::kThreads, smem, st>>>(prm, km, vm);
+  } else {
+    const int smem = P2Cfg<D>::kSmem;
+    if ((e = cudaFuncSetAttribute(pass2_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem))) return e;
+    pass2_kernel<D><<<grid, kThreads, smem, st>>>(prm, km, vm);
   }
-  return prm.vamax ? launch_dv<D, true>(prm, km, vm, st) : launch_dv<D, false>(prm, km, vm, st);
+  return cudaGetLastError();
 }
 
 // Ranks the pass-2 work items by hot-list length, longest first (ties by index,
@@ -1092,23 +1057,23 @@ cudaError_t launch_pass2_order(const Shape& s, const Workspace& ws, cudaStream_t
 
 cudaError_t launch_pass2(const Shape& s, const void* q, const void* k, const void* v, const Workspace* ws, float* out,
                          float* lse, cudaStream_t st) {
-  // with the FP16 copy of V (APA mode) P goes to the tensor cores as one FP16 term
-  const bool f16 = ws && ws->v16;
+  // P.V runs against the FP16 copy of V (contiguous, also for a paged K/V pool)
+  (void)v;
+  if (!ws || !ws->v16 || !ws->vamax) return cudaErrorInvalidValue;
   CUtensorMap km, vm;
   if (!make_kv_map(&km, k, s, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, s.pages != nullptr) ||
-      !make_kv_map(&vm, f16 ? (const void*)ws->v16 : v, s,
-                   f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, s.pages && !f16))
+      !make_kv_map(&vm, ws->v16, s, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, false))
     return cudaErrorInvalidValue;
   P2Params prm{};
   prm.s = s;
   prm.q = (const uint16_t*)q;
-  prm.mu = ws ? ws->mu : nullptr;
-  prm.state_o = ws ? ws->state_o : nullptr;
-  prm.state_ml = ws ? ws->state_ml : nullptr;
-  prm.hot_list = ws ? ws->hot_list : nullptr;
-  prm.hot_count = ws ? ws->hot_count : nullptr;
-  prm.order = ws && (size_t)s.BH() * s.nblk() <= kMaxRanked ? ws->p2_order : nullptr;
-  prm.vamax = f16 ? ws->vamax : nullptr;
+  prm.mu = ws->mu;
+  prm.state_o = ws->state_o;
+  prm.state_ml = ws->state_ml;
+  prm.hot_list = ws->hot_list;
+  prm.hot_count = ws->hot_count;
+  prm.order = (size_t)s.BH() * s.nblk() <= kMaxRanked ? ws->p2_order : nullptr;
+  prm.vamax = ws->vamax;
   prm.out = out;
   prm.lse = lse;
   prm.err = device_error_word();

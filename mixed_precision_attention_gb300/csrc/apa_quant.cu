@@ -353,7 +353,64 @@ __global__ void __launch_bounds__(kThreads) quant_kernel(Shape s, const uint16_t
   if (q2) store_image(ws.q2_blob + ((size_t)bh * nblk + blk) * qblob_bytes(d), img2, qblob_bytes(d));
 }
 
+// The all-exact path (eps = 0) runs P.V as one FP16 term against an FP16 copy
+// of V, the same copy the quantizer writes in APA mode: V divided by the head's
+// power-of-two scale v16_scale(max |v|), which is 1 unless max |v| > 2^15.  One
+// pass converts every head with divisor 1 and takes the head maxima; a second,
+// per block, re-converts its keys only if its head needs a divisor (it then also
+// overwrites what the first pass may have saturated).  Blocks take kV16Tiles key
+// tiles of one head.
+constexpr int kV16Tiles = 4;
+
+__device__ __forceinline__ uint4 v16_of(uint4 val, float inv) {
+  const uint32_t w[4] = {val.x, val.y, val.z, val.w};
+  uint32_t o[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) o[e] = cvt_f16x2(bf16f(w[e] & 0xFFFF) * inv, bf16f(w[e] >> 16) * inv);
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// fixup = 0: the first pass; 1: the re-conversion of heads whose maximum needs a divisor.
+__global__ void __launch_bounds__(kThreads) v16_kernel(Shape s, const uint16_t* __restrict__ v, Workspace ws,
+                                                        int fixup, int* err) {
+  __shared__ float red[32];
+  const int bh = blockIdx.y, T = s.T(), d = s.d;
+  float inv = 1.f;
+  if (fixup) {
+    const float sc = v16_scale(__uint_as_float(ws.vamax[bh]));
+    if (sc == 1.f) return;
+    inv = 1.f / sc;
+  }
+  float vm = 0.f;
+  for (int t = blockIdx.x * kV16Tiles; t < min(T, (int)(blockIdx.x + 1) * kV16Tiles); ++t) {
+    const int nk = min(kTile, s.Nkv - t * kTile);
+    const uint4* src = reinterpret_cast<const uint4*>(v + kv_tile_offset(s, bh, t, err));
+    uint4* dst = reinterpret_cast<uint4*>(ws.v16 + ((size_t)bh * s.Nkv + (size_t)t * kTile) * d);
+    for (int i = threadIdx.x; i < nk * d / 8; i += blockDim.x) {
+      const uint4 val = src[i];
+      if (!fixup) vm = fmaxf(vm, absmax8(val));
+      dst[i] = v16_of(val, inv);
+    }
+  }
+  if (!fixup) {
+    vm = block_max(vm, red);
+    if (threadIdx.x == 0) atomicMax(&ws.vamax[bh], __float_as_uint(vm));
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_v16(const Shape& s, const void* v, const Workspace& ws, cudaStream_t st) {
+  cudaError_t e;
+  if ((e = cudaMemsetAsync(ws.vamax, 0x00, sizeof(uint32_t) * s.BH(), st))) return e;
+  const dim3 grid((s.T() + kV16Tiles - 1) / kV16Tiles, s.BH());
+  int* err = device_error_word();
+  for (int fixup = 0; fixup < 2; ++fixup) {
+    v16_kernel<<<grid, kThreads, 0, st>>>(s, (const uint16_t*)v, ws, fixup, err);
+    if ((e = cudaGetLastError())) return e;
+  }
+  return cudaSuccess;
+}
 
 cudaError_t launch_quantize(const Shape& s, const void* q, const void* k, const void* v, const Workspace& ws,
                             bool do_q, bool do_kv, cudaStream_t st, bool lse, bool kv_in_pass1) {

@@ -65,9 +65,10 @@ def to_dev(a, dev="cuda"):
     return synth.to_torch_bf16(a, dev)
 
 
-def run_apa(q, k, v, causal=True, eps=0.005, hot_mask=True):
+def run_apa(q, k, v, causal=True, eps=0.005, hot_mask=True, **options):
     import mixed_precision_attention_gb300 as apa
-    out, lse, mask = apa.attention(to_dev(q), to_dev(k), to_dev(v), causal=causal, eps=eps, return_hot_mask=hot_mask)
+    out, lse, mask = apa.attention(to_dev(q), to_dev(k), to_dev(v), causal=causal, eps=eps, return_hot_mask=hot_mask,
+                                   **options)
     apa.check_error()
     return (out.cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64),
             None if mask is None else mask.cpu().numpy().view(np.uint32))

@@ -61,7 +61,8 @@ def test_sizes(lib):
     assert lib.apa_kv_blob_bytes(1, 1, 65, 128) == 2 * 9216
     # 128 packed rows x 72 d bytes per Q block; GQA packs G * Nq rows
     assert lib.apa_q_blob_bytes(1, 24, 8, 2048, 128) == 8 * 48 * 72 * 128
-    assert lib.apa_workspace_bytes(1, 24, 8, 2048, 122880, 128, 0.0) == 0
+    # eps = 0 (all exact): the FP16 copy of V (8 heads x 122880 keys x 128 x 2 B) and the head maxima
+    assert lib.apa_workspace_bytes(1, 24, 8, 2048, 122880, 128, 0.0) == 8 * 122880 * 128 * 2 + 256
     assert lib.apa_workspace_bytes(1, 24, 8, 2048, 122880, 128, 0.005) > 141557760
     assert lib.apa_workspace_bytes(1, 3, 2, 16, 64, 64, 0.005) == 0  # Hq % Hkv != 0
 
@@ -86,11 +87,14 @@ def test_option_flags(lib):
     # the value-weighted test keeps two floats per (b, KV head, tile): 8 tiles here
     vw = lib.apa_workspace_bytes_ex(1, 2, 1, 128, 512, 64, 0.005, 4)
     assert base + 2 * 8 * 4 <= vw <= base + 2 * 256
-    assert lib.apa_workspace_bytes_ex(1, 2, 1, 128, 512, 64, 0.005, 8) == 0
-    st = lib.apa_attention_ex(*OK_PTR, 1, 2, 1, 128, 512, 64, 1, 0.005, 8, P(0x40000), None, None, None, 0, None)
+    assert lib.apa_workspace_bytes_ex(1, 2, 1, 128, 512, 64, 0.005, 16) == 0
+    st = lib.apa_attention_ex(*OK_PTR, 1, 2, 1, 128, 512, 64, 1, 0.005, 16, P(0x40000), None, None, None, 0, None)
+    assert st == -10
+    # the ones-MMA row sums and the residual Q term share TMEM columns: refused together
+    st = lib.apa_attention_ex(*OK_PTR, 1, 2, 1, 128, 512, 64, 1, 0.005, 9, P(0x40000), None, None, None, 0, None)
     assert st == -10
     z = P(0x60000)
-    st = lib.apa_quantize_ex(*OK_PTR, 1, 2, 1, 128, 512, 64, 8, z, z, None, z, z, z, z, None)
+    st = lib.apa_quantize_ex(*OK_PTR, 1, 2, 1, 128, 512, 64, 16, z, z, None, z, z, z, z, None)
     assert st == -10
     st = lib.apa_attention_ex(*OK_PTR, 1, 2, 1, 128, 512, 64, 1, 0.005, 4, P(0x40000), None, None,
                               P(0x50000), vw - 1, None)

@@ -52,7 +52,8 @@ def test_work_counts_match_brute_force(shape, causal):
     pairs, hot_pairs, union, vis_blocks = _brute(w, hot)
     assert got["pairs"] == pairs and got["hot_pairs"] == hot_pairs
     assert got["cold_pairs"] == pairs - hot_pairs
-    assert got["F1"] == pairs * 2 * w.d + (pairs - hot_pairs) * 2 * w.d
+    # QK^T (2d) and the ones product of the row sums (N = 16: 32) on every pair, PV on cold ones
+    assert got["F1"] == pairs * (2 * w.d + 32) + (pairs - hot_pairs) * 2 * w.d
     assert got["F2"] == hot_pairs * 4 * w.d
     assert got["block_tiles_hot"] == union and got["block_tiles_vis"] == vis_blocks
 
@@ -65,3 +66,19 @@ def test_all_hot_and_none_hot():
     assert got["hot_pairs"] == got["pairs"] and got["block_tiles_hot"] == got["block_tiles_vis"]
     got = bench.algorithmic(w, np.zeros_like(full))
     assert got["hot_pairs"] == 0 and got["F2"] == 0 and got["block_tiles_hot"] == 0
+
+
+def test_stage_bytes_follow_where_the_kv_quantizer_runs():
+    # the K/V quantizer's traffic counts in the pass-1 stage when it runs inside
+    # that launch, in the quantizer stage otherwise; the total is the same
+    w = synth.WORKLOADS["llama3b_2048x122880"]
+    assert bench.pass1_hosts_kv_quantizer(w, 152)   # 128 pass-1 CTAs, 24 SMs spare
+    assert not bench.pass1_hosts_kv_quantizer(synth.WORKLOADS["batched_32k"], 152)
+    assert bench.pass1_hosts_kv_quantizer(synth.WORKLOADS["shortq_131k_d256"], 152)  # 64 one-block CTAs
+    q_in, p1_in = bench.stage_bytes(w, True)
+    q_out, p1_out = bench.stage_bytes(w, False)
+    assert q_in + p1_in == q_out + p1_out and q_out > q_in and p1_in > p1_out
+    kv = w.B * w.Hkv * w.Nkv * w.d
+    # statistics read K and V once (bf16); the quantizer reads them again and writes
+    # 0.5625 B of codes and scales per element and the 2-B FP16 copy of V
+    assert q_out - q_in == 2 * kv * 2 + 2 * kv * 0.5625 + kv * 2

@@ -53,10 +53,10 @@ def test_eps0_matches_exact(name, causal):
     assert np.array_equal(_gpu.hot_bits(mask, T), np.broadcast_to(vis, mask.shape[:2] + vis.shape))
 
 
-def _check_apa(w, q, k, v, eps, causal=True):
+def _check_apa(w, q, k, v, eps, causal=True, record=None, **options):
     ref = oracle.apa(q, k, v, causal=causal, eps=eps, diag=True)
     ex, _ = oracle.exact(q, k, v, causal=causal)
-    out, lse, mask = _gpu.run_apa(q, k, v, causal=causal, eps=eps)
+    out, lse, mask = _gpu.run_apa(q, k, v, causal=causal, eps=eps, **options)
     err = np.abs(out - ref["out"]).max()
     assert err <= 1e-2, err
     assert _gpu.cosine(out, ref["out"]) >= 0.9999
@@ -76,16 +76,82 @@ def _check_apa(w, q, k, v, eps, causal=True):
     # rows past the end of a partial last group have no lambda (NaN): nothing to check there
     ratio = np.where(np.isnan(ell), 0.0, ell) / np.where(np.isnan(lam), np.inf, np.maximum(lam, 1e-300))[..., None]
     worst = np.max(np.where(cold[..., None, :], ratio, 0.0)) if cold.any() else 0.0
+    if record is not None and not np.isinf(eps):
+        record("cold_worst_over_eps", float(worst / eps))
+        record("mask_agreement", float(agree))
     if not np.isinf(eps):
-        assert worst <= eps * 1.02, worst
+        assert worst <= eps * COLD_SLACK, worst
     return dict(out=out, mask=mask, hot_frac=g_hot[vis].mean(), worst=worst, agree=agree)
+
+
+# The GPU encodes P with ex2.approx, so its FP4 tile sums can differ from the
+# oracle's FP64 ones in the last bits, and a tile the oracle finds a hair above
+# eps * lambda can come out cold on the GPU (such a tile also counts against the
+# 99.9 % mask agreement).  COLD_SLACK bounds that excess; the measured worst
+# ratio of every case is recorded as a test property.
+COLD_SLACK = 1.02
 
 
 @pytest.mark.parametrize("name", list(SHAPES))
 @pytest.mark.parametrize("eps", [0.005, 0.02])
-def test_apa_matches_emulation(name, eps):
+def test_apa_matches_emulation(name, eps, record_property):
     w, (q, k, v) = _inputs(name)
-    _check_apa(w, q, k, v, eps)
+    _check_apa(w, q, k, v, eps, record=record_property)
+
+
+@pytest.mark.parametrize("name", ["tiny", "gqa3_ragged", "batch_ragged_d128", "d256", "long_tail"])
+@pytest.mark.parametrize("eps", [0.005, float("inf")])
+def test_rowsum_mma_matches_emulation(name, eps, record_property):
+    """APA_FLAG_ROWSUM_MMA: the tile row sums from an MMA of the E2M1 P against an
+    E2M1 ones tile ("Pass 1", step 3 on the page) instead of the register sums;
+    against the oracle with the usual bounds, and close to the default path."""
+    w, (q, k, v) = _inputs(name)
+    if np.isinf(eps):
+        ref = oracle.apa(q, k, v, eps=eps)
+        out, _, mask = _gpu.run_apa(q, k, v, eps=eps, rowsum_mma=True)
+        assert not mask.any()
+        assert np.abs(out - ref["out"]).max() <= 1e-2 and _gpu.cosine(out, ref["out"]) >= 0.9999
+        return
+    r = _check_apa(w, q, k, v, eps, record=record_property, rowsum_mma=True)
+    dflt = _gpu.run_apa(q, k, v, eps=eps)
+    T = (w.Nkv + 63) // 64
+    assert (_gpu.hot_bits(r["mask"], T) == _gpu.hot_bits(dflt[2], T)).mean() >= 0.999
+    assert np.abs(r["out"] - dflt[0]).max() <= 1e-2
+
+
+@pytest.mark.parametrize("eps", [0.0, 0.005])
+def test_apa_attention_entry_point(eps):
+    """apa_attention itself, whose workspace is allocated and freed stream-ordered on
+    the caller's stream: bit for bit the result of apa_attention_ws (the binding's
+    call) and within the usual bounds of the oracle."""
+    import ctypes
+
+    import torch
+
+    import mixed_precision_attention_gb300 as apa
+    from mixed_precision_attention_gb300 import _lib
+    w, (q, k, v) = _inputs("batch_ragged_d128")
+    tq, tk, tv = (_gpu.to_dev(a) for a in (q, k, v))
+    B, Hq, Nq, d = q.shape
+    Hkv, Nkv = k.shape[1], k.shape[2]
+    out = torch.full((B, Hq, Nq, d), float("nan"), dtype=torch.float32, device="cuda")
+    lse = torch.full((B, Hq, Nq), float("nan"), dtype=torch.float32, device="cuda")
+    mask = torch.zeros(apa.hot_mask_shape(B, Hq, Hkv, Nq, Nkv), dtype=torch.int32, device="cuda")
+    ptr = lambda t: ctypes.c_void_p(t.data_ptr())  # noqa: E731
+    st = _lib.load().apa_attention(ptr(tq), ptr(tk), ptr(tv), B, Hq, Hkv, Nq, Nkv, d, 1, eps, ptr(out), ptr(lse),
+                                   ptr(mask), ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert st == 0
+    apa.check_error()
+    ref = _gpu.run_apa(q, k, v, eps=eps)
+    assert np.array_equal(out.cpu().numpy().astype(np.float64), ref[0])
+    assert np.array_equal(lse.cpu().numpy().astype(np.float64), ref[1])
+    assert np.array_equal(mask.cpu().numpy().view(np.uint32), ref[2])
+    if eps == 0:
+        ex, _ = oracle.exact(q, k, v)
+        assert np.abs(ref[0] - ex).max() <= 4e-3
+    else:
+        emu = oracle.apa(q, k, v, eps=eps)
+        assert np.abs(ref[0] - emu["out"]).max() <= 1e-2
 
 
 @pytest.mark.parametrize("name", ["tiny", "gqa3_ragged", "batch_ragged_d128", "d256", "long_tail"])
@@ -222,7 +288,7 @@ def _value_weighted_inputs(name):
 
 @pytest.mark.parametrize("name", ["gqa3_ragged", "batch_ragged_d128", "d256", "long_tail"])
 @pytest.mark.parametrize("q_residual", [False, True])
-def test_value_weighted_matches_emulation(name, q_residual):
+def test_value_weighted_matches_emulation(name, q_residual, record_property):
     """APA_FLAG_VALUE_WEIGHTED against the oracle's weighted hot test: outputs within
     the usual bounds, masks agree, and every tile the GPU calls cold has w_t * l_t
     below eps of the oracle's final row sum (w_t the oracle's weights)."""
@@ -250,7 +316,9 @@ def test_value_weighted_matches_emulation(name, q_residual):
     lam = ref["lam"].reshape(w.B, w.Hkv, ng, 16)
     cold = vis & ~g_hot
     ratio = np.where(np.isnan(ell), 0.0, ell) / np.where(np.isnan(lam), np.inf, np.maximum(lam, 1e-300))[..., None]
-    assert np.max(np.where(cold[..., None, :], ratio, 0.0)) <= eps * 1.02
+    worst = np.max(np.where(cold[..., None, :], ratio, 0.0))
+    record_property("cold_worst_over_eps", float(worst / eps))
+    assert worst <= eps * COLD_SLACK
     # against the unweighted run: the large-norm tile is hot for at least as many groups,
     # and the masks differ wherever the oracle's do
     _, _, m0 = apa.attention(tq, tk, tv, causal=True, eps=eps, return_hot_mask=True, q_residual=q_residual)

@@ -52,7 +52,7 @@ def _rows(w, grp):
     return [(p % G, p // G) for p in range(grp * 16, min(w.G * w.Nq, (grp + 1) * 16))]
 
 
-def _check(name, eps):
+def _check(name, eps, record=None):
     w = synth.WORKLOADS[name]
     q, k, v = _inputs(name)
     out, lse, mask = _run_gpu(w, q, k, v, eps)
@@ -102,8 +102,11 @@ def _check(name, eps):
         assert _gpu.cosine(got, refo) >= 0.9999
         if not np.isinf(eps):
             assert _gpu.cosine(got, exo) >= 0.999
+    if record is not None and eps > 0 and not np.isinf(eps):
+        record("cold_worst_over_eps", float(worst / eps))
+        record("mask_agreement", float(n_agree / n_vis))
     assert n_agree / n_vis >= 0.999, n_agree / n_vis
-    assert worst <= eps * 1.02 or np.isinf(eps)
+    assert worst <= eps * COLD_SLACK or np.isinf(eps)
     if eps > 0:
         # per-row cosine to exact attention (the pages' per-pair metric): the GPU rows
         # are as close as the oracle's emulation of the same method, row by row
@@ -116,6 +119,7 @@ def _check(name, eps):
 
 
 ROW_COSINES = {}  # (workload, eps) -> per-row cosine statistics of the sampled rows
+COLD_SLACK = 1.02  # see test_gpu_attention.py
 
 
 def _row_cosines(a, b):
@@ -126,14 +130,14 @@ def _row_cosines(a, b):
 
 @pytest.mark.parametrize("name", ["llama3b_2048x122880", "batched_32k", "shortq_131k_d256"])
 @pytest.mark.parametrize("eps", ["workload", 0.0])
-def test_full_size_workloads(name, eps):
+def test_full_size_workloads(name, eps, record_property):
     w = synth.WORKLOADS[name]
-    _check(name, w.eps if eps == "workload" else eps)
+    _check(name, w.eps if eps == "workload" else eps, record_property)
 
 
 @pytest.mark.parametrize("eps", [0.0, 0.001, 0.005, 0.02, float("inf")])
-def test_prefill_8k_eps_sweep(eps):
-    hot = _check("prefill_8k", eps)
+def test_prefill_8k_eps_sweep(eps, record_property):
+    hot = _check("prefill_8k", eps, record_property)
     if eps == 0:
         assert hot == 1.0
 
@@ -147,3 +151,45 @@ def test_tiny_workload_full():
     got = out.cpu().numpy().astype(np.float64)
     assert np.abs(got - ref["out"]).max() <= 1e-2
     assert _gpu.cosine(got, ref["out"]) >= 0.9999
+
+
+@pytest.mark.parametrize("name,heads", [("llama3b_2048x122880", None), ("shortq_131k_d256", [(0, 0), (1, 7)])])
+def test_in_launch_quantizer_operands_bit_exact(name, heads):
+    """At these sizes the pass-1 CTAs leave spare SMs, so the K/V tiles are quantized
+    inside the pass-1 launch (three-block kernel at d = 128, one-block at d = 256),
+    and the key mean sums 30 and 32 ranges of 64 tiles.  The operands the call
+    leaves in the caller's workspace (at the offsets apa_workspace_operands reports)
+    equal the oracle's codes, scales, key mean and head scales bit for bit."""
+    import torch
+
+    import mixed_precision_attention_gb300 as apa
+    w = synth.WORKLOADS[name]
+    q, k, v = _inputs(name)
+    B, Hq, Hkv, Nq, Nkv, d, G = w.B, w.Hq, w.Hkv, w.Nq, w.Nkv, w.d, w.G
+    ws = torch.empty(apa.workspace_bytes(B, Hq, Hkv, Nq, Nkv, d, w.eps), dtype=torch.uint8, device="cuda")
+    tq, tk, tv = (_gpu.to_dev(a) for a in (q, k, v))
+    apa.attention(tq, tk, tv, causal=w.causal, eps=w.eps, workspace=ws)
+    apa.check_error()
+    off = apa.workspace_operands(B, Hq, Hkv, Nq, Nkv, d, w.eps)
+    T, bb, nblk, qb = (Nkv + 63) // 64, _gpu.blob_bytes(d), (G * Nq + 127) // 128, 72 * d
+
+    def part(name, nbytes):
+        return ws[off[name]:off[name] + nbytes].cpu().numpy()
+    kvb = part("kv_blob", B * Hkv * T * bb).reshape(B * Hkv, T * bb)
+    qbl = part("q_blob", B * Hkv * nblk * qb).reshape(B * Hkv, nblk * qb)
+    mu = part("mu", B * Hkv * d * 4).view(np.float32).reshape(B, Hkv, d)
+    s_k = part("s_k", B * Hkv * 4).view(np.float32).reshape(B, Hkv)
+    s_v = part("s_v", B * Hkv * 4).view(np.float32).reshape(B, Hkv)
+    s_q = part("s_q", B * Hq * 4).view(np.float32).reshape(B, Hq)
+    for b, h in heads or [(b, h) for b in range(B) for h in range(Hkv)]:
+        ok = oracle.quantize_kv(k[b:b + 1, h:h + 1], v[b:b + 1, h:h + 1])
+        assert mu[b, h].view(np.uint32).tobytes() == ok["mu"][0, 0].view(np.uint32).tobytes()
+        assert s_k[b, h] == np.float32(ok["s_k"][0, 0]) and s_v[b, h] == np.float32(ok["s_v"][0, 0])
+        kc, ksf, vc, vsf = _gpu.decode_kv_blob(kvb[b * Hkv + h], 1, 1, Nkv, d)
+        assert np.array_equal(kc, ok["kcodes"]) and np.array_equal(ksf, ok["ksf"])
+        assert np.array_equal(vc, ok["vcodes"]) and np.array_equal(vsf, ok["vsf"])
+        oq = oracle.quantize_q(np.ascontiguousarray(q[b:b + 1, h * G:(h + 1) * G]))
+        qc, qsf, pad_c, pad_s = _gpu.decode_q_blob(qbl[b * Hkv + h], 1, G, 1, Nq, d)
+        assert np.array_equal(qc, oq["codes"]) and np.array_equal(qsf, oq["sf"])
+        assert not pad_c.any() and not pad_s.any()
+        assert np.array_equal(s_q[b, h * G:(h + 1) * G], oq["s_q"][0].astype(np.float32))

@@ -167,3 +167,32 @@ def test_e2m1_rounding_of_every_bf16_value_in_range():
     # and the oracle agrees on the whole tensor
     oq = oracle.quantize_q(q)
     assert np.array_equal(qc, oq["codes"]) and np.array_equal(qsf, oq["sf"])
+
+
+# The key mean sums per-tile FP32 sums in FP64 per range of 64 tiles, then the
+# ranges: these cases span 30 and 32 ranges (the 2048 x 122880 layer's keys with
+# two of its KV heads, and the short-query d = 256 shape's 131072 keys), so the
+# multi-range reduction is compared bit for bit.
+LONG_CASES = [
+    dict(B=1, Hq=6, Hkv=2, Nq=64, Nkv=122880, d=128, n_outliers=4),
+    dict(B=1, Hq=4, Hkv=1, Nq=128, Nkv=131072, d=256, n_outliers=4),
+]
+
+
+@pytest.mark.parametrize("case", LONG_CASES)
+def test_quantizer_bit_exact_many_ranges(case):
+    w = synth.small(sink_gain=4.0, **case)
+    q, k, v = synth.generate(w)
+    assert (w.Nkv + 63) // 64 > 64 * 16  # more than 16 ranges of 64 tiles
+    g = _quant_gpu(q, k, v)
+    ok = oracle.quantize_kv(k, v)
+    oq = oracle.quantize_q(q)
+    assert np.array_equal(g["mu"].view(np.uint32), ok["mu"].view(np.uint32))
+    assert np.array_equal(g["s_k"], ok["s_k"].astype(np.float32))
+    assert np.array_equal(g["s_v"], ok["s_v"].astype(np.float32))
+    assert np.array_equal(g["s_q"], oq["s_q"].astype(np.float32))
+    kc, ksf, vc, vsf = _gpu.decode_kv_blob(g["kv_blob"], w.B, w.Hkv, w.Nkv, w.d)
+    assert np.array_equal(kc, ok["kcodes"]) and np.array_equal(ksf, ok["ksf"])
+    assert np.array_equal(vc, ok["vcodes"]) and np.array_equal(vsf, ok["vsf"])
+    qc, qsf, _, _ = _gpu.decode_q_blob(g["q_blob"], w.B, w.Hq, w.Hkv, w.Nq, w.d)
+    assert np.array_equal(qc, oq["codes"]) and np.array_equal(qsf, oq["sf"])
