@@ -43,16 +43,35 @@ def needs_build() -> bool:
     return any(os.path.getmtime(p) > t for p in _deps())
 
 
+# The test-hook variant (tests only, never loaded by the package): the same sources
+# with APA_TEST_HOOKS, which exports a switch that makes pass 1's wait for the
+# in-launch quantizer run out, and a short wait limit (~0.5 s at 2 GHz).
+TEST_HOOKS_LIB = os.path.join(LIBDIR, "libapa_testhooks.so")
+TEST_HOOKS_FLAGS = ["-DAPA_TEST_HOOKS", "-DAPA_WAIT_LIMIT_CYCLES=1000000000ull"]
+
+
+def build_test_hooks(force: bool = False) -> str:
+    """Builds the test-hook variant of the library (for the timeout test)."""
+    if not force and os.path.exists(TEST_HOOKS_LIB) and \
+            all(os.path.getmtime(p) <= os.path.getmtime(TEST_HOOKS_LIB) for p in _deps()):
+        return TEST_HOOKS_LIB
+    return _build(TEST_HOOKS_LIB, os.path.join(LIBDIR, "testhooks"), TEST_HOOKS_FLAGS)
+
+
 def build(force: bool = False, verbose: bool = False) -> str:
     if not force and not needs_build():
         return LIB
-    os.makedirs(LIBDIR, exist_ok=True)
+    return _build(LIB, LIBDIR, [], verbose)
+
+
+def _build(lib: str, objdir: str, extra: list, verbose: bool = False) -> str:
+    os.makedirs(objdir, exist_ok=True)
     nvcc = _nvcc()
     objs = []
 
     def compile_one(src):
-        obj = os.path.join(LIBDIR, os.path.basename(src)[:-3] + ".o")
-        cmd = [nvcc, *ARCH, *FLAGS, "-c", src, "-o", obj]
+        obj = os.path.join(objdir, os.path.basename(src)[:-3] + ".o")
+        cmd = [nvcc, *ARCH, *FLAGS, *extra, "-c", src, "-o", obj]
         if verbose:
             cmd += ["-Xptxas", "-v"]
         r = subprocess.run(cmd, capture_output=True, text=True)
@@ -65,12 +84,12 @@ def build(force: bool = False, verbose: bool = False) -> str:
             objs.append(obj)
             if verbose and log:
                 print(log)
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     r = subprocess.run([nvcc, *ARCH, "-shared", "-o", tmp, *objs], capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"nvcc link failed:\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

@@ -77,6 +77,9 @@ struct P1Params {
   Workspace ws;
   int n_p1;
   int lse_scales;
+  // test builds only (APA_TEST_HOOKS): a word nothing ever sets; when non-null the
+  // producer waits on it instead of the quantizer's tile flags
+  const uint32_t* test_never;
 };
 
 constexpr int kSoftWarps = 4;
@@ -219,6 +222,15 @@ __device__ __forceinline__ int await_blobs(const uint32_t* rd, int i, int n, Til
   }
 }
 
+// The producer's wait for tiles i.. of head bh: on the quantizer's flags, or (test
+// builds) on a word nothing sets, so that the wait runs out.
+template <typename TileOf>
+__device__ __forceinline__ int await_tiles(const P1Params& p, int bh, int T, int i, int n, TileOf tile_of,
+                                           int* abort_flag) {
+  if (p.test_never) return await_blobs(p.test_never, i, n, [](int) { return 0; }, abort_flag, p.err);
+  return await_blobs(p.kv_ready + (size_t)bh * T, i, n, tile_of, abort_flag, p.err);
+}
+
 // What a row keeps between encoding a tile and judging it.
 struct Pending {
   float c, mt;
@@ -318,17 +330,18 @@ __global__ void __launch_bounds__(kThreads, (D <= 128 ? 2 : 1)) pass1_kernel(con
         const int st = i % C::NS;
         if (i >= C::NS && !mbar_wait(blob_empty(st), ((i / C::NS) - 1) & 1, &abort_flag, p.err)) break;
         if (!kOnesMma && p.kv_ready && i >= written &&
-            (written = await_blobs(p.kv_ready + (size_t)bh * T, i, n, tile_of, &abort_flag, p.err)) < 0)
+            (written = await_tiles(p, bh, T, i, n, tile_of, &abort_flag)) < 0)
           break;
         const uint8_t* src = p.kv_blob + ((size_t)bh * T + tile_of(i)) * C::kBlob;
         mbar_arrive_expect_tx(blob_full(st), C::kBlob);
         bulk_g2s(sbase + C::kStageOff + st * C::kBlob, src, C::kBlob, blob_full(st));
         issued = i + 1;
       }
-      if (abort_flag) {
-        wait_bounded(q_full, 0, p.err);
-        for (int i = max(0, issued - C::NS); i < issued; ++i) wait_bounded(blob_full(i % C::NS), (i / C::NS) & 1, p.err);
-      }
+      // Every copy issued lands before the CTA exits, also when another warp gave up
+      // after this loop ended.  Normally all have landed (and no copy reused their
+      // stage since), so these parity waits return at once.
+      wait_bounded(q_full, 0, p.err);
+      for (int i = max(0, issued - C::NS); i < issued; ++i) wait_bounded(blob_full(i % C::NS), (i / C::NS) & 1, p.err);
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
@@ -803,8 +816,21 @@ __global__ void __launch_bounds__(kThreads, (D <= 128 ? 2 : 1)) pass1_kernel(con
 // serial bottleneck for three units: the S warp issues S(0,i), S(1,i), ... in
 // the order in which the units hand the S buffer on; the PV warp issues
 // PV(u,i) as each unit publishes P(u,i).
+#ifndef APA_P1_UNITS
+#define APA_P1_UNITS 3  // 128-row blocks per CTA of the multi-block kernel
+#endif
+#ifndef APA_P1_EXP_ISSUE
+#define APA_P1_EXP_ISSUE 0
+#endif
+#ifndef APA_P1_EXP_LD64
+#define APA_P1_EXP_LD64 0
+#endif
+#ifndef APA_P1_SPLIT_S
+#define APA_P1_SPLIT_S 0  // 1: one S buffer per unit instead of one the units share
+#endif
 template <int D, int U>
 struct P1MCfg {
+  static constexpr bool kSplitS = APA_P1_SPLIT_S != 0;
   static constexpr int NS = 4;
   static constexpr int kBlob = blob_bytes(D);
   static constexpr int kQBlob = qblob_bytes(D);
@@ -815,15 +841,15 @@ struct P1MCfg {
   static constexpr int kSmem = kPsfOff + U * 2 * 512 + 128;
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kSfc = 4 * sf_chunks(D);
-  static constexpr uint32_t kS = U * D;
-  static constexpr uint32_t kSFQ = kS + 64;                   // U x 4 * (D/64)
+  static constexpr uint32_t kS = U * D;                       // S, or S(u) at kS + 64 u
+  static constexpr uint32_t kSFQ = kS + 64 * (kSplitS ? U : 1);  // U x 4 * (D/64)
   static constexpr uint32_t kSFK = kSFQ + U * 4 * (D / 64);   // 2 buffers (tile % 2)
   static constexpr uint32_t kSFV = kSFK + 2 * kSfc;           // 2 buffers (tile % 2)
   static constexpr uint32_t kSFP = kSFV + 2 * kSfc;           // [U][2] buffers (tile % 2)
   static_assert(kSFP + 8 * U <= kTmemCols, "TMEM budget");
   static constexpr int kThreads = (4 * U + 3) * 32;
   // thread groups of the K/V quantizer role (each a multiple of d/16 threads)
-  static constexpr int kQuantGroups = 3;
+  static constexpr int kQuantGroups = kThreads % 3 == 0 ? 3 : 2;
   static_assert(kThreads % kQuantGroups == 0 && (kThreads / kQuantGroups) % (D / 16) == 0 &&
                     kQuantGroups <= kQuantRoleGroups,
                 "quantizer groups");
@@ -917,17 +943,18 @@ __global__ void __launch_bounds__(P1MCfg<D, U>::kThreads, 1) pass1_multi_kernel(
         const int st = i % C::NS;
         if (i >= C::NS && !mbar_wait(blob_empty(st), ((i / C::NS) - 1) & 1, &abort_flag, p.err)) break;
         if (p.kv_ready && i >= written &&
-            (written = await_blobs(p.kv_ready + (size_t)bh * T, i, n, tile_of, &abort_flag, p.err)) < 0)
+            (written = await_tiles(p, bh, T, i, n, tile_of, &abort_flag)) < 0)
           break;
         mbar_arrive_expect_tx(blob_full(st), C::kBlob);
         bulk_g2s(sbase + C::kStageOff + st * C::kBlob, p.kv_blob + ((size_t)bh * T + tile_of(i)) * C::kBlob,
                  C::kBlob, blob_full(st));
         issued = i + 1;
       }
-      if (abort_flag) {
-        wait_bounded(q_full, 0, p.err);
-        for (int i = max(0, issued - C::NS); i < issued; ++i) wait_bounded(blob_full(i % C::NS), (i / C::NS) & 1, p.err);
-      }
+      // Every copy issued lands before the CTA exits, also when another warp gave up
+      // after this loop ended.  Normally all have landed (and no copy reused their
+      // stage since), so these parity waits return at once.
+      wait_bounded(q_full, 0, p.err);
+      for (int i = max(0, issued - C::NS); i < issued; ++i) wait_bounded(blob_full(i % C::NS), (i / C::NS) & 1, p.err);
     }
   } else if (warp == kMmaS) {
     // ------------------------------------------------------------ S issuer
@@ -958,23 +985,42 @@ __global__ void __launch_bounds__(P1MCfg<D, U>::kThreads, 1) pass1_multi_kernel(
       // address field (address >> 4, no carry out of it inside shared memory)
       const uint64_t qd0 = smem_desc(sbase, 128, 4 * D, 0);
       const uint64_t kd0 = smem_desc(sbase + C::kStageOff + blob_kcodes(D), 128, 4 * D, 0);
+#if APA_P1_EXP_ISSUE
+      uint64_t kd[C::NS][D / 64];
+#pragma unroll
+      for (int st = 0; st < C::NS; ++st)
+#pragma unroll
+        for (int kk = 0; kk < D / 64; ++kk) kd[st][kk] = kd0 + ((uint32_t)(st * C::kBlob + 256 * kk) >> 4);
+#endif
       for (int i = 0; ok && i < n; ++i) {
         const int st = i % C::NS;
         const uint32_t sfk = tmem + C::kSFK + C::kSfc * (i & 1);
+#if APA_P1_EXP_ISSUE
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          if (!ok) break;
+#else
         for (int u = 0; ok && u < U; ++u) {
-          // S(u, i) once the previous user of the S buffer has read it out
-          if (u > 0) {
+#endif
+          // S(u, i) once the previous user of its S buffer has read it out: unit u-1 at
+          // tile i with one shared buffer, unit u at tile i-1 with one buffer per unit
+          if (u == 0 && !(ok = load_sfk(i))) break;  // its buffer was last read by S(*, i-2)
+          if (C::kSplitS) {
+            if (i > 0 && !(ok = mbar_spin_wait(s_free(u), (i - 1) & 1, &abort_flag, p.err))) break;
+          } else if (u > 0) {
             if (!(ok = mbar_spin_wait(s_free(u - 1), i & 1, &abort_flag, p.err))) break;
           } else {
-            // the K scales of tile i: their buffer was last read by S(*, i-2)
-            if (!(ok = load_sfk(i))) break;
             if (i > 0 && !(ok = mbar_spin_wait(s_free(U - 1), (i - 1) & 1, &abort_flag, p.err))) break;
           }
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < D / 64; ++kk)
-            mma_nvf4(tmem + C::kS, qd0 + ((uint32_t)(u * C::kQStride + 256 * kk) >> 4),
+            mma_nvf4(tmem + C::kS + (C::kSplitS ? 64 * u : 0), qd0 + ((uint32_t)(u * C::kQStride + 256 * kk) >> 4),
+#if APA_P1_EXP_ISSUE
+                     kd[st][kk], idS, tmem + C::kSFQ + 4 * ((D / 64) * u + kk),
+#else
                      kd0 + ((uint32_t)(st * C::kBlob + 256 * kk) >> 4), idS, tmem + C::kSFQ + 4 * ((D / 64) * u + kk),
+#endif
                      sfk + 4 * (kk >> 1) + 2 * (kk & 1), kk > 0);
           mma_commit(s_full(u));
         }
@@ -1057,8 +1103,13 @@ __global__ void __launch_bounds__(P1MCfg<D, U>::kThreads, 1) pass1_multi_kernel(
       if (!(ok = warp_wait(s_full(u), i & 1))) break;
       tc_fence_after();
       uint32_t sr[64];
-      tmem_ld_x32(tmem + lane_base + C::kS, sr);
-      tmem_ld_x32(tmem + lane_base + C::kS + 32, sr + 32);
+      const uint32_t tS = tmem + lane_base + C::kS + (C::kSplitS ? 64 * u : 0);
+#if APA_P1_EXP_LD64
+      tmem_ld_x64(tS, sr);
+#else
+      tmem_ld_x32(tS, sr);
+      tmem_ld_x32(tS + 32, sr + 32);
+#endif
       tmem_wait_ld();
       tc_fence_before();
       __syncwarp();
@@ -1299,7 +1350,7 @@ cudaError_t launch_d(const P1Params& prm, bool wide, bool rowsum_mma, cudaStream
   if (prm.q2_blob) return launch_dv<D, false>(prm, st);
   if (rowsum_mma) return launch_dv<D, true>(prm, st);
   if constexpr (D <= 128) {
-    if (!wide) return launch_multi<D, 3>(prm, st);
+    if (!wide) return launch_multi<D, APA_P1_UNITS>(prm, st);
   }
   return launch_dv<D, false>(prm, st);
 }
@@ -1322,7 +1373,7 @@ bool single_quantizes_kv(const Shape& s) {
 
 template <int D>
 bool multi_quantizes_kv(const Shape& s) {
-  constexpr int U = 3;
+  constexpr int U = APA_P1_UNITS;
   using C = P1MCfg<D, U>;
   int dev = 0, sms = 0, per_sm = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
@@ -1353,6 +1404,20 @@ bool pass1_quantizes_kv(const Shape& s, bool wide, bool q_residual, bool rowsum_
   return false;
 }
 
+#ifdef APA_TEST_HOOKS
+// Test builds only: while switched on, pass 1 with the K/V quantizer in its launch
+// waits on a flag that nothing sets, so that its bounded wait runs out and the
+// kernel unwinds; the call then reports APA_ERR_DEVICE through apa_check_error.
+__device__ uint32_t g_never_set;
+bool g_test_stuck = false;
+}  // namespace apa
+extern "C" int apa_test_stuck_quantizer_flags(int on) {
+  apa::g_test_stuck = on != 0;
+  return 0;
+}
+namespace apa {
+#endif
+
 cudaError_t launch_pass1(const Shape& s, const Workspace& ws, float eps, uint32_t* hot_mask, bool wide, cudaStream_t st,
                          const KvSource* kv, bool rowsum_mma) {
   P1Params prm{};
@@ -1376,6 +1441,11 @@ cudaError_t launch_pass1(const Shape& s, const Workspace& ws, float eps, uint32_
     prm.v_raw = static_cast<const uint16_t*>(kv->v);
     prm.ws = ws;
     prm.lse_scales = kv->lse ? 1 : 0;
+#ifdef APA_TEST_HOOKS
+    void* never = nullptr;
+    if (g_test_stuck && cudaGetSymbolAddress(&never, g_never_set) == cudaSuccess)
+      prm.test_never = static_cast<const uint32_t*>(never);
+#endif
   }
   prm.err = device_error_word();
   switch (s.d) {

@@ -295,9 +295,9 @@ __global__ void __launch_bounds__(kThreads, P2Cfg<D>::kCtasPerSm)
         }
         issued = i + 1;
       }
-      if (abort_flag) {  // let copies in flight land before the CTA exits
-        for (int i = max(0, issued - C::NS); i < issued; ++i) wait_bounded(kv_full(i % C::NS), (i / C::NS) & 1, p.err);
-      }
+      // every copy issued lands before the CTA exits, also when another warp gave up
+      // after this loop ended (normally they have all landed: the waits return at once)
+      for (int i = max(0, issued - C::NS); i < issued; ++i) wait_bounded(kv_full(i % C::NS), (i / C::NS) & 1, p.err);
     }
   } else if (warp == 5) {
     // ------------------------------------------------------------ S issuer
@@ -732,9 +732,9 @@ __global__ void __launch_bounds__(P2DualCfg<D>::kThreads, 1)
         for (int a = 0; a < C::kAtoms; ++a) tma_load_3d(kdst + a * 8192, &kmap, a * 64, ky, kz, k_full(st));
         issued = i + 1;
       }
-      if (abort_flag) {  // let copies in flight land before the CTA exits
-        for (int i = max(0, issued - C::NS); i < issued; ++i) wait_bounded(k_full(i % C::NS), (i / C::NS) & 1, p.err);
-      }
+      // every copy issued lands before the CTA exits, also when another warp gave up
+      // after this loop ended (normally they have all landed: the waits return at once)
+      for (int i = max(0, issued - C::NS); i < issued; ++i) wait_bounded(k_full(i % C::NS), (i / C::NS) & 1, p.err);
     }
   } else if (warp == kProdV) {
     // ------------------------------------------------------------ TMA producer of V
@@ -750,9 +750,7 @@ __global__ void __launch_bounds__(P2DualCfg<D>::kThreads, 1)
         for (int a = 0; a < C::kAtoms; ++a) tma_load_3d(vdst + a * 8192, &vmap, a * 64, t * kTile, bh, v_full(st));
         issued = i + 1;
       }
-      if (abort_flag) {
-        for (int i = max(0, issued - C::NSV); i < issued; ++i) wait_bounded(v_full(i % C::NSV), (i / C::NSV) & 1, p.err);
-      }
+      for (int i = max(0, issued - C::NSV); i < issued; ++i) wait_bounded(v_full(i % C::NSV), (i / C::NSV) & 1, p.err);
     }
   } else if (warp == kMmaS || warp == kMmaS1) {
     // ------------------------------------------------------------ S issuers: tile i into group i % 2's S

@@ -86,10 +86,12 @@ def _check_apa(w, q, k, v, eps, causal=True, record=None, **options):
 
 # The GPU encodes P with ex2.approx, so its FP4 tile sums can differ from the
 # oracle's FP64 ones in the last bits, and a tile the oracle finds a hair above
-# eps * lambda can come out cold on the GPU (such a tile also counts against the
-# 99.9 % mask agreement).  COLD_SLACK bounds that excess; the measured worst
-# ratio of every case is recorded as a test property.
-COLD_SLACK = 1.02
+# eps * lambda could come out cold on the GPU (it would also count against the
+# 99.9 % mask agreement).  No slack is allowed: on GB300 the worst GPU-cold tile
+# of any case here is 0.994 of eps (and every mask agrees), and the kernels are
+# deterministic, so the margin holds run after run.  The measured worst ratio of
+# every case is recorded as a test property (cold_worst_over_eps).
+COLD_SLACK = 1.0
 
 
 @pytest.mark.parametrize("name", list(SHAPES))

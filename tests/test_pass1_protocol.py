@@ -17,7 +17,16 @@ mbarrier waits test parity as the hardware does.  The checks:
   - every schedule ends.
 Each run draws a speed per actor and a completion rate per kind of op, so that
 schedules with a lagging issuer or long-running MMAs occur.  Planted mistakes (a
-missing wait) must be caught."""
+missing wait) must be caught.
+
+The unwind after a wait gives up is modelled too.  Some wait times out (at a random
+moment), or the producer's wait for the in-launch quantizer's flag of some tile
+does: the CTA's abort flag is set, and every wait that sees it returns false.  The
+producer always ends by waiting (bounded, ignoring the flag) for its copies to land
+(a consumer may give up after the producer's loop has ended);
+each issuer commits a drain barrier and waits for it, so that all of its tcgen05
+operations have completed; the units leave their loops.  When the CTA exits and
+frees TMEM, no bulk copy, tcgen05 operation or commit may still be in flight."""
 import random
 
 import pytest
@@ -37,23 +46,33 @@ class Violation(Exception):
     pass
 
 
-def run(n, U, NS, seed, drop=None):
+class Aborted(Exception):
+    """A wait saw the CTA's abort flag (mbar_wait returning false)."""
+
+
+def run(n, U, NS, seed, drop=None, abort_step=None, stuck_tile=None, drain=True):
     """One random schedule of one CTA walking n tiles with U units and an NS-stage
     blob ring.  drop names a wait to leave out (a planted mistake): "sfv" (the PV
     issuer's wait before copying tile i's V scales over those of tile i-2), "pbuf"
     (a unit's wait before writing P over the buffer of tile i-2), "s_free" (the S
-    issuer's wait for the previous unit to read S)."""
+    issuer's wait for the previous unit to read S).  abort_step: the scheduler step
+    at which some wait times out and sets the abort flag; stuck_tile: the tile whose
+    quantizer flag never comes (the producer's wait for it gives up); drain=False
+    plants a missing unwind (no waits for copies and drain barriers)."""
     rng = random.Random(seed)
     bars = {}
+    state = {"abort": False}
 
     def bar(name, count=1):
         if name not in bars:
             bars[name] = Bar(count)
         return bars[name]
 
-    def wait(name, phase, count=1):
+    def wait(name, phase, count=1, abortable=True):
         b = bar(name, count)
         while b.done % 2 == phase % 2:
+            if abortable and state["abort"]:
+                raise Aborted
             yield None
         if b.done != phase + 1:
             raise Violation(f"wait on {name} for phase {phase} passed at {b.done} completed phases")
@@ -80,19 +99,42 @@ def run(n, U, NS, seed, drop=None):
         return not earlier  # commit
 
     def producer():
-        for i in range(n):
-            st = i % NS
-            if i >= NS:
-                yield from wait(("blob_empty", st), i // NS - 1, 2)
-            blob[st] = None
+        issued = 0
+        try:
+            for i in range(n):
+                st = i % NS
+                if i >= NS:
+                    yield from wait(("blob_empty", st), i // NS - 1, 2)
+                if i == stuck_tile:  # the quantizer's flag of this tile never comes
+                    state["abort"] = True
+                    raise Aborted
+                blob[st] = None
 
-            def land(st=st, i=i):
-                blob[st] = i
-                bar(("blob_full", st)).arrive()
-            issue(None, "tma", land)
-            yield None
+                def land(st=st, i=i):
+                    blob[st] = i
+                    bar(("blob_full", st)).arrive()
+                issue(None, "tma", land)
+                issued = i + 1
+                yield None
+        except Aborted:
+            pass
+        if drain:  # every copy issued lands before the CTA exits (at once, normally)
+            for i in range(max(0, issued - NS), issued):
+                yield from wait(("blob_full", i % NS), i // NS, abortable=False)
+
+    def drained(thread, name):
+        if drain:
+            issue(thread, "commit", lambda: bar(name).arrive())
+            yield from wait(name, 0, abortable=False)
 
     def s_issuer():
+        try:
+            yield from s_loop()
+        except Aborted:
+            pass
+        yield from drained("s", "drain_s")
+
+    def s_loop():
         for i in range(n):
             st = i % NS
             for u in range(U):
@@ -124,6 +166,13 @@ def run(n, U, NS, seed, drop=None):
             issue("s", "commit", lambda st=st: bar(("blob_empty", st), 2).arrive())
 
     def pv_issuer():
+        try:
+            yield from pv_loop()
+        except Aborted:
+            pass
+        yield from drained("pv", "drain_pv")
+
+    def pv_loop():
         for i in range(n):
             st = i % NS
             for u in range(U):
@@ -159,6 +208,12 @@ def run(n, U, NS, seed, drop=None):
             issue("pv", "commit", lambda st=st: bar(("blob_empty", st), 2).arrive())
 
     def unit(u):
+        try:
+            yield from unit_loop(u)
+        except Aborted:
+            pass
+
+    def unit_loop(u):
         for i in range(n):
             yield from wait(("s_full", u), i)
             if sbuf["who"] != (u, i):
@@ -185,8 +240,13 @@ def run(n, U, NS, seed, drop=None):
     # decades, so that slow issuers and long-running MMAs both occur
     speed = {id(a): 10 ** rng.uniform(-2, 0) for a in live}
     rate = {k: 10 ** rng.uniform(-2, 0) for k in ("tma", "cp", "mma", "commit")}
-    for _ in range(400000):
-        if not live and not ops:
+    for step in range(400000):
+        if step == abort_step:
+            state["abort"] = True  # some wait ran out of time
+        if not live:
+            # every warp is done: the CTA frees TMEM and exits
+            if ops:
+                raise Violation(f"CTA exits with {[o[2] for o in ops]} in flight")
             return
         ready = [k for k, op in enumerate(ops) if completable(op)]
         choices = [("a", a) for a in live] + [("c", k) for k in ready]
@@ -220,6 +280,32 @@ def test_planted_missing_waits_are_caught(drop):
     for seed in range(150):
         try:
             run(10, U=3, NS=4, seed=seed, drop=drop)
+        except Violation:
+            caught += 1
+    assert caught > 0
+
+
+@pytest.mark.parametrize("n", [1, 3, 9])
+def test_unwind_after_a_timeout_ends_with_nothing_in_flight(n):
+    """A wait that gives up at any moment: every actor stops and the CTA exits with
+    no copy or tcgen05 operation in flight."""
+    for seed in range(60):
+        run(n, U=3, NS=4, seed=seed, abort_step=random.Random(seed).randrange(0, 60 * n + 1))
+
+
+@pytest.mark.parametrize("stuck", [0, 1, 4, 7])
+def test_unwind_when_the_quantizer_flag_never_comes(stuck):
+    for seed in range(40):
+        run(9, U=3, NS=4, seed=seed, stuck_tile=stuck)
+
+
+def test_planted_missing_unwind_is_caught():
+    # without the producer's wait for its copies and the issuers' drain barriers,
+    # some schedules exit with work in flight
+    caught = 0
+    for seed in range(100):
+        try:
+            run(9, U=3, NS=4, seed=seed, stuck_tile=5, drain=False)
         except Violation:
             caught += 1
     assert caught > 0
