@@ -816,21 +816,9 @@ __global__ void __launch_bounds__(kThreads, (D <= 128 ? 2 : 1)) pass1_kernel(con
 // serial bottleneck for three units: the S warp issues S(0,i), S(1,i), ... in
 // the order in which the units hand the S buffer on; the PV warp issues
 // PV(u,i) as each unit publishes P(u,i).
-#ifndef APA_P1_UNITS
-#define APA_P1_UNITS 3  // 128-row blocks per CTA of the multi-block kernel
-#endif
-#ifndef APA_P1_EXP_ISSUE
-#define APA_P1_EXP_ISSUE 0
-#endif
-#ifndef APA_P1_EXP_LD64
-#define APA_P1_EXP_LD64 0
-#endif
-#ifndef APA_P1_SPLIT_S
-#define APA_P1_SPLIT_S 0  // 1: one S buffer per unit instead of one the units share
-#endif
+constexpr int kUnits = 3;  // 128-row blocks per CTA of the multi-block kernel
 template <int D, int U>
 struct P1MCfg {
-  static constexpr bool kSplitS = APA_P1_SPLIT_S != 0;
   static constexpr int NS = 4;
   static constexpr int kBlob = blob_bytes(D);
   static constexpr int kQBlob = qblob_bytes(D);
@@ -841,15 +829,15 @@ struct P1MCfg {
   static constexpr int kSmem = kPsfOff + U * 2 * 512 + 128;
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kSfc = 4 * sf_chunks(D);
-  static constexpr uint32_t kS = U * D;                       // S, or S(u) at kS + 64 u
-  static constexpr uint32_t kSFQ = kS + 64 * (kSplitS ? U : 1);  // U x 4 * (D/64)
+  static constexpr uint32_t kS = U * D;
+  static constexpr uint32_t kSFQ = kS + 64;                   // U x 4 * (D/64)
   static constexpr uint32_t kSFK = kSFQ + U * 4 * (D / 64);   // 2 buffers (tile % 2)
   static constexpr uint32_t kSFV = kSFK + 2 * kSfc;           // 2 buffers (tile % 2)
   static constexpr uint32_t kSFP = kSFV + 2 * kSfc;           // [U][2] buffers (tile % 2)
   static_assert(kSFP + 8 * U <= kTmemCols, "TMEM budget");
   static constexpr int kThreads = (4 * U + 3) * 32;
   // thread groups of the K/V quantizer role (each a multiple of d/16 threads)
-  static constexpr int kQuantGroups = kThreads % 3 == 0 ? 3 : 2;
+  static constexpr int kQuantGroups = 3;
   static_assert(kThreads % kQuantGroups == 0 && (kThreads / kQuantGroups) % (D / 16) == 0 &&
                     kQuantGroups <= kQuantRoleGroups,
                 "quantizer groups");
@@ -985,42 +973,23 @@ __global__ void __launch_bounds__(P1MCfg<D, U>::kThreads, 1) pass1_multi_kernel(
       // address field (address >> 4, no carry out of it inside shared memory)
       const uint64_t qd0 = smem_desc(sbase, 128, 4 * D, 0);
       const uint64_t kd0 = smem_desc(sbase + C::kStageOff + blob_kcodes(D), 128, 4 * D, 0);
-#if APA_P1_EXP_ISSUE
-      uint64_t kd[C::NS][D / 64];
-#pragma unroll
-      for (int st = 0; st < C::NS; ++st)
-#pragma unroll
-        for (int kk = 0; kk < D / 64; ++kk) kd[st][kk] = kd0 + ((uint32_t)(st * C::kBlob + 256 * kk) >> 4);
-#endif
       for (int i = 0; ok && i < n; ++i) {
         const int st = i % C::NS;
         const uint32_t sfk = tmem + C::kSFK + C::kSfc * (i & 1);
-#if APA_P1_EXP_ISSUE
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-          if (!ok) break;
-#else
         for (int u = 0; ok && u < U; ++u) {
-#endif
-          // S(u, i) once the previous user of its S buffer has read it out: unit u-1 at
-          // tile i with one shared buffer, unit u at tile i-1 with one buffer per unit
-          if (u == 0 && !(ok = load_sfk(i))) break;  // its buffer was last read by S(*, i-2)
-          if (C::kSplitS) {
-            if (i > 0 && !(ok = mbar_spin_wait(s_free(u), (i - 1) & 1, &abort_flag, p.err))) break;
-          } else if (u > 0) {
+          // S(u, i) once the previous user of the S buffer has read it out
+          if (u > 0) {
             if (!(ok = mbar_spin_wait(s_free(u - 1), i & 1, &abort_flag, p.err))) break;
           } else {
+            // the K scales of tile i: their buffer was last read by S(*, i-2)
+            if (!(ok = load_sfk(i))) break;
             if (i > 0 && !(ok = mbar_spin_wait(s_free(U - 1), (i - 1) & 1, &abort_flag, p.err))) break;
           }
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < D / 64; ++kk)
-            mma_nvf4(tmem + C::kS + (C::kSplitS ? 64 * u : 0), qd0 + ((uint32_t)(u * C::kQStride + 256 * kk) >> 4),
-#if APA_P1_EXP_ISSUE
-                     kd[st][kk], idS, tmem + C::kSFQ + 4 * ((D / 64) * u + kk),
-#else
+            mma_nvf4(tmem + C::kS, qd0 + ((uint32_t)(u * C::kQStride + 256 * kk) >> 4),
                      kd0 + ((uint32_t)(st * C::kBlob + 256 * kk) >> 4), idS, tmem + C::kSFQ + 4 * ((D / 64) * u + kk),
-#endif
                      sfk + 4 * (kk >> 1) + 2 * (kk & 1), kk > 0);
           mma_commit(s_full(u));
         }
@@ -1103,13 +1072,8 @@ __global__ void __launch_bounds__(P1MCfg<D, U>::kThreads, 1) pass1_multi_kernel(
       if (!(ok = warp_wait(s_full(u), i & 1))) break;
       tc_fence_after();
       uint32_t sr[64];
-      const uint32_t tS = tmem + lane_base + C::kS + (C::kSplitS ? 64 * u : 0);
-#if APA_P1_EXP_LD64
-      tmem_ld_x64(tS, sr);
-#else
-      tmem_ld_x32(tS, sr);
-      tmem_ld_x32(tS + 32, sr + 32);
-#endif
+      tmem_ld_x32(tmem + lane_base + C::kS, sr);
+      tmem_ld_x32(tmem + lane_base + C::kS + 32, sr + 32);
       tmem_wait_ld();
       tc_fence_before();
       __syncwarp();
@@ -1350,7 +1314,7 @@ cudaError_t launch_d(const P1Params& prm, bool wide, bool rowsum_mma, cudaStream
   if (prm.q2_blob) return launch_dv<D, false>(prm, st);
   if (rowsum_mma) return launch_dv<D, true>(prm, st);
   if constexpr (D <= 128) {
-    if (!wide) return launch_multi<D, APA_P1_UNITS>(prm, st);
+    if (!wide) return launch_multi<D, kUnits>(prm, st);
   }
   return launch_dv<D, false>(prm, st);
 }
@@ -1373,7 +1337,7 @@ bool single_quantizes_kv(const Shape& s) {
 
 template <int D>
 bool multi_quantizes_kv(const Shape& s) {
-  constexpr int U = APA_P1_UNITS;
+  constexpr int U = kUnits;
   using C = P1MCfg<D, U>;
   int dev = 0, sms = 0, per_sm = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
