@@ -825,8 +825,7 @@ struct P1MCfg {
   static constexpr int kQStride = (kQBlob + 1023) / 1024 * 1024;
   static constexpr int kStageOff = U * kQStride;
   static constexpr int kPOff = kStageOff + NS * kBlob;  // [U][2] x (128 rows x 32 B)
-  static constexpr int kPsfOff = kPOff + U * 2 * 4096;  // [U][2] x 512-B scale atoms
-  static constexpr int kSmem = kPsfOff + U * 2 * 512 + 128;
+  static constexpr int kSmem = kPOff + U * 2 * 4096 + 128;  // (P's scales go straight to TMEM)
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kSfc = 4 * sf_chunks(D);
   static constexpr uint32_t kS = U * D;
@@ -1030,9 +1029,8 @@ __global__ void __launch_bounds__(P1MCfg<D, U>::kThreads, 1) pass1_multi_kernel(
             if (hot) p.hot_list[((size_t)bh * nblk + blk) * T + count[u]++] = (uint32_t)tile_of(i) | (hot << 16);
             if ((hot | invalid) != 0xFFu) {
               // P buffer (u, i % 2) and its TMEM scales were last read by PV(u, i-2); unit u
-              // waited for it before writing P(u, i)
+              // waited for it before writing P(u, i) and its scales
               const int pb = 2 * u + (i & 1);
-              tmem_cp_32x128b_x4(tmem + C::kSFP + 4 * pb, smem_desc(sbase + C::kPsfOff + 512 * pb, 128, 128, 0));
               mma_nvf4(tmem + D * u, smem_desc(sbase + C::kPOff + 4096 * pb, 128, 256, 0),
                        smem_desc(blob + blob_vcodes(D), 128, 256, 0), idO, tmem + C::kSFP + 4 * pb, sfv,
                        pv_issued[u] > 0);
@@ -1173,18 +1171,24 @@ __global__ void __launch_bounds__(P1MCfg<D, U>::kThreads, 1) pass1_multi_kernel(
           tmem_wait_st();
         }
       }
-      // P buffer (u, i % 2) was last read by PV(u, i-2).  A hot group's scales are zero.
+      // P buffer (u, i % 2) and its scales were last read by PV(u, i-2).  A hot group's
+      // scales are zero.
       if (i >= 2 && !(ok = warp_wait(pv_done(u, i & 1), ((i - 2) >> 1) & 1))) break;
       const int pbuf = 2 * u + (i & 1);
       uint8_t* pbp = smem + C::kPOff + 4096 * pbuf + (r >> 3) * 256 + (r & 7) * 16;
       *reinterpret_cast<uint4*>(pbp) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
       *reinterpret_cast<uint4*>(pbp + 128) = make_uint4(pw[4], pw[5], pw[6], pw[7]);
-      *reinterpret_cast<uint32_t*>(smem + C::kPsfOff + 512 * pbuf + sf_atom_off(r, 0)) = hot ? 0u : sfw;
+      // the row's four P scales go straight into its own TMEM lane: a 32x128b.warpx4
+      // copy of the 512-byte scale atom would put row 32c + l at lane l, column c of
+      // every lane quarter, and lane quarter qw's MMA rows read column qw, so this one
+      // word is the one the PV product reads for this row
+      tmem_st_x1(tmem + lane_base + C::kSFP + 4 * pbuf + qw, hot ? 0u : sfw);
       if (lane == 0) gbits[u][i & 1][qw] = ((uint32_t)hot_lo << (2 * qw)) | ((uint32_t)hot_hi << (2 * qw + 1));
       if (p.hot_mask && (lane == 0 || lane == 16) && hot) {
         const int gi = (blk * kBlockRows + 32 * qw + lane) / kGroupRows;
         if (gi < ngroups) atomicOr(&p.hot_mask[((size_t)bh * ngroups + gi) * nwords + t / 32], 1u << (t % 32));
       }
+      tmem_wait_st();
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();

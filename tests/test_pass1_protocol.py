@@ -6,7 +6,9 @@ softmax warps of a 128-row block as one actor).  Asynchronous work:
   - bulk copies of the per-tile NVFP4 blobs land in any order;
   - each issuing thread's MMAs complete in issue order; a tcgen05.cp lands before
     any later op of its thread but not necessarily after that thread's earlier
-    MMAs; a commit arrives once every earlier op of its thread has completed.
+    MMAs; a commit arrives once every earlier op of its thread has completed;
+  - a unit writes P to shared memory and P's scales into TMEM itself (tcgen05.st,
+    completed by tcgen05.wait::st before it hands P over).
 mbarrier waits test parity as the hardware does.  The checks:
   - every wait that passes lands on the phase it means;
   - the one S buffer is never overwritten before its unit has read it, and a unit
@@ -190,12 +192,6 @@ def run(n, U, NS, seed, drop=None, abort_step=None, stuck_tile=None, drain=True)
                 if pbuf.get((u, i & 1)) != i:
                     raise Violation(f"PV issuer found P buffer ({u},{i & 1}) holding {pbuf.get((u, i & 1))}, not {i}")
 
-                def cpp(i=i, u=u):
-                    if pbuf.get((u, i & 1)) != i:
-                        raise Violation(f"P scales of ({u},{i}) read from a buffer holding {pbuf.get((u, i & 1))}")
-                    sfp[(u, i & 1)] = i
-                issue("pv", "cp", cpp)
-
                 def mma(i=i, st=st, u=u):
                     got = (blob.get(st), sfv.get(i & 1), sfp.get((u, i & 1)), pbuf.get((u, i & 1)))
                     if got != (i, i, i, i):
@@ -227,7 +223,10 @@ def run(n, U, NS, seed, drop=None, abort_step=None, stuck_tile=None, drain=True)
                     raise Violation(f"unit {u} rescaled O with a P.V in flight at tile {i}")
             if i >= 2 and drop != "pbuf":
                 yield from wait(("pv_done", u, i & 1), (i - 2) >> 1)
+            # P to shared memory, and its scales straight into TMEM by tcgen05.st, waited
+            # for (tcgen05.wait::st) before the arrive
             pbuf[(u, i & 1)] = i
+            sfp[(u, i & 1)] = i
             bar(("p_full", u, i & 1)).arrive()
             yield None
         if n:
