@@ -36,9 +36,13 @@
 // softmax warp groups per block take alternate entries of the hot list, each
 // with its own (m, l), its own O in TMEM and its own double-buffered S, so one
 // group's exp/convert/store of P overlaps the other's S and PV MMAs.  13 warps:
-// eight softmax, a TMA producer each for K (6-stage ring) and V (4 stages), an S
-// issuer per group and one PV issuer; one P buffer per group.  The block's final state is the merge of
-// the pass-1 state, group 0's and group 1's, in that order.  The per-row work is
+// eight softmax, a TMA producer each for K (8-stage ring) and V (4 stages), an S
+// issuer per group and one PV issuer.  P never goes through shared memory: each
+// softmax thread writes its row of P (FP16) over the first half of the S slot it
+// read, and the PV product takes its A operand from TMEM; an S issuer writes the
+// next S into a slot only after the P.V that read the slot's P has completed.
+// The block's final state is the merge of the pass-1 state, group 0's and group
+// 1's, in that order.  The per-row work is
 // the same as the one-group kernel's; only the tile-to-accumulator assignment
 // (and so the rounding order of the merge) differs.
 #include <cstring>
@@ -560,28 +564,23 @@ __device__ __forceinline__ bool dual_sync_and(bool v) {
 // P.V product of an older tile, so the S MMAs run up to NSK tiles ahead.  Each
 // group has its own S-issuing warp; the PV warp serves both groups in list order.
 #ifndef APA_P2D_KSTAGES
-#define APA_P2D_KSTAGES 6  // K stages of the two-group pass 2 (even: see P2DualCfg)
+#define APA_P2D_KSTAGES 8  // K stages of the two-group pass 2 (even: see P2DualCfg)
 #endif
 #ifndef APA_P2D_VSTAGES
 #define APA_P2D_VSTAGES 4  // V stages of the two-group pass 2
-#endif
-#ifndef APA_P2D_PBUFS
-#define APA_P2D_PBUFS 1  // P buffers per group of the two-group pass 2
 #endif
 template <int D>
 struct P2DualCfg {
   static constexpr int NS = APA_P2D_KSTAGES;   // K stages
   static constexpr int NSV = APA_P2D_VSTAGES;  // V stages
-  static constexpr int NP = APA_P2D_PBUFS;   // P buffers per group
   static constexpr int kAtoms = D / 64;
   static constexpr int kQBytes = 128 * D * 2;
   static constexpr int kKVBytes = 64 * D * 2;
-  static constexpr int kPBytes = 128 * 64 * 2;
   static constexpr int kQOff = 0;
   static constexpr int kKOff = kQBytes;
   static constexpr int kVOff = kKOff + NS * kKVBytes;
-  static constexpr int kPOff = kVOff + NSV * kKVBytes;  // [2][NP] P
-  static constexpr int kMlOff = kPOff + 2 * NP * kPBytes;      // group 1's (m, l) per row for the merge
+  // (P goes from the softmax threads into TMEM, over the S slot it came from)
+  static constexpr int kMlOff = kVOff + NSV * kKVBytes;  // group 1's (m, l) per row for the merge
   static constexpr int kSIssuers = 2;  // S-issuing warps: one per group
   // The two S issuers each wait on the K arrivals of their own entries (i % 2).  With
   // NS even, entry i's K stage i % NS is only ever used by entries of the same
@@ -595,7 +594,6 @@ struct P2DualCfg {
   static constexpr int kBarOff = kMlOff + 128 * 8;
   static constexpr int kSmem = kBarOff + kNumBars * 8 + 16 + 1024;
   static_assert(kSmem <= 232448, "shared memory");
-  static_assert(NP <= 2, "pv_done slots");
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kSBase = 2 * D;  // S(u, b) at kSBase + 128 u + 64 b; O(u) at D u
   static constexpr int kThreads = 13 * 32;
@@ -639,7 +637,8 @@ __global__ void __launch_bounds__(P2DualCfg<D>::kThreads, 1)
   auto v_full = [&](int st) { return bar0 + 8u * (2 * C::NS + st); };
   auto v_empty = [&](int st) { return bar0 + 8u * (2 * C::NS + C::NSV + st); };
   auto s_full = [&](int u, int b2) { return bar0 + 8u * (C::kB0 + 8 * u + b2); };
-  auto s_free = [&](int u, int b2) { return bar0 + 8u * (C::kB0 + 8 * u + 2 + b2); };
+  // (slots kB0 + 8 u + 2, 3 are unused: a slot of S is free once the P.V that reads
+  // the P written over it has completed, so pv_done tells the S issuers)
   auto p_full = [&](int u, int b2) { return bar0 + 8u * (C::kB0 + 8 * u + 4 + b2); };
   auto pv_done = [&](int u, int b2) { return bar0 + 8u * (C::kB0 + 8 * u + 6 + b2); };
   const uint32_t drain_pv = bar0 + 8u * (C::kB0 + 16);
@@ -666,7 +665,7 @@ __global__ void __launch_bounds__(P2DualCfg<D>::kThreads, 1)
     for (int i = 0; i < C::kNumBars; ++i) {
       uint32_t count = 1;
       const int j = i - C::kB0;
-      if (j >= 0 && j < 16 && (j & 7) >= 2 && (j & 7) < 6) count = 4;  // s_free, p_full: the group's four warps
+      if (j >= 0 && j < 16 && (j & 7) >= 4 && (j & 7) < 6) count = 4;  // p_full: the group's four warps
       mbar_init(bar0 + 8u * i, count);
     }
     fence_mbar_init();
@@ -773,7 +772,8 @@ __global__ void __launch_bounds__(P2DualCfg<D>::kThreads, 1)
           }
           fence_proxy_async_smem();
         }
-        if (j >= 2 && !(ok = mbar_wait(s_free(v, b2), ((j >> 1) - 1) & 1, &abort_flag, p.err))) break;
+        // the slot holds P of this group's entry j - 2 until its P.V has read it
+        if (j >= 2 && !(ok = mbar_wait(pv_done(v, b2), ((j >> 1) - 1) & 1, &abort_flag, p.err))) break;
         tc_fence_after();
         const uint32_t kaddr = sbase + C::kKOff + st * C::kKVBytes;
 #pragma unroll
@@ -799,12 +799,12 @@ __global__ void __launch_bounds__(P2DualCfg<D>::kThreads, 1)
         if (!(ok = mbar_wait(v_full(st), (i / C::NSV) & 1, &abort_flag, p.err))) break;
         tc_fence_after();
         const uint32_t vaddr = sbase + C::kVOff + st * C::kKVBytes;
-        const uint32_t paddr = sbase + C::kPOff + (v * C::NP + j % C::NP) * C::kPBytes;
+        // P (FP16) sits in the first 32 columns of its group's S slot: 16 keys per MMA
+        const uint32_t pcol = tmem + C::kSBase + 128u * v + 64u * b2;
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
           const uint64_t bd = smem_desc(vaddr + kk * 2048, 8192, 1024, kSwizzle128B);
-          mma_bf16(tmem + (uint32_t)(D * v), smem_desc(paddr + kk * 32, 16, 1024, kSwizzle128B), bd, idO,
-                   (j > 0 || kk > 0) ? 1u : 0u);
+          mma_f16_ts(tmem + (uint32_t)(D * v), pcol + 8u * kk, bd, idO, (j > 0 || kk > 0) ? 1u : 0u);
         }
         mma_commit(pv_done(v, b2));
         mma_commit(v_empty(st));  // this stage's V has been read
@@ -831,28 +831,27 @@ __global__ void __launch_bounds__(P2DualCfg<D>::kThreads, 1)
       const bool row_hot = row_valid && ((gm >> (r >> 4)) & 1u);
       const int j0 = t * kTile;
       const int nvis = row_hot ? min(kTile, vis_last + 1 - j0) : 0;  // keys j0 .. j0+nvis-1 visible
-      uint8_t* prow = smem + C::kPOff + (u * C::NP + j % C::NP) * C::kPBytes + r * 128;
+      // P (FP16, two keys per column) goes over the first 32 columns of the S slot it
+      // came from; the slot's previous P had been read before S was written into it
+      const uint32_t pslot = tmem + lane_base + tS + 64u * (j & 1);
+      tc_fence_after();
       if (!__any_sync(0xffffffffu, nvis > 0)) {
         // neither of this warp's two groups of rows takes part in this tile: its P rows are zero
-        __syncwarp();
-        if (lane == 0) mbar_arrive(s_free(u, j & 1));
-        if (j >= C::NP && !(ok = warp_wait(pv_done(u, (j - C::NP) & 1), ((j - C::NP) >> 1) & 1))) break;
+        uint32_t z[16];
 #pragma unroll
-        for (int ch = 0; ch < 8; ++ch)
-          *reinterpret_cast<uint4*>(prow + ((ch ^ (r & 7)) << 4)) = make_uint4(0u, 0u, 0u, 0u);
-        fence_proxy_async_smem();
+        for (int x = 0; x < 16; ++x) z[x] = 0u;
+        tmem_st_x16(pslot, z);
+        tmem_st_x16(pslot + 16, z);
+        tmem_wait_st();
+        tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(p_full(u, j & 1));
         continue;
       }
-      tc_fence_after();
       uint32_t raw[64];
-      tmem_ld_x32(tmem + lane_base + tS + 64 * (j & 1), raw);
-      tmem_ld_x32(tmem + lane_base + tS + 64 * (j & 1) + 32, raw + 32);
+      tmem_ld_x32(pslot, raw);
+      tmem_ld_x32(pslot + 32, raw + 32);
       tmem_wait_ld();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(s_free(u, j & 1));
       float sv[64];
 #pragma unroll
       for (int x = 0; x < 64; ++x) sv[x] = __uint_as_float(raw[x]);
@@ -877,15 +876,17 @@ __global__ void __launch_bounds__(P2DualCfg<D>::kThreads, 1)
         }
         m2 = c;
       }
-      // this P buffer is free once PV(u, j - NP) has completed
-      if (j >= C::NP && !(ok = warp_wait(pv_done(u, (j - C::NP) & 1), ((j - C::NP) >> 1) & 1))) break;
       const float nb = (nvis <= 0 || m2 == -INFINITY) ? -INFINITY : -shift - m2;
       float ps[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int ch = 0; ch < 8; ++ch) {
-        uint32_t hi[4];
-        p8_f16(sv + 8 * ch, c2, nb, hi, ps[ch & 1], ps[2 + (ch & 1)]);
-        *reinterpret_cast<uint4*>(prow + ((ch ^ (r & 7)) << 4)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+      for (int hf = 0; hf < 2; ++hf) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int c4 = 0; c4 < 4; ++c4) {
+          const int ch = 4 * hf + c4;
+          p8_f16(sv + 8 * ch, c2, nb, pk + 4 * c4, ps[ch & 1], ps[2 + (ch & 1)]);
+        }
+        tmem_st_x16(pslot + 16u * hf, pk);
       }
       l2 = l2 * f + ((ps[0] + ps[1]) + (ps[2] + ps[3]));
       if (__any_sync(0xffffffffu, rescale)) {
@@ -902,9 +903,8 @@ __global__ void __launch_bounds__(P2DualCfg<D>::kThreads, 1)
           tmem_st_x16(tmem + lane_base + tO + c0, o);
           tmem_st_x16(tmem + lane_base + tO + c0 + 16, o + 16);
         }
-        tmem_wait_st();
       }
-      fence_proxy_async_smem();
+      tmem_wait_st();  // P (and a rescaled O) in TMEM before P.V is issued
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(p_full(u, j & 1));

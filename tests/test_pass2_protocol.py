@@ -9,14 +9,16 @@ earlier MMAs).  An mbarrier parity wait passes when the barrier's completed-phas
 count has the other parity, exactly as in hardware, so a wait made a phase early
 or two phases late passes on the wrong phase.  The checks:
   - every wait that passes lands on the phase it means (completed count = phase + 1);
-  - every MMA reads the shared-memory stage, S slot or P buffer holding its entry;
+  - every MMA reads the shared-memory stage, S slot or P buffer (or TMEM P slot)
+    holding its entry, and no S is written over a P that its P.V has not read;
   - O is rescaled, or merged, only with none of its group's P.V in flight;
   - every schedule ends (no deadlock).
-The layout the kernel uses (K ring of 6 stages owned by one S issuer per group, a V
-ring of 4) must pass every schedule; a shared K/V ring of 5 stages with two S
-issuers must be caught: there consecutive uses of a stage alternate between the
-issuers, and one of them can wait a phase early while the stage's previous load is
-still landing.  Each run draws a speed per actor and a completion rate for copies
+The layouts the kernel used (K ring of 6 stages owned by one S issuer per group, a V
+ring of 4, P in shared memory) and uses (P written over its S slot in TMEM and read
+from there by the P.V product, K ring of 8, V ring of 4) must pass every schedule.
+A shared K/V ring of 5 stages with two S issuers must be caught: there consecutive
+uses of a stage alternate between the issuers, and one of them can wait a phase
+early while the stage's previous load is still landing.  Each run draws a speed per actor and a completion rate for copies
 and for MMAs, so that lagging issuers and long-running MMAs occur."""
 import random
 
@@ -37,13 +39,16 @@ class Violation(Exception):
     pass
 
 
-def run(n, nsk, nsv, s_issuers, split, seed, pbuf_wait=True, groups=2, np_=1):
+def run(n, nsk, nsv, s_issuers, split, seed, pbuf_wait=True, groups=2, np_=1, p_in_tmem=False):
     """One random schedule of one block with n hot-list entries.  split=False: one
     ring of nsk stages holding K and V (one producer); True: a K ring (nsk) and a V
     ring (nsv), a producer each.  pbuf_wait=False drops the groups' wait for the P
     buffer (a planted mistake).  groups=1 with one S issuer and one ring is the
     one-group kernel (pass2_kernel); np_ is the number of P buffers per group.
-    Raises Violation on a wrong phase or stage."""
+    p_in_tmem: the two-group kernel's form in which a group writes P (FP16) over the
+    S slot it came from and the P.V product reads it from TMEM, so an S issuer waits
+    for the P.V of the slot's previous entry instead of for its S to be read;
+    pbuf_wait=False then drops that wait.  Raises Violation on a wrong phase or stage."""
     rng = random.Random(seed)
     bars = {}
 
@@ -56,6 +61,7 @@ def run(n, nsk, nsv, s_issuers, split, seed, pbuf_wait=True, groups=2, np_=1):
     vst = {}
     sslot = {}  # (group, slot) -> entry whose S is there
     pbuf = {}   # (group, buffer) -> entry whose P is there
+    tslot = {}  # p_in_tmem: (group, slot) -> [entry whose P is there, read by its P.V]
     pv_inflight = [0, 0]
     inflight = []  # (order key or None, callback): None = may complete in any order
 
@@ -90,11 +96,16 @@ def run(n, nsk, nsv, s_issuers, split, seed, pbuf_wait=True, groups=2, np_=1):
             if kst.get(st) != i:
                 raise Violation(f"S({i}) issued on K stage {st} holding {kst.get(st)}")
             if j >= 2:
-                yield from wait(("s_free", v, b2), (j >> 1) - 1, 1)
+                if not p_in_tmem:
+                    yield from wait(("s_free", v, b2), (j >> 1) - 1, 1)
+                elif pbuf_wait:  # the slot holds P of entry i - 2 groups until its P.V has read it
+                    yield from wait(("pv_done", v, b2), (j >> 1) - 1)
 
             def done(i=i, st=st, v=v, b2=b2):
                 if kst.get(st) != i:
                     raise Violation(f"S({i}) read K stage {st} holding {kst.get(st)}")
+                if p_in_tmem and (v, b2) in tslot and not tslot[(v, b2)][1]:
+                    raise Violation(f"S({i}) overwrote P of entry {tslot[(v, b2)][0]} before its P.V read it")
                 sslot[(v, b2)] = i
                 bar(("s_full", v, b2)).arrive()
                 bar((kring + "_empty", st), 1 if split else 2).arrive()
@@ -107,13 +118,18 @@ def run(n, nsk, nsv, s_issuers, split, seed, pbuf_wait=True, groups=2, np_=1):
             b2, pb = j & 1, (i // groups) % np_
             yield from wait(("p_full", v, b2), j >> 1, 1)
             yield from wait((vring + "_full", st), i // nsv_)
-            if vst.get(st) != i or pbuf.get((v, pb)) != i:
-                raise Violation(f"PV({i}) issued on V {vst.get(st)} / P {pbuf.get((v, pb))}")
+
+            def p_of(v=v, b2=b2, pb=pb):
+                return tslot.get((v, b2), [None])[0] if p_in_tmem else pbuf.get((v, pb))
+            if vst.get(st) != i or p_of() != i:
+                raise Violation(f"PV({i}) issued on V {vst.get(st)} / P {p_of()}")
             pv_inflight[v] += 1
 
-            def done(i=i, st=st, v=v, b2=b2, pb=pb):
-                if vst.get(st) != i or pbuf.get((v, pb)) != i:
-                    raise Violation(f"PV({i}) read V {vst.get(st)} / P {pbuf.get((v, pb))}")
+            def done(i=i, st=st, v=v, b2=b2, p_of=p_of):
+                if vst.get(st) != i or p_of() != i:
+                    raise Violation(f"PV({i}) read V {vst.get(st)} / P {p_of()}")
+                if p_in_tmem:
+                    tslot[(v, b2)][1] = True
                 pv_inflight[v] -= 1
                 bar(("pv_done", v, b2)).arrive()
                 bar((vring + "_empty", st), 1 if split else 2).arrive()
@@ -129,15 +145,21 @@ def run(n, nsk, nsv, s_issuers, split, seed, pbuf_wait=True, groups=2, np_=1):
             yield from wait(("s_full", v, j & 1), j >> 1)
             if sslot.get((v, j & 1)) != i:
                 raise Violation(f"group {v} read S slot holding {sslot.get((v, j & 1))} for {i}")
-            bar(("s_free", v, j & 1), 1).arrive()
+            if not p_in_tmem:
+                bar(("s_free", v, j & 1), 1).arrive()
             yield None
-            if j >= np_ and pbuf_wait:  # P buffer j % np_: P.V of entry j - np_ has read it
+            if j >= np_ and pbuf_wait and not p_in_tmem:  # P buffer j % np_: P.V of entry j - np_ has read it
                 yield from wait(("pv_done", v, (j - np_) & 1), (j - np_) >> 1)
             if j >= 1 and rng.random() < 0.3:  # the running maximum moved: rescale O
                 yield from wait(("pv_done", v, (j - 1) & 1), (j - 1) >> 1)
                 if pv_inflight[v]:
                     raise Violation(f"group {v} rescaled O with a P.V in flight at entry {i}")
-            pbuf[(v, j % np_)] = i
+            if p_in_tmem:  # P over the S it came from (tcgen05.st, waited for before the arrive)
+                if sslot.get((v, j & 1)) != i:
+                    raise Violation(f"group {v} wrote P of {i} over S slot holding {sslot.get((v, j & 1))}")
+                tslot[(v, j & 1)] = [i, False]
+            else:
+                pbuf[(v, j % np_)] = i
             bar(("p_full", v, j & 1), 1).arrive()
             yield None
         if v == 0:  # the merge waits for every group's last P.V
@@ -238,6 +260,31 @@ def test_one_group_planted_mistake_is_caught():
     for seed in range(200):
         try:
             run(12, nsk=4, nsv=4, s_issuers=1, split=False, seed=seed, groups=1, np_=2, pbuf_wait=False)
+        except Violation:
+            caught += 1
+    assert caught > 0
+
+
+@pytest.mark.parametrize("n", [0, 1, 2, 3, 5, 8, 13, 24])
+def test_p_in_tmem_layout_is_safe_under_random_schedules(n):
+    """The two-group kernel as it runs: P written over its S slot and read from TMEM
+    by the P.V product, K ring of 8 (each S issuer owns four stages), V ring of 4."""
+    for seed in range(60):
+        run(n, nsk=8, nsv=4, s_issuers=2, split=True, seed=seed, p_in_tmem=True)
+
+
+@pytest.mark.parametrize("nsk,nsv", [(6, 4), (8, 6), (4, 2)])
+def test_p_in_tmem_other_rings_are_safe(nsk, nsv):
+    for seed in range(40):
+        run(17, nsk=nsk, nsv=nsv, s_issuers=2, split=True, seed=seed, p_in_tmem=True)
+
+
+def test_p_in_tmem_planted_mistake_is_caught():
+    """An S issuer that writes S over a slot without waiting for the P.V of the P in it."""
+    caught = 0
+    for seed in range(200):
+        try:
+            run(12, nsk=6, nsv=4, s_issuers=2, split=True, seed=seed, p_in_tmem=True, pbuf_wait=False)
         except Violation:
             caught += 1
     assert caught > 0
