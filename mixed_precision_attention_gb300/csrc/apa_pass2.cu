@@ -77,11 +77,13 @@ constexpr int kThreads = 224;
 constexpr float kTau2 = 8.0f;  // pass-2 lazy rescale threshold (log2 units)
 
 // The barriers live at the end of the dynamic shared-memory window and there is
-// no static shared memory.  With kCtasPerSm = 2 (2 K/V stages, one P buffer,
-// 112 KB per CTA at d = 128) two CTAs would fit an SM with no alignment slack;
-// the kernel then checks that the window starts on a 1024-byte boundary (the
-// 128-byte swizzle needs it).  Measured on the 2048 x 122880 layer, two CTAs of
-// that shape were no faster than one CTA with 3 stages and 2 P buffers.
+// no static shared memory.  With kCtasPerSm = 2 (2 K/V stages, 112 KB per CTA at
+// d = 128 when P still went through shared memory) two CTAs would fit an SM with
+// no alignment slack; the kernel then checks that the window starts on a
+// 1024-byte boundary (the 128-byte swizzle needs it).  Measured on the 2048 x
+// 122880 layer, two CTAs of that shape were no faster than one CTA with 3 stages.
+// P goes from the softmax threads into TMEM, over the S slot it came from, and the
+// PV product reads it there.
 template <int D>
 struct P2Cfg {
   static constexpr int kCtasPerSm = 1;
@@ -89,13 +91,10 @@ struct P2Cfg {
   static constexpr int kAtoms = D / 64;
   static constexpr int kQBytes = 128 * D * 2;
   static constexpr int kKVBytes = 64 * D * 2;  // one of K or V per stage
-  static constexpr int kPBytes = 128 * 64 * 2;  // one 16-bit term of P
-  static constexpr int NP = kCtasPerSm == 2 ? 1 : (D >= 256 ? 1 : 2);  // P buffers
   static constexpr int kQOff = 0;
   static constexpr int kStageOff = kQBytes;
-  static constexpr int kPOff = kStageOff + NS * 2 * kKVBytes;
   static constexpr int kNumBars = 2 * NS + 10;
-  static constexpr int kBarOff = kPOff + NP * kPBytes;
+  static constexpr int kBarOff = kStageOff + NS * 2 * kKVBytes;
   static constexpr int kSlack = kCtasPerSm == 2 ? 0 : 1024;  // runtime alignment room
   static constexpr int kSmem = kBarOff + kNumBars * 8 + 16 + kSlack;
   static constexpr uint32_t kTmemCols = D + 128 <= 256 ? 256 : 512;
@@ -197,7 +196,8 @@ __global__ void __launch_bounds__(kThreads, P2Cfg<D>::kCtasPerSm)
   auto kv_full = [&](int st) { return bar0 + 8u * st; };
   auto kv_empty = [&](int st) { return bar0 + 8u * (C::NS + st); };
   auto s_full = [&](int b2) { return bar0 + 8u * (2 * C::NS + b2); };
-  auto s_free = [&](int b2) { return bar0 + 8u * (2 * C::NS + 2 + b2); };
+  // (slots 2 NS + 2, 3 are unused: an S slot is free once the P.V that reads the P
+  // written over it has completed, so pv_done tells the S issuer)
   auto p_full = [&](int b2) { return bar0 + 8u * (2 * C::NS + 4 + b2); };
   auto pv_done = [&](int b2) { return bar0 + 8u * (2 * C::NS + 6 + b2); };
   const uint32_t drain = bar0 + 8u * (2 * C::NS + 8), drain_pv = bar0 + 8u * (2 * C::NS + 9);
@@ -227,7 +227,7 @@ __global__ void __launch_bounds__(kThreads, P2Cfg<D>::kCtasPerSm)
   if (threadIdx.x == 0) {
     abort_flag = 0;
     for (int i = 0; i < C::kNumBars; ++i) {
-      const bool per_warp = (i >= 2 * C::NS + 2 && i < 2 * C::NS + 6);  // s_free, p_full: one arrive per softmax warp
+      const bool per_warp = (i >= 2 * C::NS + 4 && i < 2 * C::NS + 6);  // p_full: one arrive per softmax warp
       const bool kv_empty_bar = (i >= C::NS && i < 2 * C::NS);           // kv_empty: the S and the PV issuer
       mbar_init(bar0 + 8u * i, per_warp ? 4u : (kv_empty_bar ? 2u : 1u));
     }
@@ -324,7 +324,8 @@ __global__ void __launch_bounds__(kThreads, P2Cfg<D>::kCtasPerSm)
           }
           fence_proxy_async_smem();
         }
-        if (i >= 2 && !mbar_wait(s_free(i & 1), ((i >> 1) - 1) & 1, &abort_flag, p.err)) return false;
+        // the slot holds P of entry i - 2 until its P.V has read it
+        if (i >= 2 && !mbar_wait(pv_done(i & 1), ((i >> 1) - 1) & 1, &abort_flag, p.err)) return false;
         tc_fence_after();
         const uint32_t kaddr = sbase + C::kStageOff + st * 2 * C::kKVBytes;
 #pragma unroll
@@ -353,12 +354,12 @@ __global__ void __launch_bounds__(kThreads, P2Cfg<D>::kCtasPerSm)
         if (!(ok = mbar_wait(kv_full(i % C::NS), (i / C::NS) & 1, &abort_flag, p.err))) break;
         tc_fence_after();
         const uint32_t vaddr = sbase + C::kStageOff + (i % C::NS) * 2 * C::kKVBytes + C::kKVBytes;
-        const uint32_t paddr = sbase + C::kPOff + (i % C::NP) * C::kPBytes;
+        // P (FP16) sits in the first 32 columns of its S slot: 16 keys per MMA
+        const uint32_t pcol = tmem + C::kSCol + 64u * (i & 1);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
           const uint64_t bd = smem_desc(vaddr + kk * 2048, 8192, 1024, kSwizzle128B);
-          mma_bf16(tmem + C::kOCol, smem_desc(paddr + kk * 32, 16, 1024, kSwizzle128B), bd, idO,
-                   (i > 0 || kk > 0) ? 1u : 0u);
+          mma_f16_ts(tmem + C::kOCol, pcol + 8u * kk, bd, idO, (i > 0 || kk > 0) ? 1u : 0u);
         }
         mma_commit(pv_done(i & 1));
         mma_commit(kv_empty(i % C::NS));  // this stage's V has been read
@@ -385,30 +386,27 @@ __global__ void __launch_bounds__(kThreads, P2Cfg<D>::kCtasPerSm)
       const bool row_hot = row_valid && ((gm >> (r >> 4)) & 1u);
       const int j0 = t * kTile;
       const int nvis = row_hot ? min(kTile, vis_last + 1 - j0) : 0;  // keys j0 .. j0+nvis-1 visible
+      // P (FP16, two keys per column) goes over the first 32 columns of the S slot it
+      // came from; the slot's previous P had been read before S was written into it
+      const uint32_t pslot = tmem + lane_base + C::kSCol + 64u * (i & 1);
+      tc_fence_after();
       if (!__any_sync(0xffffffffu, nvis > 0)) {
         // neither of this warp's two groups takes part in this tile: its P rows are zero
-        __syncwarp();
-        if (lane == 0) mbar_arrive(s_free(i & 1));
-        if (i >= C::NP && !(ok = warp_wait(pv_done((i - C::NP) & 1), ((i - C::NP) >> 1) & 1))) break;
-        uint8_t* prow = smem + C::kPOff + (i % C::NP) * C::kPBytes + r * 128;
+        uint32_t z[16];
 #pragma unroll
-        for (int ch = 0; ch < 8; ++ch) {
-          const int sw = (ch ^ (r & 7)) << 4;  // same swizzled order as the computed rows: no bank conflicts
-          *reinterpret_cast<uint4*>(prow + sw) = make_uint4(0u, 0u, 0u, 0u);
-        }
-        fence_proxy_async_smem();
+        for (int x = 0; x < 16; ++x) z[x] = 0u;
+        tmem_st_x16(pslot, z);
+        tmem_st_x16(pslot + 16, z);
+        tmem_wait_st();
+        tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(p_full(i & 1));
         continue;
       }
-      tc_fence_after();
       uint32_t raw[64];
-      tmem_ld_x32(tmem + lane_base + C::kSCol + 64 * (i & 1), raw);
-      tmem_ld_x32(tmem + lane_base + C::kSCol + 64 * (i & 1) + 32, raw + 32);
+      tmem_ld_x32(pslot, raw);
+      tmem_ld_x32(pslot + 32, raw + 32);
       tmem_wait_ld();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(s_free(i & 1));
       // raw scores.  Keys past a row's last visible one are masked to -inf only on
       // the diagonal (0 < nvis < 64); a row with nothing visible here (cold group or
       // beyond the diagonal) keeps its scores but takes no part: its maximum is -inf
@@ -439,20 +437,21 @@ __global__ void __launch_bounds__(kThreads, P2Cfg<D>::kCtasPerSm)
         }
         m2 = c;
       }
-      // this P buffer is free once PV(i - NP) has completed
-      if (i >= C::NP && !(ok = warp_wait(pv_done((i - C::NP) & 1), ((i - C::NP) >> 1) & 1))) break;
-      uint8_t* prow = smem + C::kPOff + (i % C::NP) * C::kPBytes + r * 128;
       // P = 2^(x*c2 - shift - m2), one bias per row; -inf for a row with nothing
       // visible in this tile (finite scores times c2 plus -inf give 2^-inf = 0)
       const float nb = (nvis <= 0 || m2 == -INFINITY) ? -INFINITY : -shift - m2;
       float ps[4] = {0.f, 0.f, 0.f, 0.f};  // four partial row sums (short dependency chains)
 #pragma unroll
-      for (int ch = 0; ch < 8; ++ch) {
+      for (int hf = 0; hf < 2; ++hf) {
         // the row sum adds the FP32 values; their FP16 roundings (relative error
         // at most 2^-11 each) go to the tensor cores
-        uint32_t hi[4];
-        p8_f16(sv + 8 * ch, c2, nb, hi, ps[ch & 1], ps[2 + (ch & 1)]);
-        *reinterpret_cast<uint4*>(prow + ((ch ^ (r & 7)) << 4)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        uint32_t pk[16];
+#pragma unroll
+        for (int c4 = 0; c4 < 4; ++c4) {
+          const int ch = 4 * hf + c4;
+          p8_f16(sv + 8 * ch, c2, nb, pk + 4 * c4, ps[ch & 1], ps[2 + (ch & 1)]);
+        }
+        tmem_st_x16(pslot + 16u * hf, pk);
       }
       l2 = l2 * f + ((ps[0] + ps[1]) + (ps[2] + ps[3]));
       if (__any_sync(0xffffffffu, rescale)) {
@@ -469,9 +468,8 @@ __global__ void __launch_bounds__(kThreads, P2Cfg<D>::kCtasPerSm)
           tmem_st_x16(tmem + lane_base + C::kOCol + c0, o);
           tmem_st_x16(tmem + lane_base + C::kOCol + c0 + 16, o + 16);
         }
-        tmem_wait_st();
       }
-      fence_proxy_async_smem();
+      tmem_wait_st();  // P (and a rescaled O) in TMEM before P.V is issued
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(p_full(i & 1));

@@ -288,3 +288,23 @@ def test_p_in_tmem_planted_mistake_is_caught():
         except Violation:
             caught += 1
     assert caught > 0
+
+
+@pytest.mark.parametrize("ns", [2, 3, 4])
+def test_one_group_p_in_tmem_is_safe(ns):
+    """pass2_kernel with P over its S slot in TMEM (2 K/V stages at d = 256)."""
+    for n in (1, 2, 7, 15):
+        for seed in range(25):
+            run(n, nsk=ns, nsv=ns, s_issuers=1, split=False, seed=seed, groups=1, p_in_tmem=True)
+
+
+def test_one_group_p_in_tmem_planted_mistake_is_caught():
+    """(With a 2-stage ring the load of entry i already waits for the P.V of entry
+    i - 2, so the missing wait shows only with more stages.)"""
+    caught = 0
+    for seed in range(200):
+        try:
+            run(12, nsk=4, nsv=4, s_issuers=1, split=False, seed=seed, groups=1, p_in_tmem=True, pbuf_wait=False)
+        except Violation:
+            caught += 1
+    assert caught > 0
