@@ -85,6 +85,14 @@ struct P1Params {
 constexpr int kSoftWarps = 4;
 constexpr int kThreads = (kSoftWarps + 2) * 32;
 constexpr int kProducerWarp = kSoftWarps, kMmaWarp = kSoftWarps + 1;
+// Threads of the one-block kernel.  At d = 256 twice as many: in the CTAs that run
+// the K/V quantizer inside the launch, its two groups then have 192 threads each
+// instead of 96, enough for it to keep ahead of pass 1 (a d = 256 tile is 64 KB of
+// bf16); in the pass-1 CTAs the warps past the MMA warp stay idle.
+template <int D>
+constexpr int p1_threads() {
+  return D >= 256 ? 2 * kThreads : kThreads;
+}
 
 template <int D>
 struct P1Cfg {
@@ -245,14 +253,16 @@ struct Pending {
 // follows the encode directly, a hot group's P scales are written as zero, and
 // a tile costs the softmax warps one wait and two arrives.
 template <int D, bool kOnesMma>
-__global__ void __launch_bounds__(kThreads, (D <= 128 ? 2 : 1)) pass1_kernel(const P1Params p) {
+__global__ void __launch_bounds__(p1_threads<D>(), (D <= 128 ? 2 : 1)) pass1_kernel(const P1Params p) {
   using C = P1Cfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
   if (!kOnesMma && p.kv_ready && (int)blockIdx.x >= p.n_p1) {
     // the K/V quantizer, in groups that each keep a tile in flight: the tiles in
     // the order the pass-1 CTAs below visit them
-    constexpr int kGroup = kThreads / C::kQuantGroups;
+    constexpr int kGroup = p1_threads<D>() / C::kQuantGroups;
+    static_assert(kGroup % 32 == 0 && kGroup % (D / 16) == 0 && p1_threads<D>() % C::kQuantGroups == 0,
+                  "quantizer groups of whole warps");
     const int g = threadIdx.x / kGroup;
     quant_role(p.s, p.k_raw, p.v_raw, p.ws, p.kv_ready, p.kv_ready + (size_t)p.s.BH() * p.s.T(), p.lse_scales != 0,
                smem + g * quant_role_smem(D, C::kQuantBufs), p.err, g, threadIdx.x % kGroup, kGroup, C::kQuantBufs);
@@ -456,7 +466,7 @@ __global__ void __launch_bounds__(kThreads, (D <= 128 ? 2 : 1)) pass1_kernel(con
       mma_commit(drain);
       wait_bounded(drain, 0, p.err);
     }
-  } else {
+  } else if (warp < kSoftWarps) {
     // ------------------------------------------------------------ one thread per row
     const int r = threadIdx.x, P = p0 + r;
     const bool valid = P < R;
@@ -838,7 +848,7 @@ struct P1MCfg {
   // thread groups of the K/V quantizer role (each a multiple of d/16 threads)
   static constexpr int kQuantGroups = 3;
   static_assert(kThreads % kQuantGroups == 0 && (kThreads / kQuantGroups) % (D / 16) == 0 &&
-                    kQuantGroups <= kQuantRoleGroups,
+                    (kThreads / kQuantGroups) % 32 == 0 && kQuantGroups <= kQuantRoleGroups,
                 "quantizer groups");
 };
 
@@ -1285,7 +1295,7 @@ cudaError_t launch_dv(const P1Params& prm, cudaStream_t st) {
     cudaError_t e =
         cudaFuncSetAttribute(pass1_kernel<D, kOnesMma>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e) return e;
-    pass1_kernel<D, kOnesMma><<<n_p1, kThreads, smem, st>>>(prm);
+    pass1_kernel<D, kOnesMma><<<n_p1, p1_threads<D>(), smem, st>>>(prm);
     return cudaGetLastError();
   }
   if (kOnesMma) return cudaErrorInvalidValue;
@@ -1299,7 +1309,7 @@ cudaError_t launch_dv(const P1Params& prm, cudaStream_t st) {
   prm2.n_p1 = n_p1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)sms);
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(p1_threads<D>());
   cfg.dynamicSmemBytes = (size_t)smem;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
@@ -1333,7 +1343,7 @@ bool single_quantizes_kv(const Shape& s) {
   if (sms - n_p1 < 8) return false;
   if (cudaFuncSetAttribute(pass1_kernel<D, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, single_kv_smem<D>()) !=
           cudaSuccess ||
-      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, pass1_kernel<D, false>, kThreads, single_kv_smem<D>()) !=
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, pass1_kernel<D, false>, p1_threads<D>(), single_kv_smem<D>()) !=
           cudaSuccess)
     return false;
   return per_sm == 1;
