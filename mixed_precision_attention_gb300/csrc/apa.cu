@@ -138,6 +138,11 @@ size_t workspace_layout(const Shape& s, bool apa_mode, Workspace* ws, void* base
   if (!apa_mode) {  // the all-exact path: the FP16 copy of V for its P.V product
     w.vamax = (uint32_t*)take(BH * 4);
     w.v16 = (uint16_t*)take(BH * s.Nkv * d * 2);
+    if (exact_split(s) > 1) {  // the parts of its split walks
+      const size_t parts = BH * nblk * exact_split(s) * kBlockRows;
+      w.part_o = (float*)take(parts * d * 4);
+      w.part_ml = (float2*)take(parts * 8);
+    }
     if (ws) *ws = w;
     return off;
   }

@@ -99,10 +99,23 @@ struct Workspace {
   uint32_t* hot_list; // [BH*nblk][T]: tile | group mask << 16
   uint32_t* hot_count;// [BH*nblk]
   uint32_t* p2_order; // [BH*nblk]: pass-2 work items (bh * nblk + blk), longest hot list first
+  // all-exact mode, d = 256: the parts of a split walk (exact_split(s) > 1), else null
+  float* part_o;      // [BH*nblk*nsplit][128][d]
+  float2* part_ml;    // [BH*nblk*nsplit][128]
 };
 // apa_mode false (eps = 0): only the FP16 copy of V and the head maxima of V.
 // flags: APA_FLAG_* of apa.h (APA_FLAG_Q_RESIDUAL adds the residual Q blob)
 size_t workspace_layout(const Shape& s, bool apa_mode, Workspace* ws, void* base, unsigned flags = 0);
+// The parts into which the all-exact pass 2 splits each block's walk: at d = 256
+// (the one-group kernel, one CTA per 128-row block) with few blocks per (b, KV head)
+// and a long walk, one part per 1024 tiles, at most 4.  It depends on the
+// per-(b, KV head) shape only, so the sub-problems of the host entry point split
+// the same way as the whole call.
+inline int exact_split(const Shape& s) {
+  if (s.d <= 128 || s.nblk() > 4) return 1;
+  const int k = s.T() / 1024;
+  return k < 1 ? 1 : (k > 4 ? 4 : k);
+}
 
 // Power-of-two divisor that brings a head's V into FP16 range: 1 when max |v| is
 // at most 2^15, else 2^(e - 14) for max |v| in [2^e, 2^(e+1)).  Dividing by it is

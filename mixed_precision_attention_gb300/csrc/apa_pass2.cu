@@ -68,6 +68,12 @@ struct P2Params {
   float* out;                 // [B,Hq,Nq,d]
   float* lse;                 // [B,Hq,Nq] or null
   int* err;
+  // the all-exact mode of the one-group kernel (d = 256) can split each block's walk
+  // into nsplit parts, one CTA each (index item * nsplit + part), which write their
+  // states (O in the FP16-V copy's units, and (m, l)) for combine_kernel to merge
+  int nsplit;
+  float* part_o;              // [BH*nblk*nsplit][128][d]
+  float2* part_ml;            // [BH*nblk*nsplit][128]
 };
 
 constexpr int kThreads = 224;
@@ -179,13 +185,15 @@ __global__ void __launch_bounds__(kThreads, P2Cfg<D>::kCtasPerSm)
   // longest hot lists first when ranked, else heavy (late, causal) blocks first:
   // CTAs start in index order, so the longest work items start earliest
   int bh, blk;
+  const int part = p.nsplit > 1 ? (int)blockIdx.x % p.nsplit : 0;
+  const int cta = p.nsplit > 1 ? (int)blockIdx.x / p.nsplit : (int)blockIdx.x;
   if (p.order) {
-    const int item = (int)p.order[blockIdx.x];
+    const int item = (int)p.order[cta];
     bh = item / nblk;
     blk = item % nblk;
   } else {
-    bh = blockIdx.x % BH;
-    blk = nblk - 1 - (int)(blockIdx.x / BH);
+    bh = cta % BH;
+    blk = nblk - 1 - cta / BH;
   }
   const int b = bh / s.Hkv, h = bh % s.Hkv;
   const int p0 = blk * kBlockRows;
@@ -208,11 +216,13 @@ __global__ void __launch_bounds__(kThreads, P2Cfg<D>::kCtasPerSm)
     return __all_sync(0xffffffffu, okl);
   };
 
-  // the block's tile list
+  // the block's tile list; with a split walk (all-exact mode) this CTA's part of it
   const bool apa_mode = p.hot_list != nullptr;
   const int last_row = min(R, p0 + kBlockRows) - 1;
   const int t_hi = s.causal ? min(T - 1, (last_row / G + off) / kTile) : T - 1;
-  const int n = apa_mode ? (int)p.hot_count[(size_t)bh * nblk + blk] : t_hi + 1;
+  const int n_all = apa_mode ? (int)p.hot_count[(size_t)bh * nblk + blk] : t_hi + 1;
+  const int i0 = p.nsplit > 1 ? (int)((long long)n_all * part / p.nsplit) : 0;
+  const int n = p.nsplit > 1 ? (int)((long long)n_all * (part + 1) / p.nsplit) - i0 : n_all;
   const uint32_t* list = apa_mode ? p.hot_list + ((size_t)bh * nblk + blk) * T : nullptr;
   auto tile_of = [&](int i, uint32_t& gmask) -> int {
     if (apa_mode) {
@@ -221,7 +231,8 @@ __global__ void __launch_bounds__(kThreads, P2Cfg<D>::kCtasPerSm)
       return (int)(e & 0xFFFFu);
     }
     gmask = 0xFFu;
-    return i == 0 ? 0 : t_hi + 1 - i;
+    const int g = i0 + i;
+    return g == 0 ? 0 : t_hi + 1 - g;
   };
 
   if (threadIdx.x == 0) {
@@ -474,10 +485,30 @@ __global__ void __launch_bounds__(kThreads, P2Cfg<D>::kCtasPerSm)
       __syncwarp();
       if (lane == 0) mbar_arrive(p_full(i & 1));
     }
-    // ---- epilogue: merge with the pass-1 state, write out and lse
+    // ---- epilogue: merge with the pass-1 state, write out and lse (or, for one part
+    // of a split walk, this part's state)
     if (ok && n > 0) ok = warp_wait(pv_done((n - 1) & 1), ((n - 1) >> 1) & 1);
     tc_fence_after();
-    if (ok) {
+    if (ok && p.nsplit > 1) {
+      const size_t prow = ((size_t)cta * p.nsplit + part) * kBlockRows + r;
+      float* po = p.part_o + prow * D;
+#pragma unroll 1
+      for (int c0 = 0; c0 < D; c0 += 32) {
+        uint32_t o[32];
+        if (n > 0) {
+          tmem_ld_x32(tmem + lane_base + C::kOCol + c0, o);
+          tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) o[j] = 0u;
+        }
+#pragma unroll
+        for (int j = 0; j < 32; j += 4)
+          *reinterpret_cast<float4*>(po + c0 + j) = make_float4(__uint_as_float(o[j]), __uint_as_float(o[j + 1]),
+                                                                __uint_as_float(o[j + 2]), __uint_as_float(o[j + 3]));
+      }
+      p.part_ml[prow] = make_float2(m2, l2);
+    } else if (ok) {
       float m1 = -INFINITY, l1 = 0.f;
       const float* st = nullptr;
       if (p.state_o) {
@@ -1010,6 +1041,42 @@ bool make_kv_map(CUtensorMap* map, const void* base, const Shape& s, CUtensorMap
 
 // Two softmax groups per block at d <= 128; at d = 256 their two O accumulators
 // would take all 512 TMEM columns, so one group.
+// Merges the parts of a split walk (all-exact mode, pass2_kernel) in part order:
+// one CTA per 128-row block, one thread per column, the rows in turn.  The same
+// merge as the kernel's epilogue: M = the largest part frame, each part weighted by
+// 2^(m - M), O in the FP16-V copy's units scaled back, divided by the summed l.
+template <int D>
+__global__ void __launch_bounds__(D) combine_kernel(const P2Params p) {
+  const Shape& s = p.s;
+  const int nblk = s.nblk(), BH = s.BH(), G = s.G(), R = s.R();
+  const int cta = blockIdx.x, bh = cta % BH, blk = nblk - 1 - cta / BH;
+  const int b = bh / s.Hkv, h = bh % s.Hkv, c = threadIdx.x;
+  const float vsc = v16_scale(__uint_as_float(p.vamax[bh]));
+  for (int r = 0; r < kBlockRows; ++r) {
+    const int P = blk * kBlockRows + r;
+    if (P >= R) break;
+    const int pos = P / G, hq = h * G + P % G;
+    const size_t row0 = (size_t)cta * p.nsplit * kBlockRows + r;
+    float M = -INFINITY;
+    for (int k = 0; k < p.nsplit; ++k) {
+      const float2 ml = p.part_ml[row0 + (size_t)k * kBlockRows];
+      M = fmaxf(M, ml.y > 0.f ? ml.x : -INFINITY);
+    }
+    float L = 0.f, acc = 0.f;
+    for (int k = 0; k < p.nsplit; ++k) {
+      const float2 ml = p.part_ml[row0 + (size_t)k * kBlockRows];
+      const float w = (ml.y > 0.f && M > -INFINITY) ? exp2f(ml.x - M) : 0.f;
+      L = __fmaf_rn(w, ml.y, L);
+      acc = __fmaf_rn(w * vsc, p.part_o[(row0 + (size_t)k * kBlockRows) * D + c], acc);
+    }
+    p.out[(((size_t)b * s.Hq + hq) * s.Nq + pos) * D + c] = acc * (1.f / L);
+    if (c == 0 && p.lse) {
+      const float lg = M + log2f(L);
+      p.lse[((size_t)b * s.Hq + hq) * s.Nq + pos] = 0.6931471805599453f * lg;  // (all-exact mode: no key mean)
+    }
+  }
+}
+
 template <int D>
 cudaError_t launch_d(const P2Params& prm, const CUtensorMap& km, const CUtensorMap& vm, cudaStream_t st) {
   const int grid = prm.s.BH() * prm.s.nblk();
@@ -1021,7 +1088,11 @@ cudaError_t launch_d(const P2Params& prm, const CUtensorMap& km, const CUtensorM
   } else {
     const int smem = P2Cfg<D>::kSmem;
     if ((e = cudaFuncSetAttribute(pass2_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem))) return e;
-    pass2_kernel<D><<<grid, kThreads, smem, st>>>(prm, km, vm);
+    pass2_kernel<D><<<grid * max(1, prm.nsplit), kThreads, smem, st>>>(prm, km, vm);
+    if (prm.nsplit > 1) {
+      if ((e = cudaGetLastError())) return e;
+      combine_kernel<D><<<grid, D, 0, st>>>(prm);
+    }
   }
   return cudaGetLastError();
 }
@@ -1073,6 +1144,9 @@ cudaError_t launch_pass2(const Shape& s, const void* q, const void* k, const voi
   prm.out = out;
   prm.lse = lse;
   prm.err = device_error_word();
+  prm.nsplit = ws->part_o ? exact_split(s) : 1;
+  prm.part_o = ws->part_o;
+  prm.part_ml = ws->part_ml;
   switch (s.d) {
     case 64: return launch_d<64>(prm, km, vm, st);
     case 128: return launch_d<128>(prm, km, vm, st);

@@ -65,6 +65,9 @@ def test_sizes(lib):
     assert lib.apa_workspace_bytes(1, 24, 8, 2048, 122880, 128, 0.0) == 8 * 122880 * 128 * 2 + 256
     assert lib.apa_workspace_bytes(1, 24, 8, 2048, 122880, 128, 0.005) > 141557760
     assert lib.apa_workspace_bytes(1, 3, 2, 16, 64, 64, 0.005) == 0  # Hq % Hkv != 0
+    # eps = 0 at d = 256 with a long walk (2048 tiles, one block): two parts' states too
+    assert lib.apa_workspace_bytes(1, 1, 1, 16, 131072, 256, 0.0) >= 131072 * 256 * 2 + 2 * 128 * (256 * 4 + 8)
+    assert lib.apa_workspace_bytes(1, 1, 1, 16, 65536, 256, 0.0) < 65536 * 256 * 2 + 128 * 256 * 4
 
 
 def test_workspace_too_small_is_rejected(lib):

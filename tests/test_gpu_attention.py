@@ -53,6 +53,25 @@ def test_eps0_matches_exact(name, causal):
     assert np.array_equal(_gpu.hot_bits(mask, T), np.broadcast_to(vis, mask.shape[:2] + vis.shape))
 
 
+def test_eps0_split_walk_matches_exact():
+    """At d = 256 the all-exact pass 2 splits a long walk over several CTAs (one part
+    per 1024 tiles, at most 4, with at most 4 blocks per KV head) and merges their
+    states in part order: one block of 16 rows over 131072 keys (2048 tiles) runs
+    as two parts."""
+    w = synth.small(B=1, Hq=1, Hkv=1, Nq=16, Nkv=131072, d=256, n_outliers=2, sink_gain=4.0, seed=11)
+    q, k, v = synth.generate(w)
+    ex, ex_lse = oracle.exact(q, k, v, causal=True)
+    out, lse, _ = _gpu.run_apa(q, k, v, causal=True, eps=0.0)
+    assert np.abs(out - ex).max() <= 4e-3
+    assert _gpu.cosine(out, ex) >= 0.99999
+    assert np.abs(lse - ex_lse).max() <= 1e-3
+    # the same rows, non-causal (every row sees every key)
+    ex, ex_lse = oracle.exact(q, k, v, causal=False)
+    out, lse, _ = _gpu.run_apa(q, k, v, causal=False, eps=0.0)
+    assert np.abs(out - ex).max() <= 4e-3
+    assert np.abs(lse - ex_lse).max() <= 1e-3
+
+
 def _check_apa(w, q, k, v, eps, causal=True, record=None, **options):
     ref = oracle.apa(q, k, v, causal=causal, eps=eps, diag=True)
     ex, _ = oracle.exact(q, k, v, causal=causal)
