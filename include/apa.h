@@ -93,7 +93,10 @@ int apa_attention(const void* q, const void* k, const void* v, int B, int Hq, in
 /* Bytes of device workspace apa_attention_ws() needs for this problem.  At
  * eps = 0 that is the FP16 copy of V ([B][Hkv][Nkv][d] FP16, V divided by a
  * power of two per head only when max |v| > 2^15, so exact for every bf16 value
- * above the FP16 subnormals) and the heads' maxima of |v|. */
+ * above the FP16 subnormals) and the heads' maxima of |v|; at d = 256, when a KV
+ * head has at most 4 blocks of 128 packed rows and 2048 or more key tiles, also
+ * the (m, l, O) states of the parts into which each block's walk is split (one
+ * part per 1024 tiles, at most 4). */
 size_t apa_workspace_bytes(int B, int Hq, int Hkv, int Nq, int Nkv, int d, float eps);
 
 /* apa_attention() with a caller-provided device workspace of at least
