@@ -96,7 +96,10 @@ int apa_attention(const void* q, const void* k, const void* v, int B, int Hq, in
  * above the FP16 subnormals) and the heads' maxima of |v|; at d = 256, when a KV
  * head has at most 4 blocks of 128 packed rows and 2048 or more key tiles, also
  * the (m, l, O) states of the parts into which each block's walk is split (one
- * part per 1024 tiles, at most 4). */
+ * part per 1024 tiles, at most 4).  At eps > 0 it holds the quantized operands,
+ * the pass-1 states and the hot lists, and at d = 256, when a KV head has at most
+ * 4 blocks and 1024 or more key tiles, the states of the parts of pass 2's walks
+ * over the hot lists (one part per 512 tiles, at most 4). */
 size_t apa_workspace_bytes(int B, int Hq, int Hkv, int Nq, int Nkv, int d, float eps);
 
 /* apa_attention() with a caller-provided device workspace of at least

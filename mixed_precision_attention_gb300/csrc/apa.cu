@@ -170,6 +170,12 @@ size_t workspace_layout(const Shape& s, bool apa_mode, Workspace* ws, void* base
     w.vtsum = (float*)take(BH * T * 4);
   }
   w.v16 = (uint16_t*)take(BH * s.Nkv * d * 2);
+  if (apa_split(s) > 1) {  // the parts of pass 2's split walks
+    const size_t parts = BH * nblk * apa_split(s) * kBlockRows;
+    w.part_o = (float*)take(parts * d * 4);
+    w.part_ml = (float2*)take(parts * 8);
+    w.part_qmu = (float*)take(BH * nblk * kBlockRows * 4);
+  }
   if (ws) *ws = w;
   return off;
 }

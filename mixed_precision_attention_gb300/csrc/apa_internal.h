@@ -99,9 +99,11 @@ struct Workspace {
   uint32_t* hot_list; // [BH*nblk][T]: tile | group mask << 16
   uint32_t* hot_count;// [BH*nblk]
   uint32_t* p2_order; // [BH*nblk]: pass-2 work items (bh * nblk + blk), longest hot list first
-  // all-exact mode, d = 256: the parts of a split walk (exact_split(s) > 1), else null
+  // d = 256: the parts of a split pass-2 walk (exact_split(s) > 1 in the all-exact
+  // mode, apa_split(s) > 1 in APA mode), else null
   float* part_o;      // [BH*nblk*nsplit][128][d]
   float2* part_ml;    // [BH*nblk*nsplit][128]
+  float* part_qmu;    // [BH*nblk][128], APA mode: each row's LSE term q.mu / sqrt(d)
 };
 // apa_mode false (eps = 0): only the FP16 copy of V and the head maxima of V.
 // flags: APA_FLAG_* of apa.h (APA_FLAG_Q_RESIDUAL adds the residual Q blob)
@@ -114,6 +116,14 @@ size_t workspace_layout(const Shape& s, bool apa_mode, Workspace* ws, void* base
 inline int exact_split(const Shape& s) {
   if (s.d <= 128 || s.nblk() > 4) return 1;
   const int k = s.T() / 1024;
+  return k < 1 ? 1 : (k > 4 ? 4 : k);
+}
+// The same for the APA-mode pass 2, whose walk is the block's hot list: a few
+// percent of the tiles, but the longest lists still set its time when there are
+// few blocks.  One part per 512 tiles of the context, at most 4.
+inline int apa_split(const Shape& s) {
+  if (s.d <= 128 || s.nblk() > 4) return 1;
+  const int k = s.T() / 512;
   return k < 1 ? 1 : (k > 4 ? 4 : k);
 }
 

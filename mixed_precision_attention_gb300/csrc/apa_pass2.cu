@@ -68,12 +68,15 @@ struct P2Params {
   float* out;                 // [B,Hq,Nq,d]
   float* lse;                 // [B,Hq,Nq] or null
   int* err;
-  // the all-exact mode of the one-group kernel (d = 256) can split each block's walk
-  // into nsplit parts, one CTA each (index item * nsplit + part), which write their
-  // states (O in the FP16-V copy's units, and (m, l)) for combine_kernel to merge
+  // the one-group kernel (d = 256) can split each block's walk (all visible tiles, or
+  // the hot list) into nsplit parts, one CTA each, which write their states (O in the
+  // FP16-V copy's units, and (m, l)) at row (item * nsplit + part) * 128 + r, item =
+  // bh * nblk + blk, for combine_kernel to merge.  In APA mode part 0 also carries
+  // the pass-1 state, and writes each row's LSE term q.mu / sqrt(d).
   int nsplit;
   float* part_o;              // [BH*nblk*nsplit][128][d]
   float2* part_ml;            // [BH*nblk*nsplit][128]
+  float* part_qmu;            // [BH*nblk][128], APA mode only
 };
 
 constexpr int kThreads = 224;
@@ -216,7 +219,7 @@ __global__ void __launch_bounds__(kThreads, P2Cfg<D>::kCtasPerSm)
     return __all_sync(0xffffffffu, okl);
   };
 
-  // the block's tile list; with a split walk (all-exact mode) this CTA's part of it
+  // the block's tile list; with a split walk this CTA's part of it
   const bool apa_mode = p.hot_list != nullptr;
   const int last_row = min(R, p0 + kBlockRows) - 1;
   const int t_hi = s.causal ? min(T - 1, (last_row / G + off) / kTile) : T - 1;
@@ -226,7 +229,7 @@ __global__ void __launch_bounds__(kThreads, P2Cfg<D>::kCtasPerSm)
   const uint32_t* list = apa_mode ? p.hot_list + ((size_t)bh * nblk + blk) * T : nullptr;
   auto tile_of = [&](int i, uint32_t& gmask) -> int {
     if (apa_mode) {
-      const uint32_t e = list[i];
+      const uint32_t e = list[i0 + i];
       gmask = e >> 16;
       return (int)(e & 0xFFFFu);
     }
@@ -490,8 +493,29 @@ __global__ void __launch_bounds__(kThreads, P2Cfg<D>::kCtasPerSm)
     if (ok && n > 0) ok = warp_wait(pv_done((n - 1) & 1), ((n - 1) >> 1) & 1);
     tc_fence_after();
     if (ok && p.nsplit > 1) {
-      const size_t prow = ((size_t)cta * p.nsplit + part) * kBlockRows + r;
+      const size_t item = (size_t)bh * nblk + blk;
+      const size_t prow = (item * p.nsplit + part) * kBlockRows + r;
       float* po = p.part_o + prow * D;
+      // APA mode, part 0: the pass-1 state merged in first (as the epilogue below
+      // does), in the FP16-V copy's units (a division by a power of two)
+      float w1 = 0.f, w2 = 1.f, mo = m2, lo = l2, inv_vsc = 1.f;
+      const float* st = nullptr;
+      if (part == 0 && p.state_o) {
+        float m1 = -INFINITY, l1 = 0.f;
+        st = p.state_o + ((size_t)bh * nblk * kBlockRows + P) * D;
+        if (row_valid) {
+          const float2 ml = p.state_ml[(size_t)bh * nblk * kBlockRows + P];
+          m1 = ml.x;
+          l1 = ml.y;
+        }
+        const float e1 = l1 > 0.f ? m1 : -INFINITY, e2 = l2 > 0.f ? m2 : -INFINITY;
+        mo = fmaxf(e1, e2);
+        w1 = e1 == -INFINITY ? 0.f : exp2f(e1 - mo);
+        w2 = e2 == -INFINITY ? 0.f : exp2f(e2 - mo);
+        lo = w1 * l1 + w2 * l2;
+        inv_vsc = 1.f / v16_scale(__uint_as_float(p.vamax[bh]));
+        if (p.mu) p.part_qmu[item * kBlockRows + r] = qmu * rsqrtf((float)D);
+      }
 #pragma unroll 1
       for (int c0 = 0; c0 < D; c0 += 32) {
         uint32_t o[32];
@@ -502,12 +526,17 @@ __global__ void __launch_bounds__(kThreads, P2Cfg<D>::kCtasPerSm)
 #pragma unroll
           for (int j = 0; j < 32; ++j) o[j] = 0u;
         }
+        if (st && row_valid) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            o[j] = __float_as_uint(w1 * (st[c0 + j] * inv_vsc) + w2 * __uint_as_float(o[j]));
+        }
 #pragma unroll
         for (int j = 0; j < 32; j += 4)
           *reinterpret_cast<float4*>(po + c0 + j) = make_float4(__uint_as_float(o[j]), __uint_as_float(o[j + 1]),
                                                                 __uint_as_float(o[j + 2]), __uint_as_float(o[j + 3]));
       }
-      p.part_ml[prow] = make_float2(m2, l2);
+      p.part_ml[prow] = make_float2(mo, lo);
     } else if (ok) {
       float m1 = -INFINITY, l1 = 0.f;
       const float* st = nullptr;
@@ -1041,22 +1070,26 @@ bool make_kv_map(CUtensorMap* map, const void* base, const Shape& s, CUtensorMap
 
 // Two softmax groups per block at d <= 128; at d = 256 their two O accumulators
 // would take all 512 TMEM columns, so one group.
-// Merges the parts of a split walk (all-exact mode, pass2_kernel) in part order:
-// one CTA per 128-row block, one thread per column, the rows in turn.  The same
-// merge as the kernel's epilogue: M = the largest part frame, each part weighted by
-// 2^(m - M), O in the FP16-V copy's units scaled back, divided by the summed l.
+// Merges the parts of a split walk (pass2_kernel) in part order: one CTA per
+// kCombineRows rows of a 128-row block (blockIdx.x: the block, blockIdx.y: its rows),
+// one thread per column, the rows in turn.  The same merge as the kernel's
+// epilogue: M = the largest part frame, each part weighted by 2^(m - M), O in the
+// FP16-V copy's units scaled back, divided by the summed l.  In APA mode the
+// pass-1 state is already in part 0, and the LSE gets each row's q.mu / sqrt(d).
+constexpr int kCombineRows = 4;
 template <int D>
 __global__ void __launch_bounds__(D) combine_kernel(const P2Params p) {
   const Shape& s = p.s;
   const int nblk = s.nblk(), BH = s.BH(), G = s.G(), R = s.R();
   const int cta = blockIdx.x, bh = cta % BH, blk = nblk - 1 - cta / BH;
   const int b = bh / s.Hkv, h = bh % s.Hkv, c = threadIdx.x;
+  const size_t item = (size_t)bh * nblk + blk;
   const float vsc = v16_scale(__uint_as_float(p.vamax[bh]));
-  for (int r = 0; r < kBlockRows; ++r) {
+  for (int r = blockIdx.y * kCombineRows; r < (int)(blockIdx.y + 1) * kCombineRows; ++r) {
     const int P = blk * kBlockRows + r;
     if (P >= R) break;
     const int pos = P / G, hq = h * G + P % G;
-    const size_t row0 = (size_t)cta * p.nsplit * kBlockRows + r;
+    const size_t row0 = item * p.nsplit * kBlockRows + r;
     float M = -INFINITY;
     for (int k = 0; k < p.nsplit; ++k) {
       const float2 ml = p.part_ml[row0 + (size_t)k * kBlockRows];
@@ -1072,7 +1105,8 @@ __global__ void __launch_bounds__(D) combine_kernel(const P2Params p) {
     p.out[(((size_t)b * s.Hq + hq) * s.Nq + pos) * D + c] = acc * (1.f / L);
     if (c == 0 && p.lse) {
       const float lg = M + log2f(L);
-      p.lse[((size_t)b * s.Hq + hq) * s.Nq + pos] = 0.6931471805599453f * lg;  // (all-exact mode: no key mean)
+      p.lse[((size_t)b * s.Hq + hq) * s.Nq + pos] =
+          0.6931471805599453f * lg + (p.mu ? p.part_qmu[item * kBlockRows + r] : 0.f);
     }
   }
 }
@@ -1091,7 +1125,7 @@ cudaError_t launch_d(const P2Params& prm, const CUtensorMap& km, const CUtensorM
     pass2_kernel<D><<<grid * max(1, prm.nsplit), kThreads, smem, st>>>(prm, km, vm);
     if (prm.nsplit > 1) {
       if ((e = cudaGetLastError())) return e;
-      combine_kernel<D><<<grid, D, 0, st>>>(prm);
+      combine_kernel<D><<<dim3(grid, kBlockRows / kCombineRows), D, 0, st>>>(prm);
     }
   }
   return cudaGetLastError();
@@ -1144,9 +1178,10 @@ cudaError_t launch_pass2(const Shape& s, const void* q, const void* k, const voi
   prm.out = out;
   prm.lse = lse;
   prm.err = device_error_word();
-  prm.nsplit = ws->part_o ? exact_split(s) : 1;
+  prm.nsplit = ws->part_o ? (ws->hot_list ? apa_split(s) : exact_split(s)) : 1;
   prm.part_o = ws->part_o;
   prm.part_ml = ws->part_ml;
+  prm.part_qmu = ws->part_qmu;
   switch (s.d) {
     case 64: return launch_d<64>(prm, km, vm, st);
     case 128: return launch_d<128>(prm, km, vm, st);

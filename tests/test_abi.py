@@ -68,6 +68,14 @@ def test_sizes(lib):
     # eps = 0 at d = 256 with a long walk (2048 tiles, one block): two parts' states too
     assert lib.apa_workspace_bytes(1, 1, 1, 16, 131072, 256, 0.0) >= 131072 * 256 * 2 + 2 * 128 * (256 * 4 + 8)
     assert lib.apa_workspace_bytes(1, 1, 1, 16, 65536, 256, 0.0) < 65536 * 256 * 2 + 128 * 256 * 4
+    # eps > 0 at d = 256: pass 2's walk over the hot list splits one part per 512 tiles.
+    # From 1022 to 1023 tiles the workspace grows by one tile's share; from 1023 to 1024
+    # by that plus two parts' states (2 x 128 rows of O and (m, l)) and a q.mu term per
+    # row, each rounded up to 256 bytes
+    ws = lambda nkv: lib.apa_workspace_bytes(1, 1, 1, 16, nkv, 256, 0.005)  # noqa: E731
+    tile = ws(65472) - ws(65408)
+    parts = 2 * 128 * 256 * 4 + 2 * 128 * 8 + 128 * 4
+    assert parts <= ws(65536) - ws(65472) - tile <= parts + 3 * 255
 
 
 def test_workspace_too_small_is_rejected(lib):

@@ -113,6 +113,28 @@ def _check_apa(w, q, k, v, eps, causal=True, record=None, **options):
 COLD_SLACK = 1.0
 
 
+@pytest.mark.parametrize("causal", [True, False])
+def test_apa_split_walk_matches_emulation(causal, record_property):
+    """At d = 256 with few blocks per KV head, pass 2's walk over each block's hot list
+    is split over several CTAs (one part per 512 tiles, at most 4); part 0 carries the
+    pass-1 state, and the parts merge in part order.  Two blocks of 128 packed rows
+    over 65536 keys (1024 tiles) run as two parts each.  The host entry point, whose
+    per-head sub-problems split the same way, gives the same bits."""
+    import torch
+
+    import mixed_precision_attention_gb300 as apa
+    w = synth.small(B=1, Hq=4, Hkv=1, Nq=64, Nkv=65536, d=256, n_outliers=2, sink_gain=4.0, seed=5, causal=causal)
+    q, k, v = synth.generate(w)
+    r = _check_apa(w, q, k, v, 0.005, causal=causal, record=record_property)
+    assert 0 < r["hot_frac"] < 0.5
+    dev = _gpu.run_apa(q, k, v, causal=causal, eps=0.005)
+    hq, hk, hv = (synth.to_torch_bf16(a).pin_memory() for a in (q, k, v))
+    out, lse, mask = apa.attention_host(hq, hk, hv, causal=causal, eps=0.005, return_hot_mask=True)
+    assert np.array_equal(out.numpy().astype(np.float64), dev[0])
+    assert np.array_equal(lse.numpy().astype(np.float64), dev[1])
+    torch.cuda.synchronize()
+
+
 @pytest.mark.parametrize("name", list(SHAPES))
 @pytest.mark.parametrize("eps", [0.005, 0.02])
 def test_apa_matches_emulation(name, eps, record_property):
